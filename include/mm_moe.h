@@ -1,0 +1,149 @@
+/*
+ * mm_moe.h -- C ABI of a fused mixture-of-experts layer (forward + backward)
+ * for one NVIDIA GB300 (sm_103a).
+ *
+ * What it computes.  The layer of the Prime Mega MoE pages ("Prime Intellect
+ * releases Prime Mega MoE"; section "Why is MoE training communication-bound?":
+ * each token goes to a few experts and the GPU sorts tokens by expert before
+ * sending them; section "How does the fused kernel work?": dispatch, the two
+ * expert linear layers, SwiGLU and combine in one call, intermediates kept in
+ * GPU-only scratch buffers, and a backward pass added for training).  On one
+ * GPU the dispatch is a permutation of rows:
+ *
+ *   route     stable sort of the flat (token, slot) indices f = t*k + j by
+ *             expert topk_idx[t][j]  ->  offsets[E+1], perm[R], inv[R], R = T*k
+ *   forward   g = W_gate[e] x_t,  u = W_up[e] x_t,  a = silu(g) * u,
+ *             o = W_down[e] a,    y_t = sum_j topk_w[t][j] * o_(t,j)  (j ascending)
+ *   backward  of L = <y, dy>: dx, dW_gate, dW_up, dW_down, dtopk_w
+ *
+ * Conventions shared by every entry point.
+ *   - Every pointer argument except `shape` and the out-parameters of the size
+ *     and routing queries is a DEVICE pointer on the current CUDA device, 16-byte
+ *     aligned.  bf16 tensors are passed as their 16-bit patterns (uint16_t).
+ *   - Every tensor is dense and row-major in the shape written beside it.
+ *   - The library allocates and frees nothing.  The caller owns every buffer,
+ *     sized by mm_moe_workspace_size, and may reuse scratch between calls.
+ *   - Calls only enqueue work on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and return; none blocks the host except
+ *     mm_moe_read_status.  Calls on one stream are ordered; calls that share a
+ *     scratch or saved buffer on different streams race.
+ *   - Argument errors are returned before anything is enqueued.  Errors found
+ *     on the device (an expert index outside [0, E), a wait that ran out of
+ *     time) are written to a status word at the start of `scratch`, which every
+ *     forward/backward call clears first; read it with mm_moe_read_status.  No
+ *     kernel traps or asserts.
+ */
+#ifndef MM_MOE_H
+#define MM_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MM_MOE_API __attribute__((visibility("default")))
+#else
+#define MM_MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Arithmetic of the expert GEMMs.  The pages list BF16, MXFP8 (Blackwell) and
+ * an fp8_bwd mode (BF16 forward, FP8 backward) -- section "How does the fused
+ * kernel work?".  This build computes MM_MOE_BF16; the other two return
+ * MM_MOE_ENOTSUP. */
+typedef enum {
+  MM_MOE_BF16 = 0,
+  MM_MOE_MXFP8 = 1,
+  MM_MOE_FP8_BWD = 2
+} mm_moe_precision;
+
+typedef enum {
+  MM_MOE_OK = 0,
+  MM_MOE_EINVAL = 1,    /* bad shape, NULL or misaligned pointer, undersized call */
+  MM_MOE_ENOTSUP = 2,   /* precision or device not supported (needs sm_103) */
+  MM_MOE_EBADIDX = 3,   /* device: an expert index outside [0, E); that pair is dropped */
+  MM_MOE_ETIMEOUT = 4,  /* device: a pipeline wait ran out of time; outputs undefined */
+  MM_MOE_ECUDA = 5      /* a CUDA runtime call or launch failed */
+} mm_moe_status;
+
+/* Problem shape.  T tokens, H hidden, I expert intermediate, E experts, top-k.
+ * Limits: T, H, I, E, k >= 1; k <= E <= 1024; H % 128 == 0; I % 64 == 0;
+ * T * k < 2^31. */
+typedef struct {
+  int64_t T, H, I, E, k;
+  int32_t prec;      /* mm_moe_precision */
+  int32_t reserved;  /* must be 0 */
+} mm_moe_shape;
+
+/* Bytes of the two caller-owned device buffers.
+ *   scratch : per-call working memory (forward and backward both use it; its
+ *             first 256 bytes hold the device status word).
+ *   saved   : written by mm_moe_forward, read by mm_moe_backward; holds the
+ *             routing (offsets, perm, inv), the routing weights in routed order,
+ *             the expert-grouped copy of x and h = [g | u] in bf16.  It must
+ *             not change between the forward and its backward.
+ * Returns MM_MOE_EINVAL for an invalid shape. */
+MM_MOE_API mm_moe_status mm_moe_workspace_size(const mm_moe_shape* shape,
+                                    size_t* scratch_bytes, size_t* saved_bytes);
+
+/* Forward pass.
+ *   x        [T, H]    bf16   input tokens
+ *   topk_idx [T, k]    int32  expert of each (token, slot)
+ *   topk_w   [T, k]    fp32   routing weight of each (token, slot), used as given
+ *   W_gate   [E, I, H] bf16   gate projection of every expert
+ *   W_up     [E, I, H] bf16   up projection
+ *   W_down   [E, H, I] bf16   down projection
+ *   y        [T, H]    bf16   output (overwritten)
+ *   scratch, saved            caller buffers of the sizes above
+ *   stream                    cudaStream_t
+ * Internally fp32 accumulation; h, the SwiGLU output a and the weighted expert
+ * outputs are stored as bf16; the combine sums the k slots in fp32 in slot
+ * order (no atomics, bitwise deterministic). */
+MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape,
+                             const uint16_t* x, const int32_t* topk_idx, const float* topk_w,
+                             const uint16_t* W_gate, const uint16_t* W_up,
+                             const uint16_t* W_down, uint16_t* y,
+                             void* scratch, void* saved, void* stream);
+
+/* Backward pass of the forward that wrote `saved` (same shape and weights).
+ *   dy       [T, H]    bf16   upstream gradient of y
+ *   dx       [T, H]    bf16   gradient of x (overwritten)
+ *   dW_gate  [E, I, H] bf16   gradients of the weights (overwritten, not
+ *   dW_up    [E, I, H] bf16   accumulated; an expert with no routed token
+ *   dW_down  [E, H, I] bf16   gets exact zeros)
+ *   dtopk_w  [T, k]    fp32   gradient of the routing weights
+ * dtopk_w[t][j] = <a, W_down[e]^T dy_t> (equal to <dy_t, o> in exact
+ * arithmetic).  All sums have a fixed order: bitwise deterministic. */
+MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, const uint16_t* dy,
+                              const void* saved,
+                              const uint16_t* W_gate, const uint16_t* W_up,
+                              const uint16_t* W_down,
+                              uint16_t* dx, uint16_t* dW_gate, uint16_t* dW_up,
+                              uint16_t* dW_down, float* dtopk_w,
+                              void* scratch, void* stream);
+
+/* Device pointers, inside `saved`, to the routing the last forward computed
+ * (section "Why is MoE training communication-bound?": tokens sorted by
+ * expert).  offsets [E+1] int32: rows of expert e are [offsets[e], offsets[e+1]);
+ * perm [T*k] int32: flat index t*k+j of routed row r, ascending inside an
+ * expert; inv [T*k] int32: routed row of flat index f.  Host call, no sync. */
+MM_MOE_API mm_moe_status mm_moe_get_routing(const mm_moe_shape* shape, const void* saved,
+                                 const int32_t** offsets, const int32_t** perm,
+                                 const int32_t** inv);
+
+/* Synchronises `stream`, then returns the device status word of `scratch`
+ * (MM_MOE_OK, MM_MOE_EBADIDX or MM_MOE_ETIMEOUT), or MM_MOE_ECUDA when the
+ * synchronisation itself fails.  The only blocking call of the library. */
+MM_MOE_API mm_moe_status mm_moe_read_status(const void* scratch, void* stream);
+
+/* Number of kernels the last successful mm_moe_forward / mm_moe_backward call
+ * on this host thread enqueued (for launch accounting). */
+MM_MOE_API int mm_moe_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MM_MOE_H */

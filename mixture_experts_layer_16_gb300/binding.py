@@ -1,0 +1,145 @@
+"""Thin ctypes binding of libmm_moe.so (include/mm_moe.h).
+
+Argument marshalling only: every step of the layer runs in the CUDA library.
+PyTorch is used for device memory and streams.  There is no fallback: if the
+library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmm_moe.so")
+
+MM_MOE_BF16, MM_MOE_MXFP8, MM_MOE_FP8_BWD = 0, 1, 2
+PRECISION = {"bf16": MM_MOE_BF16, "mxfp8": MM_MOE_MXFP8, "fp8_bwd": MM_MOE_FP8_BWD}
+STATUS = {0: "MM_MOE_OK", 1: "MM_MOE_EINVAL", 2: "MM_MOE_ENOTSUP", 3: "MM_MOE_EBADIDX",
+          4: "MM_MOE_ETIMEOUT", 5: "MM_MOE_ECUDA"}
+MM_MOE_OK, MM_MOE_EINVAL, MM_MOE_ENOTSUP, MM_MOE_EBADIDX, MM_MOE_ETIMEOUT, MM_MOE_ECUDA = range(6)
+
+# every symbol include/mm_moe.h declares
+EXPORTS = ("mm_moe_workspace_size", "mm_moe_forward", "mm_moe_backward", "mm_moe_get_routing",
+           "mm_moe_read_status", "mm_moe_last_launch_count")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+        self.status = status
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int64), ("I", ctypes.c_int64),
+                ("E", ctypes.c_int64), ("k", ctypes.c_int64), ("prec", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+def make_shape(T, H, I, E, k, prec="bf16") -> Shape:
+    return Shape(int(T), int(H), int(I), int(E), int(k), PRECISION.get(prec, prec), 0)
+
+
+_lib: Optional[ctypes.CDLL] = None
+_vp = ctypes.c_void_p
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library once; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "mixture_experts_layer_16_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        sp = ctypes.POINTER(Shape)
+        L.mm_moe_workspace_size.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t),
+                                            ctypes.POINTER(ctypes.c_size_t)]
+        L.mm_moe_forward.argtypes = [sp] + [_vp] * 10
+        L.mm_moe_backward.argtypes = [sp] + [_vp] * 12
+        L.mm_moe_get_routing.argtypes = [sp, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                         ctypes.POINTER(_vp)]
+        L.mm_moe_read_status.argtypes = [_vp, _vp]
+        L.mm_moe_last_launch_count.argtypes = []
+        for fn in EXPORTS:
+            getattr(L, fn).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def _check(fn: str, st: int) -> None:
+    if st != MM_MOE_OK:
+        raise MoEError(fn, st)
+
+
+def mm_moe_workspace_size(shape: Shape) -> Tuple[int, int]:
+    sc, sv = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check("mm_moe_workspace_size",
+           lib().mm_moe_workspace_size(ctypes.byref(shape), ctypes.byref(sc), ctypes.byref(sv)))
+    return sc.value, sv.value
+
+
+def mm_moe_forward(shape: Shape, x, topk_idx, topk_w, W_gate, W_up, W_down, y, scratch, saved,
+                   stream=None, check: bool = True) -> int:
+    st = lib().mm_moe_forward(ctypes.byref(shape), _ptr(x), _ptr(topk_idx), _ptr(topk_w),
+                              _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(y), _ptr(scratch),
+                              _ptr(saved), _stream(stream))
+    if check:
+        _check("mm_moe_forward", st)
+    return st
+
+
+def mm_moe_backward(shape: Shape, dy, saved, W_gate, W_up, W_down, dx, dW_gate, dW_up, dW_down,
+                    dtopk_w, scratch, stream=None, check: bool = True) -> int:
+    st = lib().mm_moe_backward(ctypes.byref(shape), _ptr(dy), _ptr(saved), _ptr(W_gate),
+                               _ptr(W_up), _ptr(W_down), _ptr(dx), _ptr(dW_gate), _ptr(dW_up),
+                               _ptr(dW_down), _ptr(dtopk_w), _ptr(scratch), _stream(stream))
+    if check:
+        _check("mm_moe_backward", st)
+    return st
+
+
+def mm_moe_get_routing(shape: Shape, saved):
+    """Views of `saved` (a uint8 device tensor): offsets [E+1], perm [T*k], inv [T*k], int32."""
+    import torch
+    o, p, i = _vp(), _vp(), _vp()
+    _check("mm_moe_get_routing",
+           lib().mm_moe_get_routing(ctypes.byref(shape), _ptr(saved), ctypes.byref(o),
+                                    ctypes.byref(p), ctypes.byref(i)))
+    base = saved.data_ptr()
+    R = shape.T * shape.k
+
+    def view(ptr, n):
+        off = ptr.value - base
+        return saved[off:off + 4 * n].view(torch.int32)
+    return view(o, shape.E + 1), view(p, R), view(i, R)
+
+
+def mm_moe_read_status(scratch, stream=None) -> int:
+    return int(lib().mm_moe_read_status(_ptr(scratch), _stream(stream)))
+
+
+def mm_moe_last_launch_count() -> int:
+    return int(lib().mm_moe_last_launch_count())
+
+
+class Workspace:
+    """The two caller-owned device buffers of one layer shape, allocated with torch."""
+
+    def __init__(self, shape: Shape, device="cuda"):
+        import torch
+        self.shape = shape
+        sc, sv = mm_moe_workspace_size(shape)
+        self.scratch = torch.empty(max(sc, 256), dtype=torch.uint8, device=device)
+        self.saved = torch.empty(max(sv, 256), dtype=torch.uint8, device=device)

@@ -1,0 +1,93 @@
+// internal.h -- types shared by the translation units of the library (not part of
+// the public ABI): the workspace layout and the host-side kernel launchers.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mm_moe.h"
+
+namespace mmmoe {
+
+constexpr int BM = 128;            // rows of an M tile (routed rows or output rows)
+constexpr int BK = 64;             // K elements per pipeline stage (128 bytes of bf16)
+constexpr int ROUTE_CHUNK = 2048;  // flat (token, slot) indices per routing block
+constexpr int ROUTE_THREADS = 256;
+constexpr int MAX_E = 1024;
+
+// Device status word (first bytes of scratch).
+struct DevStatus {
+  int code;    // mm_moe_status
+  int detail;  // first bad flat index / id of the kernel whose wait ran out
+};
+
+// Byte offsets of every region inside `saved` and `scratch`.  Every region starts
+// on a 1024-byte boundary.  "Padded rows": each expert's routed rows start on a
+// multiple of BM and its tail up to the next multiple is zero, so that M tiles
+// never straddle two experts and the token-axis K loop of the weight-gradient
+// GEMMs reads zeros past an expert's last row.
+struct Layout {
+  int64_t T, H, I, E, k, R;
+  int64_t Rp;      // capacity of the padded row space: (ceil(R/BM) + E) * BM
+  int64_t NT;      // capacity in M tiles: Rp / BM
+  int64_t nblk;    // routing blocks: ceil(R / ROUTE_CHUNK)
+  int64_t n_pw;    // partial dot products per row for dtopk_w (I / BN of the dgrad-down GEMM)
+  // saved
+  size_t counts, offsets, pad_off, expert_order, meta, perm, inv, prow, rowflat, tile_expert,
+      tile_rows, w_row, x_perm, h, saved_bytes;
+  // scratch
+  size_t status, blk_counts, a, ys, dy_perm, dh, a_w, pw, dxs, scratch_bytes;
+};
+
+// meta[] slots in `saved`
+constexpr int META_NUM_TILES = 0;
+
+mm_moe_status make_layout(const mm_moe_shape* s, Layout* L);
+
+// Width of the N tile each GEMM uses for an output dimension of n columns.
+int pick_bn(int64_t n);
+
+// ------------------------------------------------------------------ launchers
+// Each returns cudaSuccess or the launch error; `launches` is incremented per kernel.
+struct Ctx {
+  cudaStream_t stream;
+  int num_sms;
+  int* launches;
+};
+
+cudaError_t launch_route(const Ctx& c, const Layout& L, const int32_t* topk_idx,
+                         const float* topk_w, char* saved, char* scratch);
+cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
+                           const char* saved, float* w_row_out, char* scratch);
+cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
+                           const char* saved, uint16_t* out);
+cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slots,
+                             const char* saved, const float* pw, uint16_t* dx, float* dtopk_w);
+
+enum GemmKind {
+  GEMM_GATEUP = 0,        // x_perm . [W_gate|W_up]^T  -> SwiGLU epilogue (h, a)
+  GEMM_DOWN = 1,          // a . W_down^T              -> w * o into token-major slots
+  GEMM_DGRAD_DOWN = 2,    // dy_perm . W_down          -> dSwiGLU epilogue (dh, a_w, pw)
+  GEMM_DGRAD_GATEUP = 3,  // dh . [W_gate;W_up]        -> dx rows into token-major slots
+  GEMM_WGRAD_DOWN = 4,    // dy_perm^T . a_w per expert -> dW_down
+  GEMM_WGRAD_GATEUP = 5,  // dh^T . x_perm per expert   -> dW_gate, dW_up
+};
+
+struct GemmArgs {
+  int kind;
+  // operands (device)
+  const uint16_t* A;    // base of the A operand tensor
+  const uint16_t* B0;   // first B tensor
+  const uint16_t* B1;   // second B tensor (W_up) or nullptr
+  // epilogue (device)
+  uint16_t* out0;
+  uint16_t* out1;
+  float* outf;
+  const uint16_t* aux;  // h for the dSwiGLU epilogue
+  const char* saved;
+  char* scratch;
+};
+
+cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g);
+
+}  // namespace mmmoe

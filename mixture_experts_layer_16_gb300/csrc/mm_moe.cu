@@ -1,0 +1,278 @@
+// mm_moe.cu -- the C ABI: argument validation, workspace layout and the launch
+// sequences of the forward and backward passes (declared in include/mm_moe.h).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+
+namespace mmmoe {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
+  if (s == nullptr || L == nullptr) return MM_MOE_EINVAL;
+  if (s->T < 1 || s->H < 1 || s->I < 1 || s->E < 1 || s->k < 1) return MM_MOE_EINVAL;
+  if (s->k > s->E || s->E > MAX_E) return MM_MOE_EINVAL;
+  if (s->H % 128 != 0 || s->I % 64 != 0) return MM_MOE_EINVAL;
+  if (s->reserved != 0) return MM_MOE_EINVAL;
+  if (s->prec < MM_MOE_BF16 || s->prec > MM_MOE_FP8_BWD) return MM_MOE_EINVAL;
+  if (s->T > (int64_t{1} << 31) / s->k) return MM_MOE_EINVAL;
+  L->T = s->T;
+  L->H = s->H;
+  L->I = s->I;
+  L->E = s->E;
+  L->k = s->k;
+  L->R = s->T * s->k;
+  L->NT = (L->R + BM - 1) / BM + L->E;
+  L->Rp = L->NT * BM;
+  if (L->Rp >= (int64_t{1} << 31)) return MM_MOE_EINVAL;
+  L->nblk = (L->R + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+  L->n_pw = L->I / pick_bn(L->I);
+  const size_t A = 1024;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, A);
+    return at;
+  };
+  const size_t E = static_cast<size_t>(L->E), R = static_cast<size_t>(L->R),
+               Rp = static_cast<size_t>(L->Rp), NT = static_cast<size_t>(L->NT),
+               H = static_cast<size_t>(L->H), I = static_cast<size_t>(L->I);
+  // saved
+  L->counts = take(4 * E);
+  L->offsets = take(4 * (E + 1));
+  L->pad_off = take(4 * (E + 1));
+  L->expert_order = take(4 * E);
+  L->meta = take(4 * 16);
+  L->perm = take(4 * R);
+  L->inv = take(4 * R);
+  L->prow = take(4 * R);
+  L->rowflat = take(4 * Rp);
+  L->tile_expert = take(4 * NT);
+  L->tile_rows = take(4 * NT);
+  L->w_row = take(4 * Rp);
+  L->x_perm = take(2 * Rp * H);
+  L->h = take(2 * Rp * 2 * I);
+  L->saved_bytes = o;
+  // scratch: status and routing blocks, then the forward and backward regions overlaid
+  o = 0;
+  L->status = take(256);
+  L->blk_counts = take(4 * static_cast<size_t>(L->nblk) * E);
+  const size_t common = o;
+  L->a = take(2 * Rp * I);
+  L->ys = take(2 * R * H);
+  const size_t fwd_end = o;
+  o = common;
+  L->dy_perm = take(2 * Rp * H);
+  L->dh = take(2 * Rp * 2 * I);
+  L->a_w = take(2 * Rp * I);
+  L->pw = take(4 * Rp * static_cast<size_t>(L->n_pw));
+  L->dxs = take(2 * R * H);
+  L->scratch_bytes = o > fwd_end ? o : fwd_end;
+  return MM_MOE_OK;
+}
+
+struct DevInfo {
+  int sms = 0;
+  mm_moe_status st = MM_MOE_ECUDA;
+};
+
+static mm_moe_status device_info(DevInfo* out) {
+  static std::mutex mu;
+  static DevInfo cache[64];
+  static bool have[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MM_MOE_ECUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[dev]) {
+    DevInfo d;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      return MM_MOE_ECUDA;
+    }
+    d.st = (major == 10 && minor == 3) ? MM_MOE_OK : MM_MOE_ENOTSUP;
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *out = cache[dev];
+  return out->st;
+}
+
+static bool aligned(const void* p, uintptr_t a) {
+  return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+static thread_local int g_last_launches = 0;
+
+}  // namespace mmmoe
+
+using namespace mmmoe;
+
+#define MM_MOE_TRY(expr)                         \
+  do {                                           \
+    if ((expr) != cudaSuccess) return MM_MOE_ECUDA; \
+  } while (0)
+
+extern "C" MM_MOE_API mm_moe_status mm_moe_workspace_size(const mm_moe_shape* shape,
+                                                          size_t* scratch_bytes,
+                                                          size_t* saved_bytes) {
+  Layout L;
+  const mm_moe_status st = make_layout(shape, &L);
+  if (st != MM_MOE_OK) return st;
+  if (scratch_bytes) *scratch_bytes = L.scratch_bytes;
+  if (saved_bytes) *saved_bytes = L.saved_bytes;
+  return MM_MOE_OK;
+}
+
+extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, const uint16_t* x,
+                                                   const int32_t* topk_idx, const float* topk_w,
+                                                   const uint16_t* W_gate, const uint16_t* W_up,
+                                                   const uint16_t* W_down, uint16_t* y,
+                                                   void* scratch, void* saved, void* stream) {
+  Layout L;
+  mm_moe_status st = make_layout(shape, &L);
+  if (st != MM_MOE_OK) return st;
+  if (shape->prec != MM_MOE_BF16) return MM_MOE_ENOTSUP;
+  if (!aligned(x, 16) || !aligned(W_gate, 16) || !aligned(W_up, 16) || !aligned(W_down, 16) ||
+      !aligned(y, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(scratch, 256) ||
+      !aligned(saved, 256))
+    return MM_MOE_EINVAL;
+  DevInfo d;
+  st = device_info(&d);
+  if (st != MM_MOE_OK) return st;
+  int launches = 0;
+  Ctx c{static_cast<cudaStream_t>(stream), d.sms, &launches};
+  char* sc = static_cast<char*>(scratch);
+  char* sv = static_cast<char*>(saved);
+  MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
+  MM_MOE_TRY(launch_route(c, L, topk_idx, topk_w, sv, sc));
+  uint16_t* x_perm = reinterpret_cast<uint16_t*>(sv + L.x_perm);
+  uint16_t* h = reinterpret_cast<uint16_t*>(sv + L.h);
+  uint16_t* a = reinterpret_cast<uint16_t*>(sc + L.a);
+  uint16_t* ys = reinterpret_cast<uint16_t*>(sc + L.ys);
+  MM_MOE_TRY(launch_permute(c, L, x, x_perm, sv, reinterpret_cast<float*>(sv + L.w_row), sc));
+  GemmArgs g{};
+  g.saved = sv;
+  g.scratch = sc;
+  g.kind = GEMM_GATEUP;
+  g.A = x_perm;
+  g.B0 = W_gate;
+  g.B1 = W_up;
+  g.out0 = h;
+  g.out1 = a;
+  MM_MOE_TRY(launch_gemm(c, L, g));
+  g = GemmArgs{};
+  g.saved = sv;
+  g.scratch = sc;
+  g.kind = GEMM_DOWN;
+  g.A = a;
+  g.B0 = W_down;
+  g.out0 = ys;
+  MM_MOE_TRY(launch_gemm(c, L, g));
+  MM_MOE_TRY(launch_combine(c, L, ys, sv, y));
+  g_last_launches = launches;
+  return MM_MOE_OK;
+}
+
+extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, const uint16_t* dy,
+                                                    const void* saved, const uint16_t* W_gate,
+                                                    const uint16_t* W_up, const uint16_t* W_down,
+                                                    uint16_t* dx, uint16_t* dW_gate,
+                                                    uint16_t* dW_up, uint16_t* dW_down,
+                                                    float* dtopk_w, void* scratch, void* stream) {
+  Layout L;
+  mm_moe_status st = make_layout(shape, &L);
+  if (st != MM_MOE_OK) return st;
+  if (shape->prec != MM_MOE_BF16) return MM_MOE_ENOTSUP;
+  if (!aligned(dy, 16) || !aligned(W_gate, 16) || !aligned(W_up, 16) || !aligned(W_down, 16) ||
+      !aligned(dx, 16) || !aligned(dW_gate, 16) || !aligned(dW_up, 16) || !aligned(dW_down, 16) ||
+      !aligned(dtopk_w, 4) || !aligned(scratch, 256) || !aligned(saved, 256))
+    return MM_MOE_EINVAL;
+  DevInfo d;
+  st = device_info(&d);
+  if (st != MM_MOE_OK) return st;
+  int launches = 0;
+  Ctx c{static_cast<cudaStream_t>(stream), d.sms, &launches};
+  char* sc = static_cast<char*>(scratch);
+  const char* sv = static_cast<const char*>(saved);
+  uint16_t* dy_perm = reinterpret_cast<uint16_t*>(sc + L.dy_perm);
+  uint16_t* dh = reinterpret_cast<uint16_t*>(sc + L.dh);
+  uint16_t* a_w = reinterpret_cast<uint16_t*>(sc + L.a_w);
+  float* pw = reinterpret_cast<float*>(sc + L.pw);
+  uint16_t* dxs = reinterpret_cast<uint16_t*>(sc + L.dxs);
+  const uint16_t* x_perm = reinterpret_cast<const uint16_t*>(sv + L.x_perm);
+  const uint16_t* h = reinterpret_cast<const uint16_t*>(sv + L.h);
+  MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
+  MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, sc));
+  GemmArgs g{};
+  g.saved = sv;
+  g.scratch = sc;
+  g.kind = GEMM_DGRAD_DOWN;
+  g.A = dy_perm;
+  g.B0 = W_down;
+  g.aux = h;
+  g.out0 = dh;
+  g.out1 = a_w;
+  g.outf = pw;
+  MM_MOE_TRY(launch_gemm(c, L, g));
+  g = GemmArgs{};
+  g.saved = sv;
+  g.scratch = sc;
+  g.kind = GEMM_DGRAD_GATEUP;
+  g.A = dh;
+  g.B0 = W_gate;
+  g.B1 = W_up;
+  g.out0 = dxs;
+  MM_MOE_TRY(launch_gemm(c, L, g));
+  MM_MOE_TRY(launch_unpermute(c, L, dxs, sv, pw, dx, dtopk_w));
+  g = GemmArgs{};
+  g.saved = sv;
+  g.scratch = sc;
+  g.kind = GEMM_WGRAD_DOWN;
+  g.A = dy_perm;
+  g.B0 = a_w;
+  g.out0 = dW_down;
+  MM_MOE_TRY(launch_gemm(c, L, g));
+  g = GemmArgs{};
+  g.saved = sv;
+  g.scratch = sc;
+  g.kind = GEMM_WGRAD_GATEUP;
+  g.A = dh;
+  g.B0 = x_perm;
+  g.out0 = dW_gate;
+  g.out1 = dW_up;
+  MM_MOE_TRY(launch_gemm(c, L, g));
+  g_last_launches = launches;
+  return MM_MOE_OK;
+}
+
+extern "C" MM_MOE_API mm_moe_status mm_moe_get_routing(const mm_moe_shape* shape,
+                                                       const void* saved,
+                                                       const int32_t** offsets,
+                                                       const int32_t** perm,
+                                                       const int32_t** inv) {
+  Layout L;
+  const mm_moe_status st = make_layout(shape, &L);
+  if (st != MM_MOE_OK) return st;
+  if (saved == nullptr) return MM_MOE_EINVAL;
+  const char* sv = static_cast<const char*>(saved);
+  if (offsets) *offsets = reinterpret_cast<const int32_t*>(sv + L.offsets);
+  if (perm) *perm = reinterpret_cast<const int32_t*>(sv + L.perm);
+  if (inv) *inv = reinterpret_cast<const int32_t*>(sv + L.inv);
+  return MM_MOE_OK;
+}
+
+extern "C" MM_MOE_API mm_moe_status mm_moe_read_status(const void* scratch, void* stream) {
+  if (scratch == nullptr) return MM_MOE_EINVAL;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MM_MOE_ECUDA;
+  DevStatus s{};
+  if (cudaMemcpy(&s, scratch, sizeof(s), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MM_MOE_ECUDA;
+  return static_cast<mm_moe_status>(s.code);
+}
+
+extern "C" MM_MOE_API int mm_moe_last_launch_count(void) { return g_last_launches; }

@@ -1,0 +1,333 @@
+// route.cu -- token routing (expert histogram, prefix scan, stable placement), the
+// row permutation into the expert-grouped layout, and the fixed-order reductions
+// back to token order (forward combine, backward un-permute).
+//
+// Prime Mega MoE pages, "Why is MoE training communication-bound?": before the
+// expert math the GPU sorts tokens by destination expert; results come back per
+// token afterwards.  On one GPU "sending" becomes a permutation of rows.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace mmmoe {
+
+__device__ __forceinline__ void set_status(DevStatus* st, int code, int detail) {
+  if (atomicCAS(&st->code, 0, code) == 0) st->detail = detail;
+}
+
+// ---------------------------------------------------------------- 1. histogram
+// One block per ROUTE_CHUNK flat indices: per-block expert counts.
+__global__ void __launch_bounds__(ROUTE_THREADS) route_count_kernel(
+    const int32_t* __restrict__ topk_idx, int R, int E, int* __restrict__ blk_counts,
+    DevStatus* status) {
+  __shared__ int hist[MAX_E];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * ROUTE_CHUNK;
+  for (int i0 = 0; i0 < ROUTE_CHUNK; i0 += blockDim.x) {
+    const int f = base + i0 + threadIdx.x;
+    int e = -1;
+    if (f < R) {
+      e = __ldg(topk_idx + f);
+      if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+        set_status(status, MM_MOE_EBADIDX, f);
+        e = -1;  // the pair is dropped
+      }
+    }
+    // warp-aggregated: one shared-memory add per distinct expert in the warp
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[e], __popc(peers));
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    blk_counts[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+// ---------------------------------------------------------------- 2. scan (one block)
+// counts, offsets (exclusive scan), padded offsets, per-block exclusive prefixes
+// (in place in blk_counts), the M-tile list and the experts ordered by row count.
+__global__ void __launch_bounds__(1024) route_scan_kernel(
+    int* __restrict__ blk_counts, int nblk, int E, int* __restrict__ counts,
+    int* __restrict__ offsets, int* __restrict__ pad_off, int* __restrict__ expert_order,
+    int* __restrict__ tile_expert, int* __restrict__ tile_rows, int* __restrict__ meta) {
+  __shared__ int s_cnt[MAX_E];
+  __shared__ int s_a[MAX_E];
+  __shared__ int s_b[MAX_E];
+  const int e = threadIdx.x;
+  int cnt = 0;
+  if (e < E) {
+    for (int b = 0; b < nblk; ++b) {
+      const int64_t i = static_cast<int64_t>(b) * E + e;
+      const int c = blk_counts[i];
+      blk_counts[i] = cnt;
+      cnt += c;
+    }
+  }
+  const int padded = (cnt + BM - 1) / BM * BM;
+  if (e < MAX_E) {
+    s_cnt[e] = (e < E) ? cnt : 0;
+    s_a[e] = (e < E) ? cnt : 0;
+    s_b[e] = (e < E) ? padded : 0;
+  }
+  __syncthreads();
+  // inclusive Hillis-Steele scans over the experts
+  for (int d = 1; d < MAX_E; d <<= 1) {
+    int va = 0, vb = 0;
+    if (e < MAX_E && e >= d) {
+      va = s_a[e - d];
+      vb = s_b[e - d];
+    }
+    __syncthreads();
+    if (e < MAX_E && e >= d) {
+      s_a[e] += va;
+      s_b[e] += vb;
+    }
+    __syncthreads();
+  }
+  if (e < E) {
+    const int off = s_a[e] - cnt;
+    const int poff = s_b[e] - padded;
+    counts[e] = cnt;
+    offsets[e] = off;
+    pad_off[e] = poff;
+    const int nt = padded / BM;
+    for (int i = 0; i < nt; ++i) {
+      tile_expert[poff / BM + i] = e;
+      tile_rows[poff / BM + i] = min(BM, cnt - i * BM);
+    }
+    // rank by descending row count, ties by expert index
+    int rank = 0;
+    for (int o = 0; o < E; ++o) {
+      const int c = s_cnt[o];
+      rank += (c > cnt) || (c == cnt && o < e);
+    }
+    expert_order[rank] = e;
+  }
+  if (e == E - 1) {
+    offsets[E] = s_a[e];
+    pad_off[E] = s_b[e];
+    meta[META_NUM_TILES] = s_b[e] / BM;
+  }
+}
+
+// ---------------------------------------------------------------- 3. stable placement
+// Each warp walks its 256 consecutive flat indices in order, 32 at a time; the
+// rank of an index among the earlier ones of the same expert is the warp's running
+// count plus the number of lower lanes with the same expert (__match_any_sync).
+// Block-level prefixes over warps and the scan's per-block prefixes complete the
+// stable position.  No atomics decide a position.
+__global__ void __launch_bounds__(ROUTE_THREADS) route_place_kernel(
+    const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int R, int E,
+    const int* __restrict__ blk_prefix, const int* __restrict__ offsets,
+    const int* __restrict__ pad_off, int* __restrict__ perm, int* __restrict__ inv,
+    int* __restrict__ prow, int* __restrict__ rowflat, float* __restrict__ w_row) {
+  constexpr int WARPS = ROUTE_THREADS / 32;
+  constexpr int PER_WARP = ROUTE_CHUNK / WARPS;  // 256
+  constexpr int ROUNDS = PER_WARP / 32;          // 8
+  __shared__ int wrun[WARPS][MAX_E];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < WARPS * MAX_E; i += blockDim.x) (&wrun[0][0])[i] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * ROUTE_CHUNK + warp * PER_WARP;
+  int my_e[ROUNDS], my_rank[ROUNDS];
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    const int f = base + r * 32 + lane;
+    int e = -1;
+    if (f < R) {
+      e = __ldg(topk_idx + f);
+      if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) e = -1;  // dropped
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    int rank = 0;
+    if (e >= 0) rank = wrun[warp][e] + __popc(peers & lt);
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wrun[warp][e] += __popc(peers);
+    __syncwarp();
+    my_e[r] = e;
+    my_rank[r] = rank;
+  }
+  __syncthreads();
+  // exclusive prefix over warps, per expert (in place)
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < WARPS; ++w) {
+      const int c = wrun[w][e];
+      wrun[w][e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    const int e = my_e[r];
+    const int f = base + r * 32 + lane;
+    if (e < 0) {
+      if (f < R) {  // a dropped pair: the reductions skip it
+        inv[f] = -1;
+        prow[f] = -1;
+      }
+      continue;
+    }
+    const int local = blk_prefix[static_cast<int64_t>(blockIdx.x) * E + e] + wrun[warp][e] + my_rank[r];
+    const int row = offsets[e] + local;
+    const int prw = pad_off[e] + local;
+    perm[row] = f;
+    inv[f] = row;
+    prow[f] = prw;
+    rowflat[prw] = f;
+    w_row[prw] = __ldg(topk_w + f);
+  }
+}
+
+cudaError_t launch_route(const Ctx& c, const Layout& L, const int32_t* topk_idx,
+                         const float* topk_w, char* saved, char* scratch) {
+  const int R = static_cast<int>(L.R), E = static_cast<int>(L.E);
+  const int nblk = static_cast<int>(L.nblk);
+  DevStatus* st = reinterpret_cast<DevStatus*>(scratch + L.status);
+  int* blk = reinterpret_cast<int*>(scratch + L.blk_counts);
+  route_count_kernel<<<nblk, ROUTE_THREADS, 0, c.stream>>>(topk_idx, R, E, blk, st);
+  ++*c.launches;
+  route_scan_kernel<<<1, 1024, 0, c.stream>>>(
+      blk, nblk, E, reinterpret_cast<int*>(saved + L.counts),
+      reinterpret_cast<int*>(saved + L.offsets), reinterpret_cast<int*>(saved + L.pad_off),
+      reinterpret_cast<int*>(saved + L.expert_order), reinterpret_cast<int*>(saved + L.tile_expert),
+      reinterpret_cast<int*>(saved + L.tile_rows), reinterpret_cast<int*>(saved + L.meta));
+  ++*c.launches;
+  route_place_kernel<<<nblk, ROUTE_THREADS, 0, c.stream>>>(
+      topk_idx, topk_w, R, E, blk, reinterpret_cast<const int*>(saved + L.offsets),
+      reinterpret_cast<const int*>(saved + L.pad_off), reinterpret_cast<int*>(saved + L.perm),
+      reinterpret_cast<int*>(saved + L.inv), reinterpret_cast<int*>(saved + L.prow),
+      reinterpret_cast<int*>(saved + L.rowflat), reinterpret_cast<float*>(saved + L.w_row));
+  ++*c.launches;
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- 4. permute
+// dst[pr] = src[token of padded row pr] (16-byte vector copies, one warp per row);
+// padding rows are written as zeros.  In the forward it also zeroes the routing
+// weight of padding rows (valid rows got theirs from the placement kernel).
+__global__ void __launch_bounds__(256) permute_rows_kernel(
+    const uint4* __restrict__ src, uint4* __restrict__ dst, int H8, int k,
+    const int* __restrict__ meta, const int* __restrict__ tile_rows,
+    const int* __restrict__ rowflat, float* __restrict__ w_row) {
+  const int n_rows = __ldg(meta + META_NUM_TILES) * BM;
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int pr = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pr < n_rows; pr += warps) {
+    const bool valid = (pr % BM) < __ldg(tile_rows + pr / BM);
+    uint4* d = dst + static_cast<int64_t>(pr) * H8;
+    if (valid) {
+      const int t = __ldg(rowflat + pr) / k;
+      const uint4* s = src + static_cast<int64_t>(t) * H8;
+#pragma unroll 4
+      for (int i = lane; i < H8; i += 32) d[i] = __ldg(s + i);
+    } else {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll 4
+      for (int i = lane; i < H8; i += 32) d[i] = z;
+      if (w_row != nullptr && lane == 0) w_row[pr] = 0.f;
+    }
+  }
+}
+
+cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
+                           const char* saved, float* w_row_out, char* scratch) {
+  (void)scratch;
+  const int grid = c.num_sms * 8;
+  permute_rows_kernel<<<grid, 256, 0, c.stream>>>(
+      reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst),
+      static_cast<int>(L.H / 8), static_cast<int>(L.k),
+      reinterpret_cast<const int*>(saved + L.meta), reinterpret_cast<const int*>(saved + L.tile_rows),
+      reinterpret_cast<const int*>(saved + L.rowflat), w_row_out);
+  ++*c.launches;
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- 5. reductions
+__device__ __forceinline__ void acc_bf16x8(float (&acc)[8], const uint4 v) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(p[i]);
+    acc[2 * i] += f.x;
+    acc[2 * i + 1] += f.y;
+  }
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
+  uint4 v;
+  __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+  return v;
+}
+
+// out[t] = sum_j slots[t*k + j] in fp32, j ascending (one warp per token).
+// With dtopk_w: also dtopk_w[t][j] = sum_n pw[prow[t*k+j]][n], n ascending.
+// Pairs dropped by the routing (prow < 0) contribute nothing.
+__global__ void __launch_bounds__(256) slot_reduce_kernel(
+    const uint4* __restrict__ slots, uint4* __restrict__ out, int T, int k, int H8,
+    const int* __restrict__ prow, const float* __restrict__ pw, int n_pw,
+    float* __restrict__ dtopk_w) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    const uint4* s = slots + static_cast<int64_t>(t) * k * H8;
+    uint4* o = out + static_cast<int64_t>(t) * H8;
+    // bit j set: slot j holds a routed row (k <= 1024 is bounded by E)
+    unsigned live_lo = 0;
+    bool all_live = true;
+    for (int j = 0; j < k; ++j) {
+      const bool live = __ldg(prow + static_cast<int64_t>(t) * k + j) >= 0;
+      all_live &= live;
+      if (j < 32 && live) live_lo |= 1u << j;
+    }
+    for (int i = lane; i < H8; i += 32) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < k; ++j) {
+        if (!all_live && (j >= 32 ? __ldg(prow + static_cast<int64_t>(t) * k + j) < 0
+                                  : !((live_lo >> j) & 1u)))
+          continue;
+        acc_bf16x8(acc, __ldg(s + static_cast<int64_t>(j) * H8 + i));
+      }
+      o[i] = pack_bf16x8(acc);
+    }
+    if (dtopk_w != nullptr) {
+      for (int j = lane; j < k; j += 32) {
+        const int64_t f = static_cast<int64_t>(t) * k + j;
+        const int r = __ldg(prow + f);
+        float acc = 0.f;
+        if (r >= 0) {
+          const float* p = pw + static_cast<int64_t>(r) * n_pw;
+          for (int n = 0; n < n_pw; ++n) acc += p[n];
+        }
+        dtopk_w[f] = acc;
+      }
+    }
+  }
+}
+
+cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
+                           const char* saved, uint16_t* out) {
+  slot_reduce_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(
+      reinterpret_cast<const uint4*>(slots), reinterpret_cast<uint4*>(out),
+      static_cast<int>(L.T), static_cast<int>(L.k), static_cast<int>(L.H / 8),
+      reinterpret_cast<const int*>(saved + L.prow), nullptr, 0, nullptr);
+  ++*c.launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slots,
+                             const char* saved, const float* pw, uint16_t* dx, float* dtopk_w) {
+  slot_reduce_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(
+      reinterpret_cast<const uint4*>(slots), reinterpret_cast<uint4*>(dx), static_cast<int>(L.T),
+      static_cast<int>(L.k), static_cast<int>(L.H / 8),
+      reinterpret_cast<const int*>(saved + L.prow), pw, static_cast<int>(L.n_pw), dtopk_w);
+  ++*c.launches;
+  return cudaGetLastError();
+}
+
+}  // namespace mmmoe

@@ -1,0 +1,84 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for sm_103a,
+loads, exports every symbol the header declares, and rejects invalid arguments
+before anything touches a device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from mixture_experts_layer_16_gb300 import binding as B
+from mixture_experts_layer_16_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return B.lib()
+
+
+def declared_symbols():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            src = open(os.path.join(inc, fn)).read()
+            names |= set(re.findall(r"MM_MOE_API\s+[\w\s\*]+?\b(mm_moe_\w+)\s*\(", src))
+    return names
+
+
+def test_exports_match_header(lib):
+    decl = declared_symbols()
+    assert decl == set(B.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (mm_moe_\w+)", out))
+    assert decl <= exported
+    for name in decl:
+        assert getattr(lib, name) is not None
+
+
+def test_workspace_size_and_shape_validation(lib):
+    sc, sv = B.mm_moe_workspace_size(B.make_shape(16384, 2048, 768, 128, 8))
+    assert sc > 0 and sv > 0
+    # the saved buffer holds x_perm and h at least: (ceil(R/128)+E)*128 padded rows
+    Rp = (16384 * 8 // 128 + 128) * 128
+    assert sv >= Rp * (2048 + 2 * 768) * 2
+    for bad in [(0, 128, 64, 8, 2), (64, 100, 64, 8, 2), (64, 128, 48, 8, 2), (64, 128, 64, 8, 9),
+                (64, 128, 64, 2048, 2), (64, 128, 64, 8, 0)]:
+        with pytest.raises(B.MoEError) as ei:
+            B.mm_moe_workspace_size(B.make_shape(*bad))
+        assert ei.value.status == B.MM_MOE_EINVAL
+    s = B.make_shape(64, 128, 64, 8, 2)
+    s.reserved = 1
+    with pytest.raises(B.MoEError):
+        B.mm_moe_workspace_size(s)
+
+
+def test_forward_backward_reject_before_launch(lib):
+    """NULL / misaligned pointers and unsupported precisions return before any CUDA call."""
+    s = B.make_shape(64, 128, 64, 8, 2)
+    null = [None] * 10
+    st = lib.mm_moe_forward(ctypes.byref(s), *([None] * 10))
+    assert st == B.MM_MOE_EINVAL
+    st = lib.mm_moe_backward(ctypes.byref(s), *([None] * 12))
+    assert st == B.MM_MOE_EINVAL
+    fake = [4096 * (i + 1) for i in range(10)]
+    mis = list(fake)
+    mis[0] += 2                                    # x misaligned
+    assert lib.mm_moe_forward(ctypes.byref(s), *mis) == B.MM_MOE_EINVAL
+    mx = B.make_shape(64, 128, 64, 8, 2, "mxfp8")
+    assert lib.mm_moe_forward(ctypes.byref(mx), *fake) == B.MM_MOE_ENOTSUP
+    assert lib.mm_moe_get_routing(ctypes.byref(s), None, None, None, None) == B.MM_MOE_EINVAL
+    assert lib.mm_moe_read_status(None, None) == B.MM_MOE_EINVAL
+    del null
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError):
+        B.lib()
