@@ -1,0 +1,440 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused MoE layer (forward + backward) on GB300.
+
+One step = mm_moe_forward + mm_moe_backward of the 16,384-token Qwen3-30B-A3B
+shaped layer (T=16384, H=2048, I=768, E=128, top-8, Zipf(1.2) routing), bf16
+with fp32 accumulation.  `value` is the whole job's algorithmic TFLOP/s
+(fwd 6*R*H*I + bwd 12*R*H*I, R = T*k, padding not counted) with inputs resident
+in HBM; `e2e` is the same metric through the public API with the step's
+activations copied from pinned host memory and the results copied back.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 run under torch.distributed.run: one independent layer replica per
+GPU (the path has no exchange step), barrier + max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd/bwd ms & TFLOP/s (30B-shape, 16k tok) as % of GB300 tensor peak"
+DEFAULT_CONFIG = "qwen3_30b_16k_zipf"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_FLOP_FACTOR = {  # algorithmic FLOPs per launch, in units of R*H*I
+    "gemm_gateup_swiglu": 4, "gemm_down_weighted": 2, "gemm_dgrad_down_dswiglu": 2,
+    "gemm_dgrad_gateup": 4, "gemm_wgrad_down": 2, "gemm_wgrad_gateup": 4}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=1024,
+                    help="tokens of the workload the CPU oracle baseline runs on")
+    ap.add_argument("--ref-sample-tokens", type=int, default=128,
+                    help="tokens per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kernels", action="store_true", help="also print the per-kernel table")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value of all ranks (every rank gets it)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(flops_per_step: float, world: int, ms_per_step_max: float) -> float:
+    """Whole-job TFLOP/s: the work of all ranks over the slowest rank's step time."""
+    return world * flops_per_step / (ms_per_step_max * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------- clocks
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+                "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                "clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="mm_moe_clocks_", suffix=".csv")
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), util=float(parts[4]),
+                                     hw=parts[6], hwt=parts[7], swt=parts[8], swp=parts[9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        load = [r for r in rows if r["util"] >= 50] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples_under_load": len(load)}
+
+
+# ---------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "mixture_experts_layer_16_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as fh:
+            h.update(fn.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
+    captured on this workload from the current sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(kernel)
+    if not ent or ent.get("workload") != workload or ent.get("sources") != source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def config_json(cfg):
+    routing = {"uniform": "uniform", "zipf": f"zipf(s={cfg.zipf_s})",
+               "zipf_trunc": f"zipf(s={cfg.zipf_s}) over {cfg.zipf_ranks} experts"}[cfg.routing]
+    return {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "k": cfg.k,
+            "routing": routing, "precision": cfg.prec,
+            "l2": "inputs larger than L2 (expert weights %.2f GB bf16)" % (
+                3 * cfg.E * cfg.H * cfg.I * 2 / 1e9),
+            "parallelism": "replicas"}
+
+
+def oracle_step(d, tokens: int):
+    """One oracle forward+backward on the first `tokens` tokens; returns (seconds, flops)."""
+    import oracle
+    import oracle.moe as om
+    sub = om.token_subset(d, range(tokens))
+    t0 = time.perf_counter()
+    f = oracle.forward(sub["x"], sub["topk_idx"], sub["topk_w"], d["W_gate"], d["W_up"],
+                       d["W_down"])
+    oracle.backward(sub["dy"], sub["x"], sub["topk_idx"], sub["topk_w"], d["W_gate"], d["W_up"],
+                    d["W_down"], fwd=f)
+    dt = time.perf_counter() - t0
+    k = d["topk_idx"].shape[1]
+    H = d["x"].shape[1]
+    I = d["W_gate"].shape[1]
+    return dt, 18.0 * tokens * k * H * I
+
+
+# ---------------------------------------------------------------- the reference arm
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    from mixture_experts_layer_16_gb300.inputs import CONFIGS, make_inputs
+    cfg = CONFIGS[args.config]
+    d = make_inputs(cfg)
+    n = min(args.ref_sample_tokens, cfg.T)
+    for _ in range(args.warmup):
+        oracle_step(d, n)
+    times = []
+    flops = 0.0
+    for _ in range(args.steps):
+        dt, flops = oracle_step(d, n)
+        times.append(dt)
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_json(cfg),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} of {cfg.T} tokens per step (all {cfg.k} routed "
+                                   f"rows each, full expert weights), numpy fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_info()
+    init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from mixture_experts_layer_16_gb300 import binding as B
+    from mixture_experts_layer_16_gb300 import build as build_mod
+    if rank == 0:
+        build_mod.build()
+    barrier(world)
+    from mixture_experts_layer_16_gb300 import MoELayer
+    from mixture_experts_layer_16_gb300.inputs import CONFIGS, make_inputs
+
+    cfg = CONFIGS[args.config]
+    d = make_inputs(cfg)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    host = {k: bf(d[k + "_bits"]) for k in ("x", "W_gate", "W_up", "W_down", "dy")}
+    host["topk_idx"] = torch.from_numpy(d["topk_idx"])
+    host["topk_w"] = torch.from_numpy(d["topk_w"])
+    g = {k: v.to(dev) for k, v in host.items()}
+    layer = MoELayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, device=dev)
+    outs = (torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev),
+            torch.empty((cfg.E, cfg.I, cfg.H), dtype=torch.bfloat16, device=dev),
+            torch.empty((cfg.E, cfg.I, cfg.H), dtype=torch.bfloat16, device=dev),
+            torch.empty((cfg.E, cfg.H, cfg.I), dtype=torch.bfloat16, device=dev),
+            torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev))
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        layer.forward(g["x"], g["topk_idx"], g["topk_w"], g["W_gate"], g["W_up"], g["W_down"],
+                      y=y)
+
+    def bwd():
+        layer.backward(g["dy"], g["W_gate"], g["W_up"], g["W_down"], out=outs)
+
+    for _ in range(max(args.warmup, 0)):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    if layer.status() != B.MM_MOE_OK:
+        raise RuntimeError("device status after warm-up: " + B.STATUS[layer.status()])
+    n_fwd_launch = n_bwd_launch = 0
+
+    # ------------------------------------------------ timed region (device-resident inputs)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        B.mm_moe_profile_start()
+        start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            fwd()
+            n_fwd_launch = B.mm_moe_last_launch_count()
+            ev[i][1].record(stream)
+            bwd()
+            n_bwd_launch = B.mm_moe_last_launch_count()
+            ev[i][2].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        prof = B.mm_moe_profile_stop()
+    clock = clocks.summary()
+    ms_step = start.elapsed_time(stop) / K
+    ms_step_max = max_over_ranks(ms_step, world, dev)
+    fwd_ms = statistics.median(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    bwd_ms = statistics.median(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    st = layer.status()
+    if st != B.MM_MOE_OK:
+        raise RuntimeError("device status after timed region: " + B.STATUS[st])
+
+    # ------------------------------------------------ e2e through host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: host[k].pin_memory() for k in ("x", "topk_idx", "topk_w", "dy")}
+        out_h = (torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory(),
+                 torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory(),
+                 torch.empty((cfg.T, cfg.k), dtype=torch.float32).pin_memory())
+        act = {k: torch.empty_like(g[k]) for k in pin}
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in out_h)
+
+        def e2e_step():
+            for k2, t in pin.items():
+                act[k2].copy_(t, non_blocking=True)
+            layer.forward(act["x"], act["topk_idx"], act["topk_w"], g["W_gate"], g["W_up"],
+                          g["W_down"], y=y)
+            layer.backward(act["dy"], g["W_gate"], g["W_up"], g["W_down"], out=outs)
+            out_h[0].copy_(y, non_blocking=True)
+            out_h[1].copy_(outs[0], non_blocking=True)
+            out_h[2].copy_(outs[4], non_blocking=True)
+
+        for _ in range(max(args.warmup, 1)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        s2, t2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(K):
+            e2e_step()
+        t2.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(s2.elapsed_time(t2) / K, world, dev)
+        e2e = {"value": aggregate_value(cfg.flops_fwd() + cfg.flops_bwd(), world, e2e_ms),
+               "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h,
+               "note": "activations x, topk_idx, topk_w, dy in; y, dx, dtopk_w out; weights "
+                       "and weight gradients stay on the device"}
+
+    if rank != 0:
+        return 0
+
+    # ------------------------------------------------ roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    RHI = float(cfg.R) * cfg.H * cfg.I
+    kern = {name: {"avg_ms": ms / n, "launches_per_step": n / K, "share": 0.0}
+            for name, (ms, n) in prof.items() if n > 0}
+    tot = sum(v["avg_ms"] * v["launches_per_step"] for v in kern.values())
+    for v in kern.values():
+        v["share"] = v["avg_ms"] * v["launches_per_step"] / tot if tot else 0.0
+    gemms = {k: v for k, v in kern.items() if k in GEMM_FLOP_FACTOR}
+    dom = max(gemms, key=lambda k: gemms[k]["avg_ms"] * gemms[k]["launches_per_step"])
+    for k, v in gemms.items():
+        v["tflops"] = GEMM_FLOP_FACTOR[k] * RHI / (v["avg_ms"] * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    achieved = gemms[dom]["tflops"]
+    roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": recorded_traffic(dom, cfg.name),
+            "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
+            "algorithmic_flops_per_launch": GEMM_FLOP_FACTOR[dom] * RHI}
+
+    # ------------------------------------------------ CPU oracle baseline (rank 0, N=1)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        n = min(args.cpu_sample_tokens, cfg.T)
+        dt, fl = oracle_step(d, n)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+               "kind": "oracle", "seconds": dt,
+               "sample": f"first {n} of {cfg.T} tokens (all {cfg.k} routed rows each, full "
+                         f"expert weights), one forward+backward, numpy fp64"}
+
+    flops = cfg.flops_fwd() + cfg.flops_bwd()
+    value = aggregate_value(flops, world, ms_step_max)
+    bpeak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_json(cfg),
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "fwd_tflops": cfg.flops_fwd() / (fwd_ms * 1e-3) / 1e12,
+        "bwd_tflops": cfg.flops_bwd() / (bwd_ms * 1e-3) / 1e12,
+        "frac_of_bf16_peak": value / world / bpeak,
+        "peak_note": f"{peak_src} bf16_tflops_sustained = {bpeak}",
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": (n_fwd_launch + n_bwd_launch) * K,
+        "clocks": clock,
+        "kernels": kern if args.kernels else {k: round(v["share"], 4) for k, v in kern.items()},
+        "sources": source_digest(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -82,8 +82,8 @@ typedef struct {
  *             first 256 bytes hold the device status word).
  *   saved   : written by mm_moe_forward, read by mm_moe_backward; holds the
  *             routing (offsets, perm, inv), the routing weights in routed order,
- *             the expert-grouped copy of x and h = [g | u] in bf16.  It must
- *             not change between the forward and its backward.
+ *             the expert-grouped copy of x, h = [g | u] and a = silu(g) * u in
+ *             bf16.  It must not change between the forward and its backward.
  * Returns MM_MOE_EINVAL for an invalid shape. */
 MM_MOE_API mm_moe_status mm_moe_workspace_size(const mm_moe_shape* shape,
                                     size_t* scratch_bytes, size_t* saved_bytes);
@@ -141,6 +141,20 @@ MM_MOE_API mm_moe_status mm_moe_read_status(const void* scratch, void* stream);
 /* Number of kernels the last successful mm_moe_forward / mm_moe_backward call
  * on this host thread enqueued (for launch accounting). */
 MM_MOE_API int mm_moe_last_launch_count(void);
+
+/* Optional per-kernel timing (tracing aid; the pages describe none).
+ * mm_moe_profile_start clears the totals and, until mm_moe_profile_stop, makes
+ * every forward/backward call on this host thread record a CUDA event before and
+ * after each kernel it enqueues (on the call's stream).  mm_moe_profile_stop
+ * synchronises those events and writes, for kernel id i < n, the summed
+ * milliseconds total_ms[i] and the number of launches launches[i] (either array
+ * may be NULL).  Ids run from 0 to mm_moe_kernel_count()-1; mm_moe_kernel_name(i)
+ * names them (static strings, NULL for an unknown id).  Returns MM_MOE_ECUDA if
+ * an event could not be read. */
+MM_MOE_API mm_moe_status mm_moe_profile_start(void);
+MM_MOE_API mm_moe_status mm_moe_profile_stop(float* total_ms, int* launches, int n);
+MM_MOE_API const char* mm_moe_kernel_name(int id);
+MM_MOE_API int mm_moe_kernel_count(void);
 
 #ifdef __cplusplus
 }

@@ -21,7 +21,8 @@ MM_MOE_OK, MM_MOE_EINVAL, MM_MOE_ENOTSUP, MM_MOE_EBADIDX, MM_MOE_ETIMEOUT, MM_MO
 
 # every symbol include/mm_moe.h declares
 EXPORTS = ("mm_moe_workspace_size", "mm_moe_forward", "mm_moe_backward", "mm_moe_get_routing",
-           "mm_moe_read_status", "mm_moe_last_launch_count")
+           "mm_moe_read_status", "mm_moe_last_launch_count", "mm_moe_profile_start",
+           "mm_moe_profile_stop", "mm_moe_kernel_name", "mm_moe_kernel_count")
 
 
 class MoEError(RuntimeError):
@@ -61,8 +62,14 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(_vp)]
         L.mm_moe_read_status.argtypes = [_vp, _vp]
         L.mm_moe_last_launch_count.argtypes = []
+        L.mm_moe_profile_start.argtypes = []
+        L.mm_moe_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_float),
+                                          ctypes.POINTER(ctypes.c_int), ctypes.c_int]
+        L.mm_moe_kernel_name.argtypes = [ctypes.c_int]
+        L.mm_moe_kernel_count.argtypes = []
         for fn in EXPORTS:
             getattr(L, fn).restype = ctypes.c_int
+        L.mm_moe_kernel_name.restype = ctypes.c_char_p
         _lib = L
     return _lib
 
@@ -132,6 +139,28 @@ def mm_moe_read_status(scratch, stream=None) -> int:
 
 def mm_moe_last_launch_count() -> int:
     return int(lib().mm_moe_last_launch_count())
+
+
+def mm_moe_kernel_count() -> int:
+    return int(lib().mm_moe_kernel_count())
+
+
+def mm_moe_kernel_name(i: int) -> str:
+    n = lib().mm_moe_kernel_name(int(i))
+    return n.decode() if n else ""
+
+
+def mm_moe_profile_start() -> None:
+    _check("mm_moe_profile_start", lib().mm_moe_profile_start())
+
+
+def mm_moe_profile_stop():
+    """{kernel name: (total ms, launches)} of the calls since mm_moe_profile_start."""
+    n = mm_moe_kernel_count()
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int * n)()
+    _check("mm_moe_profile_stop", lib().mm_moe_profile_stop(ms, cnt, n))
+    return {mm_moe_kernel_name(i): (float(ms[i]), int(cnt[i])) for i in range(n)}
 
 
 class Workspace:

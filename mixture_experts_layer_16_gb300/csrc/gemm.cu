@@ -54,6 +54,7 @@ struct GemmParams {
   uint16_t* out1;
   float* outf;
   const uint16_t* aux;
+  const uint16_t* aux2;
   DevStatus* status;
 };
 
@@ -218,6 +219,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     const int64_t pr = ti.m0 + row;
     const float w = __ldg(p.w_row + pr);
     const uint16_t* hrow = p.aux + pr * 2 * I + ti.n0;
+    const uint16_t* arow = p.aux2 + pr * I + ti.n0;
     uint16_t* dhrow = p.out0 + pr * 2 * I + ti.n0;
     uint16_t* awrow = p.out1 + pr * I + ti.n0;
     float dot = 0.f;
@@ -225,9 +227,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
       ptx::tmem_ld32(tbase + c, r);
-      float g[32], u[32];
+      float g[32], u[32], av[32];
       load32_bf16(hrow + c, g);
       load32_bf16(hrow + I + c, u);
+      load32_bf16(arow + c, av);
       ptx::tmem_wait_ld(r);
       float gp[32];
       as_float(r, gp);
@@ -236,7 +239,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
       for (int i = 0; i < 32; ++i) {
         const float s = sigmoidf_(g[i]);
         const float sg = g[i] * s;               // silu(g)
-        const float a = sg * u[i];
+        const float a = av[i];                   // the forward's a (from fp32 g, u)
         dot += a * gp[i];
         const float da = w * gp[i];
         dg[i] = da * u[i] * s * (1.0f + g[i] * (1.0f - s));
@@ -540,8 +543,11 @@ static cudaError_t run(const Ctx& c, const GemmParams& p, int grid) {
   cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<KIND, BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  static constexpr int kId[6] = {K_GEMM_GATEUP, K_GEMM_DOWN, K_GEMM_DGRAD_DOWN,
+                                 K_GEMM_DGRAD_GATEUP, K_GEMM_WGRAD_DOWN, K_GEMM_WGRAD_GATEUP};
+  prof_begin(c, kId[KIND]);
   moe_gemm_kernel<KIND, BN><<<grid, 256, C::SMEM_BYTES, c.stream>>>(p);
-  ++*c.launches;
+  prof_end(c, kId[KIND]);
   return cudaGetLastError();
 }
 
@@ -565,6 +571,7 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   p.out1 = g.out1;
   p.outf = g.outf;
   p.aux = g.aux;
+  p.aux2 = g.aux2;
   p.status = reinterpret_cast<DevStatus*>(g.scratch + L.status);
   const uint64_t Rp = static_cast<uint64_t>(L.Rp), H = L.H, I = L.I, E = L.E;
   bool ok = true;

@@ -34,9 +34,9 @@ struct Layout {
   int64_t n_pw;    // partial dot products per row for dtopk_w (I / BN of the dgrad-down GEMM)
   // saved
   size_t counts, offsets, pad_off, expert_order, meta, perm, inv, prow, rowflat, tile_expert,
-      tile_rows, w_row, x_perm, h, saved_bytes;
+      tile_rows, w_row, x_perm, h, a, saved_bytes;
   // scratch
-  size_t status, blk_counts, a, ys, dy_perm, dh, a_w, pw, dxs, scratch_bytes;
+  size_t status, blk_counts, ys, dy_perm, dh, a_w, pw, dxs, scratch_bytes;
 };
 
 // meta[] slots in `saved`
@@ -55,10 +55,32 @@ struct Ctx {
   int* launches;
 };
 
+// Kernel ids (per-kernel timing and launch accounting).
+enum KernelId {
+  K_ROUTE_COUNT = 0,
+  K_ROUTE_SCAN,
+  K_ROUTE_PLACE,
+  K_PERMUTE_X,
+  K_GEMM_GATEUP,
+  K_GEMM_DOWN,
+  K_COMBINE,
+  K_PERMUTE_DY,
+  K_GEMM_DGRAD_DOWN,
+  K_GEMM_DGRAD_GATEUP,
+  K_UNPERMUTE,
+  K_GEMM_WGRAD_DOWN,
+  K_GEMM_WGRAD_GATEUP,
+  K_COUNT
+};
+
+// Bracket one kernel launch: optional timing events, and the launch counter.
+void prof_begin(const Ctx& c, int id);
+void prof_end(const Ctx& c, int id);
+
 cudaError_t launch_route(const Ctx& c, const Layout& L, const int32_t* topk_idx,
                          const float* topk_w, char* saved, char* scratch);
 cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
-                           const char* saved, float* w_row_out, char* scratch);
+                           const char* saved, float* w_row_out, int kernel_id);
 cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
                            const char* saved, uint16_t* out);
 cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slots,
@@ -83,7 +105,8 @@ struct GemmArgs {
   uint16_t* out0;
   uint16_t* out1;
   float* outf;
-  const uint16_t* aux;  // h for the dSwiGLU epilogue
+  const uint16_t* aux;   // h = [g | u] for the dSwiGLU epilogue
+  const uint16_t* aux2;  // a = silu(g) * u saved by the forward
   const char* saved;
   char* scratch;
 };

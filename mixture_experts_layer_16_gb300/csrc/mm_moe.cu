@@ -55,13 +55,13 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->w_row = take(4 * Rp);
   L->x_perm = take(2 * Rp * H);
   L->h = take(2 * Rp * 2 * I);
+  L->a = take(2 * Rp * I);
   L->saved_bytes = o;
   // scratch: status and routing blocks, then the forward and backward regions overlaid
   o = 0;
   L->status = take(256);
   L->blk_counts = take(4 * static_cast<size_t>(L->nblk) * E);
   const size_t common = o;
-  L->a = take(2 * Rp * I);
   L->ys = take(2 * R * H);
   const size_t fwd_end = o;
   o = common;
@@ -152,9 +152,10 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   MM_MOE_TRY(launch_route(c, L, topk_idx, topk_w, sv, sc));
   uint16_t* x_perm = reinterpret_cast<uint16_t*>(sv + L.x_perm);
   uint16_t* h = reinterpret_cast<uint16_t*>(sv + L.h);
-  uint16_t* a = reinterpret_cast<uint16_t*>(sc + L.a);
+  uint16_t* a = reinterpret_cast<uint16_t*>(sv + L.a);
   uint16_t* ys = reinterpret_cast<uint16_t*>(sc + L.ys);
-  MM_MOE_TRY(launch_permute(c, L, x, x_perm, sv, reinterpret_cast<float*>(sv + L.w_row), sc));
+  MM_MOE_TRY(launch_permute(c, L, x, x_perm, sv, reinterpret_cast<float*>(sv + L.w_row),
+                            K_PERMUTE_X));
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
@@ -206,8 +207,9 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   uint16_t* dxs = reinterpret_cast<uint16_t*>(sc + L.dxs);
   const uint16_t* x_perm = reinterpret_cast<const uint16_t*>(sv + L.x_perm);
   const uint16_t* h = reinterpret_cast<const uint16_t*>(sv + L.h);
+  const uint16_t* a = reinterpret_cast<const uint16_t*>(sv + L.a);
   MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
-  MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, sc));
+  MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY));
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
@@ -215,6 +217,7 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   g.A = dy_perm;
   g.B0 = W_down;
   g.aux = h;
+  g.aux2 = a;
   g.out0 = dh;
   g.out1 = a_w;
   g.outf = pw;

@@ -188,20 +188,23 @@ cudaError_t launch_route(const Ctx& c, const Layout& L, const int32_t* topk_idx,
   const int nblk = static_cast<int>(L.nblk);
   DevStatus* st = reinterpret_cast<DevStatus*>(scratch + L.status);
   int* blk = reinterpret_cast<int*>(scratch + L.blk_counts);
+  prof_begin(c, K_ROUTE_COUNT);
   route_count_kernel<<<nblk, ROUTE_THREADS, 0, c.stream>>>(topk_idx, R, E, blk, st);
-  ++*c.launches;
+  prof_end(c, K_ROUTE_COUNT);
+  prof_begin(c, K_ROUTE_SCAN);
   route_scan_kernel<<<1, 1024, 0, c.stream>>>(
       blk, nblk, E, reinterpret_cast<int*>(saved + L.counts),
       reinterpret_cast<int*>(saved + L.offsets), reinterpret_cast<int*>(saved + L.pad_off),
       reinterpret_cast<int*>(saved + L.expert_order), reinterpret_cast<int*>(saved + L.tile_expert),
       reinterpret_cast<int*>(saved + L.tile_rows), reinterpret_cast<int*>(saved + L.meta));
-  ++*c.launches;
+  prof_end(c, K_ROUTE_SCAN);
+  prof_begin(c, K_ROUTE_PLACE);
   route_place_kernel<<<nblk, ROUTE_THREADS, 0, c.stream>>>(
       topk_idx, topk_w, R, E, blk, reinterpret_cast<const int*>(saved + L.offsets),
       reinterpret_cast<const int*>(saved + L.pad_off), reinterpret_cast<int*>(saved + L.perm),
       reinterpret_cast<int*>(saved + L.inv), reinterpret_cast<int*>(saved + L.prow),
       reinterpret_cast<int*>(saved + L.rowflat), reinterpret_cast<float*>(saved + L.w_row));
-  ++*c.launches;
+  prof_end(c, K_ROUTE_PLACE);
   return cudaGetLastError();
 }
 
@@ -234,15 +237,15 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(
 }
 
 cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
-                           const char* saved, float* w_row_out, char* scratch) {
-  (void)scratch;
+                           const char* saved, float* w_row_out, int kernel_id) {
   const int grid = c.num_sms * 8;
+  prof_begin(c, kernel_id);
   permute_rows_kernel<<<grid, 256, 0, c.stream>>>(
       reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst),
       static_cast<int>(L.H / 8), static_cast<int>(L.k),
       reinterpret_cast<const int*>(saved + L.meta), reinterpret_cast<const int*>(saved + L.tile_rows),
       reinterpret_cast<const int*>(saved + L.rowflat), w_row_out);
-  ++*c.launches;
+  prof_end(c, kernel_id);
   return cudaGetLastError();
 }
 
@@ -312,21 +315,23 @@ __global__ void __launch_bounds__(256) slot_reduce_kernel(
 
 cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
                            const char* saved, uint16_t* out) {
+  prof_begin(c, K_COMBINE);
   slot_reduce_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(
       reinterpret_cast<const uint4*>(slots), reinterpret_cast<uint4*>(out),
       static_cast<int>(L.T), static_cast<int>(L.k), static_cast<int>(L.H / 8),
       reinterpret_cast<const int*>(saved + L.prow), nullptr, 0, nullptr);
-  ++*c.launches;
+  prof_end(c, K_COMBINE);
   return cudaGetLastError();
 }
 
 cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slots,
                              const char* saved, const float* pw, uint16_t* dx, float* dtopk_w) {
+  prof_begin(c, K_UNPERMUTE);
   slot_reduce_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(
       reinterpret_cast<const uint4*>(slots), reinterpret_cast<uint4*>(dx), static_cast<int>(L.T),
       static_cast<int>(L.k), static_cast<int>(L.H / 8),
       reinterpret_cast<const int*>(saved + L.prow), pw, static_cast<int>(L.n_pw), dtopk_w);
-  ++*c.launches;
+  prof_end(c, K_UNPERMUTE);
   return cudaGetLastError();
 }
 
