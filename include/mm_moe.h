@@ -138,6 +138,31 @@ MM_MOE_API mm_moe_status mm_moe_get_routing(const mm_moe_shape* shape, const voi
  * synchronisation itself fails.  The only blocking call of the library. */
 MM_MOE_API mm_moe_status mm_moe_read_status(const void* scratch, void* stream);
 
+/* Token routing that allocates nothing and takes no scratch buffer.  The source
+ * pages have no counterpart to this entry point: it exists for callers that cannot
+ * allocate device memory when they route tokens (runtimes without a device
+ * allocator, processes whose memory pool belongs to another component, code that
+ * must not meet an out-of-memory failure on this path).
+ *   shape->T, k, E   as for mm_moe_forward (H, I and prec are ignored);
+ *                    limits: T * k <= 262144, E <= 256, k <= E
+ *   topk_idx [T, k]  int32 device, topk_w [T, k] fp32 device (inputs)
+ *   offsets [E+1], perm [T*k], inv [T*k]  int32 device outputs, the same values
+ *                    mm_moe_get_routing returns after mm_moe_forward
+ * Its working memory is one fixed 4 MiB array in the library's device image:
+ * every GPU that loads the library holds it until the process exits, and every
+ * call shares it, so calls that overlap on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Pairs whose expert
+ * index is outside [0, E) are dropped (inv = -1, offsets[E] < T * k).
+ * Returns MM_MOE_EINVAL for sizes beyond the limits or NULL / misaligned
+ * pointers, MM_MOE_ENOTSUP off sm_103, MM_MOE_ECUDA for a failed CUDA call.
+ * Enqueues on `stream` and returns without synchronising. */
+MM_MOE_API mm_moe_status mm_moe_route_noalloc(const mm_moe_shape* shape,
+                                              const int32_t* topk_idx, const float* topk_w,
+                                              int32_t* offsets, int32_t* perm, int32_t* inv,
+                                              void* stream);
+
 /* Number of kernels the last successful mm_moe_forward / mm_moe_backward call
  * on this host thread enqueued (for launch accounting). */
 MM_MOE_API int mm_moe_last_launch_count(void);

@@ -22,7 +22,8 @@ MM_MOE_OK, MM_MOE_EINVAL, MM_MOE_ENOTSUP, MM_MOE_EBADIDX, MM_MOE_ETIMEOUT, MM_MO
 # every symbol include/mm_moe.h declares
 EXPORTS = ("mm_moe_workspace_size", "mm_moe_forward", "mm_moe_backward", "mm_moe_get_routing",
            "mm_moe_read_status", "mm_moe_last_launch_count", "mm_moe_profile_start",
-           "mm_moe_profile_stop", "mm_moe_kernel_name", "mm_moe_kernel_count")
+           "mm_moe_profile_stop", "mm_moe_kernel_name", "mm_moe_kernel_count",
+           "mm_moe_route_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -67,6 +68,7 @@ def lib() -> ctypes.CDLL:
                                           ctypes.POINTER(ctypes.c_int), ctypes.c_int]
         L.mm_moe_kernel_name.argtypes = [ctypes.c_int]
         L.mm_moe_kernel_count.argtypes = []
+        L.mm_moe_route_noalloc.argtypes = [sp] + [_vp] * 6
         for fn in EXPORTS:
             getattr(L, fn).restype = ctypes.c_int
         L.mm_moe_kernel_name.restype = ctypes.c_char_p
@@ -131,6 +133,17 @@ def mm_moe_get_routing(shape: Shape, saved):
         off = ptr.value - base
         return saved[off:off + 4 * n].view(torch.int32)
     return view(o, shape.E + 1), view(p, R), view(i, R)
+
+
+def mm_moe_route_noalloc(shape: Shape, topk_idx, topk_w, offsets, perm, inv, stream=None,
+                         check: bool = True) -> int:
+    """Routing into caller-provided offsets/perm/inv with no scratch buffer (the
+    library's own fixed device array is used; calls on different streams race)."""
+    st = lib().mm_moe_route_noalloc(ctypes.byref(shape), _ptr(topk_idx), _ptr(topk_w),
+                                    _ptr(offsets), _ptr(perm), _ptr(inv), _stream(stream))
+    if check:
+        _check("mm_moe_route_noalloc", st)
+    return st
 
 
 def mm_moe_read_status(scratch, stream=None) -> int:

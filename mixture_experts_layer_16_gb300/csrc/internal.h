@@ -79,6 +79,25 @@ void prof_end(const Ctx& c, int id);
 
 cudaError_t launch_route(const Ctx& c, const Layout& L, const int32_t* topk_idx,
                          const float* topk_w, char* saved, char* scratch);
+// Every buffer the three routing kernels touch, as explicit device pointers.
+struct RouteBufs {
+  DevStatus* status;
+  int* blk_counts;  // [ceil(R / ROUTE_CHUNK) * E]
+  int* counts;      // [E]
+  int* offsets;     // [E + 1]
+  int* pad_off;     // [E + 1]
+  int* expert_order;  // [E]
+  int* tile_expert;   // [NT]
+  int* tile_rows;     // [NT]
+  int* meta;          // [16]
+  int* perm;          // [R]
+  int* inv;           // [R]
+  int* prow;          // [R]
+  int* rowflat;       // [Rp]
+  float* w_row;       // [Rp]
+};
+cudaError_t launch_route_to(const Ctx& c, int R, int E, const int32_t* topk_idx,
+                            const float* topk_w, const RouteBufs& b);
 cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
                            const char* saved, float* w_row_out, int kernel_id);
 cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,

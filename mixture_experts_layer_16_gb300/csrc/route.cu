@@ -208,6 +208,27 @@ cudaError_t launch_route(const Ctx& c, const Layout& L, const int32_t* topk_idx,
   return cudaGetLastError();
 }
 
+// The same three routing kernels with every buffer given explicitly.
+cudaError_t launch_route_to(const Ctx& c, int R, int E, const int32_t* topk_idx,
+                            const float* topk_w, const RouteBufs& b) {
+  const int nblk = (R + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+  prof_begin(c, K_ROUTE_COUNT);
+  route_count_kernel<<<nblk, ROUTE_THREADS, 0, c.stream>>>(topk_idx, R, E, b.blk_counts,
+                                                           b.status);
+  prof_end(c, K_ROUTE_COUNT);
+  prof_begin(c, K_ROUTE_SCAN);
+  route_scan_kernel<<<1, 1024, 0, c.stream>>>(b.blk_counts, nblk, E, b.counts, b.offsets,
+                                              b.pad_off, b.expert_order, b.tile_expert,
+                                              b.tile_rows, b.meta);
+  prof_end(c, K_ROUTE_SCAN);
+  prof_begin(c, K_ROUTE_PLACE);
+  route_place_kernel<<<nblk, ROUTE_THREADS, 0, c.stream>>>(
+      topk_idx, topk_w, R, E, b.blk_counts, b.offsets, b.pad_off, b.perm, b.inv, b.prow,
+      b.rowflat, b.w_row);
+  prof_end(c, K_ROUTE_PLACE);
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- 4. permute
 // dst[pr] = src[token of padded row pr] (16-byte vector copies, one warp per row);
 // padding rows are written as zeros.  In the forward it also zeroes the routing
