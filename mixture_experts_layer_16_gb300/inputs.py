@@ -70,6 +70,9 @@ CONFIGS: Dict[str, MoEConfig] = {
     "qwen3_30b_16k_zipf_empty": MoEConfig("qwen3_30b_16k_zipf_empty", T=16384, H=2048,
                                           I=768, E=128, k=8, routing="zipf_trunc",
                                           zipf_s=1.2, zipf_ranks=120, seed=4),
+    # a smaller skewed case (same layer, 8,192 tokens) for profiler captures
+    "qwen3_30b_8k_zipf": MoEConfig("qwen3_30b_8k_zipf", T=8192, H=2048, I=768, E=128, k=8,
+                                   routing="zipf", zipf_s=1.2, seed=7),
     "qwen3_235b_8k": MoEConfig("qwen3_235b_8k", T=8192, H=4096, I=1536, E=128, k=8,
                                routing="uniform", seed=5),
     "qwen3_30b_16k_mxfp8": MoEConfig("qwen3_30b_16k_mxfp8", T=16384, H=2048, I=768,
