@@ -12,9 +12,16 @@
 //   WGRAD_DOWN   dW_down[e] = dy_perm^T . (w*a)      K = the expert's rows
 //   WGRAD_GATEUP [dW_gate;dW_up][e] = dh^T . x_perm   K = the expert's rows
 //
-// Roles (256 threads): warp 0 lane 0 = TMA producer, warp 1 lane 0 = MMA issuer,
-// warp 2 = TMEM allocator, warps 4..7 = epilogue (warp 4+q reads TMEM lanes
-// 32q..32q+31, i.e. tile rows 32q..32q+31).  Every wait is bounded: on expiry the
+// CTAS = 2 runs each tile on an SM pair: the two CTAs of a 2-CTA cluster each stage
+// 128 rows of A and half of the N columns of B, and one tcgen05.mma.cta_group::2 of
+// M = 256 reads both halves.  CTAS = 1 runs 128-row tiles on single SMs.
+//
+// Roles (256 threads per CTA): warp 0 lane 0 = TMA producer, warp 1 lane 0 of the
+// pair's rank-0 CTA = MMA issuer, warp 2 = TMEM allocator, warps 4..7 = epilogue
+// (warp 4+q reads TMEM lanes 32q..32q+31, i.e. the CTA's tile rows 32q..32q+31).
+// The epilogue moves data through per-warp 32 x 32 blocks in shared memory: outputs
+// leave by TMA stores (or coalesced 16-byte stores for the scattered slot rows), and
+// the dSwiGLU inputs arrive by TMA loads.  Every wait is bounded: on expiry the
 // kernel records MM_MOE_ETIMEOUT in the status word and every role unwinds.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -37,9 +44,13 @@ struct GemmParams {
   CUtensorMap tmA;
   CUtensorMap tmB0;
   CUtensorMap tmB1;
+  CUtensorMap tmC0;  // epilogue outputs stored by TMA (32 x 32 boxes, 64-byte swizzle)
+  CUtensorMap tmC1;
+  CUtensorMap tmD0;  // epilogue inputs loaded by TMA (dSwiGLU: h and a)
+  CUtensorMap tmD1;
   int H, I, E;
   int n_tiles;  // N tiles per M block (grouped kinds) or per expert M row (per-expert kinds)
-  int m_tiles;  // M tiles per expert (per-expert kinds)
+  int m_tiles;  // M tiles (of BM * CTAS rows) per expert (per-expert kinds)
   int k_iters;  // K iterations per tile (grouped kinds)
   int n_pw;
   int max_tiles;
@@ -53,37 +64,52 @@ struct GemmParams {
   uint16_t* out0;
   uint16_t* out1;
   float* outf;
-  const uint16_t* aux;
-  const uint16_t* aux2;
   DevStatus* status;
 };
 
-template <int KIND, int BN_>
+template <int KIND, int BN_, int CTAS_>
 struct Cfg {
-  static constexpr int BN = BN_;
+  static constexpr int BN = BN_;      // N of one MMA (both CTAs of a pair together)
+  static constexpr int CTAS = CTAS_;
   static constexpr bool A_MN = KIND >= GEMM_WGRAD_DOWN;
   static constexpr bool B_MN = KIND >= GEMM_DGRAD_DOWN;
   static constexpr bool PER_EXPERT = KIND >= GEMM_WGRAD_DOWN;
+  static constexpr int B_ROWS = BN / CTAS;  // B rows (K-major) or columns (M/N-major) per CTA
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+  // epilogue staging per epilogue warp, in 2 KB blocks (32 rows x 32 bf16): TMA-loaded
+  // inputs (dSwiGLU: g, u, a) and a ring of output blocks (one block for the
+  // scattered slot rows, which the warp stores itself)
+  static constexpr bool SCATTER = KIND == GEMM_DOWN || KIND == GEMM_DGRAD_GATEUP;
+  static constexpr int EPI_IN = KIND == GEMM_DGRAD_DOWN ? 3 : 0;
+  static constexpr int EPI_OUT = SCATTER ? 1 : 4;
+  static constexpr int EPI_WARP_BYTES = (EPI_IN + EPI_OUT) * 2048;
+  static constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
+  static constexpr int SMEM_CAP = 232448 - 1024;  // opt-in limit minus static shared memory
+  static constexpr int STAGES_FIT = (SMEM_CAP - 1024 - EPI_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM * CTAS, BN, A_MN, B_MN);
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
+  static_assert(CTAS == 1 || (CTAS == 2 && B_ROWS >= 64), "CTAS");
+  static_assert(!(KIND == GEMM_GATEUP && CTAS == 2 && BN != 256), "pair gate/up tile");
+  static_assert(STAGES >= 2, "stages");
 };
 
 struct TileInfo {
   int e, mb, m0, n0, k_iters, k_row0;
 };
 
-// Decode tile t.  Grouped kinds: t -> (M block of padded routed rows, N tile), N
-// fastest.  Per-expert kinds: experts in descending row count, then (M, N) tiles.
-template <int KIND, int BN>
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
+// Decode tile t for this CTA (rank within the pair).  Grouped kinds: t -> (group of
+// CTAS 128-row blocks of padded routed rows, N tile), N fastest; the CTA takes block
+// CTAS*group + rank.  Per-expert kinds: experts in descending row count, then (M, N)
+// tiles of BM*CTAS x BN; the CTA takes rows rank*BM.. of the M tile.
+template <int KIND, int BN, int CTAS>
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int rank) {
   TileInfo ti;
-  if constexpr (Cfg<KIND, BN>::PER_EXPERT) {
+  if constexpr (Cfg<KIND, BN, CTAS>::PER_EXPERT) {
     const int per_e = p.m_tiles * p.n_tiles;
     const int ei = t / per_e;
     const int rem = t - ei * per_e;
@@ -91,16 +117,16 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
     const int nt = rem - mt * p.n_tiles;
     ti.e = __ldg(p.expert_order + ei);
     ti.mb = 0;
-    ti.m0 = mt * BM;
+    ti.m0 = mt * BM * CTAS + rank * BM;
     ti.n0 = nt * BN;
     ti.k_row0 = __ldg(p.pad_off + ti.e);
     ti.k_iters = (__ldg(p.pad_off + ti.e + 1) - ti.k_row0) / BK;
   } else {
-    const int mb = t / p.n_tiles;
-    const int nt = t - mb * p.n_tiles;
-    ti.mb = mb;
-    ti.e = __ldg(p.tile_expert + mb);
-    ti.m0 = mb * BM;
+    const int pmb = t / p.n_tiles;
+    const int nt = t - pmb * p.n_tiles;
+    ti.mb = pmb * CTAS + rank;
+    ti.e = __ldg(p.tile_expert + ti.mb);
+    ti.m0 = ti.mb * BM;
     ti.n0 = nt * (KIND == GEMM_GATEUP ? BN / 2 : BN);
     ti.k_iters = p.k_iters;
     ti.k_row0 = 0;
@@ -108,14 +134,14 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
   return ti;
 }
 
-template <int KIND, int BN>
+template <int KIND, int BN, int CTAS>
 __device__ __forceinline__ int total_tiles(const GemmParams& p) {
-  if constexpr (Cfg<KIND, BN>::PER_EXPERT) {
+  if constexpr (Cfg<KIND, BN, CTAS>::PER_EXPERT) {
     return p.E * p.m_tiles * p.n_tiles;
   } else {
     int nt = __ldg(p.meta + META_NUM_TILES);
     nt = min(nt, p.max_tiles);
-    return nt * p.n_tiles;
+    return (nt / CTAS) * p.n_tiles;
   }
 }
 
@@ -126,35 +152,36 @@ __device__ __forceinline__ void record_timeout(GemmParams const& p, volatile int
 }
 
 // ------------------------------------------------------------------ epilogue helpers
+// Each epilogue thread owns one accumulator row (TMEM lane); its 32-column chunks
+// go through a per-warp 32 x 32 bf16 block in shared memory laid out with the
+// 64-byte swizzle (16-byte chunk j of row r at r*64 + ((j ^ ((r >> 1) & 3)) * 16)),
+// conflict-free for the row-per-thread accesses and the layout the TMA engine uses.
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ void store32(uint16_t* dst, const float (&v)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    d[q] = make_uint4(pack2(v[8 * q], v[8 * q + 1]), pack2(v[8 * q + 2], v[8 * q + 3]),
-                      pack2(v[8 * q + 4], v[8 * q + 5]), pack2(v[8 * q + 6], v[8 * q + 7]));
+__device__ __forceinline__ uint8_t* swz(uint8_t* buf, int r, int j) {
+  return buf + r * 64 + ((j ^ ((r >> 1) & 3)) << 4);
 }
 
-__device__ __forceinline__ void store32_zero(uint16_t* dst) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+__device__ __forceinline__ void stage32(uint8_t* buf, int r, const float (&v)[32]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) d[q] = make_uint4(0, 0, 0, 0);
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(swz(buf, r, j)) =
+        make_uint4(pack2(v[8 * j], v[8 * j + 1]), pack2(v[8 * j + 2], v[8 * j + 3]),
+                   pack2(v[8 * j + 4], v[8 * j + 5]), pack2(v[8 * j + 6], v[8 * j + 7]));
 }
 
-__device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&v)[32]) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
+__device__ __forceinline__ void unstage32(uint8_t* buf, int r, float (&v)[32]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 w = __ldg(s + q);
+  for (int j = 0; j < 4; ++j) {
+    const uint4 w = *reinterpret_cast<const uint4*>(swz(buf, r, j));
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      v[8 * q + 2 * i] = __uint_as_float(ww[i] << 16);
-      v[8 * q + 2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
+      v[8 * j + 2 * i] = __uint_as_float(ww[i] << 16);
+      v[8 * j + 2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
     }
   }
 }
@@ -166,16 +193,86 @@ __device__ __forceinline__ void as_float(const uint32_t (&r)[32], float (&v)[32]
 
 __device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
-// Epilogue of one tile for one thread = one accumulator row.
-template <int KIND, int BN>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInfo& ti, int row,
-                                              uint32_t tbase) {
-  const int64_t I = p.I, H = p.H;
+// Per-warp epilogue state.
+struct EpiWarp {
+  uint8_t* in;        // input blocks (dSwiGLU)
+  uint8_t* out;       // output ring
+  uint64_t* ld_bar;   // input-load barrier of this warp
+  uint32_t ld_phase;
+  bool ld_pending;
+  int ob;             // next ring slot
+  int lane;
+};
+
+// Store this warp's 32 x 32 block (row r = lane) at element coordinates (c0, c1) of
+// tensor map m through the next slot of a ring of NB blocks.
+template <int NB>
+__device__ __forceinline__ void store_block(EpiWarp& w, const CUtensorMap* m, int c0, int c1,
+                                            const float (&v)[32]) {
+  uint8_t* buf = w.out + w.ob * 2048;
+  if (w.lane == 0) ptx::bulk_wait_read<NB - 1>();  // the slot's previous store has read it
+  __syncwarp();
+  stage32(buf, w.lane, v);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (w.lane == 0) {
+    ptx::tma_store_2d(m, buf, c0, c1);
+    ptx::bulk_commit();
+  }
+  w.ob = (w.ob + 1 == NB) ? 0 : w.ob + 1;
+}
+
+// Store this warp's 32 x 32 block to 32 scattered rows: row r goes to
+// out + dst_row(r) * ld + col (dst_row < 0: skipped), 4 lanes x 16 bytes per row.
+__device__ __forceinline__ void scatter_block(EpiWarp& w, uint16_t* out, int64_t ld, int dst_row,
+                                              int col, const float (&v)[32]) {
+  uint8_t* buf = w.out;
+  stage32(buf, w.lane, v);
+  __syncwarp();
+#pragma unroll
+  for (int step = 0; step < 4; ++step) {
+    const int r = step * 8 + (w.lane >> 2), j = w.lane & 3;
+    const uint4 val = *reinterpret_cast<const uint4*>(swz(buf, r, j));
+    const int fr = __shfl_sync(0xffffffffu, dst_row, r);
+    if (fr >= 0) *reinterpret_cast<uint4*>(out + static_cast<int64_t>(fr) * ld + col + j * 8) = val;
+  }
+  __syncwarp();
+}
+
+// dSwiGLU inputs of one 32-column chunk: g, u (from h) and a, rows row0..row0+31.
+__device__ __forceinline__ void load_inputs(EpiWarp& w, const GemmParams& p, int row0, int col) {
+  if (w.lane == 0) {
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive_expect_tx(w.ld_bar, 3 * 2048);
+    ptx::tma_load_2d(w.in, &p.tmD0, w.ld_bar, col, row0);
+    ptx::tma_load_2d(w.in + 2048, &p.tmD0, w.ld_bar, p.I + col, row0);
+    ptx::tma_load_2d(w.in + 4096, &p.tmD1, w.ld_bar, col, row0);
+  }
+  w.ld_pending = true;
+}
+
+__device__ __forceinline__ bool wait_inputs(EpiWarp& w, volatile int* abort) {
+  int ok = 1;
+  if (w.lane == 0) ok = ptx::mbar_wait(w.ld_bar, w.ld_phase, abort, WAIT_LIMIT_NS) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) {
+    w.ld_phase ^= 1u;
+    w.ld_pending = false;
+  }
+  return ok != 0;
+}
+
+// Epilogue of one tile for one warp (row = lane of the warp's 32 rows, q = warp).
+// `next` is the tile this CTA processes after this one (dSwiGLU prefetch), or null.
+template <int KIND, int BN, int CTAS>
+__device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInfo& ti,
+                                              const TileInfo* next, int q, uint32_t tbase,
+                                              EpiWarp& w, volatile int* abort) {
+  using C = Cfg<KIND, BN, CTAS>;
+  const int lane = w.lane, row = q * 32 + lane;
+  const int row0 = ti.m0 + q * 32;
   if constexpr (KIND == GEMM_GATEUP) {
     constexpr int HALF = BN / 2;
-    const int64_t pr = ti.m0 + row;
-    uint16_t* hrow = p.out0 + pr * 2 * I + ti.n0;
-    uint16_t* arow = p.out1 + pr * I + ti.n0;
 #pragma unroll 1
     for (int c = 0; c < HALF; c += 32) {
       uint32_t rg[32], ru[32];
@@ -188,20 +285,15 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
       as_float(ru, u);
 #pragma unroll
       for (int i = 0; i < 32; ++i) a[i] = g[i] * sigmoidf_(g[i]) * u[i];
-      store32(hrow + c, g);
-      store32(hrow + I + c, u);
-      store32(arow + c, a);
+      store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, g);
+      store_block<C::EPI_OUT>(w, &p.tmC0, p.I + ti.n0 + c, row0, u);
+      store_block<C::EPI_OUT>(w, &p.tmC1, ti.n0 + c, row0, a);
     }
   } else if constexpr (KIND == GEMM_DOWN || KIND == GEMM_DGRAD_GATEUP) {
     const int pr = ti.m0 + row;
     const bool valid = row < __ldg(p.tile_rows + ti.mb);
-    uint16_t* dst = nullptr;
-    float w = 1.0f;
-    if (valid) {
-      const int64_t f = __ldg(p.rowflat + pr);
-      dst = p.out0 + f * H + ti.n0;
-      if (KIND == GEMM_DOWN) w = __ldg(p.w_row + pr);
-    }
+    const int f = valid ? __ldg(p.rowflat + pr) : -1;
+    const float wgt = (KIND == GEMM_DOWN && valid) ? __ldg(p.w_row + pr) : 1.0f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
@@ -211,61 +303,56 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
       as_float(r, v);
       if (KIND == GEMM_DOWN) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= w;
+        for (int i = 0; i < 32; ++i) v[i] *= wgt;
       }
-      if (valid) store32(dst + c, v);
+      scatter_block(w, p.out0, p.H, f, ti.n0 + c, v);
     }
   } else if constexpr (KIND == GEMM_DGRAD_DOWN) {
     const int64_t pr = ti.m0 + row;
-    const float w = __ldg(p.w_row + pr);
-    const uint16_t* hrow = p.aux + pr * 2 * I + ti.n0;
-    const uint16_t* arow = p.aux2 + pr * I + ti.n0;
-    uint16_t* dhrow = p.out0 + pr * 2 * I + ti.n0;
-    uint16_t* awrow = p.out1 + pr * I + ti.n0;
+    const float wgt = __ldg(p.w_row + pr);
     float dot = 0.f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
+      if (!w.ld_pending) load_inputs(w, p, row0, ti.n0 + c);
+      if (!wait_inputs(w, abort)) return false;
+      float g[32], u[32], av[32];
+      unstage32(w.in, lane, g);
+      unstage32(w.in + 2048, lane, u);
+      unstage32(w.in + 4096, lane, av);
+      __syncwarp();
+      if (c + 32 < BN) load_inputs(w, p, row0, ti.n0 + c + 32);
+      else if (next != nullptr) load_inputs(w, p, next->m0 + q * 32, next->n0);
       uint32_t r[32];
       ptx::tmem_ld32(tbase + c, r);
-      float g[32], u[32], av[32];
-      load32_bf16(hrow + c, g);
-      load32_bf16(hrow + I + c, u);
-      load32_bf16(arow + c, av);
       ptx::tmem_wait_ld(r);
-      float gp[32];
-      as_float(r, gp);
-      float dg[32], du[32], aw[32];
+      float dg[32], du[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
+        const float gp = __uint_as_float(r[i]);
         const float s = sigmoidf_(g[i]);
         const float sg = g[i] * s;               // silu(g)
-        const float a = av[i];                   // the forward's a (from fp32 g, u)
-        dot += a * gp[i];
-        const float da = w * gp[i];
+        dot += av[i] * gp;                       // the forward's a (from fp32 g, u)
+        const float da = wgt * gp;
         dg[i] = da * u[i] * s * (1.0f + g[i] * (1.0f - s));
         du[i] = da * sg;
-        aw[i] = w * a;
+        av[i] *= wgt;                            // w * a, the dW_down operand
       }
-      store32(dhrow + c, dg);
-      store32(dhrow + I + c, du);
-      store32(awrow + c, aw);
+      store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, dg);
+      store_block<C::EPI_OUT>(w, &p.tmC0, p.I + ti.n0 + c, row0, du);
+      store_block<C::EPI_OUT>(w, &p.tmC1, ti.n0 + c, row0, av);
     }
     p.outf[pr * p.n_pw + ti.n0 / BN] = dot;
-  } else if constexpr (KIND == GEMM_WGRAD_DOWN) {
-    uint16_t* dst = p.out0 + (static_cast<int64_t>(ti.e) * H + ti.m0 + row) * I + ti.n0;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t r[32];
-      ptx::tmem_ld32(tbase + c, r);
-      ptx::tmem_wait_ld(r);
-      float v[32];
-      as_float(r, v);
-      store32(dst + c, v);
+  } else {  // weight gradients: dW_down [E*H, I]; dW_gate / dW_up [E*I, H]
+    const CUtensorMap* m;
+    int orow;
+    if (KIND == GEMM_WGRAD_DOWN) {
+      m = &p.tmC0;
+      orow = ti.e * p.H + row0;
+    } else {
+      const bool gate = row0 < p.I;
+      m = gate ? &p.tmC0 : &p.tmC1;
+      orow = ti.e * p.I + (gate ? row0 : row0 - p.I);
     }
-  } else {  // GEMM_WGRAD_GATEUP
-    const int m = ti.m0 + row;
-    uint16_t* dst = (m < I ? p.out0 + (static_cast<int64_t>(ti.e) * I + m) * H
-                           : p.out1 + (static_cast<int64_t>(ti.e) * I + (m - I)) * H) + ti.n0;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
@@ -273,76 +360,103 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileInf
       ptx::tmem_wait_ld(r);
       float v[32];
       as_float(r, v);
-      store32(dst + c, v);
+      store_block<C::EPI_OUT>(w, m, ti.n0 + c, orow, v);
     }
   }
+  return true;
 }
 
 // Zero tile of a per-expert GEMM whose expert has no rows (K = 0).
-template <int KIND, int BN>
-__device__ __forceinline__ void zero_tile(const GemmParams& p, const TileInfo& ti, int row) {
-  const int64_t I = p.I, H = p.H;
-  uint16_t* dst;
-  if constexpr (KIND == GEMM_WGRAD_DOWN) {
-    dst = p.out0 + (static_cast<int64_t>(ti.e) * H + ti.m0 + row) * I + ti.n0;
+template <int KIND, int BN, int CTAS>
+__device__ __forceinline__ void zero_tile(const GemmParams& p, const TileInfo& ti, int q,
+                                          EpiWarp& w) {
+  using C = Cfg<KIND, BN, CTAS>;
+  const int row0 = ti.m0 + q * 32;
+  const CUtensorMap* m;
+  int orow;
+  if (KIND == GEMM_WGRAD_DOWN) {
+    m = &p.tmC0;
+    orow = ti.e * p.H + row0;
   } else {
-    const int m = ti.m0 + row;
-    dst = (m < I ? p.out0 + (static_cast<int64_t>(ti.e) * I + m) * H
-                 : p.out1 + (static_cast<int64_t>(ti.e) * I + (m - I)) * H) + ti.n0;
+    const bool gate = row0 < p.I;
+    m = gate ? &p.tmC0 : &p.tmC1;
+    orow = ti.e * p.I + (gate ? row0 : row0 - p.I);
   }
+  float z[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) z[i] = 0.f;
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 32) store32_zero(dst + c);
+  for (int c = 0; c < BN; c += 32) store_block<C::EPI_OUT>(w, m, ti.n0 + c, orow, z);
 }
 
 // ------------------------------------------------------------------ producer loads
-template <int KIND, int BN>
+template <int CTAS>
+__device__ __forceinline__ void tma(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                    int c1) {
+  if constexpr (CTAS == 1)
+    ptx::tma_load_2d(dst, m, bar, c0, c1);
+  else
+    ptx::tma_load_2d_pair(dst, m, bar, c0, c1);
+}
+
+// This CTA's share of k block kb: its 128 rows of A and its B_ROWS rows (K-major)
+// or columns (M/N-major) of B, completing on the barrier at cluster address `bar`.
+template <int KIND, int BN, int CTAS>
 __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo& ti, int kb,
-                                            uint8_t* sa, uint8_t* sb, uint64_t* bar) {
+                                            uint8_t* sa, uint8_t* sb, uint32_t bar, int rank) {
+  using C = Cfg<KIND, BN, CTAS>;
   const int k0 = kb * BK;
+  const int nb = ti.n0 + rank * C::B_ROWS;  // first B row / column of this CTA
   if constexpr (KIND == GEMM_GATEUP) {
-    ptx::tma_load_2d(sa, &p.tmA, bar, k0, ti.m0);
-    ptx::tma_load_2d(sb, &p.tmB0, bar, k0, ti.e * p.I + ti.n0);
-    ptx::tma_load_2d(sb + (BN / 2) * 128, &p.tmB1, bar, k0, ti.e * p.I + ti.n0);
+    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
+    if (CTAS == 1) {
+      tma<CTAS>(sb, &p.tmB0, bar, k0, ti.e * p.I + ti.n0);
+      tma<CTAS>(sb + (BN / 2) * 128, &p.tmB1, bar, k0, ti.e * p.I + ti.n0);
+    } else {  // rank 0 stages the gate rows, rank 1 the up rows of the N tile
+      tma<CTAS>(sb, rank == 0 ? &p.tmB0 : &p.tmB1, bar, k0, ti.e * p.I + ti.n0);
+    }
   } else if constexpr (KIND == GEMM_DOWN) {
-    ptx::tma_load_2d(sa, &p.tmA, bar, k0, ti.m0);
-    ptx::tma_load_2d(sb, &p.tmB0, bar, k0, ti.e * p.H + ti.n0);
+    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
+    tma<CTAS>(sb, &p.tmB0, bar, k0, ti.e * p.H + nb);
   } else if constexpr (KIND == GEMM_DGRAD_DOWN) {
-    ptx::tma_load_2d(sa, &p.tmA, bar, k0, ti.m0);
+    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
 #pragma unroll
-    for (int c = 0; c < BN / 64; ++c)
-      ptx::tma_load_2d(sb + c * 8192, &p.tmB0, bar, ti.n0 + c * 64, ti.e * p.H + k0);
+    for (int c = 0; c < C::B_ROWS / 64; ++c)
+      tma<CTAS>(sb + c * 8192, &p.tmB0, bar, nb + c * 64, ti.e * p.H + k0);
   } else if constexpr (KIND == GEMM_DGRAD_GATEUP) {
-    ptx::tma_load_2d(sa, &p.tmA, bar, k0, ti.m0);
+    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
     const bool gate = k0 < p.I;
     const CUtensorMap* m = gate ? &p.tmB0 : &p.tmB1;
     const int krow = ti.e * p.I + (gate ? k0 : k0 - p.I);
 #pragma unroll
-    for (int c = 0; c < BN / 64; ++c) ptx::tma_load_2d(sb + c * 8192, m, bar, ti.n0 + c * 64, krow);
+    for (int c = 0; c < C::B_ROWS / 64; ++c) tma<CTAS>(sb + c * 8192, m, bar, nb + c * 64, krow);
   } else {  // per-expert weight gradients: both operands M/N-major, K = routed rows
     const int krow = ti.k_row0 + k0;
 #pragma unroll
-    for (int c = 0; c < BM / 64; ++c)
-      ptx::tma_load_2d(sa + c * 8192, &p.tmA, bar, ti.m0 + c * 64, krow);
+    for (int c = 0; c < BM / 64; ++c) tma<CTAS>(sa + c * 8192, &p.tmA, bar, ti.m0 + c * 64, krow);
 #pragma unroll
-    for (int c = 0; c < BN / 64; ++c)
-      ptx::tma_load_2d(sb + c * 8192, &p.tmB0, bar, ti.n0 + c * 64, krow);
+    for (int c = 0; c < C::B_ROWS / 64; ++c)
+      tma<CTAS>(sb + c * 8192, &p.tmB0, bar, nb + c * 64, krow);
   }
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int KIND, int BN>
+template <int KIND, int BN, int CTAS>
 __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using C = Cfg<KIND, BN>;
+  using C = Cfg<KIND, BN, CTAS>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES];
   __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t epi_ld_bar[4];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = CTAS == 1 ? 0 : static_cast<int>(ptx::cluster_rank());
+  const int cluster = blockIdx.x / CTAS, n_clusters = gridDim.x / CTAS;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
@@ -353,9 +467,10 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull_bar[a], 1);
-      ptx::mbar_init(&tempty_bar[a], 4);
+      ptx::mbar_init(&tempty_bar[a], 4 * CTAS);
     }
     ptx::mbar_init(&drain_bar, 1);
+    for (int q = 0; q < 4; ++q) ptx::mbar_init(&epi_ld_bar[q], 1);
     s_abort = 0;
     ptx::fence_barrier_init();
   }
@@ -365,15 +480,18 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     if (KIND == GEMM_GATEUP || KIND == GEMM_DGRAD_GATEUP) ptx::prefetch_tmap(&p.tmB1);
   }
   if (warp == 2) {
-    ptx::tmem_alloc(&s_tmem_base, C::TMEM_COLS);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc<CTAS>(&s_tmem_base, C::TMEM_COLS);
+    ptx::tmem_relinquish<CTAS>();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (CTAS == 2) ptx::cluster_sync(); else __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   volatile int* abort = &s_abort;
-  const int total = total_tiles<KIND, BN>(p);
+  const int total = total_tiles<KIND, BN, CTAS>(p);
+  // the pair's barriers that both CTAs signal live in the rank-0 CTA
+  const uint32_t lead_full0 = CTAS == 1 ? ptx::smem_u32(&full_bar[0])
+                                        : ptx::map_to_rank(ptx::smem_u32(&full_bar[0]), 0);
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- producer
@@ -383,8 +501,8 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
 #pragma unroll
     for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileInfo ti = decode_tile<KIND, BN>(p, t);
+    for (int t = cluster; t < total && ok; t += n_clusters) {
+      const TileInfo ti = decode_tile<KIND, BN, CTAS>(p, t, rank);
       for (int kb = 0; kb < ti.k_iters; ++kb) {
         if (!ptx::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, WAIT_LIMIT_NS)) {
           record_timeout(p, abort, KIND * 16 + 1);
@@ -392,8 +510,9 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
           break;
         }
         uint8_t* sa = smem + stage * C::STAGE_BYTES;
-        ptx::mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
-        issue_loads<KIND, BN>(p, ti, kb, sa, sa + C::A_BYTES, &full_bar[stage]);
+        if (rank == 0) ptx::mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES * CTAS);
+        issue_loads<KIND, BN, CTAS>(p, ti, kb, sa, sa + C::A_BYTES, lead_full0 + stage * 8u,
+                                    rank);
         last_parity[stage] = static_cast<int>(phase);
         if (++stage == C::STAGES) {
           stage = 0;
@@ -401,15 +520,16 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
         }
       }
     }
-    // drain: every issued copy has landed before the CTA may exit
+    // drain: every issued copy has landed before the CTA may exit (rank 0: its full
+    // barriers; rank 1: consumption of its stages, which implies they landed)
     for (int s = 0; s < C::STAGES; ++s) {
       if (last_parity[s] < 0) continue;
       int dummy = 0;
-      if (!ptx::mbar_wait(&full_bar[s], static_cast<uint32_t>(last_parity[s]), &dummy,
-                          WAIT_LIMIT_NS))
+      uint64_t* bar = rank == 0 ? &full_bar[s] : &empty_bar[s];
+      if (!ptx::mbar_wait(bar, static_cast<uint32_t>(last_parity[s]), &dummy, WAIT_LIMIT_NS))
         record_timeout(p, abort, KIND * 16 + 2);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------------------------------------------------------- MMA issuer
     int stage = 0;
     uint32_t phase = 0;
@@ -417,8 +537,8 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     uint32_t acc_phase = 0;
     bool ok = true;
     bool issued = false;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const TileInfo ti = decode_tile<KIND, BN>(p, t);
+    for (int t = cluster; t < total && ok; t += n_clusters) {
+      const TileInfo ti = decode_tile<KIND, BN, CTAS>(p, t, rank);
       if (ti.k_iters == 0) continue;
       if (!ptx::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort, WAIT_LIMIT_NS)) {
         record_timeout(p, abort, KIND * 16 + 3);
@@ -441,23 +561,24 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
                                          : ptx::smem_desc_sw128(a_base + kk * 32, 16, 1024);
           const uint64_t bdesc = C::B_MN ? ptx::smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
                                          : ptx::smem_desc_sw128(b_base + kk * 32, 16, 1024);
-          ptx::umma_bf16(d_tmem, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+          ptx::umma_bf16<CTAS>(d_tmem, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
         }
         issued = true;
-        ptx::umma_commit(&empty_bar[stage]);
+        ptx::umma_commit<CTAS>(&empty_bar[stage]);
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      ptx::umma_commit(&tfull_bar[acc]);
+      ptx::umma_commit<CTAS>(&tfull_bar[acc]);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
     if (issued) {
-      // drain: every issued MMA has completed before TMEM is released
-      ptx::umma_commit(&drain_bar);
+      // drain: every issued MMA has completed before TMEM or the pair's shared memory
+      // is released
+      ptx::umma_commit<CTAS>(&drain_bar, 0x1);
       int dummy = 0;
       if (!ptx::mbar_wait(&drain_bar, 0, &dummy, WAIT_LIMIT_NS))
         record_timeout(p, abort, KIND * 16 + 5);
@@ -465,15 +586,29 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp - 4;
-    const int row = q * 32 + lane;
+    EpiWarp w;
+    w.in = smem + C::STAGES * C::STAGE_BYTES + q * C::EPI_WARP_BYTES;
+    w.out = w.in + C::EPI_IN * 2048;
+    w.ld_bar = &epi_ld_bar[q];
+    w.ld_phase = 0;
+    w.ld_pending = false;
+    w.ob = 0;
+    w.lane = lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const TileInfo ti = decode_tile<KIND, BN>(p, t);
+    const uint32_t lead_tempty0 =
+        CTAS == 1 ? ptx::smem_u32(&tempty_bar[0])
+                  : ptx::map_to_rank(ptx::smem_u32(&tempty_bar[0]), 0);
+    for (int t = cluster; t < total; t += n_clusters) {
+      const TileInfo ti = decode_tile<KIND, BN, CTAS>(p, t, rank);
       if (ti.k_iters == 0) {
-        if constexpr (C::PER_EXPERT) zero_tile<KIND, BN>(p, ti, row);
+        if constexpr (C::PER_EXPERT) zero_tile<KIND, BN, CTAS>(p, ti, q, w);
         continue;
       }
+      TileInfo nx;
+      const bool has_next = t + n_clusters < total;
+      if (has_next) nx = decode_tile<KIND, BN, CTAS>(p, t + n_clusters, rank);
+      if (KIND == GEMM_DGRAD_DOWN && !w.ld_pending) load_inputs(w, p, ti.m0 + q * 32, ti.n0);
       int ok = 1;
       if (lane == 0) ok = ptx::mbar_wait(&tfull_bar[acc], acc_phase, abort, WAIT_LIMIT_NS) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -485,19 +620,33 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
       __syncwarp();
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(q * 32) << 16);
-      epilogue_tile<KIND, BN>(p, ti, row, tbase);
+      if (!epilogue_tile<KIND, BN, CTAS>(p, ti, has_next ? &nx : nullptr, q, tbase, w, abort)) {
+        if (lane == 0) record_timeout(p, abort, KIND * 16 + 7);
+        break;
+      }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&tempty_bar[acc]);
+      if (lane == 0) {
+        if constexpr (CTAS == 1) ptx::mbar_arrive(&tempty_bar[acc]);
+        else ptx::mbar_arrive_cluster(lead_tempty0 + acc * 8u);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    // drain: outstanding input loads and output stores complete before the CTA exits
+    if (w.ld_pending && lane == 0) {
+      int dummy = 0;
+      if (!ptx::mbar_wait(w.ld_bar, w.ld_phase, &dummy, WAIT_LIMIT_NS))
+        record_timeout(p, abort, KIND * 16 + 8);
+    }
+    if (lane == 0) ptx::bulk_wait_all();
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (CTAS == 2) ptx::cluster_sync(); else __syncthreads();
   ptx::tc_fence_after();
-  if (warp == 2) ptx::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  if (warp == 2) ptx::tmem_dealloc<CTAS>(tmem_base, C::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------ host side
@@ -516,9 +665,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Row-major bf16 matrix [outer, inner] -> 2-D tensor map with a box of
-// box_inner x box_outer elements and the 128-byte swizzle.
+// box_inner x box_outer elements and the given shared-memory swizzle.
 static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                     uint32_t box_inner, uint32_t box_outer) {
+                     uint32_t box_inner, uint32_t box_outer,
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -526,9 +676,14 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// 32 x 32 epilogue blocks (64-byte rows, 64-byte swizzle).
+static bool make_epi_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
+  return make_map(m, base, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int pick_bn(int64_t n) {
@@ -537,17 +692,43 @@ int pick_bn(int64_t n) {
   return 64;
 }
 
-template <int KIND, int BN>
-static cudaError_t run(const Ctx& c, const GemmParams& p, int grid) {
-  using C = Cfg<KIND, BN>;
-  cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<KIND, BN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+template <int KIND, int BN, int CTAS>
+static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) {
+  using C = Cfg<KIND, BN, CTAS>;
+  auto kern = moe_gemm_kernel<KIND, BN, CTAS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = c.stream;
+  int64_t clusters = c.num_sms / CTAS;
+  if constexpr (CTAS == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int active = 0;  // clusters resident at once (the same for every launch)
+    if (active == 0) {
+      cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) active = n;
+      else active = static_cast<int>(clusters);
+    }
+    clusters = active;
+  }
+  clusters = std::max<int64_t>(1, std::min<int64_t>(clusters, max_clusters));
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CTAS), 1, 1);
   static constexpr int kId[6] = {K_GEMM_GATEUP, K_GEMM_DOWN, K_GEMM_DGRAD_DOWN,
                                  K_GEMM_DGRAD_GATEUP, K_GEMM_WGRAD_DOWN, K_GEMM_WGRAD_GATEUP};
   prof_begin(c, kId[KIND]);
-  moe_gemm_kernel<KIND, BN><<<grid, 256, C::SMEM_BYTES, c.stream>>>(p);
+  e = cudaLaunchKernelEx(&cfg, kern, p);
   prof_end(c, kId[KIND]);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -555,6 +736,7 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   GemmParams p;
   memset(&p, 0, sizeof(p));
   const char* saved = g.saved;
+  const int ctas = L.pad == 2 * BM ? 2 : 1;
   p.H = static_cast<int>(L.H);
   p.I = static_cast<int>(L.I);
   p.E = static_cast<int>(L.E);
@@ -570,35 +752,36 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   p.out0 = g.out0;
   p.out1 = g.out1;
   p.outf = g.outf;
-  p.aux = g.aux;
-  p.aux2 = g.aux2;
   p.status = reinterpret_cast<DevStatus*>(g.scratch + L.status);
   const uint64_t Rp = static_cast<uint64_t>(L.Rp), H = L.H, I = L.I, E = L.E;
   bool ok = true;
   int bn = 0;
-  int64_t max_total = 0;
+  int64_t max_units = 0;  // tiles (of both CTAs of a pair) that exist at most
   switch (g.kind) {
     case GEMM_GATEUP:
       bn = (L.I % 128 == 0) ? 256 : 128;
       ok = make_map(&p.tmA, g.A, H, Rp, 64, BM) && make_map(&p.tmB0, g.B0, H, E * I, 64, bn / 2) &&
-           make_map(&p.tmB1, g.B1, H, E * I, 64, bn / 2);
+           make_map(&p.tmB1, g.B1, H, E * I, 64, bn / 2) &&
+           make_epi_map(&p.tmC0, g.out0, 2 * I, Rp) && make_epi_map(&p.tmC1, g.out1, I, Rp);
       p.n_tiles = static_cast<int>(L.I / (bn / 2));
       p.k_iters = static_cast<int>(L.H / BK);
-      max_total = L.NT * p.n_tiles;
+      max_units = L.NT / ctas * p.n_tiles;
       break;
     case GEMM_DOWN:
       bn = pick_bn(L.H);
-      ok = make_map(&p.tmA, g.A, I, Rp, 64, BM) && make_map(&p.tmB0, g.B0, I, E * H, 64, bn);
+      ok = make_map(&p.tmA, g.A, I, Rp, 64, BM) && make_map(&p.tmB0, g.B0, I, E * H, 64, bn / ctas);
       p.n_tiles = static_cast<int>(L.H / bn);
       p.k_iters = static_cast<int>(L.I / BK);
-      max_total = L.NT * p.n_tiles;
+      max_units = L.NT / ctas * p.n_tiles;
       break;
     case GEMM_DGRAD_DOWN:
       bn = pick_bn(L.I);
-      ok = make_map(&p.tmA, g.A, H, Rp, 64, BM) && make_map(&p.tmB0, g.B0, I, E * H, 64, 64);
+      ok = make_map(&p.tmA, g.A, H, Rp, 64, BM) && make_map(&p.tmB0, g.B0, I, E * H, 64, 64) &&
+           make_epi_map(&p.tmC0, g.out0, 2 * I, Rp) && make_epi_map(&p.tmC1, g.out1, I, Rp) &&
+           make_epi_map(&p.tmD0, g.aux, 2 * I, Rp) && make_epi_map(&p.tmD1, g.aux2, I, Rp);
       p.n_tiles = static_cast<int>(L.I / bn);
       p.k_iters = static_cast<int>(L.H / BK);
-      max_total = L.NT * p.n_tiles;
+      max_units = L.NT / ctas * p.n_tiles;
       break;
     case GEMM_DGRAD_GATEUP:
       bn = pick_bn(L.H);
@@ -606,43 +789,52 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
            make_map(&p.tmB1, g.B1, H, E * I, 64, 64);
       p.n_tiles = static_cast<int>(L.H / bn);
       p.k_iters = static_cast<int>(2 * L.I / BK);
-      max_total = L.NT * p.n_tiles;
+      max_units = L.NT / ctas * p.n_tiles;
       break;
     case GEMM_WGRAD_DOWN:
       bn = pick_bn(L.I);
-      ok = make_map(&p.tmA, g.A, H, Rp, 64, 64) && make_map(&p.tmB0, g.B0, I, Rp, 64, 64);
-      p.m_tiles = static_cast<int>(L.H / BM);
+      ok = make_map(&p.tmA, g.A, H, Rp, 64, 64) && make_map(&p.tmB0, g.B0, I, Rp, 64, 64) &&
+           make_epi_map(&p.tmC0, g.out0, I, E * H);
+      p.m_tiles = static_cast<int>(L.H / (BM * ctas));
       p.n_tiles = static_cast<int>(L.I / bn);
-      max_total = L.E * p.m_tiles * p.n_tiles;
+      max_units = L.E * p.m_tiles * p.n_tiles;
       break;
     case GEMM_WGRAD_GATEUP:
       bn = pick_bn(L.H);
-      ok = make_map(&p.tmA, g.A, 2 * I, Rp, 64, 64) && make_map(&p.tmB0, g.B0, H, Rp, 64, 64);
-      p.m_tiles = static_cast<int>(2 * L.I / BM);
+      ok = make_map(&p.tmA, g.A, 2 * I, Rp, 64, 64) && make_map(&p.tmB0, g.B0, H, Rp, 64, 64) &&
+           make_epi_map(&p.tmC0, g.out0, H, E * I) && make_epi_map(&p.tmC1, g.out1, H, E * I);
+      p.m_tiles = static_cast<int>(2 * L.I / (BM * ctas));
       p.n_tiles = static_cast<int>(L.H / bn);
-      max_total = L.E * p.m_tiles * p.n_tiles;
+      max_units = L.E * p.m_tiles * p.n_tiles;
       break;
     default:
       return cudaErrorInvalidValue;
   }
   if (!ok) return cudaErrorInvalidValue;
-  const int grid = static_cast<int>(std::min<int64_t>(c.num_sms, std::max<int64_t>(max_total, 1)));
-#define MMMOE_RUN(K, B) \
-  if (g.kind == K && bn == B) return run<K, B>(c, p, grid);
-  MMMOE_RUN(GEMM_GATEUP, 256)
-  MMMOE_RUN(GEMM_GATEUP, 128)
-  MMMOE_RUN(GEMM_DOWN, 256)
-  MMMOE_RUN(GEMM_DOWN, 128)
-  MMMOE_RUN(GEMM_DGRAD_DOWN, 256)
-  MMMOE_RUN(GEMM_DGRAD_DOWN, 128)
-  MMMOE_RUN(GEMM_DGRAD_DOWN, 64)
-  MMMOE_RUN(GEMM_DGRAD_GATEUP, 256)
-  MMMOE_RUN(GEMM_DGRAD_GATEUP, 128)
-  MMMOE_RUN(GEMM_WGRAD_DOWN, 256)
-  MMMOE_RUN(GEMM_WGRAD_DOWN, 128)
-  MMMOE_RUN(GEMM_WGRAD_DOWN, 64)
-  MMMOE_RUN(GEMM_WGRAD_GATEUP, 256)
-  MMMOE_RUN(GEMM_WGRAD_GATEUP, 128)
+#define MMMOE_RUN(K, B, N) \
+  if (g.kind == K && bn == B && ctas == N) return run<K, B, N>(c, p, max_units);
+  MMMOE_RUN(GEMM_GATEUP, 256, 2)
+  MMMOE_RUN(GEMM_DOWN, 256, 2)
+  MMMOE_RUN(GEMM_DGRAD_DOWN, 256, 2)
+  MMMOE_RUN(GEMM_DGRAD_DOWN, 128, 2)
+  MMMOE_RUN(GEMM_DGRAD_GATEUP, 256, 2)
+  MMMOE_RUN(GEMM_WGRAD_DOWN, 256, 2)
+  MMMOE_RUN(GEMM_WGRAD_DOWN, 128, 2)
+  MMMOE_RUN(GEMM_WGRAD_GATEUP, 256, 2)
+  MMMOE_RUN(GEMM_GATEUP, 256, 1)
+  MMMOE_RUN(GEMM_GATEUP, 128, 1)
+  MMMOE_RUN(GEMM_DOWN, 256, 1)
+  MMMOE_RUN(GEMM_DOWN, 128, 1)
+  MMMOE_RUN(GEMM_DGRAD_DOWN, 256, 1)
+  MMMOE_RUN(GEMM_DGRAD_DOWN, 128, 1)
+  MMMOE_RUN(GEMM_DGRAD_DOWN, 64, 1)
+  MMMOE_RUN(GEMM_DGRAD_GATEUP, 256, 1)
+  MMMOE_RUN(GEMM_DGRAD_GATEUP, 128, 1)
+  MMMOE_RUN(GEMM_WGRAD_DOWN, 256, 1)
+  MMMOE_RUN(GEMM_WGRAD_DOWN, 128, 1)
+  MMMOE_RUN(GEMM_WGRAD_DOWN, 64, 1)
+  MMMOE_RUN(GEMM_WGRAD_GATEUP, 256, 1)
+  MMMOE_RUN(GEMM_WGRAD_GATEUP, 128, 1)
 #undef MMMOE_RUN
   return cudaErrorInvalidValue;
 }

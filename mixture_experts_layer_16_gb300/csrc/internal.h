@@ -23,12 +23,14 @@ struct DevStatus {
 
 // Byte offsets of every region inside `saved` and `scratch`.  Every region starts
 // on a 1024-byte boundary.  "Padded rows": each expert's routed rows start on a
-// multiple of BM and its tail up to the next multiple is zero, so that M tiles
-// never straddle two experts and the token-axis K loop of the weight-gradient
-// GEMMs reads zeros past an expert's last row.
+// multiple of `pad` and its tail up to the next multiple is zero, so that M tiles
+// (of one SM or of an SM pair) never straddle two experts and the token-axis K loop
+// of the weight-gradient GEMMs reads zeros past an expert's last row.
 struct Layout {
   int64_t T, H, I, E, k, R;
-  int64_t Rp;      // capacity of the padded row space: (ceil(R/BM) + E) * BM
+  int64_t pad;     // each expert's rows are padded to a multiple of this: BM, or 2*BM
+                   // when the GEMMs run on SM pairs
+  int64_t Rp;      // capacity of the padded row space: (ceil(R/pad) + E) * pad
   int64_t NT;      // capacity in M tiles: Rp / BM
   int64_t nblk;    // routing blocks: ceil(R / ROUTE_CHUNK)
   int64_t n_pw;    // partial dot products per row for dtopk_w (I / BN of the dgrad-down GEMM)
@@ -43,6 +45,10 @@ struct Layout {
 constexpr int META_NUM_TILES = 0;
 
 mm_moe_status make_layout(const mm_moe_shape* s, Layout* L);
+
+// Whether shapes that allow it run their GEMMs on SM pairs (environment variable
+// MM_MOE_SM_PAIRS=0 selects single-SM tiles everywhere; default on).
+bool sm_pairs_enabled();
 
 // Width of the N tile each GEMM uses for an output dimension of n columns.
 int pick_bn(int64_t n);
@@ -96,7 +102,7 @@ struct RouteBufs {
   int* rowflat;       // [Rp]
   float* w_row;       // [Rp]
 };
-cudaError_t launch_route_to(const Ctx& c, int R, int E, const int32_t* topk_idx,
+cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* topk_idx,
                             const float* topk_w, const RouteBufs& b);
 cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
                            const char* saved, float* w_row_out, int kernel_id);

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
@@ -10,6 +11,14 @@
 namespace mmmoe {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool sm_pairs_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("MM_MOE_SM_PAIRS");
+    return !(v != nullptr && v[0] == '0');
+  }();
+  return on;
+}
 
 mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   if (s == nullptr || L == nullptr) return MM_MOE_EINVAL;
@@ -25,8 +34,10 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->E = s->E;
   L->k = s->k;
   L->R = s->T * s->k;
-  L->NT = (L->R + BM - 1) / BM + L->E;
-  L->Rp = L->NT * BM;
+  // SM-pair GEMM tiles (M = 256, N = 256) need H % 256 == 0 and I % 128 == 0
+  L->pad = (s->H % 256 == 0 && s->I % 128 == 0 && sm_pairs_enabled()) ? 2 * BM : BM;
+  L->Rp = ((L->R + L->pad - 1) / L->pad + L->E) * L->pad;
+  L->NT = L->Rp / BM;
   if (L->Rp >= (int64_t{1} << 31)) return MM_MOE_EINVAL;
   L->nblk = (L->R + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
   L->n_pw = L->I / pick_bn(L->I);

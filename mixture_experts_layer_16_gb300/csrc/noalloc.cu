@@ -109,6 +109,6 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_route_noalloc(const mm_moe_shape* sha
   // the status word keeps the previous call's value: start from zero
   if (cudaMemsetAsync(b.status, 0, sizeof(DevStatus), c.stream) != cudaSuccess)
     return MM_MOE_ECUDA;
-  if (launch_route_to(c, R, E, topk_idx, topk_w, b) != cudaSuccess) return MM_MOE_ECUDA;
+  if (launch_route_to(c, R, E, BM, topk_idx, topk_w, b) != cudaSuccess) return MM_MOE_ECUDA;
   return MM_MOE_OK;
 }

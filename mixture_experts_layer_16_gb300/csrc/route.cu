@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_count_kernel(
 // counts, offsets (exclusive scan), padded offsets, per-block exclusive prefixes
 // (in place in blk_counts), the M-tile list and the experts ordered by row count.
 __global__ void __launch_bounds__(1024) route_scan_kernel(
-    int* __restrict__ blk_counts, int nblk, int E, int* __restrict__ counts,
+    int* __restrict__ blk_counts, int nblk, int E, int pad, int* __restrict__ counts,
     int* __restrict__ offsets, int* __restrict__ pad_off, int* __restrict__ expert_order,
     int* __restrict__ tile_expert, int* __restrict__ tile_rows, int* __restrict__ meta) {
   __shared__ int s_cnt[MAX_E];
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
       cnt += c;
     }
   }
-  const int padded = (cnt + BM - 1) / BM * BM;
+  const int padded = (cnt + pad - 1) / pad * pad;
   if (e < MAX_E) {
     s_cnt[e] = (e < E) ? cnt : 0;
     s_a[e] = (e < E) ? cnt : 0;
@@ -193,7 +193,7 @@ cudaError_t launch_route(const Ctx& c, const Layout& L, const int32_t* topk_idx,
   prof_end(c, K_ROUTE_COUNT);
   prof_begin(c, K_ROUTE_SCAN);
   route_scan_kernel<<<1, 1024, 0, c.stream>>>(
-      blk, nblk, E, reinterpret_cast<int*>(saved + L.counts),
+      blk, nblk, E, static_cast<int>(L.pad), reinterpret_cast<int*>(saved + L.counts),
       reinterpret_cast<int*>(saved + L.offsets), reinterpret_cast<int*>(saved + L.pad_off),
       reinterpret_cast<int*>(saved + L.expert_order), reinterpret_cast<int*>(saved + L.tile_expert),
       reinterpret_cast<int*>(saved + L.tile_rows), reinterpret_cast<int*>(saved + L.meta));
@@ -209,7 +209,7 @@ cudaError_t launch_route(const Ctx& c, const Layout& L, const int32_t* topk_idx,
 }
 
 // The same three routing kernels with every buffer given explicitly.
-cudaError_t launch_route_to(const Ctx& c, int R, int E, const int32_t* topk_idx,
+cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* topk_idx,
                             const float* topk_w, const RouteBufs& b) {
   const int nblk = (R + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
   prof_begin(c, K_ROUTE_COUNT);
@@ -217,7 +217,7 @@ cudaError_t launch_route_to(const Ctx& c, int R, int E, const int32_t* topk_idx,
                                                            b.status);
   prof_end(c, K_ROUTE_COUNT);
   prof_begin(c, K_ROUTE_SCAN);
-  route_scan_kernel<<<1, 1024, 0, c.stream>>>(b.blk_counts, nblk, E, b.counts, b.offsets,
+  route_scan_kernel<<<1, 1024, 0, c.stream>>>(b.blk_counts, nblk, E, pad, b.counts, b.offsets,
                                               b.pad_off, b.expert_order, b.tile_expert,
                                               b.tile_rows, b.meta);
   prof_end(c, K_ROUTE_SCAN);
