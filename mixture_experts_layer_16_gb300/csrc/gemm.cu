@@ -6,9 +6,9 @@
 // layers with SwiGLU between them and the combine in the forward, and the
 // matching backward.  Six variants share the main loop:
 //   GATEUP       [g|u] = x_perm . [W_gate;W_up]^T  per expert M block, SwiGLU epilogue
-//   DOWN         o = a . W_down^T                   epilogue w*o -> token-major slot
+//   DOWN         o = a . W_down^T                   epilogue w*o (expert-grouped rows)
 //   DGRAD_DOWN   g' = dy_perm . W_down               dSwiGLU epilogue (dh, w*a, <a,g'>)
-//   DGRAD_GATEUP dx = dh . [W_gate;W_up]             epilogue -> token-major slot
+//   DGRAD_GATEUP dx = dh . [W_gate;W_up]             epilogue dx (expert-grouped rows)
 //   WGRAD_DOWN   dW_down[e] = dy_perm^T . (w*a)      K = the expert's rows
 //   WGRAD_GATEUP [dW_gate;dW_up][e] = dh^T . x_perm   K = the expert's rows
 //
@@ -20,8 +20,7 @@
 // pair's rank-0 CTA = MMA issuer, warp 2 = TMEM allocator, warps 4..7 = epilogue
 // (warp 4+q reads TMEM lanes 32q..32q+31, i.e. the CTA's tile rows 32q..32q+31).
 // The epilogue moves data through per-warp 32 x 32 blocks in shared memory: outputs
-// leave by TMA stores (or coalesced 16-byte stores for the scattered slot rows), and
-// the dSwiGLU inputs arrive by TMA loads.  Every wait is bounded: on expiry the
+// leave by TMA stores and the dSwiGLU inputs arrive by TMA loads.  Every wait is bounded: on expiry the
 // kernel records MM_MOE_ETIMEOUT in the status word and every role unwinds.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -79,11 +78,9 @@ struct Cfg {
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // epilogue staging per epilogue warp, in 2 KB blocks (32 rows x 32 bf16): TMA-loaded
-  // inputs (dSwiGLU: g, u, a) and a ring of output blocks (one block for the
-  // scattered slot rows, which the warp stores itself)
-  static constexpr bool SCATTER = KIND == GEMM_DOWN || KIND == GEMM_DGRAD_GATEUP;
+  // inputs (dSwiGLU: g, u, a) and a ring of output blocks for TMA stores
   static constexpr int EPI_IN = KIND == GEMM_DGRAD_DOWN ? 3 : 0;
-  static constexpr int EPI_OUT = SCATTER ? 1 : 4;
+  static constexpr int EPI_OUT = 4;
   static constexpr int EPI_WARP_BYTES = (EPI_IN + EPI_OUT) * 2048;
   static constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
   static constexpr int SMEM_CAP = 232448 - 1024;  // opt-in limit minus static shared memory
@@ -222,23 +219,6 @@ __device__ __forceinline__ void store_block(EpiWarp& w, const CUtensorMap* m, in
   w.ob = (w.ob + 1 == NB) ? 0 : w.ob + 1;
 }
 
-// Store this warp's 32 x 32 block to 32 scattered rows: row r goes to
-// out + dst_row(r) * ld + col (dst_row < 0: skipped), 4 lanes x 16 bytes per row.
-__device__ __forceinline__ void scatter_block(EpiWarp& w, uint16_t* out, int64_t ld, int dst_row,
-                                              int col, const float (&v)[32]) {
-  uint8_t* buf = w.out;
-  stage32(buf, w.lane, v);
-  __syncwarp();
-#pragma unroll
-  for (int step = 0; step < 4; ++step) {
-    const int r = step * 8 + (w.lane >> 2), j = w.lane & 3;
-    const uint4 val = *reinterpret_cast<const uint4*>(swz(buf, r, j));
-    const int fr = __shfl_sync(0xffffffffu, dst_row, r);
-    if (fr >= 0) *reinterpret_cast<uint4*>(out + static_cast<int64_t>(fr) * ld + col + j * 8) = val;
-  }
-  __syncwarp();
-}
-
 // dSwiGLU inputs of one 32-column chunk: g, u (from h) and a, rows row0..row0+31.
 __device__ __forceinline__ void load_inputs(EpiWarp& w, const GemmParams& p, int row0, int col) {
   if (w.lane == 0) {
@@ -290,10 +270,9 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInf
       store_block<C::EPI_OUT>(w, &p.tmC1, ti.n0 + c, row0, a);
     }
   } else if constexpr (KIND == GEMM_DOWN || KIND == GEMM_DGRAD_GATEUP) {
-    const int pr = ti.m0 + row;
-    const bool valid = row < __ldg(p.tile_rows + ti.mb);
-    const int f = valid ? __ldg(p.rowflat + pr) : -1;
-    const float wgt = (KIND == GEMM_DOWN && valid) ? __ldg(p.w_row + pr) : 1.0f;
+    // rows stay in expert-grouped order; padding rows carry weight 0 (DOWN) or zero
+    // inputs (DGRAD_GATEUP) and are never read back
+    const float wgt = KIND == GEMM_DOWN ? __ldg(p.w_row + ti.m0 + row) : 1.0f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t r[32];
@@ -305,7 +284,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInf
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= wgt;
       }
-      scatter_block(w, p.out0, p.H, f, ti.n0 + c, v);
+      store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, v);
     }
   } else if constexpr (KIND == GEMM_DGRAD_DOWN) {
     const int64_t pr = ti.m0 + row;
@@ -769,7 +748,8 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
       break;
     case GEMM_DOWN:
       bn = pick_bn(L.H);
-      ok = make_map(&p.tmA, g.A, I, Rp, 64, BM) && make_map(&p.tmB0, g.B0, I, E * H, 64, bn / ctas);
+      ok = make_map(&p.tmA, g.A, I, Rp, 64, BM) && make_map(&p.tmB0, g.B0, I, E * H, 64, bn / ctas) &&
+           make_epi_map(&p.tmC0, g.out0, H, Rp);
       p.n_tiles = static_cast<int>(L.H / bn);
       p.k_iters = static_cast<int>(L.I / BK);
       max_units = L.NT / ctas * p.n_tiles;
@@ -786,7 +766,7 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
     case GEMM_DGRAD_GATEUP:
       bn = pick_bn(L.H);
       ok = make_map(&p.tmA, g.A, 2 * I, Rp, 64, BM) && make_map(&p.tmB0, g.B0, H, E * I, 64, 64) &&
-           make_map(&p.tmB1, g.B1, H, E * I, 64, 64);
+           make_map(&p.tmB1, g.B1, H, E * I, 64, 64) && make_epi_map(&p.tmC0, g.out0, H, Rp);
       p.n_tiles = static_cast<int>(L.H / bn);
       p.k_iters = static_cast<int>(2 * L.I / BK);
       max_units = L.NT / ctas * p.n_tiles;

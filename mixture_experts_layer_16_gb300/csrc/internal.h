@@ -113,9 +113,9 @@ cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slot
 
 enum GemmKind {
   GEMM_GATEUP = 0,        // x_perm . [W_gate|W_up]^T  -> SwiGLU epilogue (h, a)
-  GEMM_DOWN = 1,          // a . W_down^T              -> w * o into token-major slots
+  GEMM_DOWN = 1,          // a . W_down^T              -> w * o, expert-grouped rows
   GEMM_DGRAD_DOWN = 2,    // dy_perm . W_down          -> dSwiGLU epilogue (dh, a_w, pw)
-  GEMM_DGRAD_GATEUP = 3,  // dh . [W_gate;W_up]        -> dx rows into token-major slots
+  GEMM_DGRAD_GATEUP = 3,  // dh . [W_gate;W_up]        -> dx, expert-grouped rows
   GEMM_WGRAD_DOWN = 4,    // dy_perm^T . a_w per expert -> dW_down
   GEMM_WGRAD_GATEUP = 5,  // dh^T . x_perm per expert   -> dW_gate, dW_up
 };

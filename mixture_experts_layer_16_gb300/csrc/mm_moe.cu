@@ -73,14 +73,14 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->status = take(256);
   L->blk_counts = take(4 * static_cast<size_t>(L->nblk) * E);
   const size_t common = o;
-  L->ys = take(2 * R * H);
+  L->ys = take(2 * Rp * H);
   const size_t fwd_end = o;
   o = common;
   L->dy_perm = take(2 * Rp * H);
   L->dh = take(2 * Rp * 2 * I);
   L->a_w = take(2 * Rp * I);
   L->pw = take(4 * Rp * static_cast<size_t>(L->n_pw));
-  L->dxs = take(2 * R * H);
+  L->dxs = take(2 * Rp * H);
   L->scratch_bytes = o > fwd_end ? o : fwd_end;
   return MM_MOE_OK;
 }

@@ -1,6 +1,6 @@
 // route.cu -- token routing (expert histogram, prefix scan, stable placement), the
-// row permutation into the expert-grouped layout, and the fixed-order reductions
-// back to token order (forward combine, backward un-permute).
+// row permutation into the expert-grouped layout, and the fixed-order gathers and
+// sums back to token order (forward combine, backward un-permute).
 //
 // Prime Mega MoE pages, "Why is MoE training communication-bound?": before the
 // expert math the GPU sorts tokens by destination expert; results come back per
@@ -289,46 +289,38 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
   return v;
 }
 
-// out[t] = sum_j slots[t*k + j] in fp32, j ascending (one warp per token).
-// With dtopk_w: also dtopk_w[t][j] = sum_n pw[prow[t*k+j]][n], n ascending.
-// Pairs dropped by the routing (prow < 0) contribute nothing.
+// out[t] = sum_j rows[prow[t*k + j]] in fp32, j ascending (one warp per token): the
+// k expert-grouped rows of a token, each H contiguous bf16.  With dtopk_w: also
+// dtopk_w[t][j] = sum_n pw[prow[t*k+j]][n], n ascending.  Pairs dropped by the
+// routing (prow < 0) contribute nothing.
 __global__ void __launch_bounds__(256) slot_reduce_kernel(
-    const uint4* __restrict__ slots, uint4* __restrict__ out, int T, int k, int H8,
+    const uint4* __restrict__ rows, uint4* __restrict__ out, int T, int k, int H8,
     const int* __restrict__ prow, const float* __restrict__ pw, int n_pw,
     float* __restrict__ dtopk_w) {
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
-    const uint4* s = slots + static_cast<int64_t>(t) * k * H8;
+    const int64_t fb = static_cast<int64_t>(t) * k;
+    const int my_row = lane < k ? __ldg(prow + fb + lane) : -1;
     uint4* o = out + static_cast<int64_t>(t) * H8;
-    // bit j set: slot j holds a routed row (k <= 1024 is bounded by E)
-    unsigned live_lo = 0;
-    bool all_live = true;
-    for (int j = 0; j < k; ++j) {
-      const bool live = __ldg(prow + static_cast<int64_t>(t) * k + j) >= 0;
-      all_live &= live;
-      if (j < 32 && live) live_lo |= 1u << j;
-    }
-    for (int i = lane; i < H8; i += 32) {
+    for (int i0 = 0; i0 < H8; i0 += 32) {
+      const int i = i0 + lane;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int j = 0; j < k; ++j) {
-        if (!all_live && (j >= 32 ? __ldg(prow + static_cast<int64_t>(t) * k + j) < 0
-                                  : !((live_lo >> j) & 1u)))
-          continue;
-        acc_bf16x8(acc, __ldg(s + static_cast<int64_t>(j) * H8 + i));
+        const int r = k <= 32 ? __shfl_sync(0xffffffffu, my_row, j) : __ldg(prow + fb + j);
+        if (r >= 0 && i < H8) acc_bf16x8(acc, __ldg(rows + static_cast<int64_t>(r) * H8 + i));
       }
-      o[i] = pack_bf16x8(acc);
+      if (i < H8) o[i] = pack_bf16x8(acc);
     }
     if (dtopk_w != nullptr) {
       for (int j = lane; j < k; j += 32) {
-        const int64_t f = static_cast<int64_t>(t) * k + j;
-        const int r = __ldg(prow + f);
+        const int r = __ldg(prow + fb + j);
         float acc = 0.f;
         if (r >= 0) {
           const float* p = pw + static_cast<int64_t>(r) * n_pw;
           for (int n = 0; n < n_pw; ++n) acc += p[n];
         }
-        dtopk_w[f] = acc;
+        dtopk_w[fb + j] = acc;
       }
     }
   }
