@@ -26,7 +26,10 @@
  *   - Calls only enqueue work on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and return; none blocks the host except
  *     mm_moe_read_status.  Calls on one stream are ordered; calls that share a
- *     scratch or saved buffer on different streams race.
+ *     scratch or saved buffer on different streams race.  The backward forks part
+ *     of its work onto an internal stream of the calling host thread and joins it
+ *     back before returning, so all its work is ordered before later work on
+ *     `stream`.
  *   - Argument errors are returned before anything is enqueued.  Errors found
  *     on the device (an expert index outside [0, E), a wait that ran out of
  *     time) are written to a status word at the start of `scratch`, which every

@@ -105,7 +105,7 @@ struct RouteBufs {
 cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* topk_idx,
                             const float* topk_w, const RouteBufs& b);
 cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
-                           const char* saved, float* w_row_out, int kernel_id);
+                           const char* saved, float* w_row_out, int kernel_id, char* scratch);
 cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
                            const char* saved, uint16_t* out);
 cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slots,

@@ -119,6 +119,29 @@ static bool aligned(const void* p, uintptr_t a) {
 
 static thread_local int g_last_launches = 0;
 
+// A second stream (and a fork/join event pair) per device and host thread, so that
+// bandwidth-bound kernels can run beside independent tensor-core kernels of the same
+// call.  Created on first use; never destroyed (they live as long as the thread).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static bool side_stream(SideStream* out) {
+  static thread_local SideStream per_dev[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  SideStream& ss = per_dev[dev];
+  if (ss.s == nullptr) {
+    if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+      return false;
+  }
+  *out = ss;
+  return true;
+}
+
 }  // namespace mmmoe
 
 using namespace mmmoe;
@@ -166,7 +189,7 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   uint16_t* a = reinterpret_cast<uint16_t*>(sv + L.a);
   uint16_t* ys = reinterpret_cast<uint16_t*>(sc + L.ys);
   MM_MOE_TRY(launch_permute(c, L, x, x_perm, sv, reinterpret_cast<float*>(sv + L.w_row),
-                            K_PERMUTE_X));
+                            K_PERMUTE_X, sc));
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
@@ -220,7 +243,7 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   const uint16_t* h = reinterpret_cast<const uint16_t*>(sv + L.h);
   const uint16_t* a = reinterpret_cast<const uint16_t*>(sv + L.a);
   MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
-  MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY));
+  MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY, sc));
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
@@ -242,7 +265,15 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   g.B1 = W_up;
   g.out0 = dxs;
   MM_MOE_TRY(launch_gemm(c, L, g));
-  MM_MOE_TRY(launch_unpermute(c, L, dxs, sv, pw, dx, dtopk_w));
+  // the un-permute (bandwidth-bound) runs on the side stream beside the
+  // weight-gradient GEMMs, which read none of its inputs and write none of its outputs
+  SideStream ss;
+  if (!side_stream(&ss)) return MM_MOE_ECUDA;
+  MM_MOE_TRY(cudaEventRecord(ss.fork, c.stream));
+  MM_MOE_TRY(cudaStreamWaitEvent(ss.s, ss.fork, 0));
+  const Ctx cs{ss.s, d.sms, &launches};
+  MM_MOE_TRY(launch_unpermute(cs, L, dxs, sv, pw, dx, dtopk_w));
+  MM_MOE_TRY(cudaEventRecord(ss.join, ss.s));
   g = GemmArgs{};
   g.saved = sv;
   g.scratch = sc;
@@ -260,6 +291,7 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   g.out0 = dW_gate;
   g.out1 = dW_up;
   MM_MOE_TRY(launch_gemm(c, L, g));
+  MM_MOE_TRY(cudaStreamWaitEvent(c.stream, ss.join, 0));  // join: the call ends on `stream`
   g_last_launches = launches;
   return MM_MOE_OK;
 }

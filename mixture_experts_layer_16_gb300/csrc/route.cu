@@ -8,7 +8,10 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace mmmoe {
 
@@ -94,7 +97,7 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
     const int nt = padded / BM;
     for (int i = 0; i < nt; ++i) {
       tile_expert[poff / BM + i] = e;
-      tile_rows[poff / BM + i] = min(BM, cnt - i * BM);
+      tile_rows[poff / BM + i] = max(0, min(BM, cnt - i * BM));  // 0: all padding
     }
     // rank by descending row count, ties by expert index
     int rank = 0;
@@ -230,42 +233,99 @@ cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* 
 }
 
 // ---------------------------------------------------------------- 4. permute
-// dst[pr] = src[token of padded row pr] (16-byte vector copies, one warp per row);
-// padding rows are written as zeros.  In the forward it also zeroes the routing
-// weight of padding rows (valid rows got theirs from the placement kernel).
-__global__ void __launch_bounds__(256) permute_rows_kernel(
-    const uint4* __restrict__ src, uint4* __restrict__ dst, int H8, int k,
+// dst[prow[t*k + j]] = src[t] for every routed pair, and zero padding rows.  Tokens
+// are walked in order so that each source row is read from HBM once and stored to
+// its k destinations.  Whole rows move by TMA bulk copies: one lane per CTA drives
+// a ring of PERM_SLOTS row buffers, loading PERM_AHEAD tokens ahead of the one it
+// stores.  Padding rows are then stored from a zero row; in the forward their
+// routing weight is zeroed too (valid rows got theirs from the placement kernel).
+constexpr int PERM_SLOTS = 8;
+constexpr int PERM_AHEAD = 4;
+constexpr uint64_t PERM_WAIT_NS = 2000000000ull;
+
+__global__ void __launch_bounds__(32) permute_rows_kernel(
+    const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int row_bytes, int T, int k,
     const int* __restrict__ meta, const int* __restrict__ tile_rows,
-    const int* __restrict__ rowflat, float* __restrict__ w_row) {
-  const int n_rows = __ldg(meta + META_NUM_TILES) * BM;
-  const int lane = threadIdx.x & 31;
-  const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int pr = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pr < n_rows; pr += warps) {
-    const bool valid = (pr % BM) < __ldg(tile_rows + pr / BM);
-    uint4* d = dst + static_cast<int64_t>(pr) * H8;
-    if (valid) {
-      const int t = __ldg(rowflat + pr) / k;
-      const uint4* s = src + static_cast<int64_t>(t) * H8;
-#pragma unroll 4
-      for (int i = lane; i < H8; i += 32) d[i] = __ldg(s + i);
-    } else {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll 4
-      for (int i = lane; i < H8; i += 32) d[i] = z;
-      if (w_row != nullptr && lane == 0) w_row[pr] = 0.f;
+    const int* __restrict__ prow, float* __restrict__ w_row, DevStatus* status) {
+  extern __shared__ __align__(128) uint8_t pbuf[];  // PERM_SLOTS rows, then a zero row
+  __shared__ __align__(8) uint64_t bar[PERM_SLOTS];
+  const int lane = threadIdx.x;
+  uint8_t* zero = pbuf + PERM_SLOTS * row_bytes;
+  for (int i = lane * 16; i < row_bytes; i += 32 * 16)
+    *reinterpret_cast<uint4*>(zero + i) = make_uint4(0, 0, 0, 0);
+  ptx::fence_proxy_async_smem();  // the zero row is read by bulk stores
+  if (lane == 0) {
+    for (int s = 0; s < PERM_SLOTS; ++s) ptx::mbar_init(&bar[s], 1);
+    ptx::fence_barrier_init();
+  }
+  __syncwarp();
+  if (lane != 0) return;
+  const int first = static_cast<int>(blockIdx.x), step = static_cast<int>(gridDim.x);
+  // --- routed rows, token by token
+  const int n_my = T > first ? (T - 1 - first) / step + 1 : 0;
+  auto issue = [&](int i) {  // load my i-th token's row into slot i % PERM_SLOTS
+    const int s = i % PERM_SLOTS;
+    const int64_t t = first + static_cast<int64_t>(i) * step;
+    ptx::mbar_arrive_expect_tx(&bar[s], static_cast<uint32_t>(row_bytes));
+    ptx::bulk_load(pbuf + s * row_bytes, src + t * row_bytes, row_bytes, &bar[s]);
+  };
+  for (int i = 0; i < PERM_AHEAD && i < n_my; ++i) issue(i);
+  int dummy = 0;
+  for (int i = 0; i < n_my; ++i) {
+    if (i + PERM_AHEAD < n_my) {
+      // the slot of token i + PERM_AHEAD last held token i + PERM_AHEAD - PERM_SLOTS,
+      // whose stores (one group, PERM_SLOTS - PERM_AHEAD groups ago) must have read it
+      ptx::bulk_wait_read<PERM_SLOTS - PERM_AHEAD - 1>();
+      issue(i + PERM_AHEAD);
+    }
+    const int s = i % PERM_SLOTS;
+    if (!ptx::mbar_wait(&bar[s], static_cast<uint32_t>((i / PERM_SLOTS) & 1), &dummy,
+                        PERM_WAIT_NS)) {
+      if (atomicCAS(&status->code, 0, MM_MOE_ETIMEOUT) == 0) status->detail = -1;
+      // the loads already issued land before the CTA exits (bounded as well)
+      for (int j = i + 1; j < i + PERM_AHEAD + 1 && j < n_my; ++j)
+        ptx::mbar_wait(&bar[j % PERM_SLOTS], static_cast<uint32_t>((j / PERM_SLOTS) & 1),
+                       &dummy, PERM_WAIT_NS);
+      ptx::bulk_wait_all();
+      return;
+    }
+    const int64_t f0 = (first + static_cast<int64_t>(i) * step) * k;
+    for (int j = 0; j < k; ++j) {
+      const int pr = __ldg(prow + f0 + j);
+      if (pr >= 0)
+        ptx::bulk_store(dst + static_cast<int64_t>(pr) * row_bytes, pbuf + s * row_bytes,
+                        row_bytes);
+    }
+    ptx::bulk_commit();
+  }
+  // --- padding rows of the M tiles
+  const int n_tiles = __ldg(meta + META_NUM_TILES);
+  for (int mb = first; mb < n_tiles; mb += step) {
+    for (int r = max(0, __ldg(tile_rows + mb)); r < BM; ++r) {
+      const int64_t pr = static_cast<int64_t>(mb) * BM + r;
+      ptx::bulk_store(dst + pr * row_bytes, zero, row_bytes);
+      if (w_row != nullptr) w_row[pr] = 0.f;
     }
   }
+  ptx::bulk_commit();
+  ptx::bulk_wait_all();
 }
 
 cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
-                           const char* saved, float* w_row_out, int kernel_id) {
-  const int grid = c.num_sms * 8;
+                           const char* saved, float* w_row_out, int kernel_id, char* scratch) {
+  const int row_bytes = static_cast<int>(L.H * 2);
+  const int smem = (PERM_SLOTS + 1) * row_bytes;
+  cudaError_t e = cudaFuncSetAttribute(permute_rows_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int per_sm = std::max(1, std::min(16, (200 * 1024) / (smem + 1024)));
   prof_begin(c, kernel_id);
-  permute_rows_kernel<<<grid, 256, 0, c.stream>>>(
-      reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst),
-      static_cast<int>(L.H / 8), static_cast<int>(L.k),
-      reinterpret_cast<const int*>(saved + L.meta), reinterpret_cast<const int*>(saved + L.tile_rows),
-      reinterpret_cast<const int*>(saved + L.rowflat), w_row_out);
+  permute_rows_kernel<<<c.num_sms * per_sm, 32, smem, c.stream>>>(
+      reinterpret_cast<const uint8_t*>(src), reinterpret_cast<uint8_t*>(dst), row_bytes,
+      static_cast<int>(L.T), static_cast<int>(L.k), reinterpret_cast<const int*>(saved + L.meta),
+      reinterpret_cast<const int*>(saved + L.tile_rows),
+      reinterpret_cast<const int*>(saved + L.prow), w_row_out,
+      reinterpret_cast<DevStatus*>(scratch + L.status));
   prof_end(c, kernel_id);
   return cudaGetLastError();
 }
