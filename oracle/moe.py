@@ -27,7 +27,12 @@ Readings where the pages are silent: SwiGLU = silu(gate) * up; topk_w is used
 as given (no renormalisation) and applied after the down projection; rows of one
 expert keep ascending flat index; MXFP8 follows oracle.mx, each GEMM operand
 quantised in 32-blocks along that GEMM's contraction axis (token-axis blocks
-start at the expert's first row, the tail zero-padded).
+start at the expert's first row, the tail zero-padded).  The layer keeps its
+intermediates h = [g | u], a, w*a and dh = [dg | du] in bf16; in the modes with
+an MXFP8 backward (mxfp8, fp8_bwd) the e4m3 rounding of an element is decided on
+that stored bf16 value, so those modes round each of these tensors to bf16
+where the layer stores it (the backward reads g, u and a as saved).  The BF16
+mode keeps every intermediate in fp64.
 
 Arithmetic is fp64 throughout; inputs are the bf16 numbers converted exactly.
 """
@@ -37,7 +42,7 @@ from typing import Dict, Optional, Sequence
 
 import numpy as np
 
-from .mx import mx_qdq
+from .mx import bf16_round, mx_qdq
 
 PRECISIONS = ("bf16", "mxfp8", "fp8_bwd")
 
@@ -85,6 +90,11 @@ def _q(v, axis, on):
     return mx_qdq(v, axis) if on else v
 
 
+def _stored(v, on):
+    """v as the layer stores it (bf16) when `on`, else unchanged."""
+    return bf16_round(v) if on else v
+
+
 def _quant_flags(prec: str):
     if prec not in PRECISIONS:
         raise ValueError(f"unknown precision {prec!r}")
@@ -98,7 +108,7 @@ def expert_forward(xe, Wg_e, Wu_e, Wd_e, prec: str = "bf16"):
     g = xq @ _q(Wg_e, 1, qf).T
     u = xq @ _q(Wu_e, 1, qf).T
     a = swiglu(g, u)
-    o = _q(a, 1, qf) @ _q(Wd_e, 1, qf).T
+    o = _q(_stored(a, qf), 1, qf) @ _q(Wd_e, 1, qf).T
     return g, u, a, o
 
 
@@ -109,15 +119,17 @@ def expert_backward(xe, dye, we, g, u, a, Wg_e, Wu_e, Wd_e, prec: str = "bf16"):
     we [n]: their routing weights; g, u, a: the forward intermediates.
     Returns dxe [n, H], dWg_e, dWu_e [I, H], dWd_e [H, I], dw [n]."""
     _, qb = _quant_flags(prec)
+    g, u, a = _stored(g, qb), _stored(u, qb), _stored(a, qb)   # as the forward saved them
     gp = _q(dye, 1, qb) @ _q(Wd_e, 0, qb)                 # g' = dy W_down[e]
     dw = np.sum(a * gp, axis=1)
     da = we[:, None] * gp
     dg, du = swiglu_grad(g, u, da)
+    dg, du = _stored(dg, qb), _stored(du, qb)
     dxe = _q(dg, 1, qb) @ _q(Wg_e, 0, qb) + _q(du, 1, qb) @ _q(Wu_e, 0, qb)
     xq = _q(xe, 0, qb)
     dWg_e = _q(dg, 0, qb).T @ xq
     dWu_e = _q(du, 0, qb).T @ xq
-    dWd_e = _q(dye, 0, qb).T @ _q(we[:, None] * a, 0, qb)
+    dWd_e = _q(dye, 0, qb).T @ _q(_stored(we[:, None] * a, qb), 0, qb)
     return dxe, dWg_e, dWu_e, dWd_e, dw
 
 

@@ -11,6 +11,9 @@ Microscaling (MX) v1.0 format for MXFP8:
   * each element is v / X rounded to nearest-even E4M3 (the 'fn' variant: no
     infinities, largest finite 448, smallest subnormal 2**-9), saturating at
     +-448, and dequantised as e4m3 * X.
+bf16_round gives the bfloat16 value of a number: the layer stores its
+intermediates in bf16, and in the MXFP8 modes an element's e4m3 rounding is
+decided on that stored value.
 """
 from __future__ import annotations
 
@@ -36,6 +39,22 @@ def e4m3_round(q: np.ndarray) -> np.ndarray:
     r = np.rint(a / step) * step                        # numpy rint: round half to even
     r = np.minimum(r, E4M3_MAX)
     return np.copysign(r, q)
+
+
+BF16_MBITS = 7           # stored fraction bits of bfloat16
+BF16_EMIN = -126         # smallest normal exponent (that of fp32)
+
+
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 value (ties to even): 8 significant bits and
+    fp32's exponent range, subnormals in steps of 2**-133.  Finite inputs below
+    the bf16 overflow threshold only."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    step = np.exp2(np.maximum(e, BF16_EMIN) - BF16_MBITS)
+    return np.copysign(np.rint(a / step) * step, v)
 
 
 def e8m0_scale_exponent(amax: np.ndarray) -> np.ndarray:
