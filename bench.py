@@ -200,16 +200,16 @@ def config_json(cfg):
             "parallelism": "replicas"}
 
 
-def oracle_step(d, tokens: int):
+def oracle_step(d, tokens: int, prec: str = "bf16"):
     """One oracle forward+backward on the first `tokens` tokens; returns (seconds, flops)."""
     import oracle
     import oracle.moe as om
     sub = om.token_subset(d, range(tokens))
     t0 = time.perf_counter()
     f = oracle.forward(sub["x"], sub["topk_idx"], sub["topk_w"], d["W_gate"], d["W_up"],
-                       d["W_down"])
+                       d["W_down"], prec)
     oracle.backward(sub["dy"], sub["x"], sub["topk_idx"], sub["topk_w"], d["W_gate"], d["W_up"],
-                    d["W_down"], fwd=f)
+                    d["W_down"], prec, fwd=f)
     dt = time.perf_counter() - t0
     k = d["topk_idx"].shape[1]
     H = d["x"].shape[1]
@@ -227,11 +227,11 @@ def run_reference(args):
     d = make_inputs(cfg)
     n = min(args.ref_sample_tokens, cfg.T)
     for _ in range(args.warmup):
-        oracle_step(d, n)
+        oracle_step(d, n, cfg.prec)
     times = []
     flops = 0.0
     for _ in range(args.steps):
-        dt, flops = oracle_step(d, n)
+        dt, flops = oracle_step(d, n, cfg.prec)
         times.append(dt)
     total = sum(times)
     value = flops * args.steps / total / 1e12
@@ -279,7 +279,7 @@ def run_ours(args):
     host["topk_idx"] = torch.from_numpy(d["topk_idx"])
     host["topk_w"] = torch.from_numpy(d["topk_w"])
     g = {k: v.to(dev) for k, v in host.items()}
-    layer = MoELayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, device=dev)
+    layer = MoELayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.prec, device=dev)
     outs = (torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev),
             torch.empty((cfg.E, cfg.I, cfg.H), dtype=torch.bfloat16, device=dev),
             torch.empty((cfg.E, cfg.I, cfg.H), dtype=torch.bfloat16, device=dev),
@@ -398,7 +398,7 @@ def run_ours(args):
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         n = min(args.cpu_sample_tokens, cfg.T)
-        dt, fl = oracle_step(d, n)
+        dt, fl = oracle_step(d, n, cfg.prec)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
                "kind": "oracle", "seconds": dt,
                "sample": f"first {n} of {cfg.T} tokens (all {cfg.k} routed rows each, full "

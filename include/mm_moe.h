@@ -54,8 +54,18 @@ extern "C" {
 
 /* Arithmetic of the expert GEMMs.  The pages list BF16, MXFP8 (Blackwell) and
  * an fp8_bwd mode (BF16 forward, FP8 backward) -- section "How does the fused
- * kernel work?".  This build computes MM_MOE_BF16; the other two return
- * MM_MOE_ENOTSUP. */
+ * kernel work?".
+ *   MM_MOE_BF16     bf16 operands, fp32 accumulation.
+ *   MM_MOE_MXFP8    every GEMM operand of the forward and the backward is
+ *                   quantised to MXFP8 (OCP Microscaling v1.0: e4m3 elements,
+ *                   one power-of-two e8m0 scale 2^(floor(log2 amax) - 8) per 32
+ *                   elements along that GEMM's K; token-axis blocks of the
+ *                   weight-gradient GEMMs start at each expert's first row, the
+ *                   last one zero-padded); fp32 accumulation.
+ *   MM_MOE_FP8_BWD  the BF16 forward and the MXFP8 backward.
+ * Stored tensors (h, a, the outputs and the gradients) stay bf16 in every mode,
+ * and the quantised operand copies live in `scratch` (which is larger for the
+ * two MXFP8 modes). */
 typedef enum {
   MM_MOE_BF16 = 0,
   MM_MOE_MXFP8 = 1,

@@ -39,6 +39,13 @@ struct Layout {
       tile_rows, w_row, x_perm, h, a, saved_bytes;
   // scratch
   size_t status, blk_counts, ys, dy_perm, dh, a_w, pw, dxs, scratch_bytes;
+  // scratch, MXFP8 operand copies (set only for the precisions that use them):
+  // forward, blocks along K: x_perm, a, W_gate, W_up, W_down
+  size_t q_x, q_a, q_wg, q_wu, q_wd;
+  // backward: dy_perm and dh along K (q_dy, q_dh), W_down along H and W_gate, W_up
+  // along I (q_wdc, q_wgc, q_wuc), and the weight-gradient operands along the
+  // token axis (q_dyc, q_dhc, q_xc, q_awc)
+  size_t q_dy, q_dh, q_wdc, q_wgc, q_wuc, q_dyc, q_dhc, q_xc, q_awc;
 };
 
 // meta[] slots in `saved`
@@ -76,6 +83,8 @@ enum KernelId {
   K_UNPERMUTE,
   K_GEMM_WGRAD_DOWN,
   K_GEMM_WGRAD_GATEUP,
+  K_MX_QDQ_ROWS,
+  K_MX_QDQ_COLS,
   K_COUNT
 };
 
@@ -110,6 +119,13 @@ cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
                            const char* saved, uint16_t* out);
 cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slots,
                              const char* saved, const float* pw, uint16_t* dx, float* dtopk_w);
+
+// MXFP8 quantise-dequantise of a bf16 [rows, cols] tensor in blocks of 32 elements,
+// along each row (along_rows) or down each column; the result is written as bf16.
+// With `meta` (device) non-null only the first meta[META_NUM_TILES] * BM rows are
+// processed (the padded routed rows that are in use).
+cudaError_t launch_mx_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
+                          int64_t cols, bool along_rows, const int* meta);
 
 enum GemmKind {
   GEMM_GATEUP = 0,        // x_perm . [W_gate|W_up]^T  -> SwiGLU epilogue (h, a)

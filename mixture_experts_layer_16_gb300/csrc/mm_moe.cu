@@ -74,6 +74,16 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->blk_counts = take(4 * static_cast<size_t>(L->nblk) * E);
   const size_t common = o;
   L->ys = take(2 * Rp * H);
+  // MXFP8 operand copies (bf16 holding the dequantised e4m3 values exactly)
+  const size_t W = 2 * E * I * H;  // bytes of one expert weight tensor
+  L->q_x = L->q_a = L->q_wg = L->q_wu = L->q_wd = 0;
+  if (s->prec == MM_MOE_MXFP8) {
+    L->q_x = take(2 * Rp * H);
+    L->q_a = take(2 * Rp * I);
+    L->q_wg = take(W);
+    L->q_wu = take(W);
+    L->q_wd = take(W);
+  }
   const size_t fwd_end = o;
   o = common;
   L->dy_perm = take(2 * Rp * H);
@@ -81,6 +91,19 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->a_w = take(2 * Rp * I);
   L->pw = take(4 * Rp * static_cast<size_t>(L->n_pw));
   L->dxs = take(2 * Rp * H);
+  L->q_dy = L->q_dh = L->q_wdc = L->q_wgc = L->q_wuc = 0;
+  L->q_dyc = L->q_dhc = L->q_xc = L->q_awc = 0;
+  if (s->prec != MM_MOE_BF16) {
+    L->q_dy = take(2 * Rp * H);
+    L->q_dh = take(2 * Rp * 2 * I);
+    L->q_wdc = take(W);
+    L->q_wgc = take(W);
+    L->q_wuc = take(W);
+    L->q_dyc = take(2 * Rp * H);
+    L->q_dhc = take(2 * Rp * 2 * I);
+    L->q_xc = take(2 * Rp * H);
+    L->q_awc = take(2 * Rp * I);
+  }
   L->scratch_bytes = o > fwd_end ? o : fwd_end;
   return MM_MOE_OK;
 }
@@ -170,7 +193,6 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   Layout L;
   mm_moe_status st = make_layout(shape, &L);
   if (st != MM_MOE_OK) return st;
-  if (shape->prec != MM_MOE_BF16) return MM_MOE_ENOTSUP;
   if (!aligned(x, 16) || !aligned(W_gate, 16) || !aligned(W_up, 16) || !aligned(W_down, 16) ||
       !aligned(y, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(scratch, 256) ||
       !aligned(saved, 256))
@@ -190,22 +212,47 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   uint16_t* ys = reinterpret_cast<uint16_t*>(sc + L.ys);
   MM_MOE_TRY(launch_permute(c, L, x, x_perm, sv, reinterpret_cast<float*>(sv + L.w_row),
                             K_PERMUTE_X, sc));
+  // Operands of the two GEMMs: the bf16 tensors, or under MXFP8 their copies
+  // quantised in 32-blocks along each GEMM's K (H for gate/up, I for down)
+  const bool mx = shape->prec == MM_MOE_MXFP8;
+  const int* meta = reinterpret_cast<const int*>(sv + L.meta);
+  const int64_t EI = L.E * L.I, EH = L.E * L.H;
+  const uint16_t *A1 = x_perm, *Bg = W_gate, *Bu = W_up, *A2 = a, *Bd = W_down;
+  if (mx) {
+    uint16_t* qx = reinterpret_cast<uint16_t*>(sc + L.q_x);
+    uint16_t* qwg = reinterpret_cast<uint16_t*>(sc + L.q_wg);
+    uint16_t* qwu = reinterpret_cast<uint16_t*>(sc + L.q_wu);
+    MM_MOE_TRY(launch_mx_qdq(c, x_perm, qx, L.Rp, L.H, true, meta));
+    MM_MOE_TRY(launch_mx_qdq(c, W_gate, qwg, EI, L.H, true, nullptr));
+    MM_MOE_TRY(launch_mx_qdq(c, W_up, qwu, EI, L.H, true, nullptr));
+    A1 = qx;
+    Bg = qwg;
+    Bu = qwu;
+  }
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
   g.kind = GEMM_GATEUP;
-  g.A = x_perm;
-  g.B0 = W_gate;
-  g.B1 = W_up;
+  g.A = A1;
+  g.B0 = Bg;
+  g.B1 = Bu;
   g.out0 = h;
   g.out1 = a;
   MM_MOE_TRY(launch_gemm(c, L, g));
+  if (mx) {
+    uint16_t* qa = reinterpret_cast<uint16_t*>(sc + L.q_a);
+    uint16_t* qwd = reinterpret_cast<uint16_t*>(sc + L.q_wd);
+    MM_MOE_TRY(launch_mx_qdq(c, a, qa, L.Rp, L.I, true, meta));
+    MM_MOE_TRY(launch_mx_qdq(c, W_down, qwd, EH, L.I, true, nullptr));
+    A2 = qa;
+    Bd = qwd;
+  }
   g = GemmArgs{};
   g.saved = sv;
   g.scratch = sc;
   g.kind = GEMM_DOWN;
-  g.A = a;
-  g.B0 = W_down;
+  g.A = A2;
+  g.B0 = Bd;
   g.out0 = ys;
   MM_MOE_TRY(launch_gemm(c, L, g));
   MM_MOE_TRY(launch_combine(c, L, ys, sv, y));
@@ -222,7 +269,6 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   Layout L;
   mm_moe_status st = make_layout(shape, &L);
   if (st != MM_MOE_OK) return st;
-  if (shape->prec != MM_MOE_BF16) return MM_MOE_ENOTSUP;
   if (!aligned(dy, 16) || !aligned(W_gate, 16) || !aligned(W_up, 16) || !aligned(W_down, 16) ||
       !aligned(dx, 16) || !aligned(dW_gate, 16) || !aligned(dW_up, 16) || !aligned(dW_down, 16) ||
       !aligned(dtopk_w, 4) || !aligned(scratch, 256) || !aligned(saved, 256))
@@ -244,25 +290,48 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   const uint16_t* a = reinterpret_cast<const uint16_t*>(sv + L.a);
   MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
   MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY, sc));
+  // MXFP8 backward (full MXFP8 and fp8_bwd): every GEMM reads copies of its operands
+  // quantised in 32-blocks along its own K
+  const bool mx = shape->prec != MM_MOE_BF16;
+  const int* meta = reinterpret_cast<const int*>(sv + L.meta);
+  const int64_t EI = L.E * L.I, EH = L.E * L.H;
+  auto q = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
+  const uint16_t* A1 = dy_perm;
+  const uint16_t* Bd = W_down;
+  if (mx) {
+    MM_MOE_TRY(launch_mx_qdq(c, dy_perm, q(L.q_dy), L.Rp, L.H, true, meta));
+    MM_MOE_TRY(launch_mx_qdq(c, W_down, q(L.q_wdc), EH, L.I, false, nullptr));
+    A1 = q(L.q_dy);
+    Bd = q(L.q_wdc);
+  }
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
   g.kind = GEMM_DGRAD_DOWN;
-  g.A = dy_perm;
-  g.B0 = W_down;
+  g.A = A1;
+  g.B0 = Bd;
   g.aux = h;
   g.aux2 = a;
   g.out0 = dh;
   g.out1 = a_w;
   g.outf = pw;
   MM_MOE_TRY(launch_gemm(c, L, g));
+  const uint16_t *A2 = dh, *Bg = W_gate, *Bu = W_up;
+  if (mx) {
+    MM_MOE_TRY(launch_mx_qdq(c, dh, q(L.q_dh), L.Rp, 2 * L.I, true, meta));
+    MM_MOE_TRY(launch_mx_qdq(c, W_gate, q(L.q_wgc), EI, L.H, false, nullptr));
+    MM_MOE_TRY(launch_mx_qdq(c, W_up, q(L.q_wuc), EI, L.H, false, nullptr));
+    A2 = q(L.q_dh);
+    Bg = q(L.q_wgc);
+    Bu = q(L.q_wuc);
+  }
   g = GemmArgs{};
   g.saved = sv;
   g.scratch = sc;
   g.kind = GEMM_DGRAD_GATEUP;
-  g.A = dh;
-  g.B0 = W_gate;
-  g.B1 = W_up;
+  g.A = A2;
+  g.B0 = Bg;
+  g.B1 = Bu;
   g.out0 = dxs;
   MM_MOE_TRY(launch_gemm(c, L, g));
   // the un-permute (bandwidth-bound) runs on the side stream beside the
@@ -274,20 +343,34 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   const Ctx cs{ss.s, d.sms, &launches};
   MM_MOE_TRY(launch_unpermute(cs, L, dxs, sv, pw, dx, dtopk_w));
   MM_MOE_TRY(cudaEventRecord(ss.join, ss.s));
+  // token-axis blocks of the weight-gradient operands: each expert's rows start on a
+  // multiple of 128 and its padding rows are zero, so 32-row blocks of the padded
+  // row space are the per-expert blocks with a zero-padded tail
+  const uint16_t *A3 = dy_perm, *B3 = a_w, *A4 = dh, *B4 = x_perm;
+  if (mx) {
+    MM_MOE_TRY(launch_mx_qdq(c, dy_perm, q(L.q_dyc), L.Rp, L.H, false, meta));
+    MM_MOE_TRY(launch_mx_qdq(c, a_w, q(L.q_awc), L.Rp, L.I, false, meta));
+    MM_MOE_TRY(launch_mx_qdq(c, dh, q(L.q_dhc), L.Rp, 2 * L.I, false, meta));
+    MM_MOE_TRY(launch_mx_qdq(c, x_perm, q(L.q_xc), L.Rp, L.H, false, meta));
+    A3 = q(L.q_dyc);
+    B3 = q(L.q_awc);
+    A4 = q(L.q_dhc);
+    B4 = q(L.q_xc);
+  }
   g = GemmArgs{};
   g.saved = sv;
   g.scratch = sc;
   g.kind = GEMM_WGRAD_DOWN;
-  g.A = dy_perm;
-  g.B0 = a_w;
+  g.A = A3;
+  g.B0 = B3;
   g.out0 = dW_down;
   MM_MOE_TRY(launch_gemm(c, L, g));
   g = GemmArgs{};
   g.saved = sv;
   g.scratch = sc;
   g.kind = GEMM_WGRAD_GATEUP;
-  g.A = dh;
-  g.B0 = x_perm;
+  g.A = A4;
+  g.B0 = B4;
   g.out0 = dW_gate;
   g.out1 = dW_up;
   MM_MOE_TRY(launch_gemm(c, L, g));

@@ -77,6 +77,9 @@ CONFIGS: Dict[str, MoEConfig] = {
                                routing="uniform", seed=5),
     "qwen3_30b_16k_mxfp8": MoEConfig("qwen3_30b_16k_mxfp8", T=16384, H=2048, I=768,
                                      E=128, k=8, routing="uniform", seed=6, prec="mxfp8"),
+    # the same inputs with a BF16 forward and an MXFP8 backward
+    "qwen3_30b_16k_fp8_bwd": MoEConfig("qwen3_30b_16k_fp8_bwd", T=16384, H=2048, I=768,
+                                       E=128, k=8, routing="uniform", seed=6, prec="fp8_bwd"),
 }
 
 BF16_ROUND_BIAS = np.uint32(0x7FFF)

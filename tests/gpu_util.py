@@ -5,7 +5,10 @@ from __future__ import annotations
 import numpy as np
 import torch
 
+import oracle
+import oracle.moe as om
 from mixture_experts_layer_16_gb300 import MoELayer, build
+from mixture_experts_layer_16_gb300.inputs import CONFIGS, make_inputs
 
 DEV = "cuda"
 
@@ -34,12 +37,12 @@ def upload(d):
     return out
 
 
-def run(d, backward=True, layer=None, dev=None):
+def run(d, backward=True, layer=None, dev=None, prec="bf16"):
     T, H = d["x"].shape
     E, I, _ = d["W_gate"].shape
     k = d["topk_idx"].shape[1]
     if layer is None:
-        layer = MoELayer(T, H, I, E, k)
+        layer = MoELayer(T, H, I, E, k, prec)
     if dev is None:
         dev = upload(d)
     y = layer.forward(dev["x"], dev["topk_idx"], dev["topk_w"], dev["W_gate"], dev["W_up"],
@@ -63,3 +66,60 @@ def rel_err(gpu, ref) -> float:
     if den == 0.0:
         return float(np.abs(g).max(initial=0.0))
     return float(np.abs(g - r).max(initial=0.0) / den)
+
+
+def check_routing(res, topk_idx, E):
+    counts, offsets, perm, inv = oracle.route(topk_idx, E)
+    assert np.array_equal(res["offsets"].cpu().numpy(), offsets.astype(np.int32))
+    assert np.array_equal(res["perm"].cpu().numpy(), perm.astype(np.int32))
+    assert np.array_equal(res["inv"].cpu().numpy(), inv.astype(np.int32))
+
+
+def full_errors(d, res, backward=True, prec="bf16"):
+    """Relative errors of every output against the oracle run in precision `prec`."""
+    f = oracle.forward(d["x"], d["topk_idx"], d["topk_w"], d["W_gate"], d["W_up"], d["W_down"],
+                       prec)
+    errs = {"y": rel_err(f32(res["y"]), f["y"])}
+    if backward:
+        b = oracle.backward(d["dy"], d["x"], d["topk_idx"], d["topk_w"], d["W_gate"], d["W_up"],
+                            d["W_down"], prec, fwd=f)
+        for key in ("dx", "dW_gate", "dW_up", "dW_down", "dtopk_w"):
+            errs[key] = rel_err(f32(res[key]), b[key])
+    return errs
+
+
+def check_full(d, res, backward=True, tol=1e-2, prec="bf16"):
+    errs = full_errors(d, res, backward, prec)
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"outside tolerance: {bad} (all: {errs})"
+    return errs
+
+
+def sampled_check(name, tol, n_tokens=48, seed=0):
+    """A full-size workload on the GPU; the oracle (in the workload's precision) on
+    sampled tokens (y, dx, dtopk_w are per token) and on the weight gradients of the
+    least and the most loaded expert (which need only that expert's rows)."""
+    cfg = CONFIGS[name]
+    d = make_inputs(cfg)
+    res, layer, dev = run(d, prec=cfg.prec)
+    assert res["status"] == 0
+    check_routing(res, d["topk_idx"], cfg.E)
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(cfg.T, size=n_tokens, replace=False))
+    sub = om.token_subset(d, toks)
+    f = oracle.forward(sub["x"], sub["topk_idx"], sub["topk_w"], d["W_gate"], d["W_up"],
+                       d["W_down"], cfg.prec)
+    b = oracle.backward(sub["dy"], sub["x"], sub["topk_idx"], sub["topk_w"], d["W_gate"],
+                        d["W_up"], d["W_down"], cfg.prec, fwd=f)
+    errs = {"y": rel_err(f32(res["y"][toks]), f["y"]),
+            "dx": rel_err(f32(res["dx"][toks]), b["dx"]),
+            "dtopk_w": rel_err(f32(res["dtopk_w"][toks]), b["dtopk_w"])}
+    counts = np.bincount(d["topk_idx"].reshape(-1), minlength=cfg.E)
+    for e in {int(np.argmin(counts)), int(np.argmax(counts))}:
+        g, u, dd = om.expert_weight_grads(d, e, cfg.prec)
+        errs[f"dW_gate[{e}]"] = rel_err(f32(res["dW_gate"][e]), g)
+        errs[f"dW_up[{e}]"] = rel_err(f32(res["dW_up"][e]), u)
+        errs[f"dW_down[{e}]"] = rel_err(f32(res["dW_down"][e]), dd)
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"outside tolerance: {bad} (all: {errs})"
+    return errs

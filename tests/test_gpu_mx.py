@@ -1,0 +1,85 @@
+"""MXFP8 and fp8_bwd on the GPU (through the C ABI) against the oracle run in the same
+precision (its MXFP8 emulation: e4m3 elements, one power-of-two scale per 32
+elements along each GEMM's K; token-axis blocks start at each expert's first row).
+
+Bar: routing bit-exact; every float output within max|gpu - oracle| / max|oracle|
+<= 5e-2, the bound the layer's specification states for MXFP8.  Besides, the
+quantisation must really happen: against the oracle in its own precision the GPU
+is much closer than against the BF16 oracle on the quantised outputs, and the
+fp8_bwd forward is the BF16 forward bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_16_gb300.inputs import custom_inputs
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+TOL = 5e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    G.ensure_built()
+
+
+SMALL = [
+    # (T, H, I, E, k, routing, seed)
+    (64, 128, 64, 8, 2, "uniform", 21),        # single-SM tiles, 64-wide N tiles
+    (1000, 384, 128, 16, 4, "uniform", 22),    # 128-wide N tiles over H, ragged tails
+    (777, 512, 256, 32, 8, "zipf", 23),        # skewed routing, SM-pair tiles
+    (900, 512, 256, 32, 8, "zipf_trunc", 24),  # experts with no token
+    (1500, 512, 384, 16, 4, "zipf", 25),       # I = 384 pair tiles
+]
+
+
+@pytest.mark.parametrize("prec", ["mxfp8", "fp8_bwd"])
+@pytest.mark.parametrize("T,H,I,E,k,routing,seed", SMALL)
+def test_small_parity(T, H, I, E, k, routing, seed, prec):
+    kw = dict(zipf_ranks=max(k, E - 4)) if routing == "zipf_trunc" else {}
+    d = custom_inputs(T, H, I, E, k, seed=seed, routing=routing, **kw)
+    res, _, _ = G.run(d, prec=prec)
+    assert res["status"] == 0
+    G.check_routing(res, d["topk_idx"], E)
+    errs = G.check_full(d, res, tol=TOL, prec=prec)
+    ref_bf16 = G.full_errors(d, res, prec="bf16")
+    # the quantised outputs follow the MXFP8 oracle, not the BF16 one
+    quantised = ("y", "dx") if prec == "mxfp8" else ("dx",)
+    for key in quantised:
+        assert errs[key] < 0.5 * ref_bf16[key], (key, errs[key], ref_bf16[key])
+
+
+def test_fp8_bwd_forward_is_the_bf16_forward():
+    d = custom_inputs(600, 256, 128, 8, 2, seed=26)
+    r_bf, _, _ = G.run(d, backward=False, prec="bf16")
+    r_fb, _, _ = G.run(d, backward=False, prec="fp8_bwd")
+    assert torch.equal(r_bf["y"], r_fb["y"])
+
+
+def test_empty_experts_get_zero_weight_gradients():
+    T, H, I, E, k = 400, 256, 128, 6, 1
+    idx = np.full((T, 1), 4, dtype=np.int32)
+    d = custom_inputs(T, H, I, E, k, seed=27, idx=idx)
+    res, _, _ = G.run(d, prec="mxfp8")
+    G.check_full(d, res, tol=TOL, prec="mxfp8")
+    for e in (0, 1, 2, 3, 5):
+        for key in ("dW_gate", "dW_up", "dW_down"):
+            assert torch.count_nonzero(res[key][e]).item() == 0
+
+
+def test_determinism():
+    d = custom_inputs(700, 256, 128, 16, 4, seed=28, routing="zipf")
+    r1, layer, dev = G.run(d, prec="mxfp8")
+    snap = {k: v.clone() for k, v in r1.items() if isinstance(v, torch.Tensor)}
+    r2, _, _ = G.run(d, layer=layer, dev=dev, prec="mxfp8")
+    for k, v in snap.items():
+        assert torch.equal(v, r2[k]), k
+
+
+def test_full_qwen3_30b_16k_mxfp8():
+    G.sampled_check("qwen3_30b_16k_mxfp8", TOL)
+
+
+def test_full_qwen3_30b_16k_fp8_bwd():
+    G.sampled_check("qwen3_30b_16k_fp8_bwd", TOL)

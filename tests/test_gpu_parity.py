@@ -10,8 +10,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
-import oracle.moe as om
 from mixture_experts_layer_16_gb300.inputs import CONFIGS, custom_inputs, make_inputs
 from tests import gpu_util as G
 
@@ -24,24 +22,11 @@ def _built():
     G.ensure_built()
 
 
-def check_routing(res, topk_idx, E):
-    counts, offsets, perm, inv = oracle.route(topk_idx, E)
-    assert np.array_equal(res["offsets"].cpu().numpy(), offsets.astype(np.int32))
-    assert np.array_equal(res["perm"].cpu().numpy(), perm.astype(np.int32))
-    assert np.array_equal(res["inv"].cpu().numpy(), inv.astype(np.int32))
+check_routing = G.check_routing
 
 
 def check_full(d, res, backward=True, tol=TOL):
-    f = oracle.forward(d["x"], d["topk_idx"], d["topk_w"], d["W_gate"], d["W_up"], d["W_down"])
-    errs = {"y": G.rel_err(G.f32(res["y"]), f["y"])}
-    if backward:
-        b = oracle.backward(d["dy"], d["x"], d["topk_idx"], d["topk_w"], d["W_gate"], d["W_up"],
-                            d["W_down"], fwd=f)
-        for key in ("dx", "dW_gate", "dW_up", "dW_down", "dtopk_w"):
-            errs[key] = G.rel_err(G.f32(res[key]), b[key])
-    bad = {k: v for k, v in errs.items() if not v <= tol}
-    assert not bad, f"outside tolerance: {bad} (all: {errs})"
-    return errs
+    return G.check_full(d, res, backward, tol)
 
 
 SMALL = [
@@ -124,30 +109,7 @@ def test_bad_expert_index_reports_status():
 
 # ---------------------------------------------------------------- full-size workloads
 def sampled_check(name, n_tokens=48, seed=0):
-    cfg = CONFIGS[name]
-    d = make_inputs(cfg)
-    res, layer, dev = G.run(d)
-    assert res["status"] == 0
-    check_routing(res, d["topk_idx"], cfg.E)
-    rng = np.random.default_rng(seed)
-    toks = np.sort(rng.choice(cfg.T, size=n_tokens, replace=False))
-    sub = om.token_subset(d, toks)
-    f = oracle.forward(sub["x"], sub["topk_idx"], sub["topk_w"], d["W_gate"], d["W_up"],
-                       d["W_down"])
-    b = oracle.backward(sub["dy"], sub["x"], sub["topk_idx"], sub["topk_w"], d["W_gate"],
-                        d["W_up"], d["W_down"], fwd=f)
-    errs = {"y": G.rel_err(G.f32(res["y"][toks]), f["y"]),
-            "dx": G.rel_err(G.f32(res["dx"][toks]), b["dx"]),
-            "dtopk_w": G.rel_err(G.f32(res["dtopk_w"][toks]), b["dtopk_w"])}
-    counts = np.bincount(d["topk_idx"].reshape(-1), minlength=cfg.E)
-    for e in {int(np.argmin(counts)), int(np.argmax(counts))}:
-        g, u, dd = om.expert_weight_grads(d, e)
-        errs[f"dW_gate[{e}]"] = G.rel_err(G.f32(res["dW_gate"][e]), g)
-        errs[f"dW_up[{e}]"] = G.rel_err(G.f32(res["dW_up"][e]), u)
-        errs[f"dW_down[{e}]"] = G.rel_err(G.f32(res["dW_down"][e]), dd)
-    bad = {k: v for k, v in errs.items() if not v <= TOL}
-    assert not bad, f"outside tolerance: {bad} (all: {errs})"
-    return errs
+    return G.sampled_check(name, TOL, n_tokens, seed)
 
 
 def test_full_qwen3_30b_4k():
