@@ -146,6 +146,23 @@ MM_MOE_API mm_moe_status mm_moe_get_routing(const mm_moe_shape* shape, const voi
                                  const int32_t** offsets, const int32_t** perm,
                                  const int32_t** inv);
 
+/* MXFP8 quantise-dequantise of a bf16 matrix, the operation the MXFP8 modes apply
+ * to every GEMM operand (OCP Microscaling v1.0 MXFP8: blocks of 32 elements share
+ * the power-of-two scale 2^(floor(log2 amax) - 8), 2^-127 for an all-zero block;
+ * each element is rounded to e4m3, nearest even, saturating at +-448).  The Prime
+ * Mega MoE pages name MXFP8 as the Blackwell precision (section "How does the
+ * fused kernel work?") but give no standalone quantiser; this one is exported
+ * for callers that keep MXFP8 copies of their own tensors.
+ *   in, out  [rows, cols] bf16, device, 16-byte aligned; out may equal in
+ *   axis     1: blocks along each row (cols % 32 == 0);
+ *            0: blocks down each column (rows % 32 == 0, cols % 8 == 0)
+ * out holds e4m3 * scale, exact in bf16 while it is at least 2^-133 (smaller
+ * values are rounded to bf16).  Returns MM_MOE_EINVAL for bad sizes or pointers
+ * (before any work is enqueued), MM_MOE_ENOTSUP off sm_103, MM_MOE_ECUDA for a
+ * failed launch. */
+MM_MOE_API mm_moe_status mm_moe_mx_qdq(const uint16_t* in, uint16_t* out, int64_t rows,
+                                       int64_t cols, int axis, void* stream);
+
 /* Synchronises `stream`, then returns the device status word of `scratch`
  * (MM_MOE_OK, MM_MOE_EBADIDX or MM_MOE_ETIMEOUT), or MM_MOE_ECUDA when the
  * synchronisation itself fails.  The only blocking call of the library. */

@@ -23,7 +23,7 @@ MM_MOE_OK, MM_MOE_EINVAL, MM_MOE_ENOTSUP, MM_MOE_EBADIDX, MM_MOE_ETIMEOUT, MM_MO
 EXPORTS = ("mm_moe_workspace_size", "mm_moe_forward", "mm_moe_backward", "mm_moe_get_routing",
            "mm_moe_read_status", "mm_moe_last_launch_count", "mm_moe_profile_start",
            "mm_moe_profile_stop", "mm_moe_kernel_name", "mm_moe_kernel_count",
-           "mm_moe_route_noalloc")
+           "mm_moe_route_noalloc", "mm_moe_mx_qdq")
 
 
 class MoEError(RuntimeError):
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
         L.mm_moe_kernel_name.argtypes = [ctypes.c_int]
         L.mm_moe_kernel_count.argtypes = []
         L.mm_moe_route_noalloc.argtypes = [sp] + [_vp] * 6
+        L.mm_moe_mx_qdq.argtypes = [_vp, _vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _vp]
         for fn in EXPORTS:
             getattr(L, fn).restype = ctypes.c_int
         L.mm_moe_kernel_name.restype = ctypes.c_char_p
@@ -144,6 +145,18 @@ def mm_moe_route_noalloc(shape: Shape, topk_idx, topk_w, offsets, perm, inv, str
     if check:
         _check("mm_moe_route_noalloc", st)
     return st
+
+
+def mm_moe_mx_qdq(inp, out, axis: int, stream=None) -> None:
+    """MXFP8 quantise-dequantise of a 2-D bf16 CUDA tensor into `out` (may be `inp`):
+    32-element blocks along rows (axis=1) or down columns (axis=0)."""
+    import torch
+    if inp.dim() != 2 or inp.dtype != torch.bfloat16 or not inp.is_contiguous():
+        raise ValueError("inp must be a contiguous 2-D bf16 tensor")
+    if out.shape != inp.shape or out.dtype != inp.dtype or not out.is_contiguous():
+        raise ValueError("out must match inp")
+    _check("mm_moe_mx_qdq", lib().mm_moe_mx_qdq(_ptr(inp), _ptr(out), inp.shape[0],
+                                                inp.shape[1], int(axis), _stream(stream)))
 
 
 def mm_moe_read_status(scratch, stream=None) -> int:

@@ -33,6 +33,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "mx.cuh"
 #include "ptx.cuh"
 
 namespace mmmoe {
@@ -47,6 +48,7 @@ struct GemmParams {
   CUtensorMap tmC1;
   CUtensorMap tmD0;  // epilogue inputs loaded by TMA (dSwiGLU: h and a)
   CUtensorMap tmD1;
+  CUtensorMap tmQ0;  // MXFP8 epilogue output (gate/up: a in 32-blocks along I)
   int H, I, E;
   int n_tiles;  // N tiles per M block (grouped kinds) or per expert M row (per-expert kinds)
   int m_tiles;  // M tiles (of BM * CTAS rows) per expert (per-expert kinds)
@@ -57,6 +59,7 @@ struct GemmParams {
   const int* tile_expert;
   const int* tile_rows;
   const int* pad_off;
+  const int* counts;
   const int* expert_order;
   const int* rowflat;
   const float* w_row;
@@ -117,7 +120,9 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int 
     ti.m0 = mt * BM * CTAS + rank * BM;
     ti.n0 = nt * BN;
     ti.k_row0 = __ldg(p.pad_off + ti.e);
-    ti.k_iters = (__ldg(p.pad_off + ti.e + 1) - ti.k_row0) / BK;
+    // K stops at the last 64-row block holding a routed row (the rows after it, up
+    // to the padded end, are zero)
+    ti.k_iters = (__ldg(p.counts + ti.e) + BK - 1) / BK;
   } else {
     const int pmb = t / p.n_tiles;
     const int nt = t - pmb * p.n_tiles;
@@ -244,7 +249,7 @@ __device__ __forceinline__ bool wait_inputs(EpiWarp& w, volatile int* abort) {
 
 // Epilogue of one tile for one warp (row = lane of the warp's 32 rows, q = warp).
 // `next` is the tile this CTA processes after this one (dSwiGLU prefetch), or null.
-template <int KIND, int BN, int CTAS>
+template <int KIND, int BN, int CTAS, bool MX>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInfo& ti,
                                               const TileInfo* next, int q, uint32_t tbase,
                                               EpiWarp& w, volatile int* abort) {
@@ -268,6 +273,10 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInf
       store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, g);
       store_block<C::EPI_OUT>(w, &p.tmC0, p.I + ti.n0 + c, row0, u);
       store_block<C::EPI_OUT>(w, &p.tmC1, ti.n0 + c, row0, a);
+      if constexpr (MX) {  // the down projection's operand: a in 32-blocks along I
+        mx::qdq_row32(a);
+        store_block<C::EPI_OUT>(w, &p.tmQ0, ti.n0 + c, row0, a);
+      }
     }
   } else if constexpr (KIND == GEMM_DOWN || KIND == GEMM_DGRAD_GATEUP) {
     // rows stay in expert-grouped order; padding rows carry weight 0 (DOWN) or zero
@@ -420,7 +429,7 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int KIND, int BN, int CTAS>
+template <int KIND, int BN, int CTAS, bool MX>
 __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<KIND, BN, CTAS>;
   extern __shared__ uint8_t smem_raw[];
@@ -599,7 +608,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
       __syncwarp();
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(q * 32) << 16);
-      if (!epilogue_tile<KIND, BN, CTAS>(p, ti, has_next ? &nx : nullptr, q, tbase, w, abort)) {
+      if (!epilogue_tile<KIND, BN, CTAS, MX>(p, ti, has_next ? &nx : nullptr, q, tbase, w, abort)) {
         if (lane == 0) record_timeout(p, abort, KIND * 16 + 7);
         break;
       }
@@ -671,10 +680,10 @@ int pick_bn(int64_t n) {
   return 64;
 }
 
-template <int KIND, int BN, int CTAS>
+template <int KIND, int BN, int CTAS, bool MX>
 static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) {
   using C = Cfg<KIND, BN, CTAS>;
-  auto kern = moe_gemm_kernel<KIND, BN, CTAS>;
+  auto kern = moe_gemm_kernel<KIND, BN, CTAS, MX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -725,6 +734,7 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   p.tile_expert = reinterpret_cast<const int*>(saved + L.tile_expert);
   p.tile_rows = reinterpret_cast<const int*>(saved + L.tile_rows);
   p.pad_off = reinterpret_cast<const int*>(saved + L.pad_off);
+  p.counts = reinterpret_cast<const int*>(saved + L.counts);
   p.expert_order = reinterpret_cast<const int*>(saved + L.expert_order);
   p.rowflat = reinterpret_cast<const int*>(saved + L.rowflat);
   p.w_row = reinterpret_cast<const float*>(saved + L.w_row);
@@ -741,7 +751,8 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
       bn = (L.I % 128 == 0) ? 256 : 128;
       ok = make_map(&p.tmA, g.A, H, Rp, 64, BM) && make_map(&p.tmB0, g.B0, H, E * I, 64, bn / 2) &&
            make_map(&p.tmB1, g.B1, H, E * I, 64, bn / 2) &&
-           make_epi_map(&p.tmC0, g.out0, 2 * I, Rp) && make_epi_map(&p.tmC1, g.out1, I, Rp);
+           make_epi_map(&p.tmC0, g.out0, 2 * I, Rp) && make_epi_map(&p.tmC1, g.out1, I, Rp) &&
+           (!g.mx || make_epi_map(&p.tmQ0, g.q0, I, Rp));
       p.n_tiles = static_cast<int>(L.I / (bn / 2));
       p.k_iters = static_cast<int>(L.H / BK);
       max_units = L.NT / ctas * p.n_tiles;
@@ -791,8 +802,14 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
       return cudaErrorInvalidValue;
   }
   if (!ok) return cudaErrorInvalidValue;
-#define MMMOE_RUN(K, B, N) \
-  if (g.kind == K && bn == B && ctas == N) return run<K, B, N>(c, p, max_units);
+  // the MXFP8 gate/up epilogue is an instantiation of its own, so the BF16 kernels
+  // keep their register budget
+  const bool mx = g.mx != 0 && g.kind == GEMM_GATEUP;
+#define MMMOE_RUN(K, B, N)                                                    \
+  if (g.kind == K && bn == B && ctas == N) {                                  \
+    if (K == GEMM_GATEUP && mx) return run<K, B, N, K == GEMM_GATEUP>(c, p, max_units); \
+    return run<K, B, N, false>(c, p, max_units);                              \
+  }
   MMMOE_RUN(GEMM_GATEUP, 256, 2)
   MMMOE_RUN(GEMM_DOWN, 256, 2)
   MMMOE_RUN(GEMM_DGRAD_DOWN, 256, 2)

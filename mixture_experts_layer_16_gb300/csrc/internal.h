@@ -42,10 +42,10 @@ struct Layout {
   // scratch, MXFP8 operand copies (set only for the precisions that use them):
   // forward, blocks along K: x_perm, a, W_gate, W_up, W_down
   size_t q_x, q_a, q_wg, q_wu, q_wd;
-  // backward: dy_perm and dh along K (q_dy, q_dh), W_down along H and W_gate, W_up
-  // along I (q_wdc, q_wgc, q_wuc), and the weight-gradient operands along the
-  // token axis (q_dyc, q_dhc, q_xc, q_awc)
-  size_t q_dy, q_dh, q_wdc, q_wgc, q_wuc, q_dyc, q_dhc, q_xc, q_awc;
+  // backward: W_down along H and W_gate, W_up along I (q_wdc, q_wgc, q_wuc), and
+  // dy_perm, dh, x_perm along the token axis (q_dyc, q_dhc, q_xc); dy_perm and dh
+  // along their K, and a_w along tokens, are quantised in place
+  size_t q_wdc, q_wgc, q_wuc, q_dyc, q_dhc, q_xc;
 };
 
 // meta[] slots in `saved`
@@ -123,9 +123,12 @@ cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slot
 // MXFP8 quantise-dequantise of a bf16 [rows, cols] tensor in blocks of 32 elements,
 // along each row (along_rows) or down each column; the result is written as bf16.
 // With `meta` (device) non-null only the first meta[META_NUM_TILES] * BM rows are
-// processed (the padded routed rows that are in use).
+// processed (the padded routed rows that are in use).  Down columns, a non-null
+// out_rows also receives the blocks along rows from the same read.  out and out_rows
+// may each equal in (every element is read once, by the thread that writes it).
 cudaError_t launch_mx_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
-                          int64_t cols, bool along_rows, const int* meta);
+                          int64_t cols, bool along_rows, const int* meta,
+                          uint16_t* out_rows = nullptr);
 
 enum GemmKind {
   GEMM_GATEUP = 0,        // x_perm . [W_gate|W_up]^T  -> SwiGLU epilogue (h, a)
@@ -150,6 +153,10 @@ struct GemmArgs {
   const uint16_t* aux2;  // a = silu(g) * u saved by the forward
   const char* saved;
   char* scratch;
+  // MXFP8 (mx != 0, gate/up only): the epilogue also writes a in 32-blocks along I
+  // to q0 (a itself still goes to out1)
+  int mx;
+  uint16_t* q0;
 };
 
 cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g);

@@ -91,18 +91,14 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->a_w = take(2 * Rp * I);
   L->pw = take(4 * Rp * static_cast<size_t>(L->n_pw));
   L->dxs = take(2 * Rp * H);
-  L->q_dy = L->q_dh = L->q_wdc = L->q_wgc = L->q_wuc = 0;
-  L->q_dyc = L->q_dhc = L->q_xc = L->q_awc = 0;
+  L->q_wdc = L->q_wgc = L->q_wuc = L->q_dyc = L->q_dhc = L->q_xc = 0;
   if (s->prec != MM_MOE_BF16) {
-    L->q_dy = take(2 * Rp * H);
-    L->q_dh = take(2 * Rp * 2 * I);
     L->q_wdc = take(W);
     L->q_wgc = take(W);
     L->q_wuc = take(W);
     L->q_dyc = take(2 * Rp * H);
     L->q_dhc = take(2 * Rp * 2 * I);
     L->q_xc = take(2 * Rp * H);
-    L->q_awc = take(2 * Rp * I);
   }
   L->scratch_bytes = o > fwd_end ? o : fwd_end;
   return MM_MOE_OK;
@@ -238,13 +234,13 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   g.B1 = Bu;
   g.out0 = h;
   g.out1 = a;
+  g.mx = mx ? 1 : 0;  // the epilogue also writes a quantised along I
+  g.q0 = mx ? reinterpret_cast<uint16_t*>(sc + L.q_a) : nullptr;
   MM_MOE_TRY(launch_gemm(c, L, g));
   if (mx) {
-    uint16_t* qa = reinterpret_cast<uint16_t*>(sc + L.q_a);
     uint16_t* qwd = reinterpret_cast<uint16_t*>(sc + L.q_wd);
-    MM_MOE_TRY(launch_mx_qdq(c, a, qa, L.Rp, L.I, true, meta));
     MM_MOE_TRY(launch_mx_qdq(c, W_down, qwd, EH, L.I, true, nullptr));
-    A2 = qa;
+    A2 = g.q0;
     Bd = qwd;
   }
   g = GemmArgs{};
@@ -299,9 +295,10 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   const uint16_t* A1 = dy_perm;
   const uint16_t* Bd = W_down;
   if (mx) {
-    MM_MOE_TRY(launch_mx_qdq(c, dy_perm, q(L.q_dy), L.Rp, L.H, true, meta));
+    // one read of dy_perm: blocks along tokens (dW_down) to q_dyc, blocks along H
+    // (this GEMM) in place
+    MM_MOE_TRY(launch_mx_qdq(c, dy_perm, q(L.q_dyc), L.Rp, L.H, false, meta, dy_perm));
     MM_MOE_TRY(launch_mx_qdq(c, W_down, q(L.q_wdc), EH, L.I, false, nullptr));
-    A1 = q(L.q_dy);
     Bd = q(L.q_wdc);
   }
   GemmArgs g{};
@@ -318,10 +315,11 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   MM_MOE_TRY(launch_gemm(c, L, g));
   const uint16_t *A2 = dh, *Bg = W_gate, *Bu = W_up;
   if (mx) {
-    MM_MOE_TRY(launch_mx_qdq(c, dh, q(L.q_dh), L.Rp, 2 * L.I, true, meta));
+    // one read of dh: blocks along tokens (dW_gate, dW_up) to q_dhc, blocks along I
+    // (the next GEMM) in place
+    MM_MOE_TRY(launch_mx_qdq(c, dh, q(L.q_dhc), L.Rp, 2 * L.I, false, meta, dh));
     MM_MOE_TRY(launch_mx_qdq(c, W_gate, q(L.q_wgc), EI, L.H, false, nullptr));
     MM_MOE_TRY(launch_mx_qdq(c, W_up, q(L.q_wuc), EI, L.H, false, nullptr));
-    A2 = q(L.q_dh);
     Bg = q(L.q_wgc);
     Bu = q(L.q_wuc);
   }
@@ -348,12 +346,9 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   // row space are the per-expert blocks with a zero-padded tail
   const uint16_t *A3 = dy_perm, *B3 = a_w, *A4 = dh, *B4 = x_perm;
   if (mx) {
-    MM_MOE_TRY(launch_mx_qdq(c, dy_perm, q(L.q_dyc), L.Rp, L.H, false, meta));
-    MM_MOE_TRY(launch_mx_qdq(c, a_w, q(L.q_awc), L.Rp, L.I, false, meta));
-    MM_MOE_TRY(launch_mx_qdq(c, dh, q(L.q_dhc), L.Rp, 2 * L.I, false, meta));
+    MM_MOE_TRY(launch_mx_qdq(c, a_w, a_w, L.Rp, L.I, false, meta));
     MM_MOE_TRY(launch_mx_qdq(c, x_perm, q(L.q_xc), L.Rp, L.H, false, meta));
     A3 = q(L.q_dyc);
-    B3 = q(L.q_awc);
     A4 = q(L.q_dhc);
     B4 = q(L.q_xc);
   }

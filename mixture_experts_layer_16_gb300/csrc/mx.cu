@@ -9,33 +9,17 @@
 // E4M3 (nearest even, saturating at +-448) after dividing by the scale.  The kernels
 // here write the dequantised values e4m3 * scale as bf16, which holds them exactly,
 // so a bf16 tensor-core GEMM with fp32 accumulation computes the MXFP8 product.
-#include <cuda_bf16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "mx.cuh"
 
 namespace mmmoe {
 
-// Shared-scale exponent of a block with absolute maximum amax (>= 0).
-__device__ __forceinline__ int mx_scale_exp(float amax) {
-  if (!(amax > 0.f)) return -127;
-  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 8;
-  return max(-127, min(127, e));  // a subnormal amax gives a very negative e: clamp
-}
-
-__device__ __forceinline__ float mx_qdq(float v, int e) {
-  const float q = ldexpf(v, -e);
-  const __nv_fp8_storage_t s = __nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
-  const __half_raw hr = __nv_cvt_fp8_to_halfraw(s, __NV_E4M3);
-  return ldexpf(__half2float(__half(hr)), e);
-}
-
-__device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
-__device__ __forceinline__ uint16_t to_bf(float f) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(f);  // exact for e4m3 * 2^e values
-  return *reinterpret_cast<const uint16_t*>(&h);
-}
+using mx::bf;
+using mx::qdq2;
+using mx::scale_exp;
+using mx::to_bf;
 
 __device__ __forceinline__ int64_t used_rows(int64_t rows, const int* meta) {
   const int64_t used = static_cast<int64_t>(__ldg(meta + META_NUM_TILES)) * BM;
@@ -43,83 +27,176 @@ __device__ __forceinline__ int64_t used_rows(int64_t rows, const int* meta) {
 }
 
 // Blocks of 32 consecutive elements of each row ([rows, C], C % 32 == 0): a thread
-// takes 8 elements, four neighbouring threads one block.  `meta` (device, may be
-// null) caps the rows processed at meta[META_NUM_TILES] * BM, the end of the padded
-// routed rows; the same holds for the column kernel below.
-__global__ void __launch_bounds__(256) mx_qdq_rows_kernel(const uint4* __restrict__ in,
-                                                          uint4* __restrict__ out, int64_t rows,
+// takes 8 elements (16 bytes), four neighbouring threads one block; each thread has
+// ROW_UNROLL such pieces in flight.  `meta` (device, may be null) caps the rows
+// processed at meta[META_NUM_TILES] * BM, the end of the padded routed rows; the
+// same holds for the column kernel below.
+constexpr int ROW_UNROLL = 4;
+
+__global__ void __launch_bounds__(256) mx_qdq_rows_kernel(const uint4* in, uint4* out, int64_t rows,
                                                           int C8, const int* __restrict__ meta) {
   if (meta != nullptr) rows = used_rows(rows, meta);
   const int64_t n = rows * C8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   // every thread of a warp runs the same number of iterations (shuffles below)
-  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; i0 < n; i0 += stride) {
-    const int64_t i = i0 + threadIdx.x;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (i < n) w = __ldg(in + i);
-    uint16_t h[8];
-    *reinterpret_cast<uint4*>(h) = w;
-    float v[8], amax = 0.f;
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; i0 < n;
+       i0 += stride * ROW_UNROLL) {
+    uint4 w[ROW_UNROLL];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      v[j] = bf(h[j]);
-      amax = fmaxf(amax, fabsf(v[j]));
+    for (int u = 0; u < ROW_UNROLL; ++u) {
+      const int64_t i = i0 + u * stride + threadIdx.x;
+      w[u] = i < n ? in[i] : make_uint4(0, 0, 0, 0);
     }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const int e = mx_scale_exp(amax);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) h[j] = to_bf(mx_qdq(v[j], e));
-    if (i < n) out[i] = *reinterpret_cast<uint4*>(h);
+    for (int u = 0; u < ROW_UNROLL; ++u) {
+      uint16_t h[8];
+      *reinterpret_cast<uint4*>(h) = w[u];
+      float v[8], amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[j] = bf(h[j]);
+        amax = fmaxf(amax, fabsf(v[j]));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const int e = scale_exp(amax);
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        qdq2(v[j], v[j + 1], e, e);
+        h[j] = to_bf(v[j]);
+        h[j + 1] = to_bf(v[j + 1]);
+      }
+      const int64_t i = i0 + u * stride + threadIdx.x;
+      if (i < n) out[i] = *reinterpret_cast<uint4*>(h);
+    }
   }
 }
 
-// Blocks of 32 consecutive rows of each column ([rows, C], rows % 32 == 0, C even): a
-// thread takes two neighbouring columns of one 32-row block, so a warp reads 128
-// contiguous bytes of each row.
-__global__ void __launch_bounds__(256) mx_qdq_cols_kernel(const uint32_t* __restrict__ in,
-                                                          uint32_t* __restrict__ out, int64_t rows,
-                                                          int C2, const int* __restrict__ meta) {
+// Blocks of 32 consecutive rows of each column ([rows, C], rows % 32 == 0, C % 32 == 0).
+// A CTA takes a tile of 32 rows x COL_TILE columns: thread t holds 8 columns
+// (16 bytes) of rows t/64, t/64 + 4, ..., so a warp reads 512 contiguous bytes of a
+// row; the four partial column maxima meet in shared memory.  With out_rows non-null
+// the same read also yields the blocks along rows (four neighbouring lanes hold one
+// 32-column block of a row), written to out_rows.
+constexpr int COL_TILE = 512;
+
+__global__ void __launch_bounds__(256) mx_qdq_cols_kernel(const uint4* in, uint4* out,
+                                                          uint4* out_rows,
+                                                          int64_t rows, int C8,
+                                                          const int* __restrict__ meta) {
+  __shared__ float part[4][COL_TILE];
   if (meta != nullptr) rows = used_rows(rows, meta);
-  const int64_t n = (rows / 32) * C2;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
-    const int64_t blk = i / C2, c = i - blk * C2;
-    const uint32_t* src = in + blk * 32 * C2 + c;
-    uint32_t w[32];
-    float amax0 = 0.f, amax1 = 0.f;
+  const int col_tiles = (C8 * 8 + COL_TILE - 1) / COL_TILE;
+  const int64_t tiles = (rows / 32) * col_tiles;
+  const int cg = threadIdx.x % 64, rs = threadIdx.x / 64;
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int64_t rb = tile / col_tiles;
+    const int c8 = static_cast<int>(tile - rb * col_tiles) * (COL_TILE / 8) + cg;
+    const bool active = c8 < C8;
+    const uint4* src = in + rb * 32 * C8 + c8;
+    uint4 w[8];
+    float amax[8];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      w[r] = __ldg(src + static_cast<int64_t>(r) * C2);
-      amax0 = fmaxf(amax0, fabsf(bf(static_cast<uint16_t>(w[r] & 0xFFFFu))));
-      amax1 = fmaxf(amax1, fabsf(bf(static_cast<uint16_t>(w[r] >> 16))));
+    for (int j = 0; j < 8; ++j) amax[j] = 0.f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      w[r] = active ? src[static_cast<int64_t>(rs + 4 * r) * C8] : make_uint4(0, 0, 0, 0);
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(&w[r]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax[j] = fmaxf(amax[j], fabsf(bf(h[j])));
     }
-    const int e0 = mx_scale_exp(amax0), e1 = mx_scale_exp(amax1);
-    uint32_t* dst = out + blk * 32 * C2 + c;
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      const uint32_t lo = to_bf(mx_qdq(bf(static_cast<uint16_t>(w[r] & 0xFFFFu)), e0));
-      const uint32_t hi = to_bf(mx_qdq(bf(static_cast<uint16_t>(w[r] >> 16)), e1));
-      dst[static_cast<int64_t>(r) * C2] = lo | (hi << 16);
+    for (int j = 0; j < 8; ++j) part[rs][cg * 8 + j] = amax[j];
+    if (out_rows != nullptr) {  // uniform: every lane takes part in the shuffles
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        uint4 o = w[r];
+        uint16_t* h = reinterpret_cast<uint16_t*>(&o);
+        float ra = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ra = fmaxf(ra, fabsf(bf(h[j])));
+        ra = fmaxf(ra, __shfl_xor_sync(0xffffffffu, ra, 1));
+        ra = fmaxf(ra, __shfl_xor_sync(0xffffffffu, ra, 2));
+        const int re = scale_exp(ra);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          float x0 = bf(h[j]), x1 = bf(h[j + 1]);
+          qdq2(x0, x1, re, re);
+          h[j] = to_bf(x0);
+          h[j + 1] = to_bf(x1);
+        }
+        if (active) out_rows[rb * 32 * C8 + c8 + static_cast<int64_t>(rs + 4 * r) * C8] = o;
+      }
+    }
+    __syncthreads();
+    int e[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = cg * 8 + j;
+      e[j] = scale_exp(fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c])));
+    }
+    __syncthreads();  // part[] is rewritten by the next tile
+    if (active) {
+      uint4* dst = out + rb * 32 * C8 + c8;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        uint16_t* h = reinterpret_cast<uint16_t*>(&w[r]);
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          float x0 = bf(h[j]), x1 = bf(h[j + 1]);
+          qdq2(x0, x1, e[j], e[j + 1]);
+          h[j] = to_bf(x0);
+          h[j + 1] = to_bf(x1);
+        }
+        dst[static_cast<int64_t>(rs + 4 * r) * C8] = w[r];
+      }
     }
   }
 }
 
 cudaError_t launch_mx_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
-                          int64_t cols, bool along_rows, const int* meta) {
-  const int grid = c.num_sms * 8;
+                          int64_t cols, bool along_rows, const int* meta, uint16_t* out_rows) {
   const int id = along_rows ? K_MX_QDQ_ROWS : K_MX_QDQ_COLS;
   prof_begin(c, id);
-  if (along_rows)
-    mx_qdq_rows_kernel<<<grid, 256, 0, c.stream>>>(reinterpret_cast<const uint4*>(in),
-                                                   reinterpret_cast<uint4*>(out), rows,
-                                                   static_cast<int>(cols / 8), meta);
-  else
-    mx_qdq_cols_kernel<<<grid, 256, 0, c.stream>>>(reinterpret_cast<const uint32_t*>(in),
-                                                   reinterpret_cast<uint32_t*>(out), rows,
-                                                   static_cast<int>(cols / 2), meta);
+  if (along_rows) {
+    mx_qdq_rows_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(
+        reinterpret_cast<const uint4*>(in), reinterpret_cast<uint4*>(out), rows,
+        static_cast<int>(cols / 8), meta);
+  } else {
+    // with `meta` the row count is known only on the device: size the grid for the
+    // capacity and let surplus CTAs exit
+    const int64_t tiles = (rows / 32) * ((cols + COL_TILE - 1) / COL_TILE);
+    const int64_t grid = tiles < c.num_sms * 6 ? tiles : c.num_sms * 6;
+    mx_qdq_cols_kernel<<<static_cast<int>(grid > 0 ? grid : 1), 256, 0, c.stream>>>(
+        reinterpret_cast<const uint4*>(in), reinterpret_cast<uint4*>(out),
+        reinterpret_cast<uint4*>(out_rows), rows, static_cast<int>(cols / 8), meta);
+  }
   prof_end(c, id);
   return cudaGetLastError();
 }
 
 }  // namespace mmmoe
+
+using namespace mmmoe;
+
+extern "C" MM_MOE_API mm_moe_status mm_moe_mx_qdq(const uint16_t* in, uint16_t* out, int64_t rows,
+                                                  int64_t cols, int axis, void* stream) {
+  if (in == nullptr || out == nullptr || rows < 1 || cols < 1) return MM_MOE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16 != 0)
+    return MM_MOE_EINVAL;
+  if (axis == 1 ? cols % 32 != 0 : (axis != 0 || rows % 32 != 0 || cols % 8 != 0))
+    return MM_MOE_EINVAL;
+  if (rows > (int64_t{1} << 40) / cols) return MM_MOE_EINVAL;
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MM_MOE_ECUDA;
+  if (major != 10 || minor != 3) return MM_MOE_ENOTSUP;
+  int launches = 0;
+  const Ctx c{static_cast<cudaStream_t>(stream), sms, &launches};
+  if (launch_mx_qdq(c, in, out, rows, cols, axis == 1, nullptr) != cudaSuccess)
+    return MM_MOE_ECUDA;
+  return MM_MOE_OK;
+}

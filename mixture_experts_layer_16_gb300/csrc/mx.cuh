@@ -1,0 +1,86 @@
+// mx.cuh -- MXFP8 block quantisation of single values (device helpers shared by the
+// quantise kernels and the GEMM epilogues that emit quantised operands).
+//
+// OCP Microscaling v1.0 MXFP8: a block of 32 elements shares the power-of-two scale
+// 2^(floor(log2 amax) - 8) (8 = the largest E4M3 exponent; 2^-127 for an all-zero
+// block); an element is v / scale rounded to E4M3 (nearest even, saturating at
+// +-448).  The helpers return the dequantised value e4m3 * scale, which bf16 holds
+// exactly.  The quantised input is always the bf16 value the layer stores.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <cstdint>
+
+namespace mmmoe {
+namespace mx {
+
+// Shared-scale exponent of a block with absolute maximum amax (>= 0).
+__device__ __forceinline__ int scale_exp(float amax) {
+  if (!(amax > 0.f)) return -127;
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 8;
+  return max(-127, min(127, e));  // a subnormal amax gives a very negative e: clamp
+}
+
+// 2^k for k in [-127, 127], exactly (2^-127 is an fp32 subnormal; the library is
+// built without flush-to-zero).
+__device__ __forceinline__ float pow2f(int k) {
+  return k >= -126 ? __uint_as_float(static_cast<uint32_t>(k + 127) << 23)
+                   : __uint_as_float(0x00400000u);
+}
+
+// Dequantised E4M3 values of a pair under block exponents ea, eb.  Scaling by a
+// power of two is exact here (|v| / 2^e < 512, and e4m3 * 2^e >= 2^-136 is an fp32
+// value), so the only rounding is the E4M3 conversion.
+__device__ __forceinline__ void qdq2(float& a, float& b, int ea, int eb) {
+  const __nv_fp8x2_storage_t s = __nv_cvt_float2_to_fp8x2(
+      make_float2(a * pow2f(-ea), b * pow2f(-eb)), __NV_SATFINITE, __NV_E4M3);
+  const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(s, __NV_E4M3)));
+  a = f.x * pow2f(ea);
+  b = f.y * pow2f(eb);
+}
+
+// bf16 bit pattern <-> value
+__device__ __forceinline__ float bf(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+__device__ __forceinline__ uint16_t to_bf(float f) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+// v rounded to bf16, as a float
+__device__ __forceinline__ float round_bf(float f) { return bf(to_bf(f)); }
+
+// One thread's 32 values form one block (a row chunk): quantise in place.  The values
+// are first rounded to bf16 (the stored value).
+__device__ __forceinline__ void qdq_row32(float (&v)[32]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = round_bf(v[i]);
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  const int e = scale_exp(amax);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) qdq2(v[i], v[i + 1], e, e);
+}
+
+// The 32 lanes of a warp hold 32 consecutive rows and each lane 32 columns: every
+// column is one block (32 rows).  Writes the quantised values to out; the values are
+// first rounded to bf16.  All 32 lanes must call it.
+__device__ __forceinline__ void qdq_col32(const float (&v)[32], float (&out)[32]) {
+  int e[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    out[i] = round_bf(v[i]);
+    // |x| as a float is ordered like its bit pattern as an unsigned integer
+    const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(out[i])));
+    e[i] = scale_exp(__uint_as_float(m));
+  }
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) qdq2(out[i], out[i + 1], e[i], e[i + 1]);
+}
+
+}  // namespace mx
+}  // namespace mmmoe

@@ -73,6 +73,12 @@ def test_forward_backward_reject_before_launch(lib):
     bad_prec = B.make_shape(64, 128, 64, 8, 2, 3)
     assert lib.mm_moe_forward(ctypes.byref(bad_prec), *fake) == B.MM_MOE_EINVAL
     assert lib.mm_moe_get_routing(ctypes.byref(s), None, None, None, None) == B.MM_MOE_EINVAL
+    # the quantiser: NULL, misaligned, ragged blocks and unknown axes
+    assert lib.mm_moe_mx_qdq(None, None, 32, 32, 1, None) == B.MM_MOE_EINVAL
+    assert lib.mm_moe_mx_qdq(4096, 4098, 32, 32, 1, None) == B.MM_MOE_EINVAL
+    assert lib.mm_moe_mx_qdq(4096, 8192, 32, 48, 1, None) == B.MM_MOE_EINVAL
+    assert lib.mm_moe_mx_qdq(4096, 8192, 40, 32, 0, None) == B.MM_MOE_EINVAL
+    assert lib.mm_moe_mx_qdq(4096, 8192, 32, 32, 2, None) == B.MM_MOE_EINVAL
     assert lib.mm_moe_read_status(None, None) == B.MM_MOE_EINVAL
     del null
 

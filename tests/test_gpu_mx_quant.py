@@ -1,0 +1,86 @@
+"""The MXFP8 quantiser through the C ABI (mm_moe_mx_qdq) against the oracle's
+mx_qdq, bit for bit: the e4m3 code and the block scale are integers decided by
+floating point, and both sides decide them on the same bf16 input.
+
+Inputs cover several binades per row, all-zero blocks, saturation (block maxima
+with mantissa above 1.75, whose scaled value lies in (448, 512)) and exact ties
+between neighbouring e4m3 values.  Values stay where every dequantised value is
+at least 2^-133, so bf16 holds the result exactly."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_16_gb300 import binding as B
+from oracle import mx as omx
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    G.ensure_built()
+
+
+def bf16_round_np(v):
+    return torch.from_numpy(np.asarray(v, np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def make(rows, cols, seed, axis=1):
+    """bf16 values whose blocks run along `axis`: binades spread far across blocks
+    (from 2^-40 to 2^40) and a little within them."""
+    if axis == 0:
+        return np.ascontiguousarray(make(cols, rows, seed, 1).T)
+    rng = np.random.default_rng(seed)
+    nb = -(-cols // 32)
+    binade = rng.integers(-40, 40, size=(rows, nb)).repeat(32, axis=1)[:, :cols]
+    v = rng.standard_normal((rows, cols)) * np.exp2(binade)
+    v *= np.exp2(rng.integers(-6, 7, size=(1, cols)))          # binades within a block
+    v[rng.random((rows, cols)) < 0.02] = 0.0
+    if rows >= 64 and cols >= 64:
+        v[32:64, 32:64] = 0.0                                  # all-zero blocks
+    # exact ties: 1.0625 lies halfway between the e4m3 values 1.0 and 1.125 (block
+    # maximum 256 sets the scale to 2^0); a block maximum of 1.9 * 2^9 saturates
+    # (1.9 * 2^8 > 448 after scaling)
+    if rows >= 32 and cols >= 96:
+        v[0:32, 64:96] = 1.0625 * np.sign(rng.standard_normal((32, 32)))
+        v[0:32, 64] = 256.0
+        v[5, 70] = 1.9 * 2 ** 9
+        v[6, 64:96] = 1.0625 * np.sign(rng.standard_normal(32))
+        v[6, 64] = 256.0
+    return bf16_round_np(v)
+
+
+@pytest.mark.parametrize("rows,cols", [(64, 128), (96, 2048), (4096, 768), (32, 8 * 37)])
+@pytest.mark.parametrize("axis", [0, 1])
+def test_quantiser_bit_exact(rows, cols, axis):
+    if axis == 1 and cols % 32:
+        pytest.skip("rows need whole blocks")
+    v = make(rows, cols, seed=rows + cols + axis, axis=axis)
+    t = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).cuda()
+    out = torch.empty_like(t)
+    B.mm_moe_mx_qdq(t, out, axis)
+    torch.cuda.synchronize()
+    want = omx.mx_qdq(v, axis)
+    got = out.double().cpu().numpy()
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, (bad[:5], got[tuple(bad[0])], want[tuple(bad[0])])
+
+
+def test_quantiser_in_place_and_idempotent():
+    v = make(128, 256, seed=3)
+    t = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).cuda()
+    B.mm_moe_mx_qdq(t, t, 1)
+    once = t.clone()
+    B.mm_moe_mx_qdq(t, t, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(once, t)
+    assert np.array_equal(once.double().cpu().numpy(), omx.mx_qdq(v, 1))
+
+
+def test_quantiser_rejects_bad_shapes():
+    t = torch.zeros((40, 48), dtype=torch.bfloat16, device="cuda")
+    lib = B.lib()
+    assert lib.mm_moe_mx_qdq(t.data_ptr(), t.data_ptr(), 40, 48, 1, None) == B.MM_MOE_EINVAL
+    assert lib.mm_moe_mx_qdq(t.data_ptr(), t.data_ptr(), 40, 48, 0, None) == B.MM_MOE_EINVAL
+    assert lib.mm_moe_mx_qdq(t.data_ptr(), t.data_ptr(), 40, 48, 2, None) == B.MM_MOE_EINVAL
