@@ -96,7 +96,11 @@ typedef struct {
  *   saved   : written by mm_moe_forward, read by mm_moe_backward; holds the
  *             routing (offsets, perm, inv), the routing weights in routed order,
  *             the expert-grouped copy of x, h = [g | u] and a = silu(g) * u in
- *             bf16.  It must not change between the forward and its backward.
+ *             bf16.  Under MM_MOE_MXFP8 the copy of x is kept quantised along the
+ *             token axis and `saved` also holds the weights quantised along their
+ *             backward contraction axis (so the backward's weight arguments must be
+ *             the forward's, as in every mode).  It must not change between the
+ *             forward and its backward.
  * Returns MM_MOE_EINVAL for an invalid shape. */
 MM_MOE_API mm_moe_status mm_moe_workspace_size(const mm_moe_shape* shape,
                                     size_t* scratch_bytes, size_t* saved_bytes);

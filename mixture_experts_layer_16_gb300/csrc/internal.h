@@ -44,8 +44,11 @@ struct Layout {
   size_t q_x, q_a, q_wg, q_wu, q_wd;
   // backward: W_down along H and W_gate, W_up along I (q_wdc, q_wgc, q_wuc), and
   // dy_perm, dh, x_perm along the token axis (q_dyc, q_dhc, q_xc); dy_perm and dh
-  // along their K, and a_w along tokens, are quantised in place
+  // along their K, and a_w along tokens, are quantised in place.  Under full MXFP8
+  // the forward writes the weight copies into `saved` (w_in_saved) and x_perm's
+  // token-axis copy over x_perm, so q_xc is unused.
   size_t q_wdc, q_wgc, q_wuc, q_dyc, q_dhc, q_xc;
+  bool w_in_saved;
 };
 
 // meta[] slots in `saved`

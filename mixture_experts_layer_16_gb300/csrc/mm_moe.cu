@@ -67,6 +67,16 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->x_perm = take(2 * Rp * H);
   L->h = take(2 * Rp * 2 * I);
   L->a = take(2 * Rp * I);
+  // full MXFP8: the backward's quantised weight copies are made by the forward's
+  // two-way pass over each weight and kept here
+  const size_t W = 2 * E * I * H;  // bytes of one expert weight tensor
+  L->w_in_saved = s->prec == MM_MOE_MXFP8;
+  L->q_wdc = L->q_wgc = L->q_wuc = 0;
+  if (L->w_in_saved) {
+    L->q_wdc = take(W);
+    L->q_wgc = take(W);
+    L->q_wuc = take(W);
+  }
   L->saved_bytes = o;
   // scratch: status and routing blocks, then the forward and backward regions overlaid
   o = 0;
@@ -75,7 +85,6 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   const size_t common = o;
   L->ys = take(2 * Rp * H);
   // MXFP8 operand copies (bf16 holding the dequantised e4m3 values exactly)
-  const size_t W = 2 * E * I * H;  // bytes of one expert weight tensor
   L->q_x = L->q_a = L->q_wg = L->q_wu = L->q_wd = 0;
   if (s->prec == MM_MOE_MXFP8) {
     L->q_x = take(2 * Rp * H);
@@ -91,14 +100,16 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->a_w = take(2 * Rp * I);
   L->pw = take(4 * Rp * static_cast<size_t>(L->n_pw));
   L->dxs = take(2 * Rp * H);
-  L->q_wdc = L->q_wgc = L->q_wuc = L->q_dyc = L->q_dhc = L->q_xc = 0;
-  if (s->prec != MM_MOE_BF16) {
+  L->q_dyc = L->q_dhc = L->q_xc = 0;
+  if (s->prec == MM_MOE_FP8_BWD) {  // the BF16 forward leaves these to the backward
     L->q_wdc = take(W);
     L->q_wgc = take(W);
     L->q_wuc = take(W);
+    L->q_xc = take(2 * Rp * H);
+  }
+  if (s->prec != MM_MOE_BF16) {
     L->q_dyc = take(2 * Rp * H);
     L->q_dhc = take(2 * Rp * 2 * I);
-    L->q_xc = take(2 * Rp * H);
   }
   L->scratch_bytes = o > fwd_end ? o : fwd_end;
   return MM_MOE_OK;
@@ -215,15 +226,18 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   const int64_t EI = L.E * L.I, EH = L.E * L.H;
   const uint16_t *A1 = x_perm, *Bg = W_gate, *Bu = W_up, *A2 = a, *Bd = W_down;
   if (mx) {
-    uint16_t* qx = reinterpret_cast<uint16_t*>(sc + L.q_x);
-    uint16_t* qwg = reinterpret_cast<uint16_t*>(sc + L.q_wg);
-    uint16_t* qwu = reinterpret_cast<uint16_t*>(sc + L.q_wu);
-    MM_MOE_TRY(launch_mx_qdq(c, x_perm, qx, L.Rp, L.H, true, meta));
-    MM_MOE_TRY(launch_mx_qdq(c, W_gate, qwg, EI, L.H, true, nullptr));
-    MM_MOE_TRY(launch_mx_qdq(c, W_up, qwu, EI, L.H, true, nullptr));
-    A1 = qx;
-    Bg = qwg;
-    Bu = qwu;
+    // two-way passes, one read each: x_perm along H for this GEMM (to q_x) and along
+    // tokens for dW_gate/dW_up (over x_perm, which the backward reads only that way);
+    // each weight along its forward K (scratch) and its backward K (saved)
+    auto sq = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
+    auto vq = [&](size_t off) { return reinterpret_cast<uint16_t*>(sv + off); };
+    MM_MOE_TRY(launch_mx_qdq(c, x_perm, x_perm, L.Rp, L.H, false, meta, sq(L.q_x)));
+    MM_MOE_TRY(launch_mx_qdq(c, W_gate, vq(L.q_wgc), EI, L.H, false, nullptr, sq(L.q_wg)));
+    MM_MOE_TRY(launch_mx_qdq(c, W_up, vq(L.q_wuc), EI, L.H, false, nullptr, sq(L.q_wu)));
+    MM_MOE_TRY(launch_mx_qdq(c, W_down, vq(L.q_wdc), EH, L.I, false, nullptr, sq(L.q_wd)));
+    A1 = sq(L.q_x);
+    Bg = sq(L.q_wg);
+    Bu = sq(L.q_wu);
   }
   GemmArgs g{};
   g.saved = sv;
@@ -238,10 +252,8 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   g.q0 = mx ? reinterpret_cast<uint16_t*>(sc + L.q_a) : nullptr;
   MM_MOE_TRY(launch_gemm(c, L, g));
   if (mx) {
-    uint16_t* qwd = reinterpret_cast<uint16_t*>(sc + L.q_wd);
-    MM_MOE_TRY(launch_mx_qdq(c, W_down, qwd, EH, L.I, true, nullptr));
     A2 = g.q0;
-    Bd = qwd;
+    Bd = reinterpret_cast<uint16_t*>(sc + L.q_wd);
   }
   g = GemmArgs{};
   g.saved = sv;
@@ -292,14 +304,18 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   const int* meta = reinterpret_cast<const int*>(sv + L.meta);
   const int64_t EI = L.E * L.I, EH = L.E * L.H;
   auto q = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
+  // the backward's quantised weights: made here (fp8_bwd) or by the forward (MXFP8)
+  auto qw = [&](size_t off) -> const uint16_t* {
+    return L.w_in_saved ? reinterpret_cast<const uint16_t*>(sv + off) : q(off);
+  };
   const uint16_t* A1 = dy_perm;
   const uint16_t* Bd = W_down;
   if (mx) {
     // one read of dy_perm: blocks along tokens (dW_down) to q_dyc, blocks along H
     // (this GEMM) in place
     MM_MOE_TRY(launch_mx_qdq(c, dy_perm, q(L.q_dyc), L.Rp, L.H, false, meta, dy_perm));
-    MM_MOE_TRY(launch_mx_qdq(c, W_down, q(L.q_wdc), EH, L.I, false, nullptr));
-    Bd = q(L.q_wdc);
+    if (!L.w_in_saved) MM_MOE_TRY(launch_mx_qdq(c, W_down, q(L.q_wdc), EH, L.I, false, nullptr));
+    Bd = qw(L.q_wdc);
   }
   GemmArgs g{};
   g.saved = sv;
@@ -318,10 +334,12 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
     // one read of dh: blocks along tokens (dW_gate, dW_up) to q_dhc, blocks along I
     // (the next GEMM) in place
     MM_MOE_TRY(launch_mx_qdq(c, dh, q(L.q_dhc), L.Rp, 2 * L.I, false, meta, dh));
-    MM_MOE_TRY(launch_mx_qdq(c, W_gate, q(L.q_wgc), EI, L.H, false, nullptr));
-    MM_MOE_TRY(launch_mx_qdq(c, W_up, q(L.q_wuc), EI, L.H, false, nullptr));
-    Bg = q(L.q_wgc);
-    Bu = q(L.q_wuc);
+    if (!L.w_in_saved) {
+      MM_MOE_TRY(launch_mx_qdq(c, W_gate, q(L.q_wgc), EI, L.H, false, nullptr));
+      MM_MOE_TRY(launch_mx_qdq(c, W_up, q(L.q_wuc), EI, L.H, false, nullptr));
+    }
+    Bg = qw(L.q_wgc);
+    Bu = qw(L.q_wuc);
   }
   g = GemmArgs{};
   g.saved = sv;
@@ -347,10 +365,12 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   const uint16_t *A3 = dy_perm, *B3 = a_w, *A4 = dh, *B4 = x_perm;
   if (mx) {
     MM_MOE_TRY(launch_mx_qdq(c, a_w, a_w, L.Rp, L.I, false, meta));
-    MM_MOE_TRY(launch_mx_qdq(c, x_perm, q(L.q_xc), L.Rp, L.H, false, meta));
+    if (!L.w_in_saved) {  // fp8_bwd: x_perm is still bf16 (full MXFP8 quantised it)
+      MM_MOE_TRY(launch_mx_qdq(c, x_perm, q(L.q_xc), L.Rp, L.H, false, meta));
+      B4 = q(L.q_xc);
+    }
     A3 = q(L.q_dyc);
     A4 = q(L.q_dhc);
-    B4 = q(L.q_xc);
   }
   g = GemmArgs{};
   g.saved = sv;
