@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernels", action="store_true", help="also print the per-kernel table")
+    ap.add_argument("--recompute", action="store_true",
+                    help="activation checkpointing: the backward re-runs the gate/up stage")
     return ap.parse_args()
 
 
@@ -286,7 +288,8 @@ def run_ours(args):
     host["topk_idx"] = torch.from_numpy(d["topk_idx"])
     host["topk_w"] = torch.from_numpy(d["topk_w"])
     g = {k: v.to(dev) for k, v in host.items()}
-    layer = MoELayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.prec, device=dev)
+    layer = MoELayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.prec, device=dev,
+                     recompute=args.recompute)
     outs = (torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev),
             torch.empty((cfg.E, cfg.I, cfg.H), dtype=torch.bfloat16, device=dev),
             torch.empty((cfg.E, cfg.I, cfg.H), dtype=torch.bfloat16, device=dev),
@@ -300,7 +303,7 @@ def run_ours(args):
                       y=y)
 
     def bwd():
-        layer.backward(g["dy"], g["W_gate"], g["W_up"], g["W_down"], out=outs)
+        layer.backward(g["dy"], g["W_gate"], g["W_up"], g["W_down"], out=outs, x=g["x"])
 
     for _ in range(max(args.warmup, 0)):
         fwd()
@@ -388,7 +391,7 @@ def run_ours(args):
                     copy.wait_event(fwd_done[b])
                     out_h[0].copy_(ys[b], non_blocking=True)
                 layer.backward(a["dy"], g["W_gate"], g["W_up"], g["W_down"],
-                               out=(dxs[b], outs[1], outs[2], outs[3], dtws[b]))
+                               out=(dxs[b], outs[1], outs[2], outs[3], dtws[b]), x=a["x"])
                 step_done[b].record(stream)
                 with torch.cuda.stream(copy):
                     copy.wait_event(step_done[b])
@@ -451,15 +454,28 @@ def run_ours(args):
     flops = cfg.flops_fwd() + cfg.flops_bwd()
     value = aggregate_value(flops, world, ms_step_max)
     bpeak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    # The path's fraction of the dense tensor peak of its precision: FP8 peak = the
+    # measured bf16 peak x 2 (nominal 4.5 / 2.25 PFLOP/s); fp8_bwd blends the two,
+    # total FLOP / (fwd FLOP / P_bf16 + bwd FLOP / P_fp8).
+    fpeak = 2.0 * bpeak
+    p_fwd = fpeak if cfg.prec == "mxfp8" else bpeak
+    p_bwd = bpeak if cfg.prec == "bf16" else fpeak
+    fwd_tf = cfg.flops_fwd() / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = cfg.flops_bwd() / (bwd_ms * 1e-3) / 1e12
+    p_tot = (cfg.flops_fwd() + cfg.flops_bwd()) / (cfg.flops_fwd() / p_fwd + cfg.flops_bwd() / p_bwd)
+    peak_fractions = {"fwd": fwd_tf / p_fwd, "bwd": bwd_tf / p_bwd, "step": value / world / p_tot,
+                      "peak_fwd_tflops": p_fwd, "peak_bwd_tflops": p_bwd,
+                      "note": "bf16 peak = measured sustained; FP8 peak = 2 x that (nominal ratio)"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_json(cfg),
+        "config": dict(config_json(cfg), recompute=bool(args.recompute)),
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-        "fwd_tflops": cfg.flops_fwd() / (fwd_ms * 1e-3) / 1e12,
-        "bwd_tflops": cfg.flops_bwd() / (bwd_ms * 1e-3) / 1e12,
+        "fwd_tflops": fwd_tf,
+        "bwd_tflops": bwd_tf,
         "frac_of_bf16_peak": value / world / bpeak,
+        "frac_of_precision_peak": peak_fractions,
         "peak_note": f"{peak_src} bf16_tflops_sustained = {bpeak}",
         "roofline": roof,
         "cpu_baseline": cpu,

@@ -81,13 +81,22 @@ typedef enum {
   MM_MOE_ECUDA = 5      /* a CUDA runtime call or launch failed */
 } mm_moe_status;
 
+/* Options of a layer (bits of mm_moe_shape.flags).
+ *   MM_MOE_RECOMPUTE  activation checkpointing, as in the pages' training runs
+ *                     (section "How fast is Prime Mega MoE?": full activation
+ *                     checkpointing): `saved` keeps only the routing; the backward
+ *                     takes x again, re-permutes it and re-runs the gate/up GEMM
+ *                     (bit-identical to the forward's) before the backward proper.
+ *                     Less memory held between the passes, one more GEMM. */
+#define MM_MOE_RECOMPUTE 1
+
 /* Problem shape.  T tokens, H hidden, I expert intermediate, E experts, top-k.
  * Limits: T, H, I, E, k >= 1; k <= E <= 1024; H % 128 == 0; I % 64 == 0;
  * T * k < 2^31. */
 typedef struct {
   int64_t T, H, I, E, k;
-  int32_t prec;      /* mm_moe_precision */
-  int32_t reserved;  /* must be 0 */
+  int32_t prec;   /* mm_moe_precision */
+  int32_t flags;  /* 0 or MM_MOE_RECOMPUTE; other bits must be 0 */
 } mm_moe_shape;
 
 /* Bytes of the two caller-owned device buffers.
@@ -99,8 +108,10 @@ typedef struct {
  *             bf16.  Under MM_MOE_MXFP8 the copy of x is kept quantised along the
  *             token axis and `saved` also holds the weights quantised along their
  *             backward contraction axis (so the backward's weight arguments must be
- *             the forward's, as in every mode).  It must not change between the
- *             forward and its backward.
+ *             the forward's, as in every mode).  With MM_MOE_RECOMPUTE it holds
+ *             only the routing and the routing weights in routed order; x, h and a
+ *             live in `scratch`.  It must not change between the forward and its
+ *             backward.
  * Returns MM_MOE_EINVAL for an invalid shape. */
 MM_MOE_API mm_moe_status mm_moe_workspace_size(const mm_moe_shape* shape,
                                     size_t* scratch_bytes, size_t* saved_bytes);
@@ -126,6 +137,8 @@ MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape,
 
 /* Backward pass of the forward that wrote `saved` (same shape and weights).
  *   dy       [T, H]    bf16   upstream gradient of y
+ *   x        [T, H]    bf16   the forward's input; read only with MM_MOE_RECOMPUTE
+ *                             (may be NULL otherwise)
  *   dx       [T, H]    bf16   gradient of x (overwritten)
  *   dW_gate  [E, I, H] bf16   gradients of the weights (overwritten, not
  *   dW_up    [E, I, H] bf16   accumulated; an expert with no routed token
@@ -136,7 +149,7 @@ MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape,
 MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, const uint16_t* dy,
                               const void* saved,
                               const uint16_t* W_gate, const uint16_t* W_up,
-                              const uint16_t* W_down,
+                              const uint16_t* W_down, const uint16_t* x,
                               uint16_t* dx, uint16_t* dW_gate, uint16_t* dW_up,
                               uint16_t* dW_down, float* dtopk_w,
                               void* scratch, void* stream);

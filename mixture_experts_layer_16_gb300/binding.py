@@ -35,11 +35,15 @@ class MoEError(RuntimeError):
 class Shape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int64), ("I", ctypes.c_int64),
                 ("E", ctypes.c_int64), ("k", ctypes.c_int64), ("prec", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32)]
 
 
-def make_shape(T, H, I, E, k, prec="bf16") -> Shape:
-    return Shape(int(T), int(H), int(I), int(E), int(k), PRECISION.get(prec, prec), 0)
+MM_MOE_RECOMPUTE = 1  # activation checkpointing (include/mm_moe.h)
+
+
+def make_shape(T, H, I, E, k, prec="bf16", recompute: bool = False) -> Shape:
+    return Shape(int(T), int(H), int(I), int(E), int(k), PRECISION.get(prec, prec),
+                 MM_MOE_RECOMPUTE if recompute else 0)
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -58,7 +62,7 @@ def lib() -> ctypes.CDLL:
         L.mm_moe_workspace_size.argtypes = [sp, ctypes.POINTER(ctypes.c_size_t),
                                             ctypes.POINTER(ctypes.c_size_t)]
         L.mm_moe_forward.argtypes = [sp] + [_vp] * 10
-        L.mm_moe_backward.argtypes = [sp] + [_vp] * 12
+        L.mm_moe_backward.argtypes = [sp] + [_vp] * 13
         L.mm_moe_get_routing.argtypes = [sp, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                          ctypes.POINTER(_vp)]
         L.mm_moe_read_status.argtypes = [_vp, _vp]
@@ -110,11 +114,12 @@ def mm_moe_forward(shape: Shape, x, topk_idx, topk_w, W_gate, W_up, W_down, y, s
     return st
 
 
-def mm_moe_backward(shape: Shape, dy, saved, W_gate, W_up, W_down, dx, dW_gate, dW_up, dW_down,
-                    dtopk_w, scratch, stream=None, check: bool = True) -> int:
+def mm_moe_backward(shape: Shape, dy, saved, W_gate, W_up, W_down, x, dx, dW_gate, dW_up,
+                    dW_down, dtopk_w, scratch, stream=None, check: bool = True) -> int:
     st = lib().mm_moe_backward(ctypes.byref(shape), _ptr(dy), _ptr(saved), _ptr(W_gate),
-                               _ptr(W_up), _ptr(W_down), _ptr(dx), _ptr(dW_gate), _ptr(dW_up),
-                               _ptr(dW_down), _ptr(dtopk_w), _ptr(scratch), _stream(stream))
+                               _ptr(W_up), _ptr(W_down), _ptr(x), _ptr(dx), _ptr(dW_gate),
+                               _ptr(dW_up), _ptr(dW_down), _ptr(dtopk_w), _ptr(scratch),
+                               _stream(stream))
     if check:
         _check("mm_moe_backward", st)
     return st

@@ -25,7 +25,7 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   if (s->T < 1 || s->H < 1 || s->I < 1 || s->E < 1 || s->k < 1) return MM_MOE_EINVAL;
   if (s->k > s->E || s->E > MAX_E) return MM_MOE_EINVAL;
   if (s->H % 128 != 0 || s->I % 64 != 0) return MM_MOE_EINVAL;
-  if (s->reserved != 0) return MM_MOE_EINVAL;
+  if ((s->flags & ~MM_MOE_RECOMPUTE) != 0) return MM_MOE_EINVAL;
   if (s->prec < MM_MOE_BF16 || s->prec > MM_MOE_FP8_BWD) return MM_MOE_EINVAL;
   if (s->T > (int64_t{1} << 31) / s->k) return MM_MOE_EINVAL;
   L->T = s->T;
@@ -39,6 +39,7 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->Rp = ((L->R + L->pad - 1) / L->pad + L->E) * L->pad;
   L->NT = L->Rp / BM;
   if (L->Rp >= (int64_t{1} << 31)) return MM_MOE_EINVAL;
+  L->recompute = (s->flags & MM_MOE_RECOMPUTE) != 0;
   L->nblk = (L->R + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
   L->n_pw = L->I / pick_bn(L->I);
   const size_t A = 1024;
@@ -64,13 +65,15 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->tile_expert = take(4 * NT);
   L->tile_rows = take(4 * NT);
   L->w_row = take(4 * Rp);
-  L->x_perm = take(2 * Rp * H);
-  L->h = take(2 * Rp * 2 * I);
-  L->a = take(2 * Rp * I);
+  if (!L->recompute) {
+    L->x_perm = take(2 * Rp * H);
+    L->h = take(2 * Rp * 2 * I);
+    L->a = take(2 * Rp * I);
+  }
   // full MXFP8: the backward's quantised weight copies are made by the forward's
-  // two-way pass over each weight and kept here
+  // two-way pass over each weight and kept here (not under recompute)
   const size_t W = 2 * E * I * H;  // bytes of one expert weight tensor
-  L->w_in_saved = s->prec == MM_MOE_MXFP8;
+  L->w_in_saved = s->prec == MM_MOE_MXFP8 && !L->recompute;
   L->q_wdc = L->q_wgc = L->q_wuc = 0;
   if (L->w_in_saved) {
     L->q_wdc = take(W);
@@ -82,6 +85,11 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   o = 0;
   L->status = take(256);
   L->blk_counts = take(4 * static_cast<size_t>(L->nblk) * E);
+  if (L->recompute) {  // live through the forward and the backward's recompute
+    L->x_perm = take(2 * Rp * H);
+    L->h = take(2 * Rp * 2 * I);
+    L->a = take(2 * Rp * I);
+  }
   const size_t common = o;
   L->ys = take(2 * Rp * H);
   // MXFP8 operand copies (bf16 holding the dequantised e4m3 values exactly)
@@ -101,7 +109,7 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->pw = take(4 * Rp * static_cast<size_t>(L->n_pw));
   L->dxs = take(2 * Rp * H);
   L->q_dyc = L->q_dhc = L->q_xc = 0;
-  if (s->prec == MM_MOE_FP8_BWD) {  // the BF16 forward leaves these to the backward
+  if (s->prec != MM_MOE_BF16 && !L->w_in_saved) {  // left to the backward
     L->q_wdc = take(W);
     L->q_wgc = take(W);
     L->q_wuc = take(W);
@@ -172,14 +180,63 @@ static bool side_stream(SideStream* out) {
   return true;
 }
 
-}  // namespace mmmoe
-
-using namespace mmmoe;
-
 #define MM_MOE_TRY(expr)                         \
   do {                                           \
     if ((expr) != cudaSuccess) return MM_MOE_ECUDA; \
   } while (0)
+
+// The forward's gate/up stage on x_perm: h = [g | u] and a = silu(g) * u.  Under
+// full MXFP8 (mx) its operands are first quantised along H: with `keep` (the forward
+// of a layer that keeps its activations) by two-way passes that also leave x_perm
+// quantised along tokens in place and the weights along their backward K in saved
+// (wsaved); otherwise by row passes.  `emit_qa`: the epilogue also writes a
+// quantised along I (the down projection's operand).  The backward under
+// MM_MOE_RECOMPUTE calls it with the forward's arguments and gets h and a bit for
+// bit (the same kernels on the same inputs).
+static mm_moe_status gateup_stage(const Ctx& c, const Layout& L, bool mx, bool keep,
+                                  bool emit_qa, uint16_t* x_perm, const uint16_t* W_gate,
+                                  const uint16_t* W_up, const uint16_t* W_down, uint16_t* h,
+                                  uint16_t* a, const char* sv, char* wsaved, char* sc) {
+  const int* meta = reinterpret_cast<const int*>(sv + L.meta);
+  const int64_t EI = L.E * L.I, EH = L.E * L.H;
+  auto sq = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
+  const uint16_t *A = x_perm, *Bg = W_gate, *Bu = W_up;
+  if (mx) {
+    if (keep) {  // one read each, both axes
+      auto vq = [&](size_t off) { return reinterpret_cast<uint16_t*>(wsaved + off); };
+      MM_MOE_TRY(launch_mx_qdq(c, x_perm, x_perm, L.Rp, L.H, false, meta, sq(L.q_x)));
+      MM_MOE_TRY(launch_mx_qdq(c, W_gate, vq(L.q_wgc), EI, L.H, false, nullptr, sq(L.q_wg)));
+      MM_MOE_TRY(launch_mx_qdq(c, W_up, vq(L.q_wuc), EI, L.H, false, nullptr, sq(L.q_wu)));
+      if (emit_qa)
+        MM_MOE_TRY(launch_mx_qdq(c, W_down, vq(L.q_wdc), EH, L.I, false, nullptr, sq(L.q_wd)));
+    } else {
+      MM_MOE_TRY(launch_mx_qdq(c, x_perm, sq(L.q_x), L.Rp, L.H, true, meta));
+      MM_MOE_TRY(launch_mx_qdq(c, W_gate, sq(L.q_wg), EI, L.H, true, nullptr));
+      MM_MOE_TRY(launch_mx_qdq(c, W_up, sq(L.q_wu), EI, L.H, true, nullptr));
+      if (emit_qa) MM_MOE_TRY(launch_mx_qdq(c, W_down, sq(L.q_wd), EH, L.I, true, nullptr));
+    }
+    A = sq(L.q_x);
+    Bg = sq(L.q_wg);
+    Bu = sq(L.q_wu);
+  }
+  GemmArgs g{};
+  g.saved = sv;
+  g.scratch = sc;
+  g.kind = GEMM_GATEUP;
+  g.A = A;
+  g.B0 = Bg;
+  g.B1 = Bu;
+  g.out0 = h;
+  g.out1 = a;
+  g.mx = (mx && emit_qa) ? 1 : 0;
+  g.q0 = g.mx ? sq(L.q_a) : nullptr;
+  MM_MOE_TRY(launch_gemm(c, L, g));
+  return MM_MOE_OK;
+}
+
+}  // namespace mmmoe
+
+using namespace mmmoe;
 
 extern "C" MM_MOE_API mm_moe_status mm_moe_workspace_size(const mm_moe_shape* shape,
                                                           size_t* scratch_bytes,
@@ -213,49 +270,23 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   char* sv = static_cast<char*>(saved);
   MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
   MM_MOE_TRY(launch_route(c, L, topk_idx, topk_w, sv, sc));
-  uint16_t* x_perm = reinterpret_cast<uint16_t*>(sv + L.x_perm);
-  uint16_t* h = reinterpret_cast<uint16_t*>(sv + L.h);
-  uint16_t* a = reinterpret_cast<uint16_t*>(sv + L.a);
+  // x_perm, h, a: kept in saved, or in scratch under MM_MOE_RECOMPUTE
+  char* act = L.recompute ? sc : sv;
+  uint16_t* x_perm = reinterpret_cast<uint16_t*>(act + L.x_perm);
+  uint16_t* h = reinterpret_cast<uint16_t*>(act + L.h);
+  uint16_t* a = reinterpret_cast<uint16_t*>(act + L.a);
   uint16_t* ys = reinterpret_cast<uint16_t*>(sc + L.ys);
   MM_MOE_TRY(launch_permute(c, L, x, x_perm, sv, reinterpret_cast<float*>(sv + L.w_row),
                             K_PERMUTE_X, sc));
   // Operands of the two GEMMs: the bf16 tensors, or under MXFP8 their copies
   // quantised in 32-blocks along each GEMM's K (H for gate/up, I for down)
   const bool mx = shape->prec == MM_MOE_MXFP8;
-  const int* meta = reinterpret_cast<const int*>(sv + L.meta);
-  const int64_t EI = L.E * L.I, EH = L.E * L.H;
-  const uint16_t *A1 = x_perm, *Bg = W_gate, *Bu = W_up, *A2 = a, *Bd = W_down;
-  if (mx) {
-    // two-way passes, one read each: x_perm along H for this GEMM (to q_x) and along
-    // tokens for dW_gate/dW_up (over x_perm, which the backward reads only that way);
-    // each weight along its forward K (scratch) and its backward K (saved)
-    auto sq = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
-    auto vq = [&](size_t off) { return reinterpret_cast<uint16_t*>(sv + off); };
-    MM_MOE_TRY(launch_mx_qdq(c, x_perm, x_perm, L.Rp, L.H, false, meta, sq(L.q_x)));
-    MM_MOE_TRY(launch_mx_qdq(c, W_gate, vq(L.q_wgc), EI, L.H, false, nullptr, sq(L.q_wg)));
-    MM_MOE_TRY(launch_mx_qdq(c, W_up, vq(L.q_wuc), EI, L.H, false, nullptr, sq(L.q_wu)));
-    MM_MOE_TRY(launch_mx_qdq(c, W_down, vq(L.q_wdc), EH, L.I, false, nullptr, sq(L.q_wd)));
-    A1 = sq(L.q_x);
-    Bg = sq(L.q_wg);
-    Bu = sq(L.q_wu);
-  }
+  st = gateup_stage(c, L, mx, L.w_in_saved, true, x_perm, W_gate, W_up, W_down, h, a, sv, sv,
+                    sc);
+  if (st != MM_MOE_OK) return st;
+  const uint16_t* A2 = mx ? reinterpret_cast<uint16_t*>(sc + L.q_a) : a;
+  const uint16_t* Bd = mx ? reinterpret_cast<uint16_t*>(sc + L.q_wd) : W_down;
   GemmArgs g{};
-  g.saved = sv;
-  g.scratch = sc;
-  g.kind = GEMM_GATEUP;
-  g.A = A1;
-  g.B0 = Bg;
-  g.B1 = Bu;
-  g.out0 = h;
-  g.out1 = a;
-  g.mx = mx ? 1 : 0;  // the epilogue also writes a quantised along I
-  g.q0 = mx ? reinterpret_cast<uint16_t*>(sc + L.q_a) : nullptr;
-  MM_MOE_TRY(launch_gemm(c, L, g));
-  if (mx) {
-    A2 = g.q0;
-    Bd = reinterpret_cast<uint16_t*>(sc + L.q_wd);
-  }
-  g = GemmArgs{};
   g.saved = sv;
   g.scratch = sc;
   g.kind = GEMM_DOWN;
@@ -271,7 +302,8 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
 extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, const uint16_t* dy,
                                                     const void* saved, const uint16_t* W_gate,
                                                     const uint16_t* W_up, const uint16_t* W_down,
-                                                    uint16_t* dx, uint16_t* dW_gate,
+                                                    const uint16_t* x, uint16_t* dx,
+                                                    uint16_t* dW_gate,
                                                     uint16_t* dW_up, uint16_t* dW_down,
                                                     float* dtopk_w, void* scratch, void* stream) {
   Layout L;
@@ -279,7 +311,8 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   if (st != MM_MOE_OK) return st;
   if (!aligned(dy, 16) || !aligned(W_gate, 16) || !aligned(W_up, 16) || !aligned(W_down, 16) ||
       !aligned(dx, 16) || !aligned(dW_gate, 16) || !aligned(dW_up, 16) || !aligned(dW_down, 16) ||
-      !aligned(dtopk_w, 4) || !aligned(scratch, 256) || !aligned(saved, 256))
+      !aligned(dtopk_w, 4) || !aligned(scratch, 256) || !aligned(saved, 256) ||
+      (L.recompute && !aligned(x, 16)))
     return MM_MOE_EINVAL;
   DevInfo d;
   st = device_info(&d);
@@ -293,10 +326,20 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   uint16_t* a_w = reinterpret_cast<uint16_t*>(sc + L.a_w);
   float* pw = reinterpret_cast<float*>(sc + L.pw);
   uint16_t* dxs = reinterpret_cast<uint16_t*>(sc + L.dxs);
-  const uint16_t* x_perm = reinterpret_cast<const uint16_t*>(sv + L.x_perm);
-  const uint16_t* h = reinterpret_cast<const uint16_t*>(sv + L.h);
-  const uint16_t* a = reinterpret_cast<const uint16_t*>(sv + L.a);
+  const char* act = L.recompute ? sc : sv;  // where x_perm, h and a are
+  const uint16_t* x_perm = reinterpret_cast<const uint16_t*>(act + L.x_perm);
+  const uint16_t* h = reinterpret_cast<const uint16_t*>(act + L.h);
+  const uint16_t* a = reinterpret_cast<const uint16_t*>(act + L.a);
   MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
+  if (L.recompute) {
+    // activation checkpointing: x_perm, h and a again, as the forward made them
+    uint16_t* xp = reinterpret_cast<uint16_t*>(sc + L.x_perm);
+    MM_MOE_TRY(launch_permute(c, L, x, xp, sv, nullptr, K_PERMUTE_X, sc));
+    st = gateup_stage(c, L, shape->prec == MM_MOE_MXFP8, false, false, xp, W_gate, W_up,
+                      W_down, reinterpret_cast<uint16_t*>(sc + L.h),
+                      reinterpret_cast<uint16_t*>(sc + L.a), sv, nullptr, sc);
+    if (st != MM_MOE_OK) return st;
+  }
   MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY, sc));
   // MXFP8 backward (full MXFP8 and fp8_bwd): every GEMM reads copies of its operands
   // quantised in 32-blocks along its own K

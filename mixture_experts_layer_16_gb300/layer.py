@@ -30,14 +30,15 @@ class MoELayer:
     """Fused MoE layer of shape (T tokens, H hidden, I expert width, E experts, top-k)."""
 
     def __init__(self, T: int, H: int, I: int, E: int, k: int, prec: str = "bf16",
-                 device: Optional[torch.device] = None):
+                 device: Optional[torch.device] = None, recompute: bool = False):
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
         self.prec = prec
+        self.recompute = recompute
         device = torch.device("cuda" if device is None else device)
         if device.type == "cuda" and device.index is None:
             device = torch.device("cuda", torch.cuda.current_device())
         self.device = device
-        self.shape = B.make_shape(T, H, I, E, k, prec)
+        self.shape = B.make_shape(T, H, I, E, k, prec, recompute)
         self.ws = B.Workspace(self.shape, self.device)
 
     # ---------------------------------------------------------------- checks
@@ -62,11 +63,16 @@ class MoELayer:
                          self.ws.scratch, self.ws.saved, stream)
         return y
 
-    def backward(self, dy, W_gate, W_up, W_down, out=None, stream=None
+    def backward(self, dy, W_gate, W_up, W_down, out=None, stream=None, x=None
                  ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor, torch.Tensor]:
-        """Gradients (dx, dW_gate, dW_up, dW_down, dtopk_w) of the last forward."""
+        """Gradients (dx, dW_gate, dW_up, dW_down, dtopk_w) of the last forward.  With
+        recompute=True the forward's input x must be passed again."""
         d, bf = self.device, torch.bfloat16
         _need(dy, "dy", (self.T, self.H), bf, d)
+        if self.recompute:
+            if x is None:
+                raise ValueError("a recompute layer's backward needs the forward's x")
+            _need(x, "x", (self.T, self.H), bf, d)
         self._check_weights(W_gate, W_up, W_down)
         if out is None:
             out = (torch.empty((self.T, self.H), dtype=bf, device=d),
@@ -78,8 +84,9 @@ class MoELayer:
         _need(dx, "dx", (self.T, self.H), bf, d)
         self._check_weights(dWg, dWu, dWd)
         _need(dtw, "dtopk_w", (self.T, self.k), torch.float32, d)
-        B.mm_moe_backward(self.shape, dy, self.ws.saved, W_gate, W_up, W_down, dx, dWg, dWu,
-                          dWd, dtw, self.ws.scratch, stream)
+        B.mm_moe_backward(self.shape, dy, self.ws.saved, W_gate, W_up, W_down,
+                          x if self.recompute else None, dx, dWg, dWu, dWd, dtw,
+                          self.ws.scratch, stream)
         return out
 
     def routing(self):

@@ -37,12 +37,12 @@ def upload(d):
     return out
 
 
-def run(d, backward=True, layer=None, dev=None, prec="bf16"):
+def run(d, backward=True, layer=None, dev=None, prec="bf16", recompute=False):
     T, H = d["x"].shape
     E, I, _ = d["W_gate"].shape
     k = d["topk_idx"].shape[1]
     if layer is None:
-        layer = MoELayer(T, H, I, E, k, prec)
+        layer = MoELayer(T, H, I, E, k, prec, recompute=recompute)
     if dev is None:
         dev = upload(d)
     y = layer.forward(dev["x"], dev["topk_idx"], dev["topk_w"], dev["W_gate"], dev["W_up"],
@@ -50,7 +50,7 @@ def run(d, backward=True, layer=None, dev=None, prec="bf16"):
     res = dict(y=y)
     if backward:
         dx, dWg, dWu, dWd, dtw = layer.backward(dev["dy"], dev["W_gate"], dev["W_up"],
-                                                dev["W_down"])
+                                                dev["W_down"], x=dev["x"])
         res.update(dx=dx, dW_gate=dWg, dW_up=dWu, dW_down=dWd, dtopk_w=dtw)
     torch.cuda.synchronize()
     res["status"] = layer.status()

@@ -53,9 +53,26 @@ def test_workspace_size_and_shape_validation(lib):
             B.mm_moe_workspace_size(B.make_shape(*bad))
         assert ei.value.status == B.MM_MOE_EINVAL
     s = B.make_shape(64, 128, 64, 8, 2)
-    s.reserved = 1
+    s.flags = 2                                    # an undefined option bit
     with pytest.raises(B.MoEError):
         B.mm_moe_workspace_size(s)
+
+
+def test_workspace_sizes_by_mode(lib):
+    """MXFP8 modes need more scratch; recompute keeps only the routing in saved."""
+    shp = (16384, 2048, 768, 128, 8)
+    sc_b, sv_b = B.mm_moe_workspace_size(B.make_shape(*shp))
+    sc_m, sv_m = B.mm_moe_workspace_size(B.make_shape(*shp, "mxfp8"))
+    sc_f, sv_f = B.mm_moe_workspace_size(B.make_shape(*shp, "fp8_bwd"))
+    sc_r, sv_r = B.mm_moe_workspace_size(B.make_shape(*shp, recompute=True))
+    assert sc_m > sc_b and sc_f > sc_b
+    assert sv_m > sv_b                        # the backward's quantised weights
+    assert sv_f == sv_b
+    Rp = (16384 * 8 // 256 + 128) * 256       # padded rows (SM-pair tiles)
+    acts = Rp * (2048 + 2 * 768 + 768) * 2    # x_perm, h, a in bf16
+    assert sv_b - sv_r >= acts                # they leave saved ...
+    assert sc_r >= sc_b + acts                # ... for scratch
+    assert sv_r < 16 << 20                    # routing and weights per row only
 
 
 def test_forward_backward_reject_before_launch(lib):
@@ -64,8 +81,13 @@ def test_forward_backward_reject_before_launch(lib):
     null = [None] * 10
     st = lib.mm_moe_forward(ctypes.byref(s), *([None] * 10))
     assert st == B.MM_MOE_EINVAL
-    st = lib.mm_moe_backward(ctypes.byref(s), *([None] * 12))
+    st = lib.mm_moe_backward(ctypes.byref(s), *([None] * 13))
     assert st == B.MM_MOE_EINVAL
+    # recompute needs x in the backward
+    rc = B.make_shape(64, 128, 64, 8, 2, recompute=True)
+    args = [4096 * (i + 1) for i in range(13)]
+    args[5] = None                                  # x
+    assert lib.mm_moe_backward(ctypes.byref(rc), *args) == B.MM_MOE_EINVAL
     fake = [4096 * (i + 1) for i in range(10)]
     mis = list(fake)
     mis[0] += 2                                    # x misaligned
