@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--kernels", action="store_true", help="also print the per-kernel table")
     ap.add_argument("--recompute", action="store_true",
                     help="activation checkpointing: the backward re-runs the gate/up stage")
+    ap.add_argument("--with-router", action="store_true",
+                    help="the step also runs the top-k router (forward before the layer, "
+                         "backward after it); topk_idx/topk_w then come from the router")
     return ap.parse_args()
 
 
@@ -209,6 +212,13 @@ def config_json(cfg):
             "parallelism": "replicas"}
 
 
+def step_flops(cfg, with_router: bool) -> float:
+    """Algorithmic FLOPs of one step: the layer (fwd 6RHI + bwd 12RHI), plus the
+    router's three products (2TEH each) when it runs."""
+    f = cfg.flops_fwd() + cfg.flops_bwd()
+    return f + (6.0 * cfg.T * cfg.E * cfg.H if with_router else 0.0)
+
+
 def oracle_step(d, tokens: int, prec: str = "bf16"):
     """One oracle forward+backward on the first `tokens` tokens; returns (seconds, flops)."""
     import oracle
@@ -297,17 +307,44 @@ def run_ours(args):
             torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev))
     y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
+    router = None
+    if args.with_router:
+        from mixture_experts_layer_16_gb300 import MoERouter
+        from mixture_experts_layer_16_gb300.inputs import router_weights
+        router = MoERouter(cfg.T, cfg.H, cfg.E, cfg.k, device=dev)
+        g["W_router"] = bf(router_weights(cfg.E, cfg.H, seed=cfg.seed)["W_router_bits"]).to(dev)
+        dW_router = torch.empty_like(g["W_router"])
+    rev = []  # ("fwd" | "bwd", start, end) events around the router calls
 
-    def fwd():
-        layer.forward(g["x"], g["topk_idx"], g["topk_w"], g["W_gate"], g["W_up"], g["W_down"],
-                      y=y)
+    def ev_t():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        return e
 
-    def bwd():
-        layer.backward(g["dy"], g["W_gate"], g["W_up"], g["W_down"], out=outs, x=g["x"])
+    def step(x, idx, w, dy, y_out, out, after_fwd=None, timed=False):
+        """One step through the public API (with the router, it chooses idx and w).
+        Returns (event between forward and backward, forward launches, backward launches)."""
+        if router is not None:
+            e0 = ev_t() if timed else None
+            idx, w = router.forward(x, g["W_router"])
+            if timed:
+                rev.append(("fwd", e0, ev_t()))
+        layer.forward(x, idx, w, g["W_gate"], g["W_up"], g["W_down"], y=y_out)
+        n_f = B.mm_moe_last_launch_count()
+        mid = ev_t() if timed else None
+        if after_fwd is not None:
+            after_fwd()
+        layer.backward(dy, g["W_gate"], g["W_up"], g["W_down"], out=out, x=x)
+        n_b = B.mm_moe_last_launch_count()
+        if router is not None:
+            e2 = ev_t() if timed else None
+            router.backward(x, g["W_router"], idx, w, out[4], out[0], dW_router)
+            if timed:
+                rev.append(("bwd", e2, ev_t()))
+        return mid, n_f, n_b
 
     for _ in range(max(args.warmup, 0)):
-        fwd()
-        bwd()
+        step(g["x"], g["topk_idx"], g["topk_w"], g["dy"], y, outs)
     torch.cuda.synchronize()
     if layer.status() != B.MM_MOE_OK:
         raise RuntimeError("device status after warm-up: " + B.STATUS[layer.status()])
@@ -315,7 +352,7 @@ def run_ours(args):
 
     # ------------------------------------------------ timed region (device-resident inputs)
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    marks = []
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         barrier(world)
@@ -323,13 +360,10 @@ def run_ours(args):
         B.mm_moe_profile_start()
         start.record(stream)
         for i in range(K):
-            ev[i][0].record(stream)
-            fwd()
-            n_fwd_launch = B.mm_moe_last_launch_count()
-            ev[i][1].record(stream)
-            bwd()
-            n_bwd_launch = B.mm_moe_last_launch_count()
-            ev[i][2].record(stream)
+            e0 = ev_t()
+            mid, n_fwd_launch, n_bwd_launch = step(g["x"], g["topk_idx"], g["topk_w"], g["dy"],
+                                                   y, outs, timed=True)
+            marks.append((e0, mid, ev_t()))
         stop.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -337,8 +371,12 @@ def run_ours(args):
     clock = clocks.summary()
     ms_step = start.elapsed_time(stop) / K
     ms_step_max = max_over_ranks(ms_step, world, dev)
-    fwd_ms = statistics.median(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
-    bwd_ms = statistics.median(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    fwd_ms = statistics.median(m[0].elapsed_time(m[1]) for m in marks)
+    bwd_ms = statistics.median(m[1].elapsed_time(m[2]) for m in marks)
+    router_ms = None
+    if router is not None:
+        router_ms = {kind: statistics.median(a.elapsed_time(b) for kk, a, b in rev if kk == kind)
+                     for kind in ("fwd", "bwd")}
     st = layer.status()
     if st != B.MM_MOE_OK:
         raise RuntimeError("device status after timed region: " + B.STATUS[st])
@@ -348,9 +386,11 @@ def run_ours(args):
     # (y, dx, dtopk_w) back, as a training loop feeding the layer would.  The copies
     # run on a second stream, double-buffered: step i+1's inputs arrive while step i
     # computes, y leaves during the backward, dx and dtopk_w during the next step.
+    # With the router, topk_idx and topk_w are made on the device and not copied.
     e2e = None
     if not args.no_e2e:
-        pin = {k: host[k].pin_memory() for k in ("x", "topk_idx", "topk_w", "dy")}
+        names = ("x", "dy") if router is not None else ("x", "topk_idx", "topk_w", "dy")
+        pin = {k: host[k].pin_memory() for k in names}
         out_h = (torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory(),
                  torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory(),
                  torch.empty((cfg.T, cfg.k), dtype=torch.float32).pin_memory())
@@ -384,14 +424,14 @@ def run_ours(args):
                             act[1 - b][k2].copy_(t, non_blocking=True)
                         h2d_done[1 - b].record(copy)
                 a = act[b]
-                layer.forward(a["x"], a["topk_idx"], a["topk_w"], g["W_gate"], g["W_up"],
-                              g["W_down"], y=ys[b])
-                fwd_done[b].record(stream)
-                with torch.cuda.stream(copy):
-                    copy.wait_event(fwd_done[b])
-                    out_h[0].copy_(ys[b], non_blocking=True)
-                layer.backward(a["dy"], g["W_gate"], g["W_up"], g["W_down"],
-                               out=(dxs[b], outs[1], outs[2], outs[3], dtws[b]), x=a["x"])
+
+                def y_out(b=b):
+                    fwd_done[b].record(stream)
+                    with torch.cuda.stream(copy):
+                        copy.wait_event(fwd_done[b])
+                        out_h[0].copy_(ys[b], non_blocking=True)
+                step(a["x"], a.get("topk_idx"), a.get("topk_w"), a["dy"], ys[b],
+                     (dxs[b], outs[1], outs[2], outs[3], dtws[b]), after_fwd=y_out)
                 step_done[b].record(stream)
                 with torch.cuda.stream(copy):
                     copy.wait_event(step_done[b])
@@ -411,11 +451,11 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier(world)
         e2e_ms = max_over_ranks(s2.elapsed_time(t2) / K, world, dev)
-        e2e = {"value": aggregate_value(cfg.flops_fwd() + cfg.flops_bwd(), world, e2e_ms),
+        e2e = {"value": aggregate_value(step_flops(cfg, router is not None), world, e2e_ms),
                "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h,
-               "note": "activations x, topk_idx, topk_w, dy in from pinned host memory and "
-                       "y, dx, dtopk_w out, every step; copies on a second stream, "
+               "note": "activations (" + ", ".join(names) + ") in from pinned host memory "
+                       "and y, dx, dtopk_w out, every step; copies on a second stream, "
                        "double-buffered (the next step's inputs arrive during this step); "
                        "weights and weight gradients stay on the device"}
 
@@ -451,7 +491,7 @@ def run_ours(args):
                "sample": f"first {n} of {cfg.T} tokens (all {cfg.k} routed rows each, full "
                          f"expert weights), one forward+backward, numpy fp64"}
 
-    flops = cfg.flops_fwd() + cfg.flops_bwd()
+    flops = step_flops(cfg, router is not None)
     value = aggregate_value(flops, world, ms_step_max)
     bpeak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     # The path's fraction of the dense tensor peak of its precision: FP8 peak = the
@@ -460,9 +500,11 @@ def run_ours(args):
     fpeak = 2.0 * bpeak
     p_fwd = fpeak if cfg.prec == "mxfp8" else bpeak
     p_bwd = bpeak if cfg.prec == "bf16" else fpeak
-    fwd_tf = cfg.flops_fwd() / (fwd_ms * 1e-3) / 1e12
-    bwd_tf = cfg.flops_bwd() / (bwd_ms * 1e-3) / 1e12
-    p_tot = (cfg.flops_fwd() + cfg.flops_bwd()) / (cfg.flops_fwd() / p_fwd + cfg.flops_bwd() / p_bwd)
+    r_f = 2.0 * cfg.T * cfg.E * cfg.H if router is not None else 0.0  # router products
+    f_fwd, f_bwd = cfg.flops_fwd() + r_f, cfg.flops_bwd() + 2.0 * r_f
+    fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+    p_tot = (f_fwd + f_bwd) / (f_fwd / p_fwd + f_bwd / p_bwd)
     peak_fractions = {"fwd": fwd_tf / p_fwd, "bwd": bwd_tf / p_bwd, "step": value / world / p_tot,
                       "peak_fwd_tflops": p_fwd, "peak_bwd_tflops": p_bwd,
                       "note": "bf16 peak = measured sustained; FP8 peak = 2 x that (nominal ratio)"}
@@ -470,7 +512,9 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(config_json(cfg), recompute=bool(args.recompute)),
+        "config": dict(config_json(cfg), recompute=bool(args.recompute),
+                       router=router is not None),
+        "router_ms": router_ms,
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "fwd_tflops": fwd_tf,
         "bwd_tflops": bwd_tf,

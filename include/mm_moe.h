@@ -163,6 +163,39 @@ MM_MOE_API mm_moe_status mm_moe_get_routing(const mm_moe_shape* shape, const voi
                                  const int32_t** offsets, const int32_t** perm,
                                  const int32_t** inv);
 
+/* The top-k router in front of the layer, and its backward.  The pages say each
+ * token goes to a small subset of the experts (section "Why is MoE training
+ * communication-bound?"; 8 of 128 in the tested models, "TL;DR") and do not
+ * describe the router.  Readings: logits = x W_router^T (no bias); the k largest
+ * logits per token in descending order, equal logits to the lower expert index;
+ * topk_w = softmax over the chosen logits (the full softmax renormalised over them);
+ * the gradient flows through topk_w only.
+ *   shape    T, H, E, k as for the layer (I and prec ignored); k <= 32, E <= 1024,
+ *            H % 8 == 0, E % 8 == 0
+ *   x        [T, H] bf16;  W_router [E, H] bf16
+ *   logits   [T, E] fp32 out (x W_router^T, fp32 accumulation)
+ *   topk_idx [T, k] int32 out;  topk_w [T, k] fp32 out
+ * The three matrix products run on cuBLAS (bf16 operands, fp32 accumulation); its
+ * handle, made once per host thread and device, holds cuBLAS's own device workspace:
+ * the one allocation these two calls make outside the caller's buffers.  Non-finite
+ * logits give an unspecified selection.  Errors as for the layer. */
+MM_MOE_API mm_moe_status mm_moe_router_forward(const mm_moe_shape* shape, const uint16_t* x,
+                                               const uint16_t* W_router, float* logits,
+                                               int32_t* topk_idx, float* topk_w, void* stream);
+
+/*   dtopk_w   [T, k] fp32: gradient of topk_w (mm_moe_backward's dtopk_w)
+ *   dlogits   [T, E] bf16 out: the logit gradient w_j (g_j - sum_i w_i g_i) at the
+ *             chosen experts, zero elsewhere (rounded to bf16 for the GEMMs)
+ *   dx        [T, H] bf16 in/out: the router's input gradient dlogits W_router is
+ *             ADDED (fp32 sum of the bf16 value and the product, rounded to bf16),
+ *             so the layer's dx can be passed straight in
+ *   dW_router [E, H] bf16 out: dlogits^T x */
+MM_MOE_API mm_moe_status mm_moe_router_backward(const mm_moe_shape* shape, const uint16_t* x,
+                                                const uint16_t* W_router,
+                                                const int32_t* topk_idx, const float* topk_w,
+                                                const float* dtopk_w, uint16_t* dlogits,
+                                                uint16_t* dx, uint16_t* dW_router, void* stream);
+
 /* MXFP8 quantise-dequantise of a bf16 matrix, the operation the MXFP8 modes apply
  * to every GEMM operand (OCP Microscaling v1.0 MXFP8: blocks of 32 elements share
  * the power-of-two scale 2^(floor(log2 amax) - 8), 2^-127 for an all-zero block;

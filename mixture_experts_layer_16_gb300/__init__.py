@@ -8,4 +8,4 @@ from .binding import (Shape, Workspace, MoEError, make_shape, mm_moe_workspace_s
                       mm_moe_forward, mm_moe_backward, mm_moe_get_routing, mm_moe_read_status,
                       mm_moe_last_launch_count, mm_moe_profile_start, mm_moe_profile_stop,
                       mm_moe_kernel_name, mm_moe_kernel_count)
-from .layer import MoELayer  # noqa: F401,E402
+from .layer import MoELayer, MoERouter  # noqa: F401,E402

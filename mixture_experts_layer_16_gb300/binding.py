@@ -23,7 +23,8 @@ MM_MOE_OK, MM_MOE_EINVAL, MM_MOE_ENOTSUP, MM_MOE_EBADIDX, MM_MOE_ETIMEOUT, MM_MO
 EXPORTS = ("mm_moe_workspace_size", "mm_moe_forward", "mm_moe_backward", "mm_moe_get_routing",
            "mm_moe_read_status", "mm_moe_last_launch_count", "mm_moe_profile_start",
            "mm_moe_profile_stop", "mm_moe_kernel_name", "mm_moe_kernel_count",
-           "mm_moe_route_noalloc", "mm_moe_mx_qdq")
+           "mm_moe_route_noalloc", "mm_moe_mx_qdq", "mm_moe_router_forward",
+           "mm_moe_router_backward")
 
 
 class MoEError(RuntimeError):
@@ -74,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.mm_moe_kernel_count.argtypes = []
         L.mm_moe_route_noalloc.argtypes = [sp] + [_vp] * 6
         L.mm_moe_mx_qdq.argtypes = [_vp, _vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _vp]
+        L.mm_moe_router_forward.argtypes = [sp] + [_vp] * 6
+        L.mm_moe_router_backward.argtypes = [sp] + [_vp] * 9
         for fn in EXPORTS:
             getattr(L, fn).restype = ctypes.c_int
         L.mm_moe_kernel_name.restype = ctypes.c_char_p
@@ -162,6 +165,25 @@ def mm_moe_mx_qdq(inp, out, axis: int, stream=None) -> None:
         raise ValueError("out must match inp")
     _check("mm_moe_mx_qdq", lib().mm_moe_mx_qdq(_ptr(inp), _ptr(out), inp.shape[0],
                                                 inp.shape[1], int(axis), _stream(stream)))
+
+
+def mm_moe_router_forward(shape: Shape, x, W_router, logits, topk_idx, topk_w, stream=None,
+                          check: bool = True) -> int:
+    st = lib().mm_moe_router_forward(ctypes.byref(shape), _ptr(x), _ptr(W_router), _ptr(logits),
+                                     _ptr(topk_idx), _ptr(topk_w), _stream(stream))
+    if check:
+        _check("mm_moe_router_forward", st)
+    return st
+
+
+def mm_moe_router_backward(shape: Shape, x, W_router, topk_idx, topk_w, dtopk_w, dlogits, dx,
+                           dW_router, stream=None, check: bool = True) -> int:
+    st = lib().mm_moe_router_backward(ctypes.byref(shape), _ptr(x), _ptr(W_router),
+                                      _ptr(topk_idx), _ptr(topk_w), _ptr(dtopk_w),
+                                      _ptr(dlogits), _ptr(dx), _ptr(dW_router), _stream(stream))
+    if check:
+        _check("mm_moe_router_backward", st)
+    return st
 
 
 def mm_moe_read_status(scratch, stream=None) -> int:

@@ -724,7 +724,15 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   GemmParams p;
   memset(&p, 0, sizeof(p));
   const char* saved = g.saved;
-  const int ctas = L.pad == 2 * BM ? 2 : 1;
+  // SM pairs where the layout allows them; the weight-gradient GEMMs (K = an
+  // expert's rows) go back to single-SM tiles when experts average fewer than
+  // WGRAD_PAIR_MIN_ROWS rows: their short main loops leave pair tiles waiting on
+  // each other and on the epilogue (4k-token 30B-shape layer: 0.52 ms on pairs,
+  // 0.42 ms on single SMs; 16k tokens: pairs 5 % faster)
+  constexpr int64_t WGRAD_PAIR_MIN_ROWS = 512;
+  const bool per_expert = g.kind == GEMM_WGRAD_DOWN || g.kind == GEMM_WGRAD_GATEUP;
+  const int ctas =
+      (L.pad == 2 * BM && !(per_expert && L.R < WGRAD_PAIR_MIN_ROWS * L.E)) ? 2 : 1;
   p.H = static_cast<int>(L.H);
   p.I = static_cast<int>(L.I);
   p.E = static_cast<int>(L.E);

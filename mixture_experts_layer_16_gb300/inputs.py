@@ -171,3 +171,11 @@ def custom_inputs(T: int, H: int, I: int, E: int, k: int, seed: int = 0,
     if idx is not None:
         d["topk_idx"] = np.ascontiguousarray(idx, dtype=np.int32)
     return d
+
+
+def router_weights(E: int, H: int, seed: int = 0) -> Dict[str, np.ndarray]:
+    """W_router [E, H] ~ N(0, 0.02), rounded to bf16 (bits and exact values); its own
+    stream, so the layer's inputs do not change."""
+    rng = np.random.default_rng(np.random.PCG64(1000003 + seed))
+    bits = bf16_bits(rng.standard_normal((E, H)).astype(np.float32) * np.float32(0.02))
+    return dict(W_router_bits=bits, W_router=bf16_to_f32(bits).astype(np.float64))

@@ -96,3 +96,45 @@ class MoELayer:
     def status(self, stream=None) -> int:
         """Synchronise and return the device status word (binding.STATUS names it)."""
         return B.mm_moe_read_status(self.ws.scratch, stream)
+
+
+class MoERouter:
+    """The top-k router in front of MoELayer: topk_idx, topk_w from x and W_router
+    [E, H], and the backward from the layer's dtopk_w (adds its dx, returns
+    dW_router).  Every step runs in the library (mm_moe_router_forward/backward)."""
+
+    def __init__(self, T: int, H: int, E: int, k: int, device: Optional[torch.device] = None):
+        self.T, self.H, self.E, self.k = T, H, E, k
+        device = torch.device("cuda" if device is None else device)
+        if device.type == "cuda" and device.index is None:
+            device = torch.device("cuda", torch.cuda.current_device())
+        self.device = device
+        self.shape = B.make_shape(T, H, 64, E, k)   # I is not used by the router
+        self.logits = torch.empty((T, E), dtype=torch.float32, device=device)
+        self.dlogits = torch.empty((T, E), dtype=torch.bfloat16, device=device)
+
+    def forward(self, x, W_router, stream=None):
+        """(topk_idx [T, k] int32, topk_w [T, k] fp32); the logits stay in self.logits."""
+        d, bf = self.device, torch.bfloat16
+        _need(x, "x", (self.T, self.H), bf, d)
+        _need(W_router, "W_router", (self.E, self.H), bf, d)
+        idx = torch.empty((self.T, self.k), dtype=torch.int32, device=d)
+        w = torch.empty((self.T, self.k), dtype=torch.float32, device=d)
+        B.mm_moe_router_forward(self.shape, x, W_router, self.logits, idx, w, stream)
+        return idx, w
+
+    def backward(self, x, W_router, topk_idx, topk_w, dtopk_w, dx, dW_router=None, stream=None):
+        """Adds the router's input gradient to dx (in place) and returns dW_router."""
+        d, bf = self.device, torch.bfloat16
+        _need(x, "x", (self.T, self.H), bf, d)
+        _need(W_router, "W_router", (self.E, self.H), bf, d)
+        _need(topk_idx, "topk_idx", (self.T, self.k), torch.int32, d)
+        _need(topk_w, "topk_w", (self.T, self.k), torch.float32, d)
+        _need(dtopk_w, "dtopk_w", (self.T, self.k), torch.float32, d)
+        _need(dx, "dx", (self.T, self.H), bf, d)
+        if dW_router is None:
+            dW_router = torch.empty((self.E, self.H), dtype=bf, device=d)
+        _need(dW_router, "dW_router", (self.E, self.H), bf, d)
+        B.mm_moe_router_backward(self.shape, x, W_router, topk_idx, topk_w, dtopk_w,
+                                 self.dlogits, dx, dW_router, stream)
+        return dW_router

@@ -95,6 +95,13 @@ def test_forward_backward_reject_before_launch(lib):
     bad_prec = B.make_shape(64, 128, 64, 8, 2, 3)
     assert lib.mm_moe_forward(ctypes.byref(bad_prec), *fake) == B.MM_MOE_EINVAL
     assert lib.mm_moe_get_routing(ctypes.byref(s), None, None, None, None) == B.MM_MOE_EINVAL
+    # the router: NULL pointers, k above 32, E not a multiple of 8
+    r = B.make_shape(64, 128, 64, 16, 4)
+    assert lib.mm_moe_router_forward(ctypes.byref(r), *([None] * 6)) == B.MM_MOE_EINVAL
+    assert lib.mm_moe_router_backward(ctypes.byref(r), *([None] * 9)) == B.MM_MOE_EINVAL
+    fake6 = [4096 * (i + 1) for i in range(6)]
+    for bad in (B.make_shape(64, 128, 64, 64, 33), B.make_shape(64, 128, 64, 12, 4)):
+        assert lib.mm_moe_router_forward(ctypes.byref(bad), *fake6) == B.MM_MOE_EINVAL
     # the quantiser: NULL, misaligned, ragged blocks and unknown axes
     assert lib.mm_moe_mx_qdq(None, None, 32, 32, 1, None) == B.MM_MOE_EINVAL
     assert lib.mm_moe_mx_qdq(4096, 4098, 32, 32, 1, None) == B.MM_MOE_EINVAL

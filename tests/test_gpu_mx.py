@@ -30,7 +30,7 @@ SMALL = [
     (1000, 384, 128, 16, 4, "uniform", 22),    # 128-wide N tiles over H, ragged tails
     (777, 512, 256, 32, 8, "zipf", 23),        # skewed routing, SM-pair tiles
     (900, 512, 256, 32, 8, "zipf_trunc", 24),  # experts with no token
-    (1500, 512, 384, 16, 4, "zipf", 25),       # I = 384 pair tiles
+    (2200, 512, 384, 16, 4, "zipf", 25),       # I = 384 pair tiles, pair wgrad
 ]
 
 

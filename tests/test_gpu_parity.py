@@ -36,10 +36,11 @@ SMALL = [
     (1000, 384, 128, 16, 4, "uniform", 3),   # H=384: 128-wide N tiles for the H dimension
     (777, 512, 256, 32, 8, "zipf", 4),       # skewed routing
     (513, 256, 64, 12, 3, "zipf_trunc", 5),  # some experts receive no token
-    # SM-pair tiles (H % 256 == 0, I % 128 == 0); experts padded to 256 rows
-    (600, 256, 128, 8, 2, "uniform", 11),    # 128-wide pair tiles over I
-    (1500, 512, 384, 16, 4, "zipf", 12),     # I = 384: 128-wide pair tiles over I
-    (2000, 768, 256, 8, 2, "uniform", 13),   # three 256-wide N tiles over H
+    # SM-pair tiles (H % 256 == 0, I % 128 == 0); experts padded to 256 rows; the
+    # weight-gradient GEMMs run on pairs from 512 routed rows per expert on average
+    (600, 256, 128, 8, 2, "uniform", 11),    # 128-wide pair tiles over I, single-SM wgrad
+    (2200, 512, 384, 16, 4, "zipf", 12),     # I = 384: 128-wide pair tiles; pair wgrad
+    (2100, 768, 256, 8, 2, "uniform", 13),   # three 256-wide N tiles over H; pair wgrad
     (900, 512, 256, 32, 8, "zipf_trunc", 14),  # pairs with empty experts
 ]
 
