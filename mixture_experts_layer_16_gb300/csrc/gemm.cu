@@ -14,14 +14,17 @@
 //
 // CTAS = 2 runs each tile on an SM pair: the two CTAs of a 2-CTA cluster each stage
 // 128 rows of A and half of the N columns of B, and one tcgen05.mma.cta_group::2 of
-// M = 256 reads both halves.  CTAS = 1 runs 128-row tiles on single SMs.
+// M = 256 reads both halves.  CTAS = 1 runs 128-row tiles on single SMs (shapes the
+// pair tiles do not divide, and the weight-gradient GEMMs of small experts).  MX = 1
+// (gate/up of the MXFP8 forward) also writes a quantised in 32-blocks along I.
 //
 // Roles (256 threads per CTA): warp 0 lane 0 = TMA producer, warp 1 lane 0 of the
 // pair's rank-0 CTA = MMA issuer, warp 2 = TMEM allocator, warps 4..7 = epilogue
 // (warp 4+q reads TMEM lanes 32q..32q+31, i.e. the CTA's tile rows 32q..32q+31).
 // The epilogue moves data through per-warp 32 x 32 blocks in shared memory: outputs
-// leave by TMA stores and the dSwiGLU inputs arrive by TMA loads.  Every wait is bounded: on expiry the
-// kernel records MM_MOE_ETIMEOUT in the status word and every role unwinds.
+// leave by TMA stores and the dSwiGLU inputs arrive by TMA loads.  Every wait is
+// bounded: on expiry the kernel records MM_MOE_ETIMEOUT in the status word and every
+// role unwinds.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
