@@ -87,6 +87,20 @@ def test_k1_unit_weight():
     check_full(d, res)
 
 
+@pytest.mark.parametrize("T,H,I,E,k,routing,seed", [
+    (1, 256, 128, 128, 8, "uniform", 15),     # one token: 8 experts with one row, 120 empty
+    (300, 128, 64, 1024, 4, "uniform", 16),   # the largest expert count
+    (40, 128, 64, 8, 8, "uniform", 17),       # k = E: every token goes to every expert
+    (3, 512, 256, 4, 2, "uniform", 18),       # SM-pair tiles holding 1-2 rows
+])
+def test_degenerate_shapes(T, H, I, E, k, routing, seed):
+    d = custom_inputs(T, H, I, E, k, seed=seed, routing=routing)
+    res, _, _ = G.run(d)
+    assert res["status"] == 0
+    check_routing(res, d["topk_idx"], E)
+    check_full(d, res)
+
+
 def test_determinism():
     d = custom_inputs(700, 256, 128, 16, 4, seed=9, routing="zipf")
     r1, layer, dev = G.run(d)
