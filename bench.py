@@ -219,6 +219,9 @@ def step_flops(cfg, with_router: bool) -> float:
     return f + (6.0 * cfg.T * cfg.E * cfg.H if with_router else 0.0)
 
 
+LAST_ORACLE_SPLIT = [0.0, 0.0]  # seconds of the last oracle_step's forward and backward
+
+
 def oracle_step(d, tokens: int, prec: str = "bf16"):
     """One oracle forward+backward on the first `tokens` tokens; returns (seconds, flops)."""
     import oracle
@@ -227,9 +230,11 @@ def oracle_step(d, tokens: int, prec: str = "bf16"):
     t0 = time.perf_counter()
     f = oracle.forward(sub["x"], sub["topk_idx"], sub["topk_w"], d["W_gate"], d["W_up"],
                        d["W_down"], prec)
+    t1 = time.perf_counter()
     oracle.backward(sub["dy"], sub["x"], sub["topk_idx"], sub["topk_w"], d["W_gate"], d["W_up"],
                     d["W_down"], prec, fwd=f)
     dt = time.perf_counter() - t0
+    LAST_ORACLE_SPLIT[:] = [t1 - t0, dt - (t1 - t0)]
     k = d["topk_idx"].shape[1]
     H = d["x"].shape[1]
     I = d["W_gate"].shape[1]
@@ -487,7 +492,8 @@ def run_ours(args):
         n = min(args.cpu_sample_tokens, cfg.T)
         dt, fl = oracle_step(d, n, cfg.prec)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
-               "kind": "oracle", "seconds": dt,
+               "kind": "oracle", "seconds": dt, "fwd_seconds": LAST_ORACLE_SPLIT[0],
+               "bwd_seconds": LAST_ORACLE_SPLIT[1],
                "sample": f"first {n} of {cfg.T} tokens (all {cfg.k} routed rows each, full "
                          f"expert weights), one forward+backward, numpy fp64"}
 
