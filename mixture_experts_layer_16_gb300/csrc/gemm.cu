@@ -32,6 +32,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -58,6 +59,7 @@ struct GemmParams {
   int k_iters;  // K iterations per tile (grouped kinds)
   int n_pw;
   int max_tiles;
+  int stall;  // failure-path test: CTA 0 arms its first stage but issues no copy
   const int* meta;
   const int* tile_expert;
   const int* tile_rows;
@@ -502,8 +504,11 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
         }
         uint8_t* sa = smem + stage * C::STAGE_BYTES;
         if (rank == 0) ptx::mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES * CTAS);
-        issue_loads<KIND, BN, CTAS>(p, ti, kb, sa, sa + C::A_BYTES, lead_full0 + stage * 8u,
-                                    rank);
+        // (with p.stall the first stage of CTA 0 never fills: the MMA issuer's bounded
+        // wait runs out and every role unwinds, the path a lost copy would take)
+        if (!(p.stall && blockIdx.x == 0 && t == cluster && kb == 0))
+          issue_loads<KIND, BN, CTAS>(p, ti, kb, sa, sa + C::A_BYTES, lead_full0 + stage * 8u,
+                                      rank);
         last_parity[stage] = static_cast<int>(phase);
         if (++stage == C::STAGES) {
           stage = 0;
@@ -753,6 +758,10 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   p.out1 = g.out1;
   p.outf = g.outf;
   p.status = reinterpret_cast<DevStatus*>(g.scratch + L.status);
+  // Failure-path test hook: MM_MOE_TEST_STALL_GEMM=<kind> makes that GEMM's first
+  // stage on CTA 0 never fill (read at every launch; unset, it does nothing)
+  if (const char* v = std::getenv("MM_MOE_TEST_STALL_GEMM"))
+    p.stall = (v[0] >= '0' && v[0] <= '5' && v[1] == '\0' && v[0] - '0' == g.kind) ? 1 : 0;
   const uint64_t Rp = static_cast<uint64_t>(L.Rp), H = L.H, I = L.I, E = L.E;
   bool ok = true;
   int bn = 0;
