@@ -27,9 +27,11 @@ Readings where the pages are silent: SwiGLU = silu(gate) * up; topk_w is used
 as given (no renormalisation) and applied after the down projection; rows of one
 expert keep ascending flat index; MXFP8 follows oracle.mx, each GEMM operand
 quantised in 32-blocks along that GEMM's contraction axis (token-axis blocks
-start at the expert's first row, the tail zero-padded).  The layer keeps its
+start at the expert's first row, the tail zero-padded); blockwise FP8 (fp8_block,
+forward and backward) follows oracle.fp8block: activations in 128-blocks along the
+contraction axis, weights in 128 x 128 blocks.  The layer keeps its
 intermediates h = [g | u], a, w*a and dh = [dg | du] in bf16; in the modes with
-an MXFP8 backward (mxfp8, fp8_bwd) the e4m3 rounding of an element is decided on
+an FP8 backward (mxfp8, fp8_bwd, fp8_block) the e4m3 rounding of an element is decided on
 that stored bf16 value, so those modes round each of these tensors to bf16
 where the layer stores it (the backward reads g, u and a as saved).  The BF16
 mode keeps every intermediate in fp64.
@@ -42,9 +44,10 @@ from typing import Dict, Optional, Sequence
 
 import numpy as np
 
+from .fp8block import qdq_1d as block_qdq_1d, qdq_2d as block_qdq_2d
 from .mx import bf16_round, mx_qdq
 
-PRECISIONS = ("bf16", "mxfp8", "fp8_bwd")
+PRECISIONS = ("bf16", "mxfp8", "fp8_bwd", "fp8_block")
 
 
 def sigmoid(z):
@@ -87,7 +90,17 @@ def route(topk_idx: np.ndarray, E: int):
 
 
 def _q(v, axis, on):
-    return mx_qdq(v, axis) if on else v
+    """An activation operand quantised along its contraction axis: on = False (as is),
+    "mx" (MXFP8, 32-blocks) or "block" (blockwise FP8, 128-blocks)."""
+    if not on:
+        return v
+    return block_qdq_1d(v, axis) if on == "block" else mx_qdq(v, axis)
+
+
+def _qw(W, axis, on):
+    """A weight operand: as an activation under MXFP8, 128 x 128 blocks (whatever the
+    contraction axis) under blockwise FP8."""
+    return block_qdq_2d(W) if on == "block" else _q(W, axis, on)
 
 
 def _stored(v, on):
@@ -96,19 +109,22 @@ def _stored(v, on):
 
 
 def _quant_flags(prec: str):
+    """The forward's and the backward's quantisation: False, "mx" or "block"."""
     if prec not in PRECISIONS:
         raise ValueError(f"unknown precision {prec!r}")
-    return prec == "mxfp8", prec in ("mxfp8", "fp8_bwd")
+    if prec == "fp8_block":
+        return "block", "block"
+    return ("mx" if prec == "mxfp8" else False), ("mx" if prec in ("mxfp8", "fp8_bwd") else False)
 
 
 def expert_forward(xe, Wg_e, Wu_e, Wd_e, prec: str = "bf16"):
     """One expert on its rows xe [n, H]: returns g, u, a [n, I] and o [n, H]."""
     qf, _ = _quant_flags(prec)
     xq = _q(xe, 1, qf)
-    g = xq @ _q(Wg_e, 1, qf).T
-    u = xq @ _q(Wu_e, 1, qf).T
+    g = xq @ _qw(Wg_e, 1, qf).T
+    u = xq @ _qw(Wu_e, 1, qf).T
     a = swiglu(g, u)
-    o = _q(_stored(a, qf), 1, qf) @ _q(Wd_e, 1, qf).T
+    o = _q(_stored(a, qf), 1, qf) @ _qw(Wd_e, 1, qf).T
     return g, u, a, o
 
 
@@ -120,12 +136,12 @@ def expert_backward(xe, dye, we, g, u, a, Wg_e, Wu_e, Wd_e, prec: str = "bf16"):
     Returns dxe [n, H], dWg_e, dWu_e [I, H], dWd_e [H, I], dw [n]."""
     _, qb = _quant_flags(prec)
     g, u, a = _stored(g, qb), _stored(u, qb), _stored(a, qb)   # as the forward saved them
-    gp = _q(dye, 1, qb) @ _q(Wd_e, 0, qb)                 # g' = dy W_down[e]
+    gp = _q(dye, 1, qb) @ _qw(Wd_e, 0, qb)                # g' = dy W_down[e]
     dw = np.sum(a * gp, axis=1)
     da = we[:, None] * gp
     dg, du = swiglu_grad(g, u, da)
     dg, du = _stored(dg, qb), _stored(du, qb)
-    dxe = _q(dg, 1, qb) @ _q(Wg_e, 0, qb) + _q(du, 1, qb) @ _q(Wu_e, 0, qb)
+    dxe = _q(dg, 1, qb) @ _qw(Wg_e, 0, qb) + _q(du, 1, qb) @ _qw(Wu_e, 0, qb)
     xq = _q(xe, 0, qb)
     dWg_e = _q(dg, 0, qb).T @ xq
     dWu_e = _q(du, 0, qb).T @ xq
