@@ -504,7 +504,7 @@ def run_ours(args):
     # measured bf16 peak x 2 (nominal 4.5 / 2.25 PFLOP/s); fp8_bwd blends the two,
     # total FLOP / (fwd FLOP / P_bf16 + bwd FLOP / P_fp8).
     fpeak = 2.0 * bpeak
-    p_fwd = fpeak if cfg.prec == "mxfp8" else bpeak
+    p_fwd = fpeak if cfg.prec in ("mxfp8", "fp8_block") else bpeak
     p_bwd = bpeak if cfg.prec == "bf16" else fpeak
     r_f = 2.0 * cfg.T * cfg.E * cfg.H if router is not None else 0.0  # router products
     f_fwd, f_bwd = cfg.flops_fwd() + r_f, cfg.flops_bwd() + 2.0 * r_f

@@ -63,13 +63,20 @@ extern "C" {
  *                   weight-gradient GEMMs start at each expert's first row, the
  *                   last one zero-padded); fp32 accumulation.
  *   MM_MOE_FP8_BWD  the BF16 forward and the MXFP8 backward.
+ *   MM_MOE_FP8_BLOCK blockwise FP8 (the pages' Hopper precision, in the form
+ *                   Blackwell tensor cores take) in the forward and the backward:
+ *                   activations in 128-element blocks along each GEMM's K (128-row
+ *                   token blocks for the weight gradients), weights in 128 x 128
+ *                   blocks, one power-of-two scale 2^ceil(log2(amax / 448)) per
+ *                   block, e4m3 elements; needs I % 128 == 0.
  * Stored tensors (h, a, the outputs and the gradients) stay bf16 in every mode,
  * and the quantised operand copies live in `scratch` (which is larger for the
  * two MXFP8 modes). */
 typedef enum {
   MM_MOE_BF16 = 0,
   MM_MOE_MXFP8 = 1,
-  MM_MOE_FP8_BWD = 2
+  MM_MOE_FP8_BWD = 2,
+  MM_MOE_FP8_BLOCK = 3
 } mm_moe_precision;
 
 typedef enum {
@@ -212,6 +219,20 @@ MM_MOE_API mm_moe_status mm_moe_router_backward(const mm_moe_shape* shape, const
  * failed launch. */
 MM_MOE_API mm_moe_status mm_moe_mx_qdq(const uint16_t* in, uint16_t* out, int64_t rows,
                                        int64_t cols, int axis, void* stream);
+
+/* Blockwise FP8 quantise-dequantise of a bf16 matrix, the operation
+ * MM_MOE_FP8_BLOCK applies to every GEMM operand: one power-of-two scale
+ * 2^ceil(log2(amax / 448)) per block (2^-127 for an all-zero block), elements
+ * rounded to e4m3 (nearest even); exported for callers that keep such copies of
+ * their own tensors.
+ *   in, out  [rows, cols] bf16, device, 16-byte aligned; out may equal in
+ *   layout   0: 128-element blocks along each row (cols % 128 == 0);
+ *            1: 128-element blocks down each column (rows % 128 == 0, cols % 8 == 0);
+ *            2: 128 x 128 tiles (rows % 128 == 0, cols % 128 == 0)
+ * Errors as for mm_moe_mx_qdq. */
+MM_MOE_API mm_moe_status mm_moe_fp8_block_qdq(const uint16_t* in, uint16_t* out,
+                                              int64_t rows, int64_t cols, int layout,
+                                              void* stream);
 
 /* Synchronises `stream`, then returns the device status word of `scratch`
  * (MM_MOE_OK, MM_MOE_EBADIDX or MM_MOE_ETIMEOUT), or MM_MOE_ECUDA when the

@@ -13,8 +13,9 @@ from typing import Optional, Tuple
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmm_moe.so")
 
-MM_MOE_BF16, MM_MOE_MXFP8, MM_MOE_FP8_BWD = 0, 1, 2
-PRECISION = {"bf16": MM_MOE_BF16, "mxfp8": MM_MOE_MXFP8, "fp8_bwd": MM_MOE_FP8_BWD}
+MM_MOE_BF16, MM_MOE_MXFP8, MM_MOE_FP8_BWD, MM_MOE_FP8_BLOCK = 0, 1, 2, 3
+PRECISION = {"bf16": MM_MOE_BF16, "mxfp8": MM_MOE_MXFP8, "fp8_bwd": MM_MOE_FP8_BWD,
+             "fp8_block": MM_MOE_FP8_BLOCK}
 STATUS = {0: "MM_MOE_OK", 1: "MM_MOE_EINVAL", 2: "MM_MOE_ENOTSUP", 3: "MM_MOE_EBADIDX",
           4: "MM_MOE_ETIMEOUT", 5: "MM_MOE_ECUDA"}
 MM_MOE_OK, MM_MOE_EINVAL, MM_MOE_ENOTSUP, MM_MOE_EBADIDX, MM_MOE_ETIMEOUT, MM_MOE_ECUDA = range(6)
@@ -24,7 +25,7 @@ EXPORTS = ("mm_moe_workspace_size", "mm_moe_forward", "mm_moe_backward", "mm_moe
            "mm_moe_read_status", "mm_moe_last_launch_count", "mm_moe_profile_start",
            "mm_moe_profile_stop", "mm_moe_kernel_name", "mm_moe_kernel_count",
            "mm_moe_route_noalloc", "mm_moe_mx_qdq", "mm_moe_router_forward",
-           "mm_moe_router_backward")
+           "mm_moe_router_backward", "mm_moe_fp8_block_qdq")
 
 
 class MoEError(RuntimeError):
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.mm_moe_kernel_count.argtypes = []
         L.mm_moe_route_noalloc.argtypes = [sp] + [_vp] * 6
         L.mm_moe_mx_qdq.argtypes = [_vp, _vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _vp]
+        L.mm_moe_fp8_block_qdq.argtypes = [_vp, _vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                           _vp]
         L.mm_moe_router_forward.argtypes = [sp] + [_vp] * 6
         L.mm_moe_router_backward.argtypes = [sp] + [_vp] * 9
         for fn in EXPORTS:
@@ -165,6 +168,19 @@ def mm_moe_mx_qdq(inp, out, axis: int, stream=None) -> None:
         raise ValueError("out must match inp")
     _check("mm_moe_mx_qdq", lib().mm_moe_mx_qdq(_ptr(inp), _ptr(out), inp.shape[0],
                                                 inp.shape[1], int(axis), _stream(stream)))
+
+
+def mm_moe_fp8_block_qdq(inp, out, layout: int, stream=None) -> None:
+    """Blockwise FP8 quantise-dequantise of a 2-D bf16 CUDA tensor into `out` (may be
+    `inp`): 128-element blocks along rows (layout 0), down columns (1), or 128 x 128
+    tiles (2)."""
+    import torch
+    if inp.dim() != 2 or inp.dtype != torch.bfloat16 or not inp.is_contiguous():
+        raise ValueError("inp must be a contiguous 2-D bf16 tensor")
+    if out.shape != inp.shape or out.dtype != inp.dtype or not out.is_contiguous():
+        raise ValueError("out must match inp")
+    _check("mm_moe_fp8_block_qdq", lib().mm_moe_fp8_block_qdq(
+        _ptr(inp), _ptr(out), inp.shape[0], inp.shape[1], int(layout), _stream(stream)))
 
 
 def mm_moe_router_forward(shape: Shape, x, W_router, logits, topk_idx, topk_w, stream=None,

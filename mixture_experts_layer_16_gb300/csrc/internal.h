@@ -50,7 +50,15 @@ struct Layout {
   // token-axis copy over x_perm, so q_xc is unused.
   size_t q_wdc, q_wgc, q_wuc, q_dyc, q_dhc, q_xc;
   bool w_in_saved;
+  // quantisation of the forward's and the backward's GEMM operands: QS_NONE, QS_MX
+  // (MXFP8) or QS_BLOCK (blockwise FP8, whose one 128 x 128-block copy of each weight
+  // serves every GEMM: q_wgc, q_wuc, q_wdc, in saved when w_in_saved, else at the
+  // front of scratch, w_common)
+  int qf, qb;
+  bool w_common;
 };
+
+enum { QS_NONE = 0, QS_MX = 1, QS_BLOCK = 2 };
 
 // meta[] slots in `saved`
 constexpr int META_NUM_TILES = 0;
@@ -89,6 +97,9 @@ enum KernelId {
   K_GEMM_WGRAD_GATEUP,
   K_MX_QDQ_ROWS,
   K_MX_QDQ_COLS,
+  K_FB_ROWS,
+  K_FB_COLS,
+  K_FB_TILES,
   K_COUNT
 };
 
@@ -133,6 +144,15 @@ cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slot
 cudaError_t launch_mx_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
                           int64_t cols, bool along_rows, const int* meta,
                           uint16_t* out_rows = nullptr);
+
+// Blockwise FP8 quantise-dequantise of a bf16 [rows, cols] tensor (power-of-two scale
+// 2^ceil(log2(amax / 448)) per block), written as bf16: 128-element blocks along each
+// row (FB_ROWS), down each column (FB_COLS; a non-null out_rows also receives the row
+// blocks of the same read; `meta` as for launch_mx_qdq), or 128 x 128 tiles
+// (FB_TILES).  out / out_rows may equal in.
+enum { FB_ROWS = 0, FB_COLS = 1, FB_TILES = 2 };
+cudaError_t launch_fb_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
+                          int64_t cols, int layout, const int* meta, uint16_t* out_rows);
 
 enum GemmKind {
   GEMM_GATEUP = 0,        // x_perm . [W_gate|W_up]^T  -> SwiGLU epilogue (h, a)

@@ -26,7 +26,8 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   if (s->k > s->E || s->E > MAX_E) return MM_MOE_EINVAL;
   if (s->H % 128 != 0 || s->I % 64 != 0) return MM_MOE_EINVAL;
   if ((s->flags & ~MM_MOE_RECOMPUTE) != 0) return MM_MOE_EINVAL;
-  if (s->prec < MM_MOE_BF16 || s->prec > MM_MOE_FP8_BWD) return MM_MOE_EINVAL;
+  if (s->prec < MM_MOE_BF16 || s->prec > MM_MOE_FP8_BLOCK) return MM_MOE_EINVAL;
+  if (s->prec == MM_MOE_FP8_BLOCK && s->I % 128 != 0) return MM_MOE_EINVAL;  // 128 x 128 blocks
   if (s->T > (int64_t{1} << 31) / s->k) return MM_MOE_EINVAL;
   L->T = s->T;
   L->H = s->H;
@@ -40,6 +41,8 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->NT = L->Rp / BM;
   if (L->Rp >= (int64_t{1} << 31)) return MM_MOE_EINVAL;
   L->recompute = (s->flags & MM_MOE_RECOMPUTE) != 0;
+  L->qf = s->prec == MM_MOE_MXFP8 ? QS_MX : s->prec == MM_MOE_FP8_BLOCK ? QS_BLOCK : QS_NONE;
+  L->qb = s->prec == MM_MOE_BF16 ? QS_NONE : s->prec == MM_MOE_FP8_BLOCK ? QS_BLOCK : QS_MX;
   L->nblk = (L->R + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
   L->n_pw = L->I / pick_bn(L->I);
   const size_t A = 1024;
@@ -70,10 +73,11 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
     L->h = take(2 * Rp * 2 * I);
     L->a = take(2 * Rp * I);
   }
-  // full MXFP8: the backward's quantised weight copies are made by the forward's
-  // two-way pass over each weight and kept here (not under recompute)
+  // a quantised forward that keeps its activations also makes the backward's
+  // weight copies (MXFP8: the forward's two-way passes; blockwise: the one copy)
   const size_t W = 2 * E * I * H;  // bytes of one expert weight tensor
-  L->w_in_saved = s->prec == MM_MOE_MXFP8 && !L->recompute;
+  L->w_in_saved = L->qf != QS_NONE && !L->recompute;
+  L->w_common = L->qf == QS_BLOCK && L->recompute;
   L->q_wdc = L->q_wgc = L->q_wuc = 0;
   if (L->w_in_saved) {
     L->q_wdc = take(W);
@@ -90,13 +94,20 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
     L->h = take(2 * Rp * 2 * I);
     L->a = take(2 * Rp * I);
   }
+  if (L->w_common) {  // blockwise weights under recompute: made by each pass, used by all
+    L->q_wdc = take(W);
+    L->q_wgc = take(W);
+    L->q_wuc = take(W);
+  }
   const size_t common = o;
   L->ys = take(2 * Rp * H);
-  // MXFP8 operand copies (bf16 holding the dequantised e4m3 values exactly)
+  // quantised operand copies of the forward (bf16 holding the dequantised values)
   L->q_x = L->q_a = L->q_wg = L->q_wu = L->q_wd = 0;
-  if (s->prec == MM_MOE_MXFP8) {
+  if (L->qf != QS_NONE) {
     L->q_x = take(2 * Rp * H);
     L->q_a = take(2 * Rp * I);
+  }
+  if (L->qf == QS_MX) {  // the forward's MXFP8 weights (blocks along their forward K)
     L->q_wg = take(W);
     L->q_wu = take(W);
     L->q_wd = take(W);
@@ -109,13 +120,15 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->pw = take(4 * Rp * static_cast<size_t>(L->n_pw));
   L->dxs = take(2 * Rp * H);
   L->q_dyc = L->q_dhc = L->q_xc = 0;
-  if (s->prec != MM_MOE_BF16 && !L->w_in_saved) {  // left to the backward
-    L->q_wdc = take(W);
-    L->q_wgc = take(W);
-    L->q_wuc = take(W);
+  if (L->qb != QS_NONE && !L->w_in_saved) {  // left to the backward
+    if (!L->w_common) {
+      L->q_wdc = take(W);
+      L->q_wgc = take(W);
+      L->q_wuc = take(W);
+    }
     L->q_xc = take(2 * Rp * H);
   }
-  if (s->prec != MM_MOE_BF16) {
+  if (L->qb != QS_NONE) {
     L->q_dyc = take(2 * Rp * H);
     L->q_dhc = take(2 * Rp * 2 * I);
   }
@@ -185,39 +198,67 @@ static bool side_stream(SideStream* out) {
     if ((expr) != cudaSuccess) return MM_MOE_ECUDA; \
   } while (0)
 
-// The forward's gate/up stage on x_perm: h = [g | u] and a = silu(g) * u.  Under
-// full MXFP8 (mx) its operands are first quantised along H: with `keep` (the forward
-// of a layer that keeps its activations) by two-way passes that also leave x_perm
-// quantised along tokens in place and the weights along their backward K in saved
-// (wsaved); otherwise by row passes.  `emit_qa`: the epilogue also writes a
-// quantised along I (the down projection's operand).  The backward under
-// MM_MOE_RECOMPUTE calls it with the forward's arguments and gets h and a bit for
-// bit (the same kernels on the same inputs).
-static mm_moe_status gateup_stage(const Ctx& c, const Layout& L, bool mx, bool keep,
-                                  bool emit_qa, uint16_t* x_perm, const uint16_t* W_gate,
+// Quantisation of an activation operand under scheme qs (QS_MX: 32-element blocks,
+// QS_BLOCK: 128-element blocks): along rows, or down columns (with out_rows non-null
+// the same read also writes the row blocks there).
+static cudaError_t act_rows(const Ctx& c, int qs, const uint16_t* in, uint16_t* out,
+                            int64_t rows, int64_t cols, const int* meta) {
+  return qs == QS_BLOCK ? launch_fb_qdq(c, in, out, rows, cols, FB_ROWS, meta, nullptr)
+                        : launch_mx_qdq(c, in, out, rows, cols, true, meta);
+}
+
+static cudaError_t act_cols(const Ctx& c, int qs, const uint16_t* in, uint16_t* out,
+                            int64_t rows, int64_t cols, const int* meta,
+                            uint16_t* out_rows = nullptr) {
+  return qs == QS_BLOCK ? launch_fb_qdq(c, in, out, rows, cols, FB_COLS, meta, out_rows)
+                        : launch_mx_qdq(c, in, out, rows, cols, false, meta, out_rows);
+}
+
+// The forward's gate/up stage on x_perm: h = [g | u] and a = silu(g) * u.  Under a
+// quantised forward (L.qf) its operands are first quantised along H.  MXFP8: with
+// `keep` (the forward of a layer that keeps its activations) by two-way passes that
+// also leave x_perm quantised along tokens in place and the weights along their
+// backward K in `wbase` (saved); otherwise by row passes; `emit_qa` makes the epilogue
+// also write a quantised along I for the down projection.  Blockwise FP8: the one
+// 128 x 128-block copy of each of the three weights goes to `wbase` (saved, or the
+// front of scratch under recompute); x_perm as for MXFP8; `emit_qa` adds a row pass
+// over a.  The backward under MM_MOE_RECOMPUTE calls it with the forward's arguments
+// and gets h and a bit for bit (the same kernels on the same inputs).
+static mm_moe_status gateup_stage(const Ctx& c, const Layout& L, bool keep, bool emit_qa,
+                                  uint16_t* x_perm, const uint16_t* W_gate,
                                   const uint16_t* W_up, const uint16_t* W_down, uint16_t* h,
-                                  uint16_t* a, const char* sv, char* wsaved, char* sc) {
+                                  uint16_t* a, const char* sv, char* wbase, char* sc) {
   const int* meta = reinterpret_cast<const int*>(sv + L.meta);
   const int64_t EI = L.E * L.I, EH = L.E * L.H;
   auto sq = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
+  auto wq = [&](size_t off) { return reinterpret_cast<uint16_t*>(wbase + off); };
   const uint16_t *A = x_perm, *Bg = W_gate, *Bu = W_up;
-  if (mx) {
+  if (L.qf != QS_NONE) {
+    if (keep)  // x_perm, one read: along H for this GEMM, along tokens in place
+      MM_MOE_TRY(act_cols(c, L.qf, x_perm, x_perm, L.Rp, L.H, meta, sq(L.q_x)));
+    else
+      MM_MOE_TRY(act_rows(c, L.qf, x_perm, sq(L.q_x), L.Rp, L.H, meta));
+    A = sq(L.q_x);
+  }
+  if (L.qf == QS_MX) {
     if (keep) {  // one read each, both axes
-      auto vq = [&](size_t off) { return reinterpret_cast<uint16_t*>(wsaved + off); };
-      MM_MOE_TRY(launch_mx_qdq(c, x_perm, x_perm, L.Rp, L.H, false, meta, sq(L.q_x)));
-      MM_MOE_TRY(launch_mx_qdq(c, W_gate, vq(L.q_wgc), EI, L.H, false, nullptr, sq(L.q_wg)));
-      MM_MOE_TRY(launch_mx_qdq(c, W_up, vq(L.q_wuc), EI, L.H, false, nullptr, sq(L.q_wu)));
+      MM_MOE_TRY(launch_mx_qdq(c, W_gate, wq(L.q_wgc), EI, L.H, false, nullptr, sq(L.q_wg)));
+      MM_MOE_TRY(launch_mx_qdq(c, W_up, wq(L.q_wuc), EI, L.H, false, nullptr, sq(L.q_wu)));
       if (emit_qa)
-        MM_MOE_TRY(launch_mx_qdq(c, W_down, vq(L.q_wdc), EH, L.I, false, nullptr, sq(L.q_wd)));
+        MM_MOE_TRY(launch_mx_qdq(c, W_down, wq(L.q_wdc), EH, L.I, false, nullptr, sq(L.q_wd)));
     } else {
-      MM_MOE_TRY(launch_mx_qdq(c, x_perm, sq(L.q_x), L.Rp, L.H, true, meta));
       MM_MOE_TRY(launch_mx_qdq(c, W_gate, sq(L.q_wg), EI, L.H, true, nullptr));
       MM_MOE_TRY(launch_mx_qdq(c, W_up, sq(L.q_wu), EI, L.H, true, nullptr));
       if (emit_qa) MM_MOE_TRY(launch_mx_qdq(c, W_down, sq(L.q_wd), EH, L.I, true, nullptr));
     }
-    A = sq(L.q_x);
     Bg = sq(L.q_wg);
     Bu = sq(L.q_wu);
+  } else if (L.qf == QS_BLOCK) {  // the copies every GEMM of the layer reads
+    MM_MOE_TRY(launch_fb_qdq(c, W_gate, wq(L.q_wgc), EI, L.H, FB_TILES, nullptr, nullptr));
+    MM_MOE_TRY(launch_fb_qdq(c, W_up, wq(L.q_wuc), EI, L.H, FB_TILES, nullptr, nullptr));
+    MM_MOE_TRY(launch_fb_qdq(c, W_down, wq(L.q_wdc), EH, L.I, FB_TILES, nullptr, nullptr));
+    Bg = wq(L.q_wgc);
+    Bu = wq(L.q_wuc);
   }
   GemmArgs g{};
   g.saved = sv;
@@ -228,9 +269,10 @@ static mm_moe_status gateup_stage(const Ctx& c, const Layout& L, bool mx, bool k
   g.B1 = Bu;
   g.out0 = h;
   g.out1 = a;
-  g.mx = (mx && emit_qa) ? 1 : 0;
+  g.mx = (L.qf == QS_MX && emit_qa) ? 1 : 0;
   g.q0 = g.mx ? sq(L.q_a) : nullptr;
   MM_MOE_TRY(launch_gemm(c, L, g));
+  if (L.qf == QS_BLOCK && emit_qa) MM_MOE_TRY(act_rows(c, QS_BLOCK, a, sq(L.q_a), L.Rp, L.I, meta));
   return MM_MOE_OK;
 }
 
@@ -280,12 +322,14 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
                             K_PERMUTE_X, sc));
   // Operands of the two GEMMs: the bf16 tensors, or under MXFP8 their copies
   // quantised in 32-blocks along each GEMM's K (H for gate/up, I for down)
-  const bool mx = shape->prec == MM_MOE_MXFP8;
-  st = gateup_stage(c, L, mx, L.w_in_saved, true, x_perm, W_gate, W_up, W_down, h, a, sv, sv,
+  char* wbase = L.w_common ? sc : sv;  // where the backward's (blockwise: all) weight copies go
+  st = gateup_stage(c, L, L.w_in_saved, true, x_perm, W_gate, W_up, W_down, h, a, sv, wbase,
                     sc);
   if (st != MM_MOE_OK) return st;
-  const uint16_t* A2 = mx ? reinterpret_cast<uint16_t*>(sc + L.q_a) : a;
-  const uint16_t* Bd = mx ? reinterpret_cast<uint16_t*>(sc + L.q_wd) : W_down;
+  const uint16_t* A2 = L.qf != QS_NONE ? reinterpret_cast<uint16_t*>(sc + L.q_a) : a;
+  const uint16_t* Bd = L.qf == QS_MX      ? reinterpret_cast<uint16_t*>(sc + L.q_wd)
+                       : L.qf == QS_BLOCK ? reinterpret_cast<uint16_t*>(wbase + L.q_wdc)
+                                          : W_down;
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
@@ -335,29 +379,31 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
     // activation checkpointing: x_perm, h and a again, as the forward made them
     uint16_t* xp = reinterpret_cast<uint16_t*>(sc + L.x_perm);
     MM_MOE_TRY(launch_permute(c, L, x, xp, sv, nullptr, K_PERMUTE_X, sc));
-    st = gateup_stage(c, L, shape->prec == MM_MOE_MXFP8, false, false, xp, W_gate, W_up,
-                      W_down, reinterpret_cast<uint16_t*>(sc + L.h),
-                      reinterpret_cast<uint16_t*>(sc + L.a), sv, nullptr, sc);
+    st = gateup_stage(c, L, false, false, xp, W_gate, W_up, W_down,
+                      reinterpret_cast<uint16_t*>(sc + L.h),
+                      reinterpret_cast<uint16_t*>(sc + L.a), sv, sc, sc);
     if (st != MM_MOE_OK) return st;
   }
   MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY, sc));
-  // MXFP8 backward (full MXFP8 and fp8_bwd): every GEMM reads copies of its operands
-  // quantised in 32-blocks along its own K
-  const bool mx = shape->prec != MM_MOE_BF16;
+  // A quantised backward (MXFP8 for full MXFP8 and fp8_bwd, blockwise FP8): every
+  // GEMM reads copies of its operands quantised along its own K
+  const int qb = L.qb;
   const int* meta = reinterpret_cast<const int*>(sv + L.meta);
   const int64_t EI = L.E * L.I, EH = L.E * L.H;
   auto q = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
-  // the backward's quantised weights: made here (fp8_bwd) or by the forward (MXFP8)
+  // the backward's quantised weights: made by the forward (saved), by the recompute
+  // (blockwise, front of scratch), or here (MXFP8 along their backward K)
   auto qw = [&](size_t off) -> const uint16_t* {
     return L.w_in_saved ? reinterpret_cast<const uint16_t*>(sv + off) : q(off);
   };
+  const bool make_w = qb == QS_MX && !L.w_in_saved;
   const uint16_t* A1 = dy_perm;
   const uint16_t* Bd = W_down;
-  if (mx) {
+  if (qb != QS_NONE) {
     // one read of dy_perm: blocks along tokens (dW_down) to q_dyc, blocks along H
     // (this GEMM) in place
-    MM_MOE_TRY(launch_mx_qdq(c, dy_perm, q(L.q_dyc), L.Rp, L.H, false, meta, dy_perm));
-    if (!L.w_in_saved) MM_MOE_TRY(launch_mx_qdq(c, W_down, q(L.q_wdc), EH, L.I, false, nullptr));
+    MM_MOE_TRY(act_cols(c, qb, dy_perm, q(L.q_dyc), L.Rp, L.H, meta, dy_perm));
+    if (make_w) MM_MOE_TRY(launch_mx_qdq(c, W_down, q(L.q_wdc), EH, L.I, false, nullptr));
     Bd = qw(L.q_wdc);
   }
   GemmArgs g{};
@@ -373,11 +419,11 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   g.outf = pw;
   MM_MOE_TRY(launch_gemm(c, L, g));
   const uint16_t *A2 = dh, *Bg = W_gate, *Bu = W_up;
-  if (mx) {
+  if (qb != QS_NONE) {
     // one read of dh: blocks along tokens (dW_gate, dW_up) to q_dhc, blocks along I
     // (the next GEMM) in place
-    MM_MOE_TRY(launch_mx_qdq(c, dh, q(L.q_dhc), L.Rp, 2 * L.I, false, meta, dh));
-    if (!L.w_in_saved) {
+    MM_MOE_TRY(act_cols(c, qb, dh, q(L.q_dhc), L.Rp, 2 * L.I, meta, dh));
+    if (make_w) {
       MM_MOE_TRY(launch_mx_qdq(c, W_gate, q(L.q_wgc), EI, L.H, false, nullptr));
       MM_MOE_TRY(launch_mx_qdq(c, W_up, q(L.q_wuc), EI, L.H, false, nullptr));
     }
@@ -403,13 +449,14 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   MM_MOE_TRY(launch_unpermute(cs, L, dxs, sv, pw, dx, dtopk_w));
   MM_MOE_TRY(cudaEventRecord(ss.join, ss.s));
   // token-axis blocks of the weight-gradient operands: each expert's rows start on a
-  // multiple of 128 and its padding rows are zero, so 32-row blocks of the padded
-  // row space are the per-expert blocks with a zero-padded tail
+  // multiple of 128 and its padding rows are zero, so 32- or 128-row blocks of the
+  // padded row space are the per-expert blocks with a zero-padded tail
   const uint16_t *A3 = dy_perm, *B3 = a_w, *A4 = dh, *B4 = x_perm;
-  if (mx) {
-    MM_MOE_TRY(launch_mx_qdq(c, a_w, a_w, L.Rp, L.I, false, meta));
-    if (!L.w_in_saved) {  // fp8_bwd: x_perm is still bf16 (full MXFP8 quantised it)
-      MM_MOE_TRY(launch_mx_qdq(c, x_perm, q(L.q_xc), L.Rp, L.H, false, meta));
+  if (qb != QS_NONE) {
+    MM_MOE_TRY(act_cols(c, qb, a_w, a_w, L.Rp, L.I, meta));
+    if (!L.w_in_saved) {  // x_perm still bf16 (a quantised forward that keeps it left
+                          // it quantised along tokens)
+      MM_MOE_TRY(act_cols(c, qb, x_perm, q(L.q_xc), L.Rp, L.H, meta));
       B4 = q(L.q_xc);
     }
     A3 = q(L.q_dyc);

@@ -43,7 +43,7 @@ class MoEConfig:
     zipf_s: float = 1.2
     zipf_ranks: int = 0           # only for 'zipf_trunc'
     seed: int = 0
-    prec: str = "bf16"            # 'bf16' | 'mxfp8' | 'fp8_bwd'
+    prec: str = "bf16"            # 'bf16' | 'mxfp8' | 'fp8_bwd' | 'fp8_block'
 
     @property
     def R(self) -> int:
@@ -80,6 +80,10 @@ CONFIGS: Dict[str, MoEConfig] = {
     # the same inputs with a BF16 forward and an MXFP8 backward
     "qwen3_30b_16k_fp8_bwd": MoEConfig("qwen3_30b_16k_fp8_bwd", T=16384, H=2048, I=768,
                                        E=128, k=8, routing="uniform", seed=6, prec="fp8_bwd"),
+    # and in blockwise FP8 (forward and backward)
+    "qwen3_30b_16k_fp8block": MoEConfig("qwen3_30b_16k_fp8block", T=16384, H=2048, I=768,
+                                        E=128, k=8, routing="uniform", seed=6,
+                                        prec="fp8_block"),
 }
 
 BF16_ROUND_BIAS = np.uint32(0x7FFF)

@@ -92,7 +92,7 @@ def test_forward_backward_reject_before_launch(lib):
     mis = list(fake)
     mis[0] += 2                                    # x misaligned
     assert lib.mm_moe_forward(ctypes.byref(s), *mis) == B.MM_MOE_EINVAL
-    bad_prec = B.make_shape(64, 128, 64, 8, 2, 3)
+    bad_prec = B.make_shape(64, 128, 64, 8, 2, 4)
     assert lib.mm_moe_forward(ctypes.byref(bad_prec), *fake) == B.MM_MOE_EINVAL
     assert lib.mm_moe_get_routing(ctypes.byref(s), None, None, None, None) == B.MM_MOE_EINVAL
     # the router: NULL pointers, k above 32, E not a multiple of 8

@@ -24,9 +24,9 @@ def same(a, b):
     assert not bad, bad
 
 
-@pytest.mark.parametrize("prec", ["bf16", "mxfp8", "fp8_bwd"])
+@pytest.mark.parametrize("prec", ["bf16", "mxfp8", "fp8_bwd", "fp8_block"])
 @pytest.mark.parametrize("T,H,I,E,k,routing,seed", [
-    (300, 256, 192, 8, 2, "uniform", 31),      # single-SM tiles
+    (300, 384, 128, 8, 2, "uniform", 31),      # single-SM tiles
     (900, 512, 256, 32, 8, "zipf_trunc", 32),  # SM pairs, empty experts
 ])
 def test_recompute_matches_kept_activations(T, H, I, E, k, routing, seed, prec):
