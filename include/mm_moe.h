@@ -112,10 +112,11 @@ typedef struct {
  *   saved   : written by mm_moe_forward, read by mm_moe_backward; holds the
  *             routing (offsets, perm, inv), the routing weights in routed order,
  *             the expert-grouped copy of x, h = [g | u] and a = silu(g) * u in
- *             bf16.  Under MM_MOE_MXFP8 the copy of x is kept quantised along the
- *             token axis and `saved` also holds the weights quantised along their
- *             backward contraction axis (so the backward's weight arguments must be
- *             the forward's, as in every mode).  With MM_MOE_RECOMPUTE it holds
+ *             bf16.  Under MM_MOE_MXFP8 and MM_MOE_FP8_BLOCK the copy of x is kept
+ *             quantised along the token axis and `saved` also holds quantised copies
+ *             of the weights (MXFP8: along their backward contraction axis;
+ *             blockwise: the one copy every GEMM reads), so the backward's weight
+ *             arguments must be the forward's, as in every mode.  With MM_MOE_RECOMPUTE it holds
  *             only the routing and the routing weights in routed order; x, h and a
  *             live in `scratch`.  It must not change between the forward and its
  *             backward.
