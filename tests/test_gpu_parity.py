@@ -10,6 +10,8 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
+import oracle.moe as om
 from mixture_experts_layer_16_gb300.inputs import CONFIGS, custom_inputs, make_inputs
 from tests import gpu_util as G
 
@@ -99,6 +101,31 @@ def test_degenerate_shapes(T, H, I, E, k, routing, seed):
     assert res["status"] == 0
     check_routing(res, d["topk_idx"], E)
     check_full(d, res)
+
+
+@pytest.mark.parametrize("T,E,k,how", [
+    (65536, 1024, 8, "uniform"),   # 524,288 routed rows over 1,024 experts (256 routing blocks)
+    (65536, 128, 1, "one"),        # every token to one expert: a 512-tile expert
+    (50000, 256, 4, "zipf"),       # skewed, ragged row count
+])
+def test_routing_large(T, E, k, how):
+    """Routing alone at sizes far above the parity shapes (H and I minimal): offsets,
+    perm and inv bit-exact, y still within tolerance on sampled tokens."""
+    H, I = 128, 64
+    rng = np.random.default_rng(T + E + k)
+    if how == "one":
+        idx = np.full((T, 1), 77, dtype=np.int32)
+        d = custom_inputs(T, H, I, E, k, seed=60, idx=idx)
+    else:
+        d = custom_inputs(T, H, I, E, k, seed=61, routing=how)
+    res, _, _ = G.run(d, backward=False)
+    assert res["status"] == 0
+    check_routing(res, d["topk_idx"], E)
+    toks = np.sort(rng.choice(T, 64, replace=False))
+    sub = om.token_subset(d, toks)
+    f = oracle.forward(sub["x"], sub["topk_idx"], sub["topk_w"], d["W_gate"], d["W_up"],
+                       d["W_down"])
+    assert G.rel_err(G.f32(res["y"][toks]), f["y"]) <= TOL
 
 
 def test_determinism():
