@@ -34,7 +34,8 @@ DEFAULT_CONFIG = "qwen3_30b_16k_zipf"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GEMM_FLOP_FACTOR = {  # algorithmic FLOPs per launch, in units of R*H*I
     "gemm_gateup_swiglu": 4, "gemm_down_weighted": 2, "gemm_dgrad_down_dswiglu": 2,
-    "gemm_dgrad_gateup": 4, "gemm_wgrad_down": 2, "gemm_wgrad_gateup": 4}
+    "gemm_dgrad_gateup": 4, "gemm_wgrad_down": 2, "gemm_wgrad_gateup": 4,
+    "gemm_wgrad": 6}  # the last: both weight gradients in one launch
 
 
 def parse_args():

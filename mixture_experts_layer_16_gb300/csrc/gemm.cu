@@ -11,6 +11,10 @@
 //   DGRAD_GATEUP dx = dh . [W_gate;W_up]             epilogue dx (expert-grouped rows)
 //   WGRAD_DOWN   dW_down[e] = dy_perm^T . (w*a)      K = the expert's rows
 //   WGRAD_GATEUP [dW_gate;dW_up][e] = dh^T . x_perm   K = the expert's rows
+//   WGRAD_BOTH   the two weight gradients in one launch: each expert's WGRAD_DOWN
+//                tiles, then its WGRAD_GATEUP tiles, experts by descending row count
+//                (one list evens out the clusters' loads: the per-kind lists leave
+//                a tail of 9-17 % on skewed routing, the joint one about 3 %)
 //
 // CTAS = 2 runs each tile on an SM pair: the two CTAs of a 2-CTA cluster each stage
 // 128 rows of A and half of the N columns of B, and one tcgen05.mma.cta_group::2 of
@@ -53,9 +57,14 @@ struct GemmParams {
   CUtensorMap tmD0;  // epilogue inputs loaded by TMA (dSwiGLU: h and a)
   CUtensorMap tmD1;
   CUtensorMap tmQ0;  // MXFP8 epilogue output (gate/up: a in 32-blocks along I)
+  CUtensorMap tmA2;  // WGRAD_BOTH: the dW_down part's operands and output
+  CUtensorMap tmB2;
+  CUtensorMap tmC2;
   int H, I, E;
   int n_tiles;  // N tiles per M block (grouped kinds) or per expert M row (per-expert kinds)
   int m_tiles;  // M tiles (of BM * CTAS rows) per expert (per-expert kinds)
+  int n_tiles2;  // WGRAD_BOTH: N and M tiles per expert of the dW_down part (n_tiles
+  int m_tiles2;  // and m_tiles are then those of the dW_gate / dW_up part)
   int k_iters;  // K iterations per tile (grouped kinds)
   int n_pw;
   int max_tiles;
@@ -105,21 +114,36 @@ struct Cfg {
 
 struct TileInfo {
   int e, mb, m0, n0, k_iters, k_row0;
+  int down;  // per-expert kinds: 1 = a dW_down tile, 0 = a dW_gate / dW_up tile
 };
+
+// Per-expert tiles of kind KIND: (dW_down tiles, dW_gate / dW_up tiles) per expert.
+template <int KIND>
+__device__ __forceinline__ int2 expert_tiles(const GemmParams& p) {
+  if constexpr (KIND == GEMM_WGRAD_DOWN) return make_int2(p.m_tiles * p.n_tiles, 0);
+  else if constexpr (KIND == GEMM_WGRAD_GATEUP) return make_int2(0, p.m_tiles * p.n_tiles);
+  else return make_int2(p.m_tiles2 * p.n_tiles2, p.m_tiles * p.n_tiles);
+}
 
 // Decode tile t for this CTA (rank within the pair).  Grouped kinds: t -> (group of
 // CTAS 128-row blocks of padded routed rows, N tile), N fastest; the CTA takes block
 // CTAS*group + rank.  Per-expert kinds: experts in descending row count, then (M, N)
-// tiles of BM*CTAS x BN; the CTA takes rows rank*BM.. of the M tile.
+// tiles of BM*CTAS x BN (an expert's dW_down tiles first); the CTA takes rows
+// rank*BM.. of the M tile.
 template <int KIND, int BN, int CTAS>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int rank) {
   TileInfo ti;
+  ti.down = 0;
   if constexpr (Cfg<KIND, BN, CTAS>::PER_EXPERT) {
-    const int per_e = p.m_tiles * p.n_tiles;
+    const int2 per = expert_tiles<KIND>(p);
+    const int per_e = per.x + per.y;
     const int ei = t / per_e;
-    const int rem = t - ei * per_e;
-    const int mt = rem / p.n_tiles;
-    const int nt = rem - mt * p.n_tiles;
+    int rem = t - ei * per_e;
+    ti.down = rem < per.x ? 1 : 0;
+    if (!ti.down) rem -= per.x;
+    const int ntl = ti.down && KIND == GEMM_WGRAD_BOTH ? p.n_tiles2 : p.n_tiles;
+    const int mt = rem / ntl;
+    const int nt = rem - mt * ntl;
     ti.e = __ldg(p.expert_order + ei);
     ti.mb = 0;
     ti.m0 = mt * BM * CTAS + rank * BM;
@@ -144,7 +168,8 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int 
 template <int KIND, int BN, int CTAS>
 __device__ __forceinline__ int total_tiles(const GemmParams& p) {
   if constexpr (Cfg<KIND, BN, CTAS>::PER_EXPERT) {
-    return p.E * p.m_tiles * p.n_tiles;
+    const int2 per = expert_tiles<KIND>(p);
+    return p.E * (per.x + per.y);
   } else {
     int nt = __ldg(p.meta + META_NUM_TILES);
     nt = min(nt, p.max_tiles);
@@ -338,8 +363,8 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInf
   } else {  // weight gradients: dW_down [E*H, I]; dW_gate / dW_up [E*I, H]
     const CUtensorMap* m;
     int orow;
-    if (KIND == GEMM_WGRAD_DOWN) {
-      m = &p.tmC0;
+    if (ti.down) {
+      m = KIND == GEMM_WGRAD_BOTH ? &p.tmC2 : &p.tmC0;
       orow = ti.e * p.H + row0;
     } else {
       const bool gate = row0 < p.I;
@@ -367,8 +392,8 @@ __device__ __forceinline__ void zero_tile(const GemmParams& p, const TileInfo& t
   const int row0 = ti.m0 + q * 32;
   const CUtensorMap* m;
   int orow;
-  if (KIND == GEMM_WGRAD_DOWN) {
-    m = &p.tmC0;
+  if (ti.down) {
+    m = KIND == GEMM_WGRAD_BOTH ? &p.tmC2 : &p.tmC0;
     orow = ti.e * p.H + row0;
   } else {
     const bool gate = row0 < p.I;
@@ -425,11 +450,13 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
     for (int c = 0; c < C::B_ROWS / 64; ++c) tma<CTAS>(sb + c * 8192, m, bar, nb + c * 64, krow);
   } else {  // per-expert weight gradients: both operands M/N-major, K = routed rows
     const int krow = ti.k_row0 + k0;
+    const bool second = KIND == GEMM_WGRAD_BOTH && ti.down;
+    const CUtensorMap* ma = second ? &p.tmA2 : &p.tmA;
+    const CUtensorMap* mb = second ? &p.tmB2 : &p.tmB0;
 #pragma unroll
-    for (int c = 0; c < BM / 64; ++c) tma<CTAS>(sa + c * 8192, &p.tmA, bar, ti.m0 + c * 64, krow);
+    for (int c = 0; c < BM / 64; ++c) tma<CTAS>(sa + c * 8192, ma, bar, ti.m0 + c * 64, krow);
 #pragma unroll
-    for (int c = 0; c < C::B_ROWS / 64; ++c)
-      tma<CTAS>(sb + c * 8192, &p.tmB0, bar, nb + c * 64, krow);
+    for (int c = 0; c < C::B_ROWS / 64; ++c) tma<CTAS>(sb + c * 8192, mb, bar, nb + c * 64, krow);
   }
 }
 
@@ -471,6 +498,10 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     ptx::prefetch_tmap(&p.tmA);
     ptx::prefetch_tmap(&p.tmB0);
     if (KIND == GEMM_GATEUP || KIND == GEMM_DGRAD_GATEUP) ptx::prefetch_tmap(&p.tmB1);
+    if (KIND == GEMM_WGRAD_BOTH) {
+      ptx::prefetch_tmap(&p.tmA2);
+      ptx::prefetch_tmap(&p.tmB2);
+    }
   }
   if (warp == 2) {
     ptx::tmem_alloc<CTAS>(&s_tmem_base, C::TMEM_COLS);
@@ -688,6 +719,11 @@ int pick_bn(int64_t n) {
   return 64;
 }
 
+bool wgrad_both_ok(const Layout& L) {
+  const int bn = pick_bn(L.H);
+  return bn >= 128 && pick_bn(L.I) == bn;
+}
+
 template <int KIND, int BN, int CTAS, bool MX>
 static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) {
   using C = Cfg<KIND, BN, CTAS>;
@@ -719,8 +755,9 @@ static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) 
   }
   clusters = std::max<int64_t>(1, std::min<int64_t>(clusters, max_clusters));
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CTAS), 1, 1);
-  static constexpr int kId[6] = {K_GEMM_GATEUP, K_GEMM_DOWN, K_GEMM_DGRAD_DOWN,
-                                 K_GEMM_DGRAD_GATEUP, K_GEMM_WGRAD_DOWN, K_GEMM_WGRAD_GATEUP};
+  static constexpr int kId[7] = {K_GEMM_GATEUP,       K_GEMM_DOWN,       K_GEMM_DGRAD_DOWN,
+                                 K_GEMM_DGRAD_GATEUP, K_GEMM_WGRAD_DOWN, K_GEMM_WGRAD_GATEUP,
+                                 K_GEMM_WGRAD};
   prof_begin(c, kId[KIND]);
   e = cudaLaunchKernelEx(&cfg, kern, p);
   prof_end(c, kId[KIND]);
@@ -738,7 +775,7 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   // each other and on the epilogue (4k-token 30B-shape layer: 0.52 ms on pairs,
   // 0.42 ms on single SMs; 16k tokens: pairs 5 % faster)
   constexpr int64_t WGRAD_PAIR_MIN_ROWS = 512;
-  const bool per_expert = g.kind == GEMM_WGRAD_DOWN || g.kind == GEMM_WGRAD_GATEUP;
+  const bool per_expert = g.kind >= GEMM_WGRAD_DOWN;
   const int ctas =
       (L.pad == 2 * BM && !(per_expert && L.R < WGRAD_PAIR_MIN_ROWS * L.E)) ? 2 : 1;
   p.H = static_cast<int>(L.H);
@@ -761,7 +798,7 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   // Failure-path test hook: MM_MOE_TEST_STALL_GEMM=<kind> makes that GEMM's first
   // stage on CTA 0 never fill (read at every launch; unset, it does nothing)
   if (const char* v = std::getenv("MM_MOE_TEST_STALL_GEMM"))
-    p.stall = (v[0] >= '0' && v[0] <= '5' && v[1] == '\0' && v[0] - '0' == g.kind) ? 1 : 0;
+    p.stall = (v[0] >= '0' && v[0] <= '6' && v[1] == '\0' && v[0] - '0' == g.kind) ? 1 : 0;
   const uint64_t Rp = static_cast<uint64_t>(L.Rp), H = L.H, I = L.I, E = L.E;
   bool ok = true;
   int bn = 0;
@@ -818,6 +855,19 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
       p.n_tiles = static_cast<int>(L.H / bn);
       max_units = L.E * p.m_tiles * p.n_tiles;
       break;
+    case GEMM_WGRAD_BOTH:
+      if (!wgrad_both_ok(L)) return cudaErrorInvalidValue;
+      bn = pick_bn(L.H);
+      ok = make_map(&p.tmA, g.A, 2 * I, Rp, 64, 64) && make_map(&p.tmB0, g.B0, H, Rp, 64, 64) &&
+           make_epi_map(&p.tmC0, g.out0, H, E * I) && make_epi_map(&p.tmC1, g.out1, H, E * I) &&
+           make_map(&p.tmA2, g.A2, H, Rp, 64, 64) && make_map(&p.tmB2, g.B2, I, Rp, 64, 64) &&
+           make_epi_map(&p.tmC2, g.out2, I, E * H);
+      p.m_tiles = static_cast<int>(2 * L.I / (BM * ctas));
+      p.n_tiles = static_cast<int>(L.H / bn);
+      p.m_tiles2 = static_cast<int>(L.H / (BM * ctas));
+      p.n_tiles2 = static_cast<int>(L.I / bn);
+      max_units = L.E * (p.m_tiles * p.n_tiles + p.m_tiles2 * p.n_tiles2);
+      break;
     default:
       return cudaErrorInvalidValue;
   }
@@ -838,6 +888,8 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   MMMOE_RUN(GEMM_WGRAD_DOWN, 256, 2)
   MMMOE_RUN(GEMM_WGRAD_DOWN, 128, 2)
   MMMOE_RUN(GEMM_WGRAD_GATEUP, 256, 2)
+  MMMOE_RUN(GEMM_WGRAD_BOTH, 256, 2)
+  MMMOE_RUN(GEMM_WGRAD_BOTH, 128, 2)
   MMMOE_RUN(GEMM_GATEUP, 256, 1)
   MMMOE_RUN(GEMM_GATEUP, 128, 1)
   MMMOE_RUN(GEMM_DOWN, 256, 1)
@@ -852,6 +904,8 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   MMMOE_RUN(GEMM_WGRAD_DOWN, 64, 1)
   MMMOE_RUN(GEMM_WGRAD_GATEUP, 256, 1)
   MMMOE_RUN(GEMM_WGRAD_GATEUP, 128, 1)
+  MMMOE_RUN(GEMM_WGRAD_BOTH, 256, 1)
+  MMMOE_RUN(GEMM_WGRAD_BOTH, 128, 1)
 #undef MMMOE_RUN
   return cudaErrorInvalidValue;
 }

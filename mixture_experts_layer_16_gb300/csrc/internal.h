@@ -95,6 +95,7 @@ enum KernelId {
   K_UNPERMUTE,
   K_GEMM_WGRAD_DOWN,
   K_GEMM_WGRAD_GATEUP,
+  K_GEMM_WGRAD,
   K_MX_QDQ_ROWS,
   K_MX_QDQ_COLS,
   K_FB_ROWS,
@@ -161,6 +162,7 @@ enum GemmKind {
   GEMM_DGRAD_GATEUP = 3,  // dh . [W_gate;W_up]        -> dx, expert-grouped rows
   GEMM_WGRAD_DOWN = 4,    // dy_perm^T . a_w per expert -> dW_down
   GEMM_WGRAD_GATEUP = 5,  // dh^T . x_perm per expert   -> dW_gate, dW_up
+  GEMM_WGRAD_BOTH = 6,    // both weight gradients in one launch, tiles ordered by expert
 };
 
 struct GemmArgs {
@@ -175,6 +177,11 @@ struct GemmArgs {
   float* outf;
   const uint16_t* aux;   // h = [g | u] for the dSwiGLU epilogue
   const uint16_t* aux2;  // a = silu(g) * u saved by the forward
+  // GEMM_WGRAD_BOTH: A, B0, out0, out1 as GEMM_WGRAD_GATEUP; A2, B2, out2 as the A,
+  // B0, out0 of GEMM_WGRAD_DOWN
+  const uint16_t* A2;
+  const uint16_t* B2;
+  uint16_t* out2;
   const char* saved;
   char* scratch;
   // MXFP8 (mx != 0, gate/up only): the epilogue also writes a in 32-blocks along I
@@ -184,5 +191,7 @@ struct GemmArgs {
 };
 
 cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g);
+// whether GEMM_WGRAD_BOTH serves this layout (both weight gradients tile N alike)
+bool wgrad_both_ok(const Layout& L);
 
 }  // namespace mmmoe

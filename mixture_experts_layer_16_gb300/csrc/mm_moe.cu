@@ -462,22 +462,31 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
     A3 = q(L.q_dyc);
     A4 = q(L.q_dhc);
   }
+  // both weight gradients in one launch where they tile N alike (one list of tiles,
+  // experts by descending row count, balances the clusters' loads far better than
+  // two lists); otherwise one launch each
+  const bool both = wgrad_both_ok(L);
   g = GemmArgs{};
   g.saved = sv;
   g.scratch = sc;
-  g.kind = GEMM_WGRAD_DOWN;
-  g.A = A3;
-  g.B0 = B3;
-  g.out0 = dW_down;
-  MM_MOE_TRY(launch_gemm(c, L, g));
-  g = GemmArgs{};
-  g.saved = sv;
-  g.scratch = sc;
-  g.kind = GEMM_WGRAD_GATEUP;
+  g.kind = both ? GEMM_WGRAD_BOTH : GEMM_WGRAD_GATEUP;
   g.A = A4;
   g.B0 = B4;
   g.out0 = dW_gate;
   g.out1 = dW_up;
+  g.A2 = A3;
+  g.B2 = B3;
+  g.out2 = dW_down;
+  if (!both) {
+    GemmArgs gd{};
+    gd.saved = sv;
+    gd.scratch = sc;
+    gd.kind = GEMM_WGRAD_DOWN;
+    gd.A = A3;
+    gd.B0 = B3;
+    gd.out0 = dW_down;
+    MM_MOE_TRY(launch_gemm(c, L, gd));
+  }
   MM_MOE_TRY(launch_gemm(c, L, g));
   MM_MOE_TRY(cudaStreamWaitEvent(c.stream, ss.join, 0));  // join: the call ends on `stream`
   g_last_launches = launches;

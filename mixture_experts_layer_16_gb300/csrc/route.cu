@@ -60,7 +60,20 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
   const int e = threadIdx.x;
   int cnt = 0;
   if (e < E) {
-    for (int b = 0; b < nblk; ++b) {
+    // SCAN_BATCH independent loads in flight, then their running sums
+    constexpr int SCAN_BATCH = 16;
+    int b = 0;
+    for (; b + SCAN_BATCH <= nblk; b += SCAN_BATCH) {
+      int c[SCAN_BATCH];
+#pragma unroll
+      for (int j = 0; j < SCAN_BATCH; ++j) c[j] = blk_counts[static_cast<int64_t>(b + j) * E + e];
+#pragma unroll
+      for (int j = 0; j < SCAN_BATCH; ++j) {
+        blk_counts[static_cast<int64_t>(b + j) * E + e] = cnt;
+        cnt += c[j];
+      }
+    }
+    for (; b < nblk; ++b) {
       const int64_t i = static_cast<int64_t>(b) * E + e;
       const int c = blk_counts[i];
       blk_counts[i] = cnt;
