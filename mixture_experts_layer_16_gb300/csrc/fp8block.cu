@@ -10,6 +10,7 @@
 // holds them exactly, so the bf16 tensor-core GEMMs compute the FP8 products.
 #include <cuda_runtime.h>
 
+#include "fp8block.cuh"
 #include "internal.h"
 #include "mx.cuh"
 
@@ -18,17 +19,8 @@ namespace mmmoe {
 using mx::bf;
 using mx::qdq2;
 using mx::to_bf;
-
-constexpr int FB = 128;  // block length
-
-// ceil(log2(amax / 448)) clipped to [-127, 127], -127 for amax = 0.  With amax =
-// m * 2^E (m in [1, 2)) and 448 = 1.75 * 2^8 it is E - 8, plus 1 when m > 1.75.
-__device__ __forceinline__ int ceil_exp(float amax) {
-  if (!(amax > 0.f)) return -127;
-  const uint32_t b = __float_as_uint(amax);
-  const int e = static_cast<int>((b >> 23) & 0xFFu) - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u);
-  return max(-127, min(127, e));
-}
+using fb::ceil_exp;
+using fb::FB;
 
 __device__ __forceinline__ uint4 qdq8(uint4 w, const int (&e)[8]) {
   uint16_t* h = reinterpret_cast<uint16_t*>(&w);
@@ -82,13 +74,16 @@ __global__ void __launch_bounds__(256) fb_rows_kernel(const uint4* in, uint4* ou
 // the tile again (from L2) and writes it quantised.  With out_rows non-null the
 // second pass also writes the blocks along rows (16 lanes hold one 128-column block of
 // a row; C % 128 == 0).  out and out_rows may equal in: every element is read and
-// written by one thread, in that order.
+// written by one thread, in that order.  With a gather the rows come from a
+// token-major `in` (padding rows read as zeros).
 constexpr int FB_TILE = 512;
 
 __global__ void __launch_bounds__(256) fb_cols_kernel(const uint4* in, uint4* out,
                                                       uint4* out_rows, int64_t rows, int C8,
-                                                      const int* __restrict__ meta) {
+                                                      const int* __restrict__ meta,
+                                                      const RowGather gather) {
   __shared__ float part[4][FB_TILE];
+  __shared__ int src_row[FB];  // the tile's source rows (-1: zero), resolved once
   const int64_t R = used(rows, meta);
   const int col_tiles = (C8 * 8 + FB_TILE - 1) / FB_TILE;
   const int64_t tiles = (R / FB) * col_tiles;
@@ -98,13 +93,17 @@ __global__ void __launch_bounds__(256) fb_cols_kernel(const uint4* in, uint4* ou
     const int c8 = static_cast<int>(tile - rb * col_tiles) * (FB_TILE / 8) + cg;
     const bool active = c8 < C8;
     const int64_t base = rb * FB * C8 + c8;
+    __syncthreads();  // the previous tile's second pass has read src_row[]
+    if (threadIdx.x < FB) src_row[threadIdx.x] = gather_src(rb * FB + threadIdx.x, gather);
+    __syncthreads();
     float m[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) m[j] = 0.f;
     if (active) {
 #pragma unroll 8
       for (int r = 0; r < FB / 4; ++r) {
-        const uint4 w = in[base + static_cast<int64_t>(rs + 4 * r) * C8];
+        const int sr = src_row[rs + 4 * r];
+        const uint4 w = sr >= 0 ? in[static_cast<int64_t>(sr) * C8 + c8] : make_uint4(0, 0, 0, 0);
         const uint16_t* h = reinterpret_cast<const uint16_t*>(&w);
 #pragma unroll
         for (int j = 0; j < 8; ++j) m[j] = fmaxf(m[j], fabsf(bf(h[j])));
@@ -123,7 +122,9 @@ __global__ void __launch_bounds__(256) fb_cols_kernel(const uint4* in, uint4* ou
 #pragma unroll 4
     for (int r = 0; r < FB / 4; ++r) {
       const int64_t at = base + static_cast<int64_t>(rs + 4 * r) * C8;
-      const uint4 w = active ? in[at] : make_uint4(0, 0, 0, 0);
+      const int sr = src_row[rs + 4 * r];
+      const uint4 w = active && sr >= 0 ? in[static_cast<int64_t>(sr) * C8 + c8]
+                                        : make_uint4(0, 0, 0, 0);
       if (out_rows != nullptr) {  // uniform: every lane takes part in the shuffles
         float rm = amax8(w);
 #pragma unroll
@@ -176,7 +177,8 @@ __global__ void __launch_bounds__(256) fb_tiles_kernel(const uint4* in, uint4* o
 }
 
 cudaError_t launch_fb_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
-                          int64_t cols, int layout, const int* meta, uint16_t* out_rows) {
+                          int64_t cols, int layout, const int* meta, uint16_t* out_rows,
+                          RowGather gather) {
   const int C8 = static_cast<int>(cols / 8);
   const uint4* i4 = reinterpret_cast<const uint4*>(in);
   uint4* o4 = reinterpret_cast<uint4*>(out);
@@ -190,7 +192,7 @@ cudaError_t launch_fb_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64
     const int grid = static_cast<int>(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
     prof_begin(c, K_FB_COLS);
     fb_cols_kernel<<<grid, 256, 0, c.stream>>>(i4, o4, reinterpret_cast<uint4*>(out_rows), rows,
-                                               C8, meta);
+                                               C8, meta, gather);
     prof_end(c, K_FB_COLS);
   } else {
     const int64_t tiles = (rows / FB) * (cols / FB);

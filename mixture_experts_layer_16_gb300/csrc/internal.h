@@ -129,31 +129,56 @@ struct RouteBufs {
 };
 cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* topk_idx,
                             const float* topk_w, const RouteBufs& b);
+// dst = src's token rows in the padded expert-grouped order, padding rows zero; with
+// quant = QS_MX / QS_BLOCK each row is quantised along its columns (32- / 128-element
+// blocks) on the way, once per token before its k copies are stored.
 cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
-                           const char* saved, float* w_row_out, int kernel_id, char* scratch);
+                           const char* saved, float* w_row_out, int kernel_id, char* scratch,
+                           int quant = 0);
 cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
                            const char* saved, uint16_t* out);
 cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slots,
                              const char* saved, const float* pw, uint16_t* dx, float* dtopk_w);
 
+// Rows of the padded expert-grouped space read straight from a token-major [T, cols]
+// tensor: padded row pr is token rowflat[pr] / k, or a zero row when pr is padding (its
+// place in its BM-row block at or past tile_rows[pr / BM]).
+struct RowGather {
+  const int* rowflat;
+  const int* tile_rows;
+  int k;
+};
+
+// Source row of padded row pr: its index in `in`, or -1 for a zero row.  Both loads
+// are issued together; rowflat of a padding row (never written) is read and dropped.
+__device__ __forceinline__ int gather_src(int64_t pr, const RowGather& g) {
+  if (g.rowflat == nullptr) return static_cast<int>(pr);
+  const int64_t mb = pr / BM;
+  const int f = __ldg(g.rowflat + pr);
+  const int valid = __ldg(g.tile_rows + mb);
+  return pr - mb * BM < valid ? f / g.k : -1;
+}
+
 // MXFP8 quantise-dequantise of a bf16 [rows, cols] tensor in blocks of 32 elements,
 // along each row (along_rows) or down each column; the result is written as bf16.
 // With `meta` (device) non-null only the first meta[META_NUM_TILES] * BM rows are
 // processed (the padded routed rows that are in use).  Down columns, a non-null
-// out_rows also receives the blocks along rows from the same read.  out and out_rows
+// out_rows also receives the blocks along rows from the same read, and a gather with a
+// non-null rowflat reads the rows from a token-major `in` instead.  out and out_rows
 // may each equal in (every element is read once, by the thread that writes it).
 cudaError_t launch_mx_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
                           int64_t cols, bool along_rows, const int* meta,
-                          uint16_t* out_rows = nullptr);
+                          uint16_t* out_rows = nullptr, RowGather gather = RowGather{});
 
 // Blockwise FP8 quantise-dequantise of a bf16 [rows, cols] tensor (power-of-two scale
 // 2^ceil(log2(amax / 448)) per block), written as bf16: 128-element blocks along each
 // row (FB_ROWS), down each column (FB_COLS; a non-null out_rows also receives the row
-// blocks of the same read; `meta` as for launch_mx_qdq), or 128 x 128 tiles
-// (FB_TILES).  out / out_rows may equal in.
+// blocks of the same read; `meta` and `gather` as for launch_mx_qdq), or 128 x 128
+// tiles (FB_TILES).  out / out_rows may equal in.
 enum { FB_ROWS = 0, FB_COLS = 1, FB_TILES = 2 };
 cudaError_t launch_fb_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
-                          int64_t cols, int layout, const int* meta, uint16_t* out_rows);
+                          int64_t cols, int layout, const int* meta, uint16_t* out_rows,
+                          RowGather gather = RowGather{});
 
 enum GemmKind {
   GEMM_GATEUP = 0,        // x_perm . [W_gate|W_up]^T  -> SwiGLU epilogue (h, a)

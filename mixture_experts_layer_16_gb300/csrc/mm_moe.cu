@@ -209,37 +209,56 @@ static cudaError_t act_rows(const Ctx& c, int qs, const uint16_t* in, uint16_t* 
 
 static cudaError_t act_cols(const Ctx& c, int qs, const uint16_t* in, uint16_t* out,
                             int64_t rows, int64_t cols, const int* meta,
-                            uint16_t* out_rows = nullptr) {
-  return qs == QS_BLOCK ? launch_fb_qdq(c, in, out, rows, cols, FB_COLS, meta, out_rows)
-                        : launch_mx_qdq(c, in, out, rows, cols, false, meta, out_rows);
+                            uint16_t* out_rows = nullptr, RowGather gather = RowGather{}) {
+  return qs == QS_BLOCK ? launch_fb_qdq(c, in, out, rows, cols, FB_COLS, meta, out_rows, gather)
+                        : launch_mx_qdq(c, in, out, rows, cols, false, meta, out_rows, gather);
 }
 
-// The forward's gate/up stage on x_perm: h = [g | u] and a = silu(g) * u.  Under a
-// quantised forward (L.qf) its operands are first quantised along H.  MXFP8: with
-// `keep` (the forward of a layer that keeps its activations) by two-way passes that
-// also leave x_perm quantised along tokens in place and the weights along their
-// backward K in `wbase` (saved); otherwise by row passes; `emit_qa` makes the epilogue
-// also write a quantised along I for the down projection.  Blockwise FP8: the one
-// 128 x 128-block copy of each of the three weights goes to `wbase` (saved, or the
-// front of scratch under recompute); x_perm as for MXFP8; `emit_qa` adds a row pass
-// over a.  The backward under MM_MOE_RECOMPUTE calls it with the forward's arguments
-// and gets h and a bit for bit (the same kernels on the same inputs).
+// The padded expert-grouped rows of a token-major tensor, for act_cols.
+static RowGather routed_rows(const Layout& L, const char* sv) {
+  return RowGather{reinterpret_cast<const int*>(sv + L.rowflat),
+                   reinterpret_cast<const int*>(sv + L.tile_rows), static_cast<int>(L.k)};
+}
+
+// Under a quantised forward the permutation of x writes x's blocks along H (the
+// gate/up operand) straight to q_x, quantising each token row once; the blocks along
+// tokens (the dW_gate / dW_up operand), when wanted, are gathered from x into
+// `x_cols`.  No bf16 copy of the permuted rows is made.  Otherwise x_perm is the
+// bf16 permuted copy.  Returns gate/up's A operand.
+static const uint16_t* permute_x(const Ctx& c, const Layout& L, const uint16_t* x,
+                                 uint16_t* x_perm, uint16_t* x_cols, const char* sv,
+                                 float* w_row_out, char* sc, cudaError_t* err) {
+  if (L.qf == QS_NONE) {
+    *err = launch_permute(c, L, x, x_perm, sv, w_row_out, K_PERMUTE_X, sc);
+    return x_perm;
+  }
+  uint16_t* q_x = reinterpret_cast<uint16_t*>(sc + L.q_x);
+  *err = launch_permute(c, L, x, q_x, sv, w_row_out, K_PERMUTE_X, sc, L.qf);
+  if (*err == cudaSuccess && x_cols != nullptr)
+    *err = act_cols(c, L.qf, x, x_cols, L.Rp, L.H, reinterpret_cast<const int*>(sv + L.meta),
+                    nullptr, routed_rows(L, sv));
+  return q_x;
+}
+
+// The forward's gate/up stage on A (from permute_x): h = [g | u] and a = silu(g) * u.
+// Under a quantised forward (L.qf) the weights are first quantised along H.  MXFP8:
+// with `keep` (the forward of a layer that keeps its activations) by two-way passes
+// that also write the weights along their backward K to `wbase` (saved); otherwise by
+// row passes; `emit_qa` makes the epilogue also write a quantised along I for the down
+// projection.  Blockwise FP8: the one 128 x 128-block copy of each of the three
+// weights goes to `wbase` (saved, or the front of scratch under recompute); `emit_qa`
+// adds a row pass over a.  The backward under MM_MOE_RECOMPUTE calls it with the
+// forward's arguments and gets h and a bit for bit (the same kernels on the same
+// inputs).
 static mm_moe_status gateup_stage(const Ctx& c, const Layout& L, bool keep, bool emit_qa,
-                                  uint16_t* x_perm, const uint16_t* W_gate,
+                                  const uint16_t* A, const uint16_t* W_gate,
                                   const uint16_t* W_up, const uint16_t* W_down, uint16_t* h,
                                   uint16_t* a, const char* sv, char* wbase, char* sc) {
   const int* meta = reinterpret_cast<const int*>(sv + L.meta);
   const int64_t EI = L.E * L.I, EH = L.E * L.H;
   auto sq = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
   auto wq = [&](size_t off) { return reinterpret_cast<uint16_t*>(wbase + off); };
-  const uint16_t *A = x_perm, *Bg = W_gate, *Bu = W_up;
-  if (L.qf != QS_NONE) {
-    if (keep)  // x_perm, one read: along H for this GEMM, along tokens in place
-      MM_MOE_TRY(act_cols(c, L.qf, x_perm, x_perm, L.Rp, L.H, meta, sq(L.q_x)));
-    else
-      MM_MOE_TRY(act_rows(c, L.qf, x_perm, sq(L.q_x), L.Rp, L.H, meta));
-    A = sq(L.q_x);
-  }
+  const uint16_t *Bg = W_gate, *Bu = W_up;
   if (L.qf == QS_MX) {
     if (keep) {  // one read each, both axes
       MM_MOE_TRY(launch_mx_qdq(c, W_gate, wq(L.q_wgc), EI, L.H, false, nullptr, sq(L.q_wg)));
@@ -318,13 +337,15 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   uint16_t* h = reinterpret_cast<uint16_t*>(act + L.h);
   uint16_t* a = reinterpret_cast<uint16_t*>(act + L.a);
   uint16_t* ys = reinterpret_cast<uint16_t*>(sc + L.ys);
-  MM_MOE_TRY(launch_permute(c, L, x, x_perm, sv, reinterpret_cast<float*>(sv + L.w_row),
-                            K_PERMUTE_X, sc));
-  // Operands of the two GEMMs: the bf16 tensors, or under MXFP8 their copies
-  // quantised in 32-blocks along each GEMM's K (H for gate/up, I for down)
+  // Operands of the two GEMMs: the bf16 tensors, or in a quantised forward their
+  // copies quantised along each GEMM's K (H for gate/up, I for down).  A forward that
+  // keeps its activations also leaves x's blocks along tokens in x_perm's place.
+  cudaError_t err = cudaSuccess;
+  const uint16_t* A1 = permute_x(c, L, x, x_perm, L.w_in_saved ? x_perm : nullptr, sv,
+                                 reinterpret_cast<float*>(sv + L.w_row), sc, &err);
+  MM_MOE_TRY(err);
   char* wbase = L.w_common ? sc : sv;  // where the backward's (blockwise: all) weight copies go
-  st = gateup_stage(c, L, L.w_in_saved, true, x_perm, W_gate, W_up, W_down, h, a, sv, wbase,
-                    sc);
+  st = gateup_stage(c, L, L.w_in_saved, true, A1, W_gate, W_up, W_down, h, a, sv, wbase, sc);
   if (st != MM_MOE_OK) return st;
   const uint16_t* A2 = L.qf != QS_NONE ? reinterpret_cast<uint16_t*>(sc + L.q_a) : a;
   const uint16_t* Bd = L.qf == QS_MX      ? reinterpret_cast<uint16_t*>(sc + L.q_wd)
@@ -378,16 +399,20 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   if (L.recompute) {
     // activation checkpointing: x_perm, h and a again, as the forward made them
     uint16_t* xp = reinterpret_cast<uint16_t*>(sc + L.x_perm);
-    MM_MOE_TRY(launch_permute(c, L, x, xp, sv, nullptr, K_PERMUTE_X, sc));
-    st = gateup_stage(c, L, false, false, xp, W_gate, W_up, W_down,
+    cudaError_t err = cudaSuccess;
+    const uint16_t* A0 = permute_x(c, L, x, xp, nullptr, sv, nullptr, sc, &err);
+    MM_MOE_TRY(err);
+    st = gateup_stage(c, L, false, false, A0, W_gate, W_up, W_down,
                       reinterpret_cast<uint16_t*>(sc + L.h),
                       reinterpret_cast<uint16_t*>(sc + L.a), sv, sc, sc);
     if (st != MM_MOE_OK) return st;
   }
-  MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY, sc));
   // A quantised backward (MXFP8 for full MXFP8 and fp8_bwd, blockwise FP8): every
-  // GEMM reads copies of its operands quantised along its own K
+  // GEMM reads copies of its operands quantised along its own K.  The permutation of
+  // dy then writes dy's blocks along H (this GEMM's operand) to dy_perm, and dy's
+  // blocks along tokens (the dW_down operand) are gathered from dy.
   const int qb = L.qb;
+  MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY, sc, qb));
   const int* meta = reinterpret_cast<const int*>(sv + L.meta);
   const int64_t EI = L.E * L.I, EH = L.E * L.H;
   auto q = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
@@ -400,9 +425,7 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   const uint16_t* A1 = dy_perm;
   const uint16_t* Bd = W_down;
   if (qb != QS_NONE) {
-    // one read of dy_perm: blocks along tokens (dW_down) to q_dyc, blocks along H
-    // (this GEMM) in place
-    MM_MOE_TRY(act_cols(c, qb, dy_perm, q(L.q_dyc), L.Rp, L.H, meta, dy_perm));
+    MM_MOE_TRY(act_cols(c, qb, dy, q(L.q_dyc), L.Rp, L.H, meta, nullptr, routed_rows(L, sv)));
     if (make_w) MM_MOE_TRY(launch_mx_qdq(c, W_down, q(L.q_wdc), EH, L.I, false, nullptr));
     Bd = qw(L.q_wdc);
   }
@@ -454,9 +477,12 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   const uint16_t *A3 = dy_perm, *B3 = a_w, *A4 = dh, *B4 = x_perm;
   if (qb != QS_NONE) {
     MM_MOE_TRY(act_cols(c, qb, a_w, a_w, L.Rp, L.I, meta));
-    if (!L.w_in_saved) {  // x_perm still bf16 (a quantised forward that keeps it left
-                          // it quantised along tokens)
-      MM_MOE_TRY(act_cols(c, qb, x_perm, q(L.q_xc), L.Rp, L.H, meta));
+    if (!L.w_in_saved) {  // (a quantised forward that keeps its activations left x's
+                          // blocks along tokens in x_perm's place)
+      if (L.qf == QS_NONE)  // fp8_bwd: x_perm is the forward's bf16 copy
+        MM_MOE_TRY(act_cols(c, qb, x_perm, q(L.q_xc), L.Rp, L.H, meta));
+      else  // recompute under a quantised forward: from x itself
+        MM_MOE_TRY(act_cols(c, qb, x, q(L.q_xc), L.Rp, L.H, meta, nullptr, routed_rows(L, sv)));
       B4 = q(L.q_xc);
     }
     A3 = q(L.q_dyc);

@@ -77,14 +77,17 @@ __global__ void __launch_bounds__(256) mx_qdq_rows_kernel(const uint4* in, uint4
 // (16 bytes) of rows t/64, t/64 + 4, ..., so a warp reads 512 contiguous bytes of a
 // row; the four partial column maxima meet in shared memory.  With out_rows non-null
 // the same read also yields the blocks along rows (four neighbouring lanes hold one
-// 32-column block of a row), written to out_rows.
+// 32-column block of a row), written to out_rows.  With a gather the rows come from a
+// token-major `in` (padding rows read as zeros).
 constexpr int COL_TILE = 512;
 
 __global__ void __launch_bounds__(256) mx_qdq_cols_kernel(const uint4* in, uint4* out,
                                                           uint4* out_rows,
                                                           int64_t rows, int C8,
-                                                          const int* __restrict__ meta) {
+                                                          const int* __restrict__ meta,
+                                                          const RowGather gather) {
   __shared__ float part[4][COL_TILE];
+  __shared__ int src_row[32];  // the tile's source rows (-1: zero), resolved once
   if (meta != nullptr) rows = used_rows(rows, meta);
   const int col_tiles = (C8 * 8 + COL_TILE - 1) / COL_TILE;
   const int64_t tiles = (rows / 32) * col_tiles;
@@ -93,14 +96,16 @@ __global__ void __launch_bounds__(256) mx_qdq_cols_kernel(const uint4* in, uint4
     const int64_t rb = tile / col_tiles;
     const int c8 = static_cast<int>(tile - rb * col_tiles) * (COL_TILE / 8) + cg;
     const bool active = c8 < C8;
-    const uint4* src = in + rb * 32 * C8 + c8;
+    if (threadIdx.x < 32) src_row[threadIdx.x] = gather_src(rb * 32 + threadIdx.x, gather);
+    __syncthreads();
     uint4 w[8];
     float amax[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) amax[j] = 0.f;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      w[r] = active ? src[static_cast<int64_t>(rs + 4 * r) * C8] : make_uint4(0, 0, 0, 0);
+      const int sr = src_row[rs + 4 * r];
+      w[r] = active && sr >= 0 ? in[static_cast<int64_t>(sr) * C8 + c8] : make_uint4(0, 0, 0, 0);
       const uint16_t* h = reinterpret_cast<const uint16_t*>(&w[r]);
 #pragma unroll
       for (int j = 0; j < 8; ++j) amax[j] = fmaxf(amax[j], fabsf(bf(h[j])));
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(256) mx_qdq_cols_kernel(const uint4* in, uint4
       const int c = cg * 8 + j;
       e[j] = scale_exp(fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c])));
     }
-    __syncthreads();  // part[] is rewritten by the next tile
+    __syncthreads();  // part[] and src_row[] are rewritten by the next tile
     if (active) {
       uint4* dst = out + rb * 32 * C8 + c8;
 #pragma unroll
@@ -155,7 +160,8 @@ __global__ void __launch_bounds__(256) mx_qdq_cols_kernel(const uint4* in, uint4
 }
 
 cudaError_t launch_mx_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
-                          int64_t cols, bool along_rows, const int* meta, uint16_t* out_rows) {
+                          int64_t cols, bool along_rows, const int* meta, uint16_t* out_rows,
+                          RowGather gather) {
   const int id = along_rows ? K_MX_QDQ_ROWS : K_MX_QDQ_COLS;
   prof_begin(c, id);
   if (along_rows) {
@@ -169,7 +175,7 @@ cudaError_t launch_mx_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64
     const int64_t grid = tiles < c.num_sms * 6 ? tiles : c.num_sms * 6;
     mx_qdq_cols_kernel<<<static_cast<int>(grid > 0 ? grid : 1), 256, 0, c.stream>>>(
         reinterpret_cast<const uint4*>(in), reinterpret_cast<uint4*>(out),
-        reinterpret_cast<uint4*>(out_rows), rows, static_cast<int>(cols / 8), meta);
+        reinterpret_cast<uint4*>(out_rows), rows, static_cast<int>(cols / 8), meta, gather);
   }
   prof_end(c, id);
   return cudaGetLastError();

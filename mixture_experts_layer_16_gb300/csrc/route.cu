@@ -10,7 +10,9 @@
 
 #include <algorithm>
 
+#include "fp8block.cuh"
 #include "internal.h"
+#include "mx.cuh"
 #include "ptx.cuh"
 
 namespace mmmoe {
@@ -248,14 +250,77 @@ cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* 
 // ---------------------------------------------------------------- 4. permute
 // dst[prow[t*k + j]] = src[t] for every routed pair, and zero padding rows.  Tokens
 // are walked in order so that each source row is read from HBM once and stored to
-// its k destinations.  Whole rows move by TMA bulk copies: one lane per CTA drives
+// its k destinations.  Whole rows move by TMA bulk copies: lane 0 of each CTA drives
 // a ring of PERM_SLOTS row buffers, loading PERM_AHEAD tokens ahead of the one it
 // stores.  Padding rows are then stored from a zero row; in the forward their
 // routing weight is zeroed too (valid rows got theirs from the placement kernel).
+// QM = QS_MX / QS_BLOCK: the warp quantises each row in shared memory (32- / 128-
+// element blocks along the row) between its load and its stores, so the k copies are
+// the row's quantised values; a zero row quantises to itself.
 constexpr int PERM_SLOTS = 8;
 constexpr int PERM_AHEAD = 4;
 constexpr uint64_t PERM_WAIT_NS = 2000000000ull;
 
+// Quantise one bf16 row of n elements in shared memory in place (all 32 lanes).
+template <int QM>
+__device__ __forceinline__ void quantise_row(uint8_t* row, int n, int lane) {
+  uint4* r4 = reinterpret_cast<uint4*>(row);
+  if constexpr (QM == QS_MX) {  // a lane per 32-element block (four 16-byte pieces)
+    for (int b = lane; b < n / 32; b += 32) {
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = r4[4 * b + q];
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[8 * q + j] = mx::bf(h[j]);
+      }
+      mx::qdq_row32(v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        uint16_t* h = reinterpret_cast<uint16_t*>(&w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) h[j] = mx::to_bf(v[8 * q + j]);
+        r4[4 * b + q] = w;
+      }
+    }
+  } else {  // a lane per half block (64 elements), neighbouring lanes pair up
+    const int nh = n / 64;  // even: n % 128 == 0
+    for (int h0 = 0; h0 < nh; h0 += 32) {
+      const int hb = h0 + lane;
+      const bool act = hb < nh;  // the partner lane (lane ^ 1) has the same value
+      float v[64];
+      float m = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint4 w = act ? r4[8 * hb + q] : make_uint4(0, 0, 0, 0);
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[8 * q + j] = mx::bf(h[j]);
+          m = fmaxf(m, fabsf(v[8 * q + j]));
+        }
+      }
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      const int e = fb::ceil_exp(m);
+#pragma unroll
+      for (int j = 0; j < 64; j += 2) mx::qdq2(v[j], v[j + 1], e, e);
+      if (act) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint4 w;
+          uint16_t* h = reinterpret_cast<uint16_t*>(&w);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) h[j] = mx::to_bf(v[8 * q + j]);
+          r4[8 * hb + q] = w;
+        }
+      }
+    }
+  }
+}
+
+template <int QM>
 __global__ void __launch_bounds__(32) permute_rows_kernel(
     const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int row_bytes, int T, int k,
     const int* __restrict__ meta, const int* __restrict__ tile_rows,
@@ -272,7 +337,7 @@ __global__ void __launch_bounds__(32) permute_rows_kernel(
     ptx::fence_barrier_init();
   }
   __syncwarp();
-  if (lane != 0) return;
+  if (QM == QS_NONE && lane != 0) return;
   const int first = static_cast<int>(blockIdx.x), step = static_cast<int>(gridDim.x);
   // --- routed rows, token by token
   const int n_my = T > first ? (T - 1 - first) / step + 1 : 0;
@@ -282,35 +347,52 @@ __global__ void __launch_bounds__(32) permute_rows_kernel(
     ptx::mbar_arrive_expect_tx(&bar[s], static_cast<uint32_t>(row_bytes));
     ptx::bulk_load(pbuf + s * row_bytes, src + t * row_bytes, row_bytes, &bar[s]);
   };
-  for (int i = 0; i < PERM_AHEAD && i < n_my; ++i) issue(i);
+  if (lane == 0)
+    for (int i = 0; i < PERM_AHEAD && i < n_my; ++i) issue(i);
   int dummy = 0;
   for (int i = 0; i < n_my; ++i) {
-    if (i + PERM_AHEAD < n_my) {
+    if (lane == 0 && i + PERM_AHEAD < n_my) {
       // the slot of token i + PERM_AHEAD last held token i + PERM_AHEAD - PERM_SLOTS,
       // whose stores (one group, PERM_SLOTS - PERM_AHEAD groups ago) must have read it
       ptx::bulk_wait_read<PERM_SLOTS - PERM_AHEAD - 1>();
       issue(i + PERM_AHEAD);
     }
     const int s = i % PERM_SLOTS;
-    if (!ptx::mbar_wait(&bar[s], static_cast<uint32_t>((i / PERM_SLOTS) & 1), &dummy,
-                        PERM_WAIT_NS)) {
-      if (atomicCAS(&status->code, 0, MM_MOE_ETIMEOUT) == 0) status->detail = -1;
-      // the loads already issued land before the CTA exits (bounded as well)
-      for (int j = i + 1; j < i + PERM_AHEAD + 1 && j < n_my; ++j)
-        ptx::mbar_wait(&bar[j % PERM_SLOTS], static_cast<uint32_t>((j / PERM_SLOTS) & 1),
-                       &dummy, PERM_WAIT_NS);
-      ptx::bulk_wait_all();
+    const uint32_t parity = static_cast<uint32_t>((i / PERM_SLOTS) & 1);
+    int ok = 1;
+    if (lane == 0) ok = ptx::mbar_wait(&bar[s], parity, &dummy, PERM_WAIT_NS) ? 1 : 0;
+    if constexpr (QM != QS_NONE) ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) {
+        if (atomicCAS(&status->code, 0, MM_MOE_ETIMEOUT) == 0) status->detail = -1;
+        // the loads already issued land before the CTA exits (bounded as well)
+        for (int j = i + 1; j < i + PERM_AHEAD + 1 && j < n_my; ++j)
+          ptx::mbar_wait(&bar[j % PERM_SLOTS], static_cast<uint32_t>((j / PERM_SLOTS) & 1),
+                         &dummy, PERM_WAIT_NS);
+        ptx::bulk_wait_all();
+      }
       return;
     }
-    const int64_t f0 = (first + static_cast<int64_t>(i) * step) * k;
-    for (int j = 0; j < k; ++j) {
-      const int pr = __ldg(prow + f0 + j);
-      if (pr >= 0)
-        ptx::bulk_store(dst + static_cast<int64_t>(pr) * row_bytes, pbuf + s * row_bytes,
-                        row_bytes);
+    if constexpr (QM != QS_NONE) {
+      // the other lanes observe the completed phase too (it returns at once), which
+      // makes the row's bytes visible to them
+      if (lane != 0) ptx::mbar_wait(&bar[s], parity, &dummy, PERM_WAIT_NS);
+      quantise_row<QM>(pbuf + s * row_bytes, row_bytes / 2, lane);
+      ptx::fence_proxy_async_smem();  // the stores below read the quantised row
+      __syncwarp();
     }
-    ptx::bulk_commit();
+    if (lane == 0) {
+      const int64_t f0 = (first + static_cast<int64_t>(i) * step) * k;
+      for (int j = 0; j < k; ++j) {
+        const int pr = __ldg(prow + f0 + j);
+        if (pr >= 0)
+          ptx::bulk_store(dst + static_cast<int64_t>(pr) * row_bytes, pbuf + s * row_bytes,
+                          row_bytes);
+      }
+      ptx::bulk_commit();
+    }
   }
+  if (lane != 0) return;
   // --- padding rows of the M tiles
   const int n_tiles = __ldg(meta + META_NUM_TILES);
   for (int mb = first; mb < n_tiles; mb += step) {
@@ -325,15 +407,18 @@ __global__ void __launch_bounds__(32) permute_rows_kernel(
 }
 
 cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
-                           const char* saved, float* w_row_out, int kernel_id, char* scratch) {
+                           const char* saved, float* w_row_out, int kernel_id, char* scratch,
+                           int quant) {
   const int row_bytes = static_cast<int>(L.H * 2);
   const int smem = (PERM_SLOTS + 1) * row_bytes;
-  cudaError_t e = cudaFuncSetAttribute(permute_rows_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto* kern = quant == QS_MX      ? permute_rows_kernel<QS_MX>
+               : quant == QS_BLOCK ? permute_rows_kernel<QS_BLOCK>
+                                   : permute_rows_kernel<QS_NONE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int per_sm = std::max(1, std::min(16, (200 * 1024) / (smem + 1024)));
   prof_begin(c, kernel_id);
-  permute_rows_kernel<<<c.num_sms * per_sm, 32, smem, c.stream>>>(
+  kern<<<c.num_sms * per_sm, 32, smem, c.stream>>>(
       reinterpret_cast<const uint8_t*>(src), reinterpret_cast<uint8_t*>(dst), row_bytes,
       static_cast<int>(L.T), static_cast<int>(L.k), reinterpret_cast<const int*>(saved + L.meta),
       reinterpret_cast<const int*>(saved + L.tile_rows),
