@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernels", action="store_true", help="also print the per-kernel table")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step recorded once in a CUDA graph and replayed")
     ap.add_argument("--recompute", action="store_true",
                     help="activation checkpointing: the backward re-runs the gate/up stage")
     ap.add_argument("--with-router", action="store_true",
@@ -465,6 +467,38 @@ def run_ours(args):
                        "double-buffered (the next step's inputs arrive during this step); "
                        "weights and weight gradients stay on the device"}
 
+    # ------------------------------------------------ the same step as one CUDA graph
+    # (reported beside the eager number, which stays the line's value): the layer's
+    # forward and backward recorded once on device-resident inputs, then replayed
+    graph = None
+    if args.graph and router is None:
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):     # one eager step on the capture stream first
+            step(g["x"], g["topk_idx"], g["topk_w"], g["dy"], y, outs)
+        stream.wait_stream(cs)
+        torch.cuda.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            step(g["x"], g["topk_idx"], g["topk_w"], g["dy"], y, outs)
+        for _ in range(max(args.warmup, 3)):
+            cg.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        s3, t3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s3.record(stream)
+        for _ in range(K):
+            cg.replay()
+        t3.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        g_ms = max_over_ranks(s3.elapsed_time(t3) / K, world, dev)
+        if layer.status() != B.MM_MOE_OK:
+            raise RuntimeError("device status after the graph replays: " + B.STATUS[layer.status()])
+        graph = {"value": aggregate_value(step_flops(cfg, False), world, g_ms), "unit": "TFLOP/s",
+                 "ms_per_step": g_ms,
+                 "note": "forward + backward recorded once in a CUDA graph, replayed K times"}
+
     if rank != 0:
         return 0
 
@@ -531,6 +565,7 @@ def run_ours(args):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "graph": graph,
         # this library's kernels: the layer's, and the router's selection and logit
         # gradient when it runs (its three products are cuBLAS kernels, not counted)
         "gpu_launches": (n_fwd_launch + n_bwd_launch + (2 if router is not None else 0)) * K,
