@@ -4,7 +4,7 @@
 //
 // Prime Mega MoE pages, "How does the fused kernel work?": the two expert linear
 // layers with SwiGLU between them and the combine in the forward, and the
-// matching backward.  Six variants share the main loop:
+// matching backward.  Seven kinds share the main loop:
 //   GATEUP       [g|u] = x_perm . [W_gate;W_up]^T  per expert M block, SwiGLU epilogue
 //   DOWN         o = a . W_down^T                   epilogue w*o (expert-grouped rows)
 //   DGRAD_DOWN   g' = dy_perm . W_down               dSwiGLU epilogue (dh, w*a, <a,g'>)
