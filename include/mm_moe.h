@@ -117,9 +117,10 @@ typedef struct {
  *             of the weights (MXFP8: along their backward contraction axis;
  *             blockwise: the one copy every GEMM reads), so the backward's weight
  *             arguments must be the forward's, as in every mode.  With MM_MOE_RECOMPUTE it holds
- *             only the routing and the routing weights in routed order; x, h and a
- *             live in `scratch`.  It must not change between the forward and its
- *             backward.
+ *             only the routing and the routing weights in routed order; the
+ *             expert-grouped x (under a quantised forward only its quantised copy), h
+ *             and a live in `scratch`.  It must not change between the forward and
+ *             its backward.
  * Returns MM_MOE_EINVAL for an invalid shape. */
 MM_MOE_API mm_moe_status mm_moe_workspace_size(const mm_moe_shape* shape,
                                     size_t* scratch_bytes, size_t* saved_bytes);

@@ -22,6 +22,7 @@ bool sm_pairs_enabled() {
 
 mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   if (s == nullptr || L == nullptr) return MM_MOE_EINVAL;
+  *L = Layout{};  // offsets a mode does not use stay 0
   if (s->T < 1 || s->H < 1 || s->I < 1 || s->E < 1 || s->k < 1) return MM_MOE_EINVAL;
   if (s->k > s->E || s->E > MAX_E) return MM_MOE_EINVAL;
   if (s->H % 128 != 0 || s->I % 64 != 0) return MM_MOE_EINVAL;
@@ -90,7 +91,10 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->status = take(256);
   L->blk_counts = take(4 * static_cast<size_t>(L->nblk) * E);
   if (L->recompute) {  // live through the forward and the backward's recompute
-    L->x_perm = take(2 * Rp * H);
+    // (a quantised forward permutes x straight into its quantised copy q_x and the
+    // backward gathers x's token-axis blocks from x: no x_perm; its offset is then
+    // never dereferenced)
+    if (L->qf == QS_NONE) L->x_perm = take(2 * Rp * H);
     L->h = take(2 * Rp * 2 * I);
     L->a = take(2 * Rp * I);
   }
@@ -397,7 +401,8 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   const uint16_t* a = reinterpret_cast<const uint16_t*>(act + L.a);
   MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
   if (L.recompute) {
-    // activation checkpointing: x_perm, h and a again, as the forward made them
+    // activation checkpointing: gate/up's operand (x_perm, or q_x under a quantised
+    // forward), h and a again, as the forward made them
     uint16_t* xp = reinterpret_cast<uint16_t*>(sc + L.x_perm);
     cudaError_t err = cudaSuccess;
     const uint16_t* A0 = permute_x(c, L, x, xp, nullptr, sv, nullptr, sc, &err);
