@@ -284,8 +284,8 @@ def run_ours(args):
     import torch
 
     world, rank, local = dist_info()
+    torch.cuda.set_device(local)      # each rank's GPU before its NCCL group forms
     init_dist(world, "nccl")
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
     from mixture_experts_layer_16_gb300 import binding as B
