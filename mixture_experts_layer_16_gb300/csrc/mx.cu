@@ -87,73 +87,76 @@ __global__ void __launch_bounds__(256) mx_qdq_cols_kernel(const uint4* in, uint4
                                                           const int* __restrict__ meta,
                                                           const RowGather gather) {
   __shared__ float part[4][COL_TILE];
-  __shared__ int src_row[32];  // the tile's source rows (-1: zero), resolved once
+  __shared__ int src_row[32];  // the row block's source rows (-1: zero)
   if (meta != nullptr) rows = used_rows(rows, meta);
   const int col_tiles = (C8 * 8 + COL_TILE - 1) / COL_TILE;
-  const int64_t tiles = (rows / 32) * col_tiles;
+  const int64_t row_blocks = rows / 32;
   const int cg = threadIdx.x % 64, rs = threadIdx.x / 64;
-  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-    const int64_t rb = tile / col_tiles;
-    const int c8 = static_cast<int>(tile - rb * col_tiles) * (COL_TILE / 8) + cg;
-    const bool active = c8 < C8;
+  // a CTA takes whole 32-row blocks, their column tiles in turn: the block's source
+  // rows are resolved once
+  for (int64_t rb = blockIdx.x; rb < row_blocks; rb += gridDim.x) {
     if (threadIdx.x < 32) src_row[threadIdx.x] = gather_src(rb * 32 + threadIdx.x, gather);
     __syncthreads();
-    uint4 w[8];
-    float amax[8];
+    for (int ct = 0; ct < col_tiles; ++ct) {
+      const int c8 = ct * (COL_TILE / 8) + cg;
+      const bool active = c8 < C8;
+      uint4 w[8];
+      float amax[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) amax[j] = 0.f;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const int sr = src_row[rs + 4 * r];
-      w[r] = active && sr >= 0 ? in[static_cast<int64_t>(sr) * C8 + c8] : make_uint4(0, 0, 0, 0);
-      const uint16_t* h = reinterpret_cast<const uint16_t*>(&w[r]);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) amax[j] = fmaxf(amax[j], fabsf(bf(h[j])));
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) part[rs][cg * 8 + j] = amax[j];
-    if (out_rows != nullptr) {  // uniform: every lane takes part in the shuffles
+      for (int j = 0; j < 8; ++j) amax[j] = 0.f;
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        uint4 o = w[r];
-        uint16_t* h = reinterpret_cast<uint16_t*>(&o);
-        float ra = 0.f;
+        const int sr = src_row[rs + 4 * r];
+        w[r] = active && sr >= 0 ? in[static_cast<int64_t>(sr) * C8 + c8] : make_uint4(0, 0, 0, 0);
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&w[r]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ra = fmaxf(ra, fabsf(bf(h[j])));
-        ra = fmaxf(ra, __shfl_xor_sync(0xffffffffu, ra, 1));
-        ra = fmaxf(ra, __shfl_xor_sync(0xffffffffu, ra, 2));
-        const int re = scale_exp(ra);
-#pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          float x0 = bf(h[j]), x1 = bf(h[j + 1]);
-          qdq2(x0, x1, re, re);
-          h[j] = to_bf(x0);
-          h[j + 1] = to_bf(x1);
-        }
-        if (active) out_rows[rb * 32 * C8 + c8 + static_cast<int64_t>(rs + 4 * r) * C8] = o;
+        for (int j = 0; j < 8; ++j) amax[j] = fmaxf(amax[j], fabsf(bf(h[j])));
       }
-    }
-    __syncthreads();
-    int e[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = cg * 8 + j;
-      e[j] = scale_exp(fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c])));
-    }
-    __syncthreads();  // part[] and src_row[] are rewritten by the next tile
-    if (active) {
-      uint4* dst = out + rb * 32 * C8 + c8;
+      for (int j = 0; j < 8; ++j) part[rs][cg * 8 + j] = amax[j];
+      if (out_rows != nullptr) {  // uniform: every lane takes part in the shuffles
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        uint16_t* h = reinterpret_cast<uint16_t*>(&w[r]);
+        for (int r = 0; r < 8; ++r) {
+          uint4 o = w[r];
+          uint16_t* h = reinterpret_cast<uint16_t*>(&o);
+          float ra = 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; j += 2) {
-          float x0 = bf(h[j]), x1 = bf(h[j + 1]);
-          qdq2(x0, x1, e[j], e[j + 1]);
-          h[j] = to_bf(x0);
-          h[j + 1] = to_bf(x1);
+          for (int j = 0; j < 8; ++j) ra = fmaxf(ra, fabsf(bf(h[j])));
+          ra = fmaxf(ra, __shfl_xor_sync(0xffffffffu, ra, 1));
+          ra = fmaxf(ra, __shfl_xor_sync(0xffffffffu, ra, 2));
+          const int re = scale_exp(ra);
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            float x0 = bf(h[j]), x1 = bf(h[j + 1]);
+            qdq2(x0, x1, re, re);
+            h[j] = to_bf(x0);
+            h[j + 1] = to_bf(x1);
+          }
+          if (active) out_rows[rb * 32 * C8 + c8 + static_cast<int64_t>(rs + 4 * r) * C8] = o;
         }
-        dst[static_cast<int64_t>(rs + 4 * r) * C8] = w[r];
+      }
+      __syncthreads();
+      int e[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = cg * 8 + j;
+        e[j] = scale_exp(fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c])));
+      }
+      __syncthreads();  // part[] (and, at the next row block, src_row[]) is rewritten
+      if (active) {
+        uint4* dst = out + rb * 32 * C8 + c8;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          uint16_t* h = reinterpret_cast<uint16_t*>(&w[r]);
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            float x0 = bf(h[j]), x1 = bf(h[j + 1]);
+            qdq2(x0, x1, e[j], e[j + 1]);
+            h[j] = to_bf(x0);
+            h[j + 1] = to_bf(x1);
+          }
+          dst[static_cast<int64_t>(rs + 4 * r) * C8] = w[r];
+        }
       }
     }
   }
@@ -171,8 +174,8 @@ cudaError_t launch_mx_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64
   } else {
     // with `meta` the row count is known only on the device: size the grid for the
     // capacity and let surplus CTAs exit
-    const int64_t tiles = (rows / 32) * ((cols + COL_TILE - 1) / COL_TILE);
-    const int64_t grid = tiles < c.num_sms * 6 ? tiles : c.num_sms * 6;
+    const int64_t blocks = rows / 32;  // 32-row blocks (a CTA takes whole ones)
+    const int64_t grid = blocks < c.num_sms * 6 ? blocks : c.num_sms * 6;
     mx_qdq_cols_kernel<<<static_cast<int>(grid > 0 ? grid : 1), 256, 0, c.stream>>>(
         reinterpret_cast<const uint4*>(in), reinterpret_cast<uint4*>(out),
         reinterpret_cast<uint4*>(out_rows), rows, static_cast<int>(cols / 8), meta, gather);
