@@ -254,32 +254,53 @@ static const uint16_t* permute_x(const Ctx& c, const Layout& L, const uint16_t* 
 // adds a row pass over a.  The backward under MM_MOE_RECOMPUTE calls it with the
 // forward's arguments and gets h and a bit for bit (the same kernels on the same
 // inputs).
-static mm_moe_status gateup_stage(const Ctx& c, const Layout& L, bool keep, bool emit_qa,
-                                  const uint16_t* A, const uint16_t* W_gate,
-                                  const uint16_t* W_up, const uint16_t* W_down, uint16_t* h,
-                                  uint16_t* a, const char* sv, char* wbase, char* sc) {
-  const int* meta = reinterpret_cast<const int*>(sv + L.meta);
+// The weight copies of a quantised forward (see gateup_stage); they read only the
+// weights, so the forward runs them on its side stream beside the routing.
+static cudaError_t weight_copies(const Ctx& c, const Layout& L, bool keep, bool emit_qa,
+                                 const uint16_t* W_gate, const uint16_t* W_up,
+                                 const uint16_t* W_down, char* wbase, char* sc) {
   const int64_t EI = L.E * L.I, EH = L.E * L.H;
   auto sq = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
   auto wq = [&](size_t off) { return reinterpret_cast<uint16_t*>(wbase + off); };
-  const uint16_t *Bg = W_gate, *Bu = W_up;
+  cudaError_t e = cudaSuccess;
   if (L.qf == QS_MX) {
     if (keep) {  // one read each, both axes
-      MM_MOE_TRY(launch_mx_qdq(c, W_gate, wq(L.q_wgc), EI, L.H, false, nullptr, sq(L.q_wg)));
-      MM_MOE_TRY(launch_mx_qdq(c, W_up, wq(L.q_wuc), EI, L.H, false, nullptr, sq(L.q_wu)));
-      if (emit_qa)
-        MM_MOE_TRY(launch_mx_qdq(c, W_down, wq(L.q_wdc), EH, L.I, false, nullptr, sq(L.q_wd)));
+      e = launch_mx_qdq(c, W_gate, wq(L.q_wgc), EI, L.H, false, nullptr, sq(L.q_wg));
+      if (e == cudaSuccess)
+        e = launch_mx_qdq(c, W_up, wq(L.q_wuc), EI, L.H, false, nullptr, sq(L.q_wu));
+      if (e == cudaSuccess && emit_qa)
+        e = launch_mx_qdq(c, W_down, wq(L.q_wdc), EH, L.I, false, nullptr, sq(L.q_wd));
     } else {
-      MM_MOE_TRY(launch_mx_qdq(c, W_gate, sq(L.q_wg), EI, L.H, true, nullptr));
-      MM_MOE_TRY(launch_mx_qdq(c, W_up, sq(L.q_wu), EI, L.H, true, nullptr));
-      if (emit_qa) MM_MOE_TRY(launch_mx_qdq(c, W_down, sq(L.q_wd), EH, L.I, true, nullptr));
+      e = launch_mx_qdq(c, W_gate, sq(L.q_wg), EI, L.H, true, nullptr);
+      if (e == cudaSuccess) e = launch_mx_qdq(c, W_up, sq(L.q_wu), EI, L.H, true, nullptr);
+      if (e == cudaSuccess && emit_qa)
+        e = launch_mx_qdq(c, W_down, sq(L.q_wd), EH, L.I, true, nullptr);
     }
+  } else if (L.qf == QS_BLOCK) {  // the copies every GEMM of the layer reads
+    e = launch_fb_qdq(c, W_gate, wq(L.q_wgc), EI, L.H, FB_TILES, nullptr, nullptr);
+    if (e == cudaSuccess)
+      e = launch_fb_qdq(c, W_up, wq(L.q_wuc), EI, L.H, FB_TILES, nullptr, nullptr);
+    if (e == cudaSuccess)
+      e = launch_fb_qdq(c, W_down, wq(L.q_wdc), EH, L.I, FB_TILES, nullptr, nullptr);
+  }
+  return e;
+}
+
+static mm_moe_status gateup_stage(const Ctx& c, const Layout& L, bool keep, bool emit_qa,
+                                  const uint16_t* A, const uint16_t* W_gate,
+                                  const uint16_t* W_up, const uint16_t* W_down, uint16_t* h,
+                                  uint16_t* a, const char* sv, char* wbase, char* sc,
+                                  bool weights_ready = false) {
+  const int* meta = reinterpret_cast<const int*>(sv + L.meta);
+  auto sq = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
+  auto wq = [&](size_t off) { return reinterpret_cast<uint16_t*>(wbase + off); };
+  if (!weights_ready)
+    MM_MOE_TRY(weight_copies(c, L, keep, emit_qa, W_gate, W_up, W_down, wbase, sc));
+  const uint16_t *Bg = W_gate, *Bu = W_up;
+  if (L.qf == QS_MX) {
     Bg = sq(L.q_wg);
     Bu = sq(L.q_wu);
-  } else if (L.qf == QS_BLOCK) {  // the copies every GEMM of the layer reads
-    MM_MOE_TRY(launch_fb_qdq(c, W_gate, wq(L.q_wgc), EI, L.H, FB_TILES, nullptr, nullptr));
-    MM_MOE_TRY(launch_fb_qdq(c, W_up, wq(L.q_wuc), EI, L.H, FB_TILES, nullptr, nullptr));
-    MM_MOE_TRY(launch_fb_qdq(c, W_down, wq(L.q_wdc), EH, L.I, FB_TILES, nullptr, nullptr));
+  } else if (L.qf == QS_BLOCK) {
     Bg = wq(L.q_wgc);
     Bu = wq(L.q_wuc);
   }
@@ -334,6 +355,20 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   char* sc = static_cast<char*>(scratch);
   char* sv = static_cast<char*>(saved);
   MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
+  // A quantised forward's weight copies read only the weights: they run on the side
+  // stream beside the routing, the permutation and the token-axis gather, which write
+  // none of the buffers they write, and gate/up waits for them
+  char* wbase = L.w_common ? sc : sv;  // where the backward's (blockwise: all) weight copies go
+  const bool side = L.qf != QS_NONE;
+  SideStream ss;
+  if (side) {
+    if (!side_stream(&ss)) return MM_MOE_ECUDA;
+    MM_MOE_TRY(cudaEventRecord(ss.fork, c.stream));
+    MM_MOE_TRY(cudaStreamWaitEvent(ss.s, ss.fork, 0));
+    const Ctx cs{ss.s, d.sms, &launches};
+    MM_MOE_TRY(weight_copies(cs, L, L.w_in_saved, true, W_gate, W_up, W_down, wbase, sc));
+    MM_MOE_TRY(cudaEventRecord(ss.join, ss.s));
+  }
   MM_MOE_TRY(launch_route(c, L, topk_idx, topk_w, sv, sc));
   // x_perm, h, a: kept in saved, or in scratch under MM_MOE_RECOMPUTE
   char* act = L.recompute ? sc : sv;
@@ -348,8 +383,9 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   const uint16_t* A1 = permute_x(c, L, x, x_perm, L.w_in_saved ? x_perm : nullptr, sv,
                                  reinterpret_cast<float*>(sv + L.w_row), sc, &err);
   MM_MOE_TRY(err);
-  char* wbase = L.w_common ? sc : sv;  // where the backward's (blockwise: all) weight copies go
-  st = gateup_stage(c, L, L.w_in_saved, true, A1, W_gate, W_up, W_down, h, a, sv, wbase, sc);
+  if (side) MM_MOE_TRY(cudaStreamWaitEvent(c.stream, ss.join, 0));
+  st = gateup_stage(c, L, L.w_in_saved, true, A1, W_gate, W_up, W_down, h, a, sv, wbase, sc,
+                    side);
   if (st != MM_MOE_OK) return st;
   const uint16_t* A2 = L.qf != QS_NONE ? reinterpret_cast<uint16_t*>(sc + L.q_a) : a;
   const uint16_t* Bd = L.qf == QS_MX      ? reinterpret_cast<uint16_t*>(sc + L.q_wd)
