@@ -257,7 +257,10 @@ MM_MOE_API mm_moe_status mm_moe_read_status(const void* scratch, void* stream);
  * threads) race and must be serialised by the caller.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that device
  * current; make that first call before any stream capture.  Pairs whose expert
- * index is outside [0, E) are dropped (inv = -1, offsets[E] < T * k).
+ * index is outside [0, E) are dropped: their inv is -1, offsets[E] (the routed
+ * rows) is then below T * k and perm[offsets[E] .. T*k) is left unwritten.  This
+ * is the only report of such pairs: the call has no status word a caller can read
+ * (mm_moe_read_status reads a caller's scratch, which this call does not take).
  * Returns MM_MOE_EINVAL for sizes beyond the limits or NULL / misaligned
  * pointers, MM_MOE_ENOTSUP off sm_103, MM_MOE_ECUDA for a failed CUDA call.
  * Enqueues on `stream` and returns without synchronising. */

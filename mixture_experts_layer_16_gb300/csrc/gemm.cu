@@ -177,9 +177,13 @@ __device__ __forceinline__ int total_tiles(const GemmParams& p) {
   }
 }
 
+// A wait ran out: this CTA's roles give up (*abort), and on an SM pair the peer CTA's
+// too (peer_abort: the shared::cluster address of its abort flag, 0 on single SMs),
+// so that neither CTA waits out its own limits for work the other will never do.
 __device__ __forceinline__ void record_timeout(GemmParams const& p, volatile int* abort,
-                                               int detail) {
+                                               int detail, uint32_t peer_abort = 0) {
   *abort = 1;
+  if (peer_abort != 0) ptx::st_cluster_u32(peer_abort, 1u);
   if (atomicCAS(&p.status->code, 0, MM_MOE_ETIMEOUT) == 0) p.status->detail = detail;
 }
 
@@ -512,6 +516,8 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
   ptx::tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   volatile int* abort = &s_abort;
+  const uint32_t peer_abort =
+      CTAS == 1 ? 0u : ptx::map_to_rank(ptx::smem_u32(&s_abort), static_cast<uint32_t>(rank ^ 1));
   const int total = total_tiles<KIND, BN, CTAS>(p);
   // the pair's barriers that both CTAs signal live in the rank-0 CTA
   const uint32_t lead_full0 = CTAS == 1 ? ptx::smem_u32(&full_bar[0])
@@ -529,7 +535,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
       const TileInfo ti = decode_tile<KIND, BN, CTAS>(p, t, rank);
       for (int kb = 0; kb < ti.k_iters; ++kb) {
         if (!ptx::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, WAIT_LIMIT_NS)) {
-          record_timeout(p, abort, KIND * 16 + 1);
+          record_timeout(p, abort, KIND * 16 + 1, peer_abort);
           ok = false;
           break;
         }
@@ -548,13 +554,16 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
       }
     }
     // drain: every issued copy has landed before the CTA may exit (rank 0: its full
-    // barriers; rank 1: consumption of its stages, which implies they landed)
+    // barriers; rank 1: consumption of its stages, which implies they landed).  After
+    // a failure the stages may never complete: all waits share one time budget.
+    const uint64_t deadline = ptx::globaltimer() + WAIT_LIMIT_NS;
     for (int s = 0; s < C::STAGES; ++s) {
       if (last_parity[s] < 0) continue;
-      int dummy = 0;
       uint64_t* bar = rank == 0 ? &full_bar[s] : &empty_bar[s];
-      if (!ptx::mbar_wait(bar, static_cast<uint32_t>(last_parity[s]), &dummy, WAIT_LIMIT_NS))
+      if (!ptx::mbar_wait_until(bar, static_cast<uint32_t>(last_parity[s]), deadline)) {
         record_timeout(p, abort, KIND * 16 + 2);
+        break;
+      }
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------------------------------------------------------- MMA issuer
@@ -568,14 +577,14 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
       const TileInfo ti = decode_tile<KIND, BN, CTAS>(p, t, rank);
       if (ti.k_iters == 0) continue;
       if (!ptx::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort, WAIT_LIMIT_NS)) {
-        record_timeout(p, abort, KIND * 16 + 3);
+        record_timeout(p, abort, KIND * 16 + 3, peer_abort);
         break;
       }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
       for (int kb = 0; kb < ti.k_iters; ++kb) {
         if (!ptx::mbar_wait(&full_bar[stage], phase, abort, WAIT_LIMIT_NS)) {
-          record_timeout(p, abort, KIND * 16 + 4);
+          record_timeout(p, abort, KIND * 16 + 4, peer_abort);
           ok = false;
           break;
         }
@@ -640,7 +649,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
       if (lane == 0) ok = ptx::mbar_wait(&tfull_bar[acc], acc_phase, abort, WAIT_LIMIT_NS) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
-        if (lane == 0) record_timeout(p, abort, KIND * 16 + 6);
+        if (lane == 0) record_timeout(p, abort, KIND * 16 + 6, peer_abort);
         break;
       }
       ptx::tc_fence_after();
@@ -648,7 +657,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(q * 32) << 16);
       if (!epilogue_tile<KIND, BN, CTAS, MX>(p, ti, has_next ? &nx : nullptr, q, tbase, w, abort)) {
-        if (lane == 0) record_timeout(p, abort, KIND * 16 + 7);
+        if (lane == 0) record_timeout(p, abort, KIND * 16 + 7, peer_abort);
         break;
       }
       ptx::tc_fence_before();

@@ -197,6 +197,40 @@ static bool side_stream(SideStream* out) {
   return true;
 }
 
+// A fork of the caller's stream onto the side stream that is joined back on every
+// return: join() on the normal path, the destructor on an error return after the
+// fork, so that no path leaves forked work unordered before later work on the
+// caller's stream (or an unjoined fork in a stream capture).
+class Fork {
+ public:
+  Fork() = default;
+  Fork(const Fork&) = delete;
+  Fork& operator=(const Fork&) = delete;
+  ~Fork() { (void)join(); }
+  // Returns false when the side stream or the fork could not be made.
+  bool open(cudaStream_t main) {
+    if (!side_stream(&ss_)) return false;
+    main_ = main;
+    if (cudaEventRecord(ss_.fork, main) != cudaSuccess) return false;
+    if (cudaStreamWaitEvent(ss_.s, ss_.fork, 0) != cudaSuccess) return false;
+    open_ = true;
+    return true;
+  }
+  cudaStream_t side() const { return ss_.s; }
+  cudaError_t join() {
+    if (!open_) return cudaSuccess;
+    open_ = false;
+    cudaError_t e = cudaEventRecord(ss_.join, ss_.s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(main_, ss_.join, 0);
+    return e;
+  }
+
+ private:
+  SideStream ss_;
+  cudaStream_t main_ = nullptr;
+  bool open_ = false;
+};
+
 #define MM_MOE_TRY(expr)                         \
   do {                                           \
     if ((expr) != cudaSuccess) return MM_MOE_ECUDA; \
@@ -360,14 +394,11 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   // none of the buffers they write, and gate/up waits for them
   char* wbase = L.w_common ? sc : sv;  // where the backward's (blockwise: all) weight copies go
   const bool side = L.qf != QS_NONE;
-  SideStream ss;
+  Fork fork;
   if (side) {
-    if (!side_stream(&ss)) return MM_MOE_ECUDA;
-    MM_MOE_TRY(cudaEventRecord(ss.fork, c.stream));
-    MM_MOE_TRY(cudaStreamWaitEvent(ss.s, ss.fork, 0));
-    const Ctx cs{ss.s, d.sms, &launches};
+    if (!fork.open(c.stream)) return MM_MOE_ECUDA;
+    const Ctx cs{fork.side(), d.sms, &launches};
     MM_MOE_TRY(weight_copies(cs, L, L.w_in_saved, true, W_gate, W_up, W_down, wbase, sc));
-    MM_MOE_TRY(cudaEventRecord(ss.join, ss.s));
   }
   MM_MOE_TRY(launch_route(c, L, topk_idx, topk_w, sv, sc));
   // x_perm, h, a: kept in saved, or in scratch under MM_MOE_RECOMPUTE
@@ -383,7 +414,7 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   const uint16_t* A1 = permute_x(c, L, x, x_perm, L.w_in_saved ? x_perm : nullptr, sv,
                                  reinterpret_cast<float*>(sv + L.w_row), sc, &err);
   MM_MOE_TRY(err);
-  if (side) MM_MOE_TRY(cudaStreamWaitEvent(c.stream, ss.join, 0));
+  MM_MOE_TRY(fork.join());
   st = gateup_stage(c, L, L.w_in_saved, true, A1, W_gate, W_up, W_down, h, a, sv, wbase, sc,
                     side);
   if (st != MM_MOE_OK) return st;
@@ -505,13 +536,10 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   MM_MOE_TRY(launch_gemm(c, L, g));
   // the un-permute (bandwidth-bound) runs on the side stream beside the
   // weight-gradient GEMMs, which read none of its inputs and write none of its outputs
-  SideStream ss;
-  if (!side_stream(&ss)) return MM_MOE_ECUDA;
-  MM_MOE_TRY(cudaEventRecord(ss.fork, c.stream));
-  MM_MOE_TRY(cudaStreamWaitEvent(ss.s, ss.fork, 0));
-  const Ctx cs{ss.s, d.sms, &launches};
+  Fork fork;
+  if (!fork.open(c.stream)) return MM_MOE_ECUDA;
+  const Ctx cs{fork.side(), d.sms, &launches};
   MM_MOE_TRY(launch_unpermute(cs, L, dxs, sv, pw, dx, dtopk_w));
-  MM_MOE_TRY(cudaEventRecord(ss.join, ss.s));
   // token-axis blocks of the weight-gradient operands: each expert's rows start on a
   // multiple of 128 and its padding rows are zero, so 32- or 128-row blocks of the
   // padded row space are the per-expert blocks with a zero-padded tail
@@ -555,7 +583,7 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
     MM_MOE_TRY(launch_gemm(c, L, gd));
   }
   MM_MOE_TRY(launch_gemm(c, L, g));
-  MM_MOE_TRY(cudaStreamWaitEvent(c.stream, ss.join, 0));  // join: the call ends on `stream`
+  MM_MOE_TRY(fork.join());  // the call ends on `stream`
   g_last_launches = launches;
   return MM_MOE_OK;
 }

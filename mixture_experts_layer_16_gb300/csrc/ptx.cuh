@@ -79,6 +79,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Wait like mbar_wait, but give up at the absolute %globaltimer value `deadline_ns`
+// (several waits of one unwind share one time budget).
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity,
+                                                uint64_t deadline_ns) {
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer() > deadline_ns) return false;
+  }
+}
+
+// Store a 32-bit value to shared memory at a shared::cluster address (own or peer CTA).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v)
+               : "memory");
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (own or peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)

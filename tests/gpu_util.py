@@ -98,7 +98,8 @@ def check_full(d, res, backward=True, tol=1e-2, prec="bf16"):
 def sampled_check(name, tol, n_tokens=48, seed=0):
     """A full-size workload on the GPU; the oracle (in the workload's precision) on
     sampled tokens (y, dx, dtopk_w are per token) and on the weight gradients of the
-    least and the most loaded expert (which need only that expert's rows)."""
+    least, the median and the most loaded expert (each needs only that expert's rows;
+    the median one has a mid-size token-axis K, not a multiple of the K step)."""
     cfg = CONFIGS[name]
     d = make_inputs(cfg)
     res, layer, dev = run(d, prec=cfg.prec)
@@ -115,7 +116,9 @@ def sampled_check(name, tol, n_tokens=48, seed=0):
             "dx": rel_err(f32(res["dx"][toks]), b["dx"]),
             "dtopk_w": rel_err(f32(res["dtopk_w"][toks]), b["dtopk_w"])}
     counts = np.bincount(d["topk_idx"].reshape(-1), minlength=cfg.E)
-    for e in {int(np.argmin(counts)), int(np.argmax(counts))}:
+    order = np.argsort(counts, kind="stable")
+    median = int(order[len(order) // 2])
+    for e in {int(order[0]), median, int(order[-1])}:
         g, u, dd = om.expert_weight_grads(d, e, cfg.prec)
         errs[f"dW_gate[{e}]"] = rel_err(f32(res["dW_gate"][e]), g)
         errs[f"dW_up[{e}]"] = rel_err(f32(res["dW_up"][e]), u)

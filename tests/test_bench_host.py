@@ -69,3 +69,18 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--config", "tiny", "--steps", "1", "--warmup", "0"],
                        capture_output=True, text=True, env=env, timeout=120, cwd=ROOT)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_peak_regime_follows_the_clock_record():
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks = {"sm_max_mhz": 2070.0}
+    # the region held the maximum clock with no cap: the burst GEMM peak applies
+    assert bench.peak_regime({"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []},
+                             peaks)[0] == "burst"
+    # the power cap pulled the clock down: the sustained (power-capped) peak applies
+    assert bench.peak_regime({"sm_mhz": 1781.0, "sm_max_mhz": 2070.0,
+                              "reasons": ["sw_power_cap"]}, peaks)[0] == "sustained"
+    assert bench.peak_regime({"sm_mhz": 1700.0, "sm_max_mhz": 2070.0, "reasons": []},
+                             peaks)[0] == "sustained"
+    assert bench.peak_regime({"sm_mhz": None, "reasons": ["no samples"]}, peaks)[0] == "sustained"

@@ -5,8 +5,9 @@ MM_MOE_TEST_STALL_GEMM=0 makes the gate/up GEMM's first pipeline stage on CTA 0 
 fill (its barrier is armed, no copy is issued).  The MMA issuer's wait gives up after
 its limit (2 s), every role of the kernel unwinds with bounded waits, the status word
 reads MM_MOE_ETIMEOUT, and the CUDA context is fine: the same layer then runs the
-forward and backward again and matches the oracle.  Single-SM tiles (H = 128) only:
-the SM-pair unwind adds the peer's bounded drains and is covered by reading."""
+forward and backward again and matches the oracle.  Both tile forms are covered:
+single-SM tiles (H = 128) and SM pairs (H = 256, I = 128), where the CTA whose wait
+ran out also stops its peer and both drain within one shared time budget."""
 import pytest
 import torch
 
@@ -33,3 +34,19 @@ def test_stalled_stage_reports_timeout_and_context_survives(monkeypatch):
     G.check_routing(res2, d["topk_idx"], 8)
     G.check_full(d, res2)
     assert torch.cuda.is_available()
+
+
+def test_stalled_stage_on_sm_pairs_unwinds_and_context_survives(monkeypatch):
+    # H % 256 == 0 and I % 128 == 0: the GEMMs run on SM pairs.  The stalled stage
+    # belongs to the pair's first CTA; the MMA issuer's wait runs out, the abort
+    # reaches the peer CTA, both drain within one shared budget and meet at the final
+    # cluster barrier.
+    d = custom_inputs(512, 256, 128, 8, 2, seed=42)
+    monkeypatch.setenv("MM_MOE_TEST_STALL_GEMM", "0")
+    res, layer, dev = G.run(d, backward=False)
+    assert res["status"] == B.MM_MOE_ETIMEOUT
+    monkeypatch.delenv("MM_MOE_TEST_STALL_GEMM")
+    res2, _, _ = G.run(d, layer=layer, dev=dev)
+    assert res2["status"] == B.MM_MOE_OK
+    G.check_routing(res2, d["topk_idx"], 8)
+    G.check_full(d, res2)

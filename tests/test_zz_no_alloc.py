@@ -3,14 +3,17 @@
 Some callers cannot allocate device memory at the moment they route tokens; this
 entry point keeps its working memory in a fixed array inside the library.  Here it
 is called through the C ABI twice in a row, on different routings, and each
-result must equal the routing the regular forward pass exports (bit for bit:
-the outputs are integers).  The file sorts last so that a run stopping at the
-first failure has already run every other test.
+result must equal both the routing the regular forward pass exports and the
+oracle's stable counting sort (bit for bit: the outputs are integers).  One more
+case runs at the documented limits (T * k = 262,144 routed rows over 256 experts).
+The file sorts last so that a run stopping at the first failure has already run
+every other test.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from mixture_experts_layer_16_gb300 import binding as B
 from mixture_experts_layer_16_gb300.inputs import custom_inputs
 from tests import gpu_util as G
@@ -35,6 +38,13 @@ def _noalloc(d, T, E, k):
     return off, perm, inv
 
 
+def _check_oracle(off, perm, inv, topk_idx, E):
+    _, offsets, p, i = oracle.route(topk_idx, E)
+    assert np.array_equal(off.cpu().numpy(), offsets.astype(np.int32))
+    assert np.array_equal(perm.cpu().numpy(), p.astype(np.int32))
+    assert np.array_equal(inv.cpu().numpy(), i.astype(np.int32))
+
+
 def test_noalloc_routing_matches_forward_twice():
     cases = [(3000, 256, 128, 64, 8, "zipf", 21), (1777, 256, 128, 48, 4, "uniform", 22)]
     for T, H, I, E, k, routing, seed in cases:          # two calls in a row
@@ -44,6 +54,21 @@ def test_noalloc_routing_matches_forward_twice():
         assert torch.equal(off, ref["offsets"])
         assert torch.equal(perm, ref["perm"])
         assert torch.equal(inv, ref["inv"])
+        _check_oracle(off, perm, inv, d["topk_idx"], E)
+
+
+def test_noalloc_routing_at_its_limits():
+    # T * k = 262,144 rows over E = 256 experts, Zipf-skewed: the largest sizes the
+    # fixed array holds, against the oracle
+    T, E, k = 32768, 256, 8
+    rng = np.random.default_rng(23)
+    p = 1.0 / np.arange(1, E + 1) ** 1.2
+    g = np.log(p)[None, :] + rng.gumbel(size=(T, E))          # Gumbel-top-k draws
+    idx = np.argsort(-g, axis=1)[:, :k].astype(np.int32)
+    idx = rng.permutation(E).astype(np.int32)[idx]
+    d = {"topk_idx": idx, "topk_w": np.full((T, k), 1.0 / k, np.float32)}
+    off, perm, inv = _noalloc(d, T, E, k)
+    _check_oracle(off, perm, inv, idx, E)
 
 
 def test_noalloc_rejects_sizes_beyond_its_limit():
