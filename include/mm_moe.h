@@ -61,8 +61,9 @@ extern "C" {
  *                   one power-of-two e8m0 scale 2^(floor(log2 amax) - 8) per 32
  *                   elements along that GEMM's K; token-axis blocks of the
  *                   weight-gradient GEMMs start at each expert's first row, the
- *                   last one zero-padded); fp32 accumulation.
- *   MM_MOE_FP8_BWD  the BF16 forward and the MXFP8 backward.
+ *                   last one zero-padded) and multiplied on the block-scaled FP8
+ *                   tensor cores; fp32 accumulation.  Needs I % 128 == 0.
+ *   MM_MOE_FP8_BWD  the BF16 forward and the MXFP8 backward (I % 128 == 0).
  *   MM_MOE_FP8_BLOCK blockwise FP8 (the pages' Hopper precision, in the form
  *                   Blackwell tensor cores take) in the forward and the backward:
  *                   activations in 128-element blocks along each GEMM's K (128-row
@@ -71,7 +72,7 @@ extern "C" {
  *                   block, e4m3 elements; needs I % 128 == 0.
  * Stored tensors (h, a, the outputs and the gradients) stay bf16 in every mode,
  * and the quantised operand copies live in `scratch` (which is larger for the
- * two MXFP8 modes). */
+ * quantised modes). */
 typedef enum {
   MM_MOE_BF16 = 0,
   MM_MOE_MXFP8 = 1,
@@ -98,8 +99,8 @@ typedef enum {
 #define MM_MOE_RECOMPUTE 1
 
 /* Problem shape.  T tokens, H hidden, I expert intermediate, E experts, top-k.
- * Limits: T, H, I, E, k >= 1; k <= E <= 1024; H % 128 == 0; I % 64 == 0;
- * T * k < 2^31. */
+ * Limits: T, H, I, E, k >= 1; k <= E <= 1024; H % 128 == 0; I % 64 == 0 (I % 128
+ * == 0 in the quantised precisions); T * k < 2^31. */
 typedef struct {
   int64_t T, H, I, E, k;
   int32_t prec;   /* mm_moe_precision */
@@ -221,6 +222,25 @@ MM_MOE_API mm_moe_status mm_moe_router_backward(const mm_moe_shape* shape, const
  * failed launch. */
 MM_MOE_API mm_moe_status mm_moe_mx_qdq(const uint16_t* in, uint16_t* out, int64_t rows,
                                        int64_t cols, int axis, void* stream);
+
+/* MXFP8 quantisation of a bf16 matrix into the form the MXFP8 modes' GEMMs read on
+ * the block-scaled tensor cores (tcgen05.mma kind::mxf8f6f4.block_scale): e4m3 codes
+ * and E8M0 scale codes (2^e stored as e + 127), with the block rule of mm_moe_mx_qdq
+ * (the Prime Mega MoE pages' Blackwell precision, section "How does the fused kernel
+ * work?"); exported for callers that keep MXFP8 copies of their own tensors.
+ *   in      [rows, cols] bf16 device; rows % 128 == 0, cols % 128 == 0
+ *   codes   [rows, cols] uint8 device out: the e4m3 code of each element
+ *   scales  rows * cols / 32 uint8 device out: the scale code of each block.  Call the
+ *           rows of the GEMM operand mn (for axis 1 the matrix rows, for axis 0 its
+ *           columns) and the 32-element blocks along K kb; the code of (mn, kb) is at
+ *           byte ((kb / 4) * (MN / 128) + mn / 128) * 512 + (mn % 32) * 16
+ *           + ((mn / 32) % 4) * 4 + kb % 4, MN being the number of operand rows
+ *           (512-byte atoms of 128 rows x 4 blocks, as the tensor cores take them).
+ *   axis    1: blocks along each row; 0: blocks of 32 rows down each column
+ * All pointers 16-byte aligned.  Errors as for mm_moe_mx_qdq. */
+MM_MOE_API mm_moe_status mm_moe_mx_quantize(const uint16_t* in, uint8_t* codes,
+                                            uint8_t* scales, int64_t rows, int64_t cols,
+                                            int axis, void* stream);
 
 /* Blockwise FP8 quantise-dequantise of a bf16 matrix, the operation
  * MM_MOE_FP8_BLOCK applies to every GEMM operand: one power-of-two scale

@@ -25,7 +25,7 @@ EXPORTS = ("mm_moe_workspace_size", "mm_moe_forward", "mm_moe_backward", "mm_moe
            "mm_moe_read_status", "mm_moe_last_launch_count", "mm_moe_profile_start",
            "mm_moe_profile_stop", "mm_moe_kernel_name", "mm_moe_kernel_count",
            "mm_moe_route_noalloc", "mm_moe_mx_qdq", "mm_moe_router_forward",
-           "mm_moe_router_backward", "mm_moe_fp8_block_qdq")
+           "mm_moe_router_backward", "mm_moe_fp8_block_qdq", "mm_moe_mx_quantize")
 
 
 class MoEError(RuntimeError):
@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.mm_moe_mx_qdq.argtypes = [_vp, _vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _vp]
         L.mm_moe_fp8_block_qdq.argtypes = [_vp, _vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                            _vp]
+        L.mm_moe_mx_quantize.argtypes = [_vp, _vp, _vp, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int, _vp]
         L.mm_moe_router_forward.argtypes = [sp] + [_vp] * 6
         L.mm_moe_router_backward.argtypes = [sp] + [_vp] * 9
         for fn in EXPORTS:
@@ -168,6 +170,23 @@ def mm_moe_mx_qdq(inp, out, axis: int, stream=None) -> None:
         raise ValueError("out must match inp")
     _check("mm_moe_mx_qdq", lib().mm_moe_mx_qdq(_ptr(inp), _ptr(out), inp.shape[0],
                                                 inp.shape[1], int(axis), _stream(stream)))
+
+
+def mm_moe_mx_quantize(inp, codes, scales, axis: int, stream=None) -> None:
+    """MXFP8 quantisation of a 2-D bf16 CUDA tensor [rows, cols] (multiples of 128)
+    into e4m3 codes (uint8, same shape) and E8M0 scales (uint8, rows * cols / 32 bytes
+    in the block-scaled tensor cores' atom arrangement): 32-element blocks along rows
+    (axis=1) or down columns (axis=0)."""
+    import torch
+    if inp.dim() != 2 or inp.dtype != torch.bfloat16 or not inp.is_contiguous():
+        raise ValueError("inp must be a contiguous 2-D bf16 tensor")
+    if codes.shape != inp.shape or codes.dtype != torch.uint8 or not codes.is_contiguous():
+        raise ValueError("codes must be a contiguous uint8 tensor of inp's shape")
+    if scales.dtype != torch.uint8 or scales.numel() != inp.numel() // 32:
+        raise ValueError("scales must hold rows * cols / 32 uint8")
+    _check("mm_moe_mx_quantize", lib().mm_moe_mx_quantize(
+        _ptr(inp), _ptr(codes), _ptr(scales), inp.shape[0], inp.shape[1], int(axis),
+        _stream(stream)))
 
 
 def mm_moe_fp8_block_qdq(inp, out, layout: int, stream=None) -> None:

@@ -1,726 +1,12 @@
-// gemm.cu -- the expert GEMMs of the layer as one persistent, warp-specialised
-// tcgen05 kernel template for sm_103a (TMA -> 128B-swizzled shared memory ring ->
-// tcgen05.mma with fp32 accumulators in TMEM, double-buffered -> epilogue warps).
-//
-// Prime Mega MoE pages, "How does the fused kernel work?": the two expert linear
-// layers with SwiGLU between them and the combine in the forward, and the
-// matching backward.  Seven kinds share the main loop:
-//   GATEUP       [g|u] = x_perm . [W_gate;W_up]^T  per expert M block, SwiGLU epilogue
-//   DOWN         o = a . W_down^T                   epilogue w*o (expert-grouped rows)
-//   DGRAD_DOWN   g' = dy_perm . W_down               dSwiGLU epilogue (dh, w*a, <a,g'>)
-//   DGRAD_GATEUP dx = dh . [W_gate;W_up]             epilogue dx (expert-grouped rows)
-//   WGRAD_DOWN   dW_down[e] = dy_perm^T . (w*a)      K = the expert's rows
-//   WGRAD_GATEUP [dW_gate;dW_up][e] = dh^T . x_perm   K = the expert's rows
-//   WGRAD_BOTH   the two weight gradients in one launch: each expert's WGRAD_DOWN
-//                tiles, then its WGRAD_GATEUP tiles, experts by descending row count
-//                (one list evens out the clusters' loads: the per-kind lists leave
-//                a tail of 9-17 % on skewed routing, the joint one about 3 %)
-//
-// CTAS = 2 runs each tile on an SM pair: the two CTAs of a 2-CTA cluster each stage
-// 128 rows of A and half of the N columns of B, and one tcgen05.mma.cta_group::2 of
-// M = 256 reads both halves.  CTAS = 1 runs 128-row tiles on single SMs (shapes the
-// pair tiles do not divide, and the weight-gradient GEMMs of small experts).  MX = 1
-// (gate/up of the MXFP8 forward) also writes a quantised in 32-blocks along I.
-//
-// Roles (256 threads per CTA): warp 0 lane 0 = TMA producer, warp 1 lane 0 of the
-// pair's rank-0 CTA = MMA issuer, warp 2 = TMEM allocator, warps 4..7 = epilogue
-// (warp 4+q reads TMEM lanes 32q..32q+31, i.e. the CTA's tile rows 32q..32q+31).
-// The epilogue moves data through per-warp 32 x 32 blocks in shared memory: outputs
-// leave by TMA stores and the dSwiGLU inputs arrive by TMA loads.  Every wait is
-// bounded: on expiry the kernel records MM_MOE_ETIMEOUT in the status word and every
-// role unwinds.
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-#include <cudaTypedefs.h>
-
-#include <algorithm>
-#include <cstdio>
-#include <cstdlib>
-#include <cstring>
-#include <mutex>
-
-#include "internal.h"
-#include "mx.cuh"
-#include "ptx.cuh"
+// gemm.cu -- host side of the expert GEMMs: the tensor maps and tile counts of each
+// kind, the choice of tile width and of single SMs or SM pairs, and the bf16
+// instantiations of the kernel template in gemm.cuh (the MXFP8 ones are in
+// gemm_fp8.cu).
+#include "gemm.cuh"
 
 namespace mmmoe {
 
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
-
-struct GemmParams {
-  CUtensorMap tmA;
-  CUtensorMap tmB0;
-  CUtensorMap tmB1;
-  CUtensorMap tmC0;  // epilogue outputs stored by TMA (32 x 32 boxes, 64-byte swizzle)
-  CUtensorMap tmC1;
-  CUtensorMap tmD0;  // epilogue inputs loaded by TMA (dSwiGLU: h and a)
-  CUtensorMap tmD1;
-  CUtensorMap tmQ0;  // MXFP8 epilogue output (gate/up: a in 32-blocks along I)
-  CUtensorMap tmA2;  // WGRAD_BOTH: the dW_down part's operands and output
-  CUtensorMap tmB2;
-  CUtensorMap tmC2;
-  int H, I, E;
-  int n_tiles;  // N tiles per M block (grouped kinds) or per expert M row (per-expert kinds)
-  int m_tiles;  // M tiles (of BM * CTAS rows) per expert (per-expert kinds)
-  int n_tiles2;  // WGRAD_BOTH: N and M tiles per expert of the dW_down part (n_tiles
-  int m_tiles2;  // and m_tiles are then those of the dW_gate / dW_up part)
-  int k_iters;  // K iterations per tile (grouped kinds)
-  int n_pw;
-  int max_tiles;
-  int stall;  // failure-path test: CTA 0 arms its first stage but issues no copy
-  const int* meta;
-  const int* tile_expert;
-  const int* tile_rows;
-  const int* pad_off;
-  const int* counts;
-  const int* expert_order;
-  const int* rowflat;
-  const float* w_row;
-  uint16_t* out0;
-  uint16_t* out1;
-  float* outf;
-  DevStatus* status;
-};
-
-template <int KIND, int BN_, int CTAS_>
-struct Cfg {
-  static constexpr int BN = BN_;      // N of one MMA (both CTAs of a pair together)
-  static constexpr int CTAS = CTAS_;
-  static constexpr bool A_MN = KIND >= GEMM_WGRAD_DOWN;
-  static constexpr bool B_MN = KIND >= GEMM_DGRAD_DOWN;
-  static constexpr bool PER_EXPERT = KIND >= GEMM_WGRAD_DOWN;
-  static constexpr int B_ROWS = BN / CTAS;  // B rows (K-major) or columns (M/N-major) per CTA
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = B_ROWS * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // epilogue staging per epilogue warp, in 2 KB blocks (32 rows x 32 bf16): TMA-loaded
-  // inputs (dSwiGLU: g, u, a) and a ring of output blocks for TMA stores
-  static constexpr int EPI_IN = KIND == GEMM_DGRAD_DOWN ? 3 : 0;
-  static constexpr int EPI_OUT = 4;
-  static constexpr int EPI_WARP_BYTES = (EPI_IN + EPI_OUT) * 2048;
-  static constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
-  static constexpr int SMEM_CAP = 232448 - 1024;  // opt-in limit minus static shared memory
-  static constexpr int STAGES_FIT = (SMEM_CAP - 1024 - EPI_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(BM * CTAS, BN, A_MN, B_MN);
-  static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
-  static_assert(CTAS == 1 || (CTAS == 2 && B_ROWS >= 64), "CTAS");
-  static_assert(!(KIND == GEMM_GATEUP && CTAS == 2 && BN != 256), "pair gate/up tile");
-  static_assert(STAGES >= 2, "stages");
-};
-
-struct TileInfo {
-  int e, mb, m0, n0, k_iters, k_row0;
-  int down;  // per-expert kinds: 1 = a dW_down tile, 0 = a dW_gate / dW_up tile
-};
-
-// Per-expert tiles of kind KIND: (dW_down tiles, dW_gate / dW_up tiles) per expert.
-template <int KIND>
-__device__ __forceinline__ int2 expert_tiles(const GemmParams& p) {
-  if constexpr (KIND == GEMM_WGRAD_DOWN) return make_int2(p.m_tiles * p.n_tiles, 0);
-  else if constexpr (KIND == GEMM_WGRAD_GATEUP) return make_int2(0, p.m_tiles * p.n_tiles);
-  else return make_int2(p.m_tiles2 * p.n_tiles2, p.m_tiles * p.n_tiles);
-}
-
-// Decode tile t for this CTA (rank within the pair).  Grouped kinds: t -> (group of
-// CTAS 128-row blocks of padded routed rows, N tile), N fastest; the CTA takes block
-// CTAS*group + rank.  Per-expert kinds: experts in descending row count, then (M, N)
-// tiles of BM*CTAS x BN (an expert's dW_down tiles first); the CTA takes rows
-// rank*BM.. of the M tile.
-template <int KIND, int BN, int CTAS>
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int rank) {
-  TileInfo ti;
-  ti.down = 0;
-  if constexpr (Cfg<KIND, BN, CTAS>::PER_EXPERT) {
-    const int2 per = expert_tiles<KIND>(p);
-    const int per_e = per.x + per.y;
-    const int ei = t / per_e;
-    int rem = t - ei * per_e;
-    ti.down = rem < per.x ? 1 : 0;
-    if (!ti.down) rem -= per.x;
-    const int ntl = ti.down && KIND == GEMM_WGRAD_BOTH ? p.n_tiles2 : p.n_tiles;
-    const int mt = rem / ntl;
-    const int nt = rem - mt * ntl;
-    ti.e = __ldg(p.expert_order + ei);
-    ti.mb = 0;
-    ti.m0 = mt * BM * CTAS + rank * BM;
-    ti.n0 = nt * BN;
-    ti.k_row0 = __ldg(p.pad_off + ti.e);
-    // K stops at the last 64-row block holding a routed row (the rows after it, up
-    // to the padded end, are zero)
-    ti.k_iters = (__ldg(p.counts + ti.e) + BK - 1) / BK;
-  } else {
-    const int pmb = t / p.n_tiles;
-    const int nt = t - pmb * p.n_tiles;
-    ti.mb = pmb * CTAS + rank;
-    ti.e = __ldg(p.tile_expert + ti.mb);
-    ti.m0 = ti.mb * BM;
-    ti.n0 = nt * (KIND == GEMM_GATEUP ? BN / 2 : BN);
-    ti.k_iters = p.k_iters;
-    ti.k_row0 = 0;
-  }
-  return ti;
-}
-
-template <int KIND, int BN, int CTAS>
-__device__ __forceinline__ int total_tiles(const GemmParams& p) {
-  if constexpr (Cfg<KIND, BN, CTAS>::PER_EXPERT) {
-    const int2 per = expert_tiles<KIND>(p);
-    return p.E * (per.x + per.y);
-  } else {
-    int nt = __ldg(p.meta + META_NUM_TILES);
-    nt = min(nt, p.max_tiles);
-    return (nt / CTAS) * p.n_tiles;
-  }
-}
-
-// A wait ran out: this CTA's roles give up (*abort), and on an SM pair the peer CTA's
-// too (peer_abort: the shared::cluster address of its abort flag, 0 on single SMs),
-// so that neither CTA waits out its own limits for work the other will never do.
-__device__ __forceinline__ void record_timeout(GemmParams const& p, volatile int* abort,
-                                               int detail, uint32_t peer_abort = 0) {
-  *abort = 1;
-  if (peer_abort != 0) ptx::st_cluster_u32(peer_abort, 1u);
-  if (atomicCAS(&p.status->code, 0, MM_MOE_ETIMEOUT) == 0) p.status->detail = detail;
-}
-
-// ------------------------------------------------------------------ epilogue helpers
-// Each epilogue thread owns one accumulator row (TMEM lane); its 32-column chunks
-// go through a per-warp 32 x 32 bf16 block in shared memory laid out with the
-// 64-byte swizzle (16-byte chunk j of row r at r*64 + ((j ^ ((r >> 1) & 3)) * 16)),
-// conflict-free for the row-per-thread accesses and the layout the TMA engine uses.
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ uint8_t* swz(uint8_t* buf, int r, int j) {
-  return buf + r * 64 + ((j ^ ((r >> 1) & 3)) << 4);
-}
-
-__device__ __forceinline__ void stage32(uint8_t* buf, int r, const float (&v)[32]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    *reinterpret_cast<uint4*>(swz(buf, r, j)) =
-        make_uint4(pack2(v[8 * j], v[8 * j + 1]), pack2(v[8 * j + 2], v[8 * j + 3]),
-                   pack2(v[8 * j + 4], v[8 * j + 5]), pack2(v[8 * j + 6], v[8 * j + 7]));
-}
-
-__device__ __forceinline__ void unstage32(uint8_t* buf, int r, float (&v)[32]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 w = *reinterpret_cast<const uint4*>(swz(buf, r, j));
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[8 * j + 2 * i] = __uint_as_float(ww[i] << 16);
-      v[8 * j + 2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
-    }
-  }
-}
-
-__device__ __forceinline__ void as_float(const uint32_t (&r)[32], float (&v)[32]) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
-
-// Per-warp epilogue state.
-struct EpiWarp {
-  uint8_t* in;        // input blocks (dSwiGLU)
-  uint8_t* out;       // output ring
-  uint64_t* ld_bar;   // input-load barrier of this warp
-  uint32_t ld_phase;
-  bool ld_pending;
-  int ob;             // next ring slot
-  int lane;
-};
-
-// Store this warp's 32 x 32 block (row r = lane) at element coordinates (c0, c1) of
-// tensor map m through the next slot of a ring of NB blocks.
-template <int NB>
-__device__ __forceinline__ void store_block(EpiWarp& w, const CUtensorMap* m, int c0, int c1,
-                                            const float (&v)[32]) {
-  uint8_t* buf = w.out + w.ob * 2048;
-  if (w.lane == 0) ptx::bulk_wait_read<NB - 1>();  // the slot's previous store has read it
-  __syncwarp();
-  stage32(buf, w.lane, v);
-  ptx::fence_proxy_async_smem();
-  __syncwarp();
-  if (w.lane == 0) {
-    ptx::tma_store_2d(m, buf, c0, c1);
-    ptx::bulk_commit();
-  }
-  w.ob = (w.ob + 1 == NB) ? 0 : w.ob + 1;
-}
-
-// dSwiGLU inputs of one 32-column chunk: g, u (from h) and a, rows row0..row0+31.
-__device__ __forceinline__ void load_inputs(EpiWarp& w, const GemmParams& p, int row0, int col) {
-  if (w.lane == 0) {
-    ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive_expect_tx(w.ld_bar, 3 * 2048);
-    ptx::tma_load_2d(w.in, &p.tmD0, w.ld_bar, col, row0);
-    ptx::tma_load_2d(w.in + 2048, &p.tmD0, w.ld_bar, p.I + col, row0);
-    ptx::tma_load_2d(w.in + 4096, &p.tmD1, w.ld_bar, col, row0);
-  }
-  w.ld_pending = true;
-}
-
-__device__ __forceinline__ bool wait_inputs(EpiWarp& w, volatile int* abort) {
-  int ok = 1;
-  if (w.lane == 0) ok = ptx::mbar_wait(w.ld_bar, w.ld_phase, abort, WAIT_LIMIT_NS) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) {
-    w.ld_phase ^= 1u;
-    w.ld_pending = false;
-  }
-  return ok != 0;
-}
-
-// Epilogue of one tile for one warp (row = lane of the warp's 32 rows, q = warp).
-// `next` is the tile this CTA processes after this one (dSwiGLU prefetch), or null.
-template <int KIND, int BN, int CTAS, bool MX>
-__device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInfo& ti,
-                                              const TileInfo* next, int q, uint32_t tbase,
-                                              EpiWarp& w, volatile int* abort) {
-  using C = Cfg<KIND, BN, CTAS>;
-  const int lane = w.lane, row = q * 32 + lane;
-  const int row0 = ti.m0 + q * 32;
-  if constexpr (KIND == GEMM_GATEUP) {
-    constexpr int HALF = BN / 2;
-#pragma unroll 1
-    for (int c = 0; c < HALF; c += 32) {
-      uint32_t rg[32], ru[32];
-      ptx::tmem_ld32(tbase + c, rg);
-      ptx::tmem_ld32(tbase + HALF + c, ru);
-      ptx::tmem_wait_ld(rg);
-      ptx::reg_fence(ru);
-      float g[32], u[32], a[32];
-      as_float(rg, g);
-      as_float(ru, u);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) a[i] = g[i] * sigmoidf_(g[i]) * u[i];
-      store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, g);
-      store_block<C::EPI_OUT>(w, &p.tmC0, p.I + ti.n0 + c, row0, u);
-      store_block<C::EPI_OUT>(w, &p.tmC1, ti.n0 + c, row0, a);
-      if constexpr (MX) {  // the down projection's operand: a in 32-blocks along I
-        mx::qdq_row32(a);
-        store_block<C::EPI_OUT>(w, &p.tmQ0, ti.n0 + c, row0, a);
-      }
-    }
-  } else if constexpr (KIND == GEMM_DOWN || KIND == GEMM_DGRAD_GATEUP) {
-    // rows stay in expert-grouped order; padding rows carry weight 0 (DOWN) or zero
-    // inputs (DGRAD_GATEUP) and are never read back
-    const float wgt = KIND == GEMM_DOWN ? __ldg(p.w_row + ti.m0 + row) : 1.0f;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t r[32];
-      ptx::tmem_ld32(tbase + c, r);
-      ptx::tmem_wait_ld(r);
-      float v[32];
-      as_float(r, v);
-      if (KIND == GEMM_DOWN) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= wgt;
-      }
-      store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, v);
-    }
-  } else if constexpr (KIND == GEMM_DGRAD_DOWN) {
-    const int64_t pr = ti.m0 + row;
-    const float wgt = __ldg(p.w_row + pr);
-    float dot = 0.f;
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      if (!w.ld_pending) load_inputs(w, p, row0, ti.n0 + c);
-      if (!wait_inputs(w, abort)) return false;
-      float g[32], u[32], av[32];
-      unstage32(w.in, lane, g);
-      unstage32(w.in + 2048, lane, u);
-      unstage32(w.in + 4096, lane, av);
-      __syncwarp();
-      if (c + 32 < BN) load_inputs(w, p, row0, ti.n0 + c + 32);
-      else if (next != nullptr) load_inputs(w, p, next->m0 + q * 32, next->n0);
-      uint32_t r[32];
-      ptx::tmem_ld32(tbase + c, r);
-      ptx::tmem_wait_ld(r);
-      float dg[32], du[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float gp = __uint_as_float(r[i]);
-        const float s = sigmoidf_(g[i]);
-        const float sg = g[i] * s;               // silu(g)
-        dot += av[i] * gp;                       // the forward's a (from fp32 g, u)
-        const float da = wgt * gp;
-        dg[i] = da * u[i] * s * (1.0f + g[i] * (1.0f - s));
-        du[i] = da * sg;
-        av[i] *= wgt;                            // w * a, the dW_down operand
-      }
-      store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, dg);
-      store_block<C::EPI_OUT>(w, &p.tmC0, p.I + ti.n0 + c, row0, du);
-      store_block<C::EPI_OUT>(w, &p.tmC1, ti.n0 + c, row0, av);
-    }
-    p.outf[pr * p.n_pw + ti.n0 / BN] = dot;
-  } else {  // weight gradients: dW_down [E*H, I]; dW_gate / dW_up [E*I, H]
-    const CUtensorMap* m;
-    int orow;
-    if (ti.down) {
-      m = KIND == GEMM_WGRAD_BOTH ? &p.tmC2 : &p.tmC0;
-      orow = ti.e * p.H + row0;
-    } else {
-      const bool gate = row0 < p.I;
-      m = gate ? &p.tmC0 : &p.tmC1;
-      orow = ti.e * p.I + (gate ? row0 : row0 - p.I);
-    }
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t r[32];
-      ptx::tmem_ld32(tbase + c, r);
-      ptx::tmem_wait_ld(r);
-      float v[32];
-      as_float(r, v);
-      store_block<C::EPI_OUT>(w, m, ti.n0 + c, orow, v);
-    }
-  }
-  return true;
-}
-
-// Zero tile of a per-expert GEMM whose expert has no rows (K = 0).
-template <int KIND, int BN, int CTAS>
-__device__ __forceinline__ void zero_tile(const GemmParams& p, const TileInfo& ti, int q,
-                                          EpiWarp& w) {
-  using C = Cfg<KIND, BN, CTAS>;
-  const int row0 = ti.m0 + q * 32;
-  const CUtensorMap* m;
-  int orow;
-  if (ti.down) {
-    m = KIND == GEMM_WGRAD_BOTH ? &p.tmC2 : &p.tmC0;
-    orow = ti.e * p.H + row0;
-  } else {
-    const bool gate = row0 < p.I;
-    m = gate ? &p.tmC0 : &p.tmC1;
-    orow = ti.e * p.I + (gate ? row0 : row0 - p.I);
-  }
-  float z[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) z[i] = 0.f;
-#pragma unroll 1
-  for (int c = 0; c < BN; c += 32) store_block<C::EPI_OUT>(w, m, ti.n0 + c, orow, z);
-}
-
-// ------------------------------------------------------------------ producer loads
-template <int CTAS>
-__device__ __forceinline__ void tma(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
-                                    int c1) {
-  if constexpr (CTAS == 1)
-    ptx::tma_load_2d(dst, m, bar, c0, c1);
-  else
-    ptx::tma_load_2d_pair(dst, m, bar, c0, c1);
-}
-
-// This CTA's share of k block kb: its 128 rows of A and its B_ROWS rows (K-major)
-// or columns (M/N-major) of B, completing on the barrier at cluster address `bar`.
-template <int KIND, int BN, int CTAS>
-__device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo& ti, int kb,
-                                            uint8_t* sa, uint8_t* sb, uint32_t bar, int rank) {
-  using C = Cfg<KIND, BN, CTAS>;
-  const int k0 = kb * BK;
-  const int nb = ti.n0 + rank * C::B_ROWS;  // first B row / column of this CTA
-  if constexpr (KIND == GEMM_GATEUP) {
-    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
-    if (CTAS == 1) {
-      tma<CTAS>(sb, &p.tmB0, bar, k0, ti.e * p.I + ti.n0);
-      tma<CTAS>(sb + (BN / 2) * 128, &p.tmB1, bar, k0, ti.e * p.I + ti.n0);
-    } else {  // rank 0 stages the gate rows, rank 1 the up rows of the N tile
-      tma<CTAS>(sb, rank == 0 ? &p.tmB0 : &p.tmB1, bar, k0, ti.e * p.I + ti.n0);
-    }
-  } else if constexpr (KIND == GEMM_DOWN) {
-    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
-    tma<CTAS>(sb, &p.tmB0, bar, k0, ti.e * p.H + nb);
-  } else if constexpr (KIND == GEMM_DGRAD_DOWN) {
-    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
-#pragma unroll
-    for (int c = 0; c < C::B_ROWS / 64; ++c)
-      tma<CTAS>(sb + c * 8192, &p.tmB0, bar, nb + c * 64, ti.e * p.H + k0);
-  } else if constexpr (KIND == GEMM_DGRAD_GATEUP) {
-    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
-    const bool gate = k0 < p.I;
-    const CUtensorMap* m = gate ? &p.tmB0 : &p.tmB1;
-    const int krow = ti.e * p.I + (gate ? k0 : k0 - p.I);
-#pragma unroll
-    for (int c = 0; c < C::B_ROWS / 64; ++c) tma<CTAS>(sb + c * 8192, m, bar, nb + c * 64, krow);
-  } else {  // per-expert weight gradients: both operands M/N-major, K = routed rows
-    const int krow = ti.k_row0 + k0;
-    const bool second = KIND == GEMM_WGRAD_BOTH && ti.down;
-    const CUtensorMap* ma = second ? &p.tmA2 : &p.tmA;
-    const CUtensorMap* mb = second ? &p.tmB2 : &p.tmB0;
-#pragma unroll
-    for (int c = 0; c < BM / 64; ++c) tma<CTAS>(sa + c * 8192, ma, bar, ti.m0 + c * 64, krow);
-#pragma unroll
-    for (int c = 0; c < C::B_ROWS / 64; ++c) tma<CTAS>(sb + c * 8192, mb, bar, nb + c * 64, krow);
-  }
-}
-
-// ------------------------------------------------------------------ the kernel
-template <int KIND, int BN, int CTAS, bool MX>
-__global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using C = Cfg<KIND, BN, CTAS>;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[C::STAGES];
-  __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
-  __shared__ __align__(8) uint64_t tfull_bar[2];
-  __shared__ __align__(8) uint64_t tempty_bar[2];
-  __shared__ __align__(8) uint64_t drain_bar;
-  __shared__ __align__(8) uint64_t epi_ld_bar[4];
-  __shared__ uint32_t s_tmem_base;
-  __shared__ int s_abort;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = CTAS == 1 ? 0 : static_cast<int>(ptx::cluster_rank());
-  const int cluster = blockIdx.x / CTAS, n_clusters = gridDim.x / CTAS;
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      ptx::mbar_init(&full_bar[s], 1);
-      ptx::mbar_init(&empty_bar[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(&tfull_bar[a], 1);
-      ptx::mbar_init(&tempty_bar[a], 4 * CTAS);
-    }
-    ptx::mbar_init(&drain_bar, 1);
-    for (int q = 0; q < 4; ++q) ptx::mbar_init(&epi_ld_bar[q], 1);
-    s_abort = 0;
-    ptx::fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(&p.tmA);
-    ptx::prefetch_tmap(&p.tmB0);
-    if (KIND == GEMM_GATEUP || KIND == GEMM_DGRAD_GATEUP) ptx::prefetch_tmap(&p.tmB1);
-    if (KIND == GEMM_WGRAD_BOTH) {
-      ptx::prefetch_tmap(&p.tmA2);
-      ptx::prefetch_tmap(&p.tmB2);
-    }
-  }
-  if (warp == 2) {
-    ptx::tmem_alloc<CTAS>(&s_tmem_base, C::TMEM_COLS);
-    ptx::tmem_relinquish<CTAS>();
-  }
-  ptx::tc_fence_before();
-  if constexpr (CTAS == 2) ptx::cluster_sync(); else __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem_base = s_tmem_base;
-  volatile int* abort = &s_abort;
-  const uint32_t peer_abort =
-      CTAS == 1 ? 0u : ptx::map_to_rank(ptx::smem_u32(&s_abort), static_cast<uint32_t>(rank ^ 1));
-  const int total = total_tiles<KIND, BN, CTAS>(p);
-  // the pair's barriers that both CTAs signal live in the rank-0 CTA
-  const uint32_t lead_full0 = CTAS == 1 ? ptx::smem_u32(&full_bar[0])
-                                        : ptx::map_to_rank(ptx::smem_u32(&full_bar[0]), 0);
-
-  if (warp == 0 && lane == 0) {
-    // ---------------------------------------------------------------- producer
-    int stage = 0;
-    uint32_t phase = 0;
-    int last_parity[C::STAGES];
-#pragma unroll
-    for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
-    bool ok = true;
-    for (int t = cluster; t < total && ok; t += n_clusters) {
-      const TileInfo ti = decode_tile<KIND, BN, CTAS>(p, t, rank);
-      for (int kb = 0; kb < ti.k_iters; ++kb) {
-        if (!ptx::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, WAIT_LIMIT_NS)) {
-          record_timeout(p, abort, KIND * 16 + 1, peer_abort);
-          ok = false;
-          break;
-        }
-        uint8_t* sa = smem + stage * C::STAGE_BYTES;
-        if (rank == 0) ptx::mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES * CTAS);
-        // (with p.stall the first stage of CTA 0 never fills: the MMA issuer's bounded
-        // wait runs out and every role unwinds, the path a lost copy would take)
-        if (!(p.stall && blockIdx.x == 0 && t == cluster && kb == 0))
-          issue_loads<KIND, BN, CTAS>(p, ti, kb, sa, sa + C::A_BYTES, lead_full0 + stage * 8u,
-                                      rank);
-        last_parity[stage] = static_cast<int>(phase);
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    // drain: every issued copy has landed before the CTA may exit (rank 0: its full
-    // barriers; rank 1: consumption of its stages, which implies they landed).  After
-    // a failure the stages may never complete: all waits share one time budget.
-    const uint64_t deadline = ptx::globaltimer() + WAIT_LIMIT_NS;
-    for (int s = 0; s < C::STAGES; ++s) {
-      if (last_parity[s] < 0) continue;
-      uint64_t* bar = rank == 0 ? &full_bar[s] : &empty_bar[s];
-      if (!ptx::mbar_wait_until(bar, static_cast<uint32_t>(last_parity[s]), deadline)) {
-        record_timeout(p, abort, KIND * 16 + 2);
-        break;
-      }
-    }
-  } else if (warp == 1 && lane == 0 && rank == 0) {
-    // ---------------------------------------------------------------- MMA issuer
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    bool issued = false;
-    for (int t = cluster; t < total && ok; t += n_clusters) {
-      const TileInfo ti = decode_tile<KIND, BN, CTAS>(p, t, rank);
-      if (ti.k_iters == 0) continue;
-      if (!ptx::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort, WAIT_LIMIT_NS)) {
-        record_timeout(p, abort, KIND * 16 + 3, peer_abort);
-        break;
-      }
-      ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-      for (int kb = 0; kb < ti.k_iters; ++kb) {
-        if (!ptx::mbar_wait(&full_bar[stage], phase, abort, WAIT_LIMIT_NS)) {
-          record_timeout(p, abort, KIND * 16 + 4, peer_abort);
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t a_base = ptx::smem_u32(smem + stage * C::STAGE_BYTES);
-        const uint32_t b_base = a_base + C::A_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t adesc = C::A_MN ? ptx::smem_desc_sw128(a_base + kk * 2048, 8192, 1024)
-                                         : ptx::smem_desc_sw128(a_base + kk * 32, 16, 1024);
-          const uint64_t bdesc = C::B_MN ? ptx::smem_desc_sw128(b_base + kk * 2048, 8192, 1024)
-                                         : ptx::smem_desc_sw128(b_base + kk * 32, 16, 1024);
-          ptx::umma_bf16<CTAS>(d_tmem, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
-        }
-        issued = true;
-        ptx::umma_commit<CTAS>(&empty_bar[stage]);
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      if (!ok) break;
-      ptx::umma_commit<CTAS>(&tfull_bar[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-    }
-    if (issued) {
-      // drain: every issued MMA has completed before TMEM or the pair's shared memory
-      // is released
-      ptx::umma_commit<CTAS>(&drain_bar, 0x1);
-      int dummy = 0;
-      if (!ptx::mbar_wait(&drain_bar, 0, &dummy, WAIT_LIMIT_NS))
-        record_timeout(p, abort, KIND * 16 + 5);
-    }
-  } else if (warp >= 4) {
-    // ---------------------------------------------------------------- epilogue
-    const int q = warp - 4;
-    EpiWarp w;
-    w.in = smem + C::STAGES * C::STAGE_BYTES + q * C::EPI_WARP_BYTES;
-    w.out = w.in + C::EPI_IN * 2048;
-    w.ld_bar = &epi_ld_bar[q];
-    w.ld_phase = 0;
-    w.ld_pending = false;
-    w.ob = 0;
-    w.lane = lane;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    const uint32_t lead_tempty0 =
-        CTAS == 1 ? ptx::smem_u32(&tempty_bar[0])
-                  : ptx::map_to_rank(ptx::smem_u32(&tempty_bar[0]), 0);
-    for (int t = cluster; t < total; t += n_clusters) {
-      const TileInfo ti = decode_tile<KIND, BN, CTAS>(p, t, rank);
-      if (ti.k_iters == 0) {
-        if constexpr (C::PER_EXPERT) zero_tile<KIND, BN, CTAS>(p, ti, q, w);
-        continue;
-      }
-      TileInfo nx;
-      const bool has_next = t + n_clusters < total;
-      if (has_next) nx = decode_tile<KIND, BN, CTAS>(p, t + n_clusters, rank);
-      if (KIND == GEMM_DGRAD_DOWN && !w.ld_pending) load_inputs(w, p, ti.m0 + q * 32, ti.n0);
-      int ok = 1;
-      if (lane == 0) ok = ptx::mbar_wait(&tfull_bar[acc], acc_phase, abort, WAIT_LIMIT_NS) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) record_timeout(p, abort, KIND * 16 + 6, peer_abort);
-        break;
-      }
-      ptx::tc_fence_after();
-      __syncwarp();
-      const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) +
-                             (static_cast<uint32_t>(q * 32) << 16);
-      if (!epilogue_tile<KIND, BN, CTAS, MX>(p, ti, has_next ? &nx : nullptr, q, tbase, w, abort)) {
-        if (lane == 0) record_timeout(p, abort, KIND * 16 + 7, peer_abort);
-        break;
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (CTAS == 1) ptx::mbar_arrive(&tempty_bar[acc]);
-        else ptx::mbar_arrive_cluster(lead_tempty0 + acc * 8u);
-      }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-    }
-    // drain: outstanding input loads and output stores complete before the CTA exits
-    if (w.ld_pending && lane == 0) {
-      int dummy = 0;
-      if (!ptx::mbar_wait(w.ld_bar, w.ld_phase, &dummy, WAIT_LIMIT_NS))
-        record_timeout(p, abort, KIND * 16 + 8);
-    }
-    if (lane == 0) ptx::bulk_wait_all();
-    __syncwarp();
-  }
-
-  ptx::tc_fence_before();
-  if constexpr (CTAS == 2) ptx::cluster_sync(); else __syncthreads();
-  ptx::tc_fence_after();
-  if (warp == 2) ptx::tmem_dealloc<CTAS>(tmem_base, C::TMEM_COLS);
-}
-
-// ------------------------------------------------------------------ host side
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-// Row-major bf16 matrix [outer, inner] -> 2-D tensor map with a box of
-// box_inner x box_outer elements and the given shared-memory swizzle.
-static bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                     uint32_t box_inner, uint32_t box_outer,
-                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// 32 x 32 epilogue blocks (64-byte rows, 64-byte swizzle).
-static bool make_epi_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer) {
-  return make_map(m, base, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
-}
+using gemm::GemmParams;
 
 int pick_bn(int64_t n) {
   if (n % 256 == 0) return 256;
@@ -733,162 +19,12 @@ bool wgrad_both_ok(const Layout& L) {
   return bn >= 128 && pick_bn(L.I) == bn;
 }
 
-template <int KIND, int BN, int CTAS, bool MX>
-static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) {
-  using C = Cfg<KIND, BN, CTAS>;
-  auto kern = moe_gemm_kernel<KIND, BN, CTAS, MX>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = c.stream;
-  int64_t clusters = c.num_sms / CTAS;
-  if constexpr (CTAS == 2) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    static int active = 0;  // clusters resident at once (the same for every launch)
-    if (active == 0) {
-      cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) active = n;
-      else active = static_cast<int>(clusters);
-    }
-    clusters = active;
-  }
-  clusters = std::max<int64_t>(1, std::min<int64_t>(clusters, max_clusters));
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CTAS), 1, 1);
-  static constexpr int kId[7] = {K_GEMM_GATEUP,       K_GEMM_DOWN,       K_GEMM_DGRAD_DOWN,
-                                 K_GEMM_DGRAD_GATEUP, K_GEMM_WGRAD_DOWN, K_GEMM_WGRAD_GATEUP,
-                                 K_GEMM_WGRAD};
-  prof_begin(c, kId[KIND]);
-  e = cudaLaunchKernelEx(&cfg, kern, p);
-  prof_end(c, kId[KIND]);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
+namespace gemm {
 
-cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
-  GemmParams p;
-  memset(&p, 0, sizeof(p));
-  const char* saved = g.saved;
-  // SM pairs where the layout allows them; the weight-gradient GEMMs (K = an
-  // expert's rows) go back to single-SM tiles when experts average fewer than
-  // WGRAD_PAIR_MIN_ROWS rows: their short main loops leave pair tiles waiting on
-  // each other and on the epilogue (4k-token 30B-shape layer: 0.52 ms on pairs,
-  // 0.42 ms on single SMs; 16k tokens: pairs 5 % faster)
-  constexpr int64_t WGRAD_PAIR_MIN_ROWS = 512;
-  const bool per_expert = g.kind >= GEMM_WGRAD_DOWN;
-  const int ctas =
-      (L.pad == 2 * BM && !(per_expert && L.R < WGRAD_PAIR_MIN_ROWS * L.E)) ? 2 : 1;
-  p.H = static_cast<int>(L.H);
-  p.I = static_cast<int>(L.I);
-  p.E = static_cast<int>(L.E);
-  p.n_pw = static_cast<int>(L.n_pw);
-  p.max_tiles = static_cast<int>(L.NT);
-  p.meta = reinterpret_cast<const int*>(saved + L.meta);
-  p.tile_expert = reinterpret_cast<const int*>(saved + L.tile_expert);
-  p.tile_rows = reinterpret_cast<const int*>(saved + L.tile_rows);
-  p.pad_off = reinterpret_cast<const int*>(saved + L.pad_off);
-  p.counts = reinterpret_cast<const int*>(saved + L.counts);
-  p.expert_order = reinterpret_cast<const int*>(saved + L.expert_order);
-  p.rowflat = reinterpret_cast<const int*>(saved + L.rowflat);
-  p.w_row = reinterpret_cast<const float*>(saved + L.w_row);
-  p.out0 = g.out0;
-  p.out1 = g.out1;
-  p.outf = g.outf;
-  p.status = reinterpret_cast<DevStatus*>(g.scratch + L.status);
-  // Failure-path test hook: MM_MOE_TEST_STALL_GEMM=<kind> makes that GEMM's first
-  // stage on CTA 0 never fill (read at every launch; unset, it does nothing)
-  if (const char* v = std::getenv("MM_MOE_TEST_STALL_GEMM"))
-    p.stall = (v[0] >= '0' && v[0] <= '6' && v[1] == '\0' && v[0] - '0' == g.kind) ? 1 : 0;
-  const uint64_t Rp = static_cast<uint64_t>(L.Rp), H = L.H, I = L.I, E = L.E;
-  bool ok = true;
-  int bn = 0;
-  int64_t max_units = 0;  // tiles (of both CTAs of a pair) that exist at most
-  switch (g.kind) {
-    case GEMM_GATEUP:
-      bn = (L.I % 128 == 0) ? 256 : 128;
-      ok = make_map(&p.tmA, g.A, H, Rp, 64, BM) && make_map(&p.tmB0, g.B0, H, E * I, 64, bn / 2) &&
-           make_map(&p.tmB1, g.B1, H, E * I, 64, bn / 2) &&
-           make_epi_map(&p.tmC0, g.out0, 2 * I, Rp) && make_epi_map(&p.tmC1, g.out1, I, Rp) &&
-           (!g.mx || make_epi_map(&p.tmQ0, g.q0, I, Rp));
-      p.n_tiles = static_cast<int>(L.I / (bn / 2));
-      p.k_iters = static_cast<int>(L.H / BK);
-      max_units = L.NT / ctas * p.n_tiles;
-      break;
-    case GEMM_DOWN:
-      bn = pick_bn(L.H);
-      ok = make_map(&p.tmA, g.A, I, Rp, 64, BM) && make_map(&p.tmB0, g.B0, I, E * H, 64, bn / ctas) &&
-           make_epi_map(&p.tmC0, g.out0, H, Rp);
-      p.n_tiles = static_cast<int>(L.H / bn);
-      p.k_iters = static_cast<int>(L.I / BK);
-      max_units = L.NT / ctas * p.n_tiles;
-      break;
-    case GEMM_DGRAD_DOWN:
-      bn = pick_bn(L.I);
-      ok = make_map(&p.tmA, g.A, H, Rp, 64, BM) && make_map(&p.tmB0, g.B0, I, E * H, 64, 64) &&
-           make_epi_map(&p.tmC0, g.out0, 2 * I, Rp) && make_epi_map(&p.tmC1, g.out1, I, Rp) &&
-           make_epi_map(&p.tmD0, g.aux, 2 * I, Rp) && make_epi_map(&p.tmD1, g.aux2, I, Rp);
-      p.n_tiles = static_cast<int>(L.I / bn);
-      p.k_iters = static_cast<int>(L.H / BK);
-      max_units = L.NT / ctas * p.n_tiles;
-      break;
-    case GEMM_DGRAD_GATEUP:
-      bn = pick_bn(L.H);
-      ok = make_map(&p.tmA, g.A, 2 * I, Rp, 64, BM) && make_map(&p.tmB0, g.B0, H, E * I, 64, 64) &&
-           make_map(&p.tmB1, g.B1, H, E * I, 64, 64) && make_epi_map(&p.tmC0, g.out0, H, Rp);
-      p.n_tiles = static_cast<int>(L.H / bn);
-      p.k_iters = static_cast<int>(2 * L.I / BK);
-      max_units = L.NT / ctas * p.n_tiles;
-      break;
-    case GEMM_WGRAD_DOWN:
-      bn = pick_bn(L.I);
-      ok = make_map(&p.tmA, g.A, H, Rp, 64, 64) && make_map(&p.tmB0, g.B0, I, Rp, 64, 64) &&
-           make_epi_map(&p.tmC0, g.out0, I, E * H);
-      p.m_tiles = static_cast<int>(L.H / (BM * ctas));
-      p.n_tiles = static_cast<int>(L.I / bn);
-      max_units = L.E * p.m_tiles * p.n_tiles;
-      break;
-    case GEMM_WGRAD_GATEUP:
-      bn = pick_bn(L.H);
-      ok = make_map(&p.tmA, g.A, 2 * I, Rp, 64, 64) && make_map(&p.tmB0, g.B0, H, Rp, 64, 64) &&
-           make_epi_map(&p.tmC0, g.out0, H, E * I) && make_epi_map(&p.tmC1, g.out1, H, E * I);
-      p.m_tiles = static_cast<int>(2 * L.I / (BM * ctas));
-      p.n_tiles = static_cast<int>(L.H / bn);
-      max_units = L.E * p.m_tiles * p.n_tiles;
-      break;
-    case GEMM_WGRAD_BOTH:
-      if (!wgrad_both_ok(L)) return cudaErrorInvalidValue;
-      bn = pick_bn(L.H);
-      ok = make_map(&p.tmA, g.A, 2 * I, Rp, 64, 64) && make_map(&p.tmB0, g.B0, H, Rp, 64, 64) &&
-           make_epi_map(&p.tmC0, g.out0, H, E * I) && make_epi_map(&p.tmC1, g.out1, H, E * I) &&
-           make_map(&p.tmA2, g.A2, H, Rp, 64, 64) && make_map(&p.tmB2, g.B2, I, Rp, 64, 64) &&
-           make_epi_map(&p.tmC2, g.out2, I, E * H);
-      p.m_tiles = static_cast<int>(2 * L.I / (BM * ctas));
-      p.n_tiles = static_cast<int>(L.H / bn);
-      p.m_tiles2 = static_cast<int>(L.H / (BM * ctas));
-      p.n_tiles2 = static_cast<int>(L.I / bn);
-      max_units = L.E * (p.m_tiles * p.n_tiles + p.m_tiles2 * p.n_tiles2);
-      break;
-    default:
-      return cudaErrorInvalidValue;
-  }
-  if (!ok) return cudaErrorInvalidValue;
-  // the MXFP8 gate/up epilogue is an instantiation of its own, so the BF16 kernels
-  // keep their register budget
-  const bool mx = g.mx != 0 && g.kind == GEMM_GATEUP;
-#define MMMOE_RUN(K, B, N)                                                    \
-  if (g.kind == K && bn == B && ctas == N) {                                  \
-    if (K == GEMM_GATEUP && mx) return run<K, B, N, K == GEMM_GATEUP>(c, p, max_units); \
-    return run<K, B, N, false>(c, p, max_units);                              \
-  }
+cudaError_t run_bf16(const Ctx& c, const GemmParams& p, int kind, int bn, int ctas,
+                     int64_t max_units) {
+#define MMMOE_RUN(K, B, N) \
+  if (kind == K && bn == B && ctas == N) return run<K, B, N, false>(c, p, max_units);
   MMMOE_RUN(GEMM_GATEUP, 256, 2)
   MMMOE_RUN(GEMM_DOWN, 256, 2)
   MMMOE_RUN(GEMM_DGRAD_DOWN, 256, 2)
@@ -917,6 +53,167 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   MMMOE_RUN(GEMM_WGRAD_BOTH, 128, 1)
 #undef MMMOE_RUN
   return cudaErrorInvalidValue;
+}
+
+}  // namespace gemm
+
+cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
+  using namespace gemm;
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  const char* saved = g.saved;
+  const bool f8 = g.fp8;
+  // SM pairs where the layout allows them; the weight-gradient GEMMs (K = an
+  // expert's rows) go back to single-SM tiles when experts average fewer than
+  // WGRAD_PAIR_MIN_ROWS rows: their short main loops leave pair tiles waiting on
+  // each other and on the epilogue (4k-token 30B-shape layer: 0.52 ms on pairs,
+  // 0.42 ms on single SMs; 16k tokens: pairs 5 % faster)
+  constexpr int64_t WGRAD_PAIR_MIN_ROWS = 512;
+  const bool per_expert = g.kind >= GEMM_WGRAD_DOWN;
+  int ctas = (L.pad == 2 * BM && !(per_expert && L.R < WGRAD_PAIR_MIN_ROWS * L.E)) ? 2 : 1;
+  p.H = static_cast<int>(L.H);
+  p.I = static_cast<int>(L.I);
+  p.E = static_cast<int>(L.E);
+  p.n_pw = static_cast<int>(L.n_pw);
+  p.max_tiles = static_cast<int>(L.NT);
+  p.meta = reinterpret_cast<const int*>(saved + L.meta);
+  p.tile_expert = reinterpret_cast<const int*>(saved + L.tile_expert);
+  p.tile_rows = reinterpret_cast<const int*>(saved + L.tile_rows);
+  p.pad_off = reinterpret_cast<const int*>(saved + L.pad_off);
+  p.counts = reinterpret_cast<const int*>(saved + L.counts);
+  p.expert_order = reinterpret_cast<const int*>(saved + L.expert_order);
+  p.rowflat = reinterpret_cast<const int*>(saved + L.rowflat);
+  p.w_row = reinterpret_cast<const float*>(saved + L.w_row);
+  p.out0 = g.out0;
+  p.out1 = g.out1;
+  p.outf = g.outf;
+  p.status = reinterpret_cast<DevStatus*>(g.scratch + L.status);
+  // Failure-path test hook: MM_MOE_TEST_STALL_GEMM=<kind> makes that GEMM's first
+  // stage on CTA 0 never fill (read at every launch; unset, it does nothing)
+  if (const char* v = std::getenv("MM_MOE_TEST_STALL_GEMM"))
+    p.stall = (v[0] >= '0' && v[0] <= '6' && v[1] == '\0' && v[0] - '0' == g.kind) ? 1 : 0;
+  const uint64_t Rp = static_cast<uint64_t>(L.Rp), H = L.H, I = L.I, E = L.E;
+  // operand maps: bf16 (64-element K boxes, 64-wide M/N-major boxes) or e4m3 codes
+  // (128-element K boxes, 128-wide M/N-major boxes); box_rows = rows of a K-major box
+  auto kmaj = [&](CUtensorMap* m, const void* base, uint64_t K, uint64_t rows,
+                  uint32_t box_rows) {
+    return f8 ? make_fp8_map(m, base, K, rows, box_rows)
+              : make_map(m, base, K, rows, 64, box_rows);
+  };
+  auto mnmaj = [&](CUtensorMap* m, const void* base, uint64_t MN, uint64_t krows) {
+    return f8 ? make_fp8_map(m, base, MN, krows, 128) : make_map(m, base, MN, krows, 64, 64);
+  };
+  // scale map of an operand with MN rows and K columns (fp8 only)
+  auto sfm = [&](CUtensorMap* m, const uint8_t* base, uint64_t MN, uint64_t K) {
+    return !f8 || make_sf_map(m, base, MN * K / 32);
+  };
+  const int kstep = f8 ? 128 : BK;
+  bool ok = true;
+  int bn = 0;
+  int64_t max_units = 0;  // tiles (of both CTAs of a pair) that exist at most
+  switch (g.kind) {
+    case GEMM_GATEUP:
+      bn = (f8 || L.I % 128 == 0) ? 256 : 128;
+      ok = kmaj(&p.tmA, g.A, H, Rp, BM) && kmaj(&p.tmB0, g.B0, H, E * I, bn / 2) &&
+           kmaj(&p.tmB1, g.B1, H, E * I, bn / 2) && make_epi_map(&p.tmC0, g.out0, 2 * I, Rp) &&
+           make_epi_map(&p.tmC1, g.out1, I, Rp) && sfm(&p.tmSA, g.sA, Rp, H) &&
+           sfm(&p.tmSB0, g.sB0, E * I, H) && sfm(&p.tmSB1, g.sB1, E * I, H);
+      p.sfa_mnb = static_cast<int>(Rp / 128);
+      p.sfb_mnb = static_cast<int>(E * I / 128);
+      p.q_codes = g.q_codes;
+      p.q_sf = g.q_sf;
+      p.q_mnb = static_cast<int>(Rp / 128);
+      p.n_tiles = static_cast<int>(L.I / (bn / 2));
+      p.k_iters = static_cast<int>(L.H / kstep);
+      max_units = L.NT / ctas * p.n_tiles;
+      break;
+    case GEMM_DOWN:
+      bn = pick_bn(L.H);
+      ok = kmaj(&p.tmA, g.A, I, Rp, BM) && kmaj(&p.tmB0, g.B0, I, E * H, bn / ctas) &&
+           make_epi_map(&p.tmC0, g.out0, H, Rp) && sfm(&p.tmSA, g.sA, Rp, I) &&
+           sfm(&p.tmSB0, g.sB0, E * H, I);
+      p.sfa_mnb = static_cast<int>(Rp / 128);
+      p.sfb_mnb = static_cast<int>(E * H / 128);
+      p.n_tiles = static_cast<int>(L.H / bn);
+      p.k_iters = static_cast<int>(L.I / kstep);
+      max_units = L.NT / ctas * p.n_tiles;
+      break;
+    case GEMM_DGRAD_DOWN:
+      bn = pick_bn(L.I);
+      if (f8 && bn != 256) ctas = 1;  // M/N-major e4m3 boxes are 128 wide per CTA
+      ok = kmaj(&p.tmA, g.A, H, Rp, BM) && mnmaj(&p.tmB0, g.B0, I, E * H) &&
+           make_epi_map(&p.tmC0, g.out0, 2 * I, Rp) && make_epi_map(&p.tmC1, g.out1, I, Rp) &&
+           make_epi_map(&p.tmD0, g.aux, 2 * I, Rp) && make_epi_map(&p.tmD1, g.aux2, I, Rp) &&
+           sfm(&p.tmSA, g.sA, Rp, H) && sfm(&p.tmSB0, g.sB0, I, E * H);
+      p.sfa_mnb = static_cast<int>(Rp / 128);
+      p.sfb_mnb = static_cast<int>(I / 128);
+      p.n_tiles = static_cast<int>(L.I / bn);
+      p.k_iters = static_cast<int>(L.H / kstep);
+      max_units = L.NT / ctas * p.n_tiles;
+      break;
+    case GEMM_DGRAD_GATEUP:
+      bn = pick_bn(L.H);
+      if (f8 && bn != 256) ctas = 1;
+      ok = kmaj(&p.tmA, g.A, 2 * I, Rp, BM) && mnmaj(&p.tmB0, g.B0, H, E * I) &&
+           mnmaj(&p.tmB1, g.B1, H, E * I) && make_epi_map(&p.tmC0, g.out0, H, Rp) &&
+           sfm(&p.tmSA, g.sA, Rp, 2 * I) && sfm(&p.tmSB0, g.sB0, H, E * I) &&
+           sfm(&p.tmSB1, g.sB1, H, E * I);
+      p.sfa_mnb = static_cast<int>(Rp / 128);
+      p.sfb_mnb = static_cast<int>(H / 128);
+      p.n_tiles = static_cast<int>(L.H / bn);
+      p.k_iters = static_cast<int>(2 * L.I / kstep);
+      max_units = L.NT / ctas * p.n_tiles;
+      break;
+    case GEMM_WGRAD_DOWN:
+      bn = pick_bn(L.I);
+      if (f8 && bn != 256) ctas = 1;
+      ok = mnmaj(&p.tmA, g.A, H, Rp) && mnmaj(&p.tmB0, g.B0, I, Rp) &&
+           make_epi_map(&p.tmC0, g.out0, I, E * H) && sfm(&p.tmSA, g.sA, H, Rp) &&
+           sfm(&p.tmSB0, g.sB0, I, Rp);
+      p.sfa_mnb = static_cast<int>(H / 128);
+      p.sfb_mnb = static_cast<int>(I / 128);
+      p.m_tiles = static_cast<int>(L.H / (BM * ctas));
+      p.n_tiles = static_cast<int>(L.I / bn);
+      max_units = L.E * p.m_tiles * p.n_tiles;
+      break;
+    case GEMM_WGRAD_GATEUP:
+      bn = pick_bn(L.H);
+      if (f8 && bn != 256) ctas = 1;
+      ok = mnmaj(&p.tmA, g.A, 2 * I, Rp) && mnmaj(&p.tmB0, g.B0, H, Rp) &&
+           make_epi_map(&p.tmC0, g.out0, H, E * I) && make_epi_map(&p.tmC1, g.out1, H, E * I) &&
+           sfm(&p.tmSA, g.sA, 2 * I, Rp) && sfm(&p.tmSB0, g.sB0, H, Rp);
+      p.sfa_mnb = static_cast<int>(2 * I / 128);
+      p.sfb_mnb = static_cast<int>(H / 128);
+      p.m_tiles = static_cast<int>(2 * L.I / (BM * ctas));
+      p.n_tiles = static_cast<int>(L.H / bn);
+      max_units = L.E * p.m_tiles * p.n_tiles;
+      break;
+    case GEMM_WGRAD_BOTH:
+      if (!wgrad_both_ok(L)) return cudaErrorInvalidValue;
+      bn = pick_bn(L.H);
+      if (f8 && bn != 256) ctas = 1;
+      ok = mnmaj(&p.tmA, g.A, 2 * I, Rp) && mnmaj(&p.tmB0, g.B0, H, Rp) &&
+           make_epi_map(&p.tmC0, g.out0, H, E * I) && make_epi_map(&p.tmC1, g.out1, H, E * I) &&
+           mnmaj(&p.tmA2, g.A2, H, Rp) && mnmaj(&p.tmB2, g.B2, I, Rp) &&
+           make_epi_map(&p.tmC2, g.out2, I, E * H) && sfm(&p.tmSA, g.sA, 2 * I, Rp) &&
+           sfm(&p.tmSB0, g.sB0, H, Rp) && sfm(&p.tmSA2, g.sA2, H, Rp) &&
+           sfm(&p.tmSB2, g.sB2, I, Rp);
+      p.sfa_mnb = static_cast<int>(2 * I / 128);
+      p.sfb_mnb = static_cast<int>(H / 128);
+      p.sfa2_mnb = static_cast<int>(H / 128);
+      p.sfb2_mnb = static_cast<int>(I / 128);
+      p.m_tiles = static_cast<int>(2 * L.I / (BM * ctas));
+      p.n_tiles = static_cast<int>(L.H / bn);
+      p.m_tiles2 = static_cast<int>(L.H / (BM * ctas));
+      p.n_tiles2 = static_cast<int>(L.I / bn);
+      max_units = L.E * (p.m_tiles * p.n_tiles + p.m_tiles2 * p.n_tiles2);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  return f8 ? run_fp8(c, p, g.kind, bn, ctas, max_units)
+            : run_bf16(c, p, g.kind, bn, ctas, max_units);
 }
 
 }  // namespace mmmoe

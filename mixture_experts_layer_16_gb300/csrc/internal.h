@@ -40,15 +40,19 @@ struct Layout {
       tile_rows, w_row, x_perm, h, a, saved_bytes;
   // scratch
   size_t status, blk_counts, ys, dy_perm, dh, a_w, pw, dxs, scratch_bytes;
-  // scratch, MXFP8 operand copies (set only for the precisions that use them):
+  // scratch, quantised operand copies (set only for the precisions that use them;
+  // MXFP8: e4m3 codes [rows, cols] followed by their E8M0 scales, rows * cols / 32
+  // bytes in the mx::sf_offset arrangement; blockwise FP8: bf16 dequantised values):
   // forward, blocks along K: x_perm, a, W_gate, W_up, W_down
   size_t q_x, q_a, q_wg, q_wu, q_wd;
   // backward: W_down along H and W_gate, W_up along I (q_wdc, q_wgc, q_wuc), and
-  // dy_perm, dh, x_perm along the token axis (q_dyc, q_dhc, q_xc); dy_perm and dh
-  // along their K, and a_w along tokens, are quantised in place.  Under full MXFP8
-  // the forward writes the weight copies into `saved` (w_in_saved) and x_perm's
-  // token-axis copy over x_perm, so q_xc is unused.
-  size_t q_wdc, q_wgc, q_wuc, q_dyc, q_dhc, q_xc;
+  // dy_perm, dh, x_perm along the token axis (q_dyc, q_dhc, q_xc); MXFP8 also dh along
+  // I (q_dhr) and a_w along tokens (q_awc), and the permutation writes dy along H into
+  // dy_perm's place (blockwise FP8: dy_perm, dh along I and a_w quantised in place).
+  // Under a quantised forward that keeps its activations the forward writes the weight
+  // copies into `saved` (w_in_saved) and x's token-axis copy over x_perm, so q_xc is
+  // unused.
+  size_t q_wdc, q_wgc, q_wuc, q_dyc, q_dhc, q_xc, q_dhr, q_awc;
   bool w_in_saved;
   // quantisation of the forward's and the backward's GEMM operands: QS_NONE, QS_MX
   // (MXFP8) or QS_BLOCK (blockwise FP8, whose one 128 x 128-block copy of each weight
@@ -101,6 +105,8 @@ enum KernelId {
   K_FB_ROWS,
   K_FB_COLS,
   K_FB_TILES,
+  K_MXQ_ROWS,
+  K_MXQ_COLS,
   K_COUNT
 };
 
@@ -130,11 +136,13 @@ struct RouteBufs {
 cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* topk_idx,
                             const float* topk_w, const RouteBufs& b);
 // dst = src's token rows in the padded expert-grouped order, padding rows zero; with
-// quant = QS_MX / QS_BLOCK each row is quantised along its columns (32- / 128-element
-// blocks) on the way, once per token before its k copies are stored.
-cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
+// quant = QS_BLOCK each row is quantise-dequantised along its columns (128-element
+// blocks, bf16 out) on the way, once per token before its k copies are stored; with
+// quant = QS_MX dst receives each row's e4m3 codes ([Rp, H] bytes) and `sf` its scale
+// codes (mx::sf_offset over the Rp padded rows).
+cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, void* dst,
                            const char* saved, float* w_row_out, int kernel_id, char* scratch,
-                           int quant = 0);
+                           int quant = 0, uint8_t* sf = nullptr);
 cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
                            const char* saved, uint16_t* out);
 cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slots,
@@ -170,6 +178,28 @@ cudaError_t launch_mx_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64
                           int64_t cols, bool along_rows, const int* meta,
                           uint16_t* out_rows = nullptr, RowGather gather = RowGather{});
 
+// MXFP8 quantisation into e4m3 codes and E8M0 scales (the block-scaled tensor-core
+// operand format; scale arrangement mx::sf_offset).  in: bf16 [rows, cols], rows and
+// cols multiples of 128.  along_rows: blocks of 32 along each row (the MMA rows are
+// the tensor's rows, mn_blocks = rows / 128); else blocks of 32 rows down each column
+// (the MMA rows are the columns, mn_blocks = cols / 128), optionally with the row
+// blocks of the same read too (codes_rows / sf_rows), and with a gather the rows come
+// from a token-major `in`.  `meta` (device, may be null) limits the rows processed to
+// meta[META_NUM_TILES] * BM (the padded routed rows in use); the scale arrangement
+// still spans all `rows`.
+struct MxqArgs {
+  const uint16_t* in;
+  uint8_t* codes;
+  uint8_t* sf;
+  int64_t rows, cols;
+  bool along_rows;
+  const int* meta;
+  uint8_t* codes_rows;
+  uint8_t* sf_rows;
+  RowGather gather;
+};
+cudaError_t launch_mxq(const Ctx& c, const MxqArgs& a);
+
 // Blockwise FP8 quantise-dequantise of a bf16 [rows, cols] tensor (power-of-two scale
 // 2^ceil(log2(amax / 448)) per block), written as bf16: 128-element blocks along each
 // row (FB_ROWS), down each column (FB_COLS; a non-null out_rows also receives the row
@@ -192,27 +222,35 @@ enum GemmKind {
 
 struct GemmArgs {
   int kind;
-  // operands (device)
-  const uint16_t* A;    // base of the A operand tensor
-  const uint16_t* B0;   // first B tensor
-  const uint16_t* B1;   // second B tensor (W_up) or nullptr
+  // MXFP8 operands: e4m3 codes and E8M0 scales (mx::sf_offset) on the block-scaled
+  // tensor cores; else bf16 operands
+  bool fp8;
+  // operands (device): bf16 tensors, or with fp8 their codes
+  const void* A;    // base of the A operand tensor
+  const void* B0;   // first B tensor
+  const void* B1;   // second B tensor (W_up) or nullptr
+  const uint8_t* sA;   // fp8: scales of A, B0, B1
+  const uint8_t* sB0;
+  const uint8_t* sB1;
   // epilogue (device)
   uint16_t* out0;
   uint16_t* out1;
   float* outf;
   const uint16_t* aux;   // h = [g | u] for the dSwiGLU epilogue
   const uint16_t* aux2;  // a = silu(g) * u saved by the forward
-  // GEMM_WGRAD_BOTH: A, B0, out0, out1 as GEMM_WGRAD_GATEUP; A2, B2, out2 as the A,
-  // B0, out0 of GEMM_WGRAD_DOWN
-  const uint16_t* A2;
-  const uint16_t* B2;
+  // GEMM_WGRAD_BOTH: A, B0, out0, out1 as GEMM_WGRAD_GATEUP; A2, B2 (sA2, sB2), out2 as
+  // the A, B0, out0 of GEMM_WGRAD_DOWN
+  const void* A2;
+  const void* B2;
+  const uint8_t* sA2;
+  const uint8_t* sB2;
   uint16_t* out2;
   const char* saved;
   char* scratch;
-  // MXFP8 (mx != 0, gate/up only): the epilogue also writes a in 32-blocks along I
-  // to q0 (a itself still goes to out1)
-  int mx;
-  uint16_t* q0;
+  // fp8 gate/up: the epilogue also writes a in MXFP8 along I (codes [Rp, I] and
+  // scales) for the down projection; null: not written
+  uint8_t* q_codes;
+  uint8_t* q_sf;
 };
 
 cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g);

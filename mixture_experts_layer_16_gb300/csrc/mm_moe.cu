@@ -20,6 +20,13 @@ bool sm_pairs_enabled() {
   return on;
 }
 
+// Bytes of one quantised copy of a [rows, cols] operand under scheme qs: MXFP8 keeps
+// e4m3 codes (rows * cols bytes) followed by the E8M0 scales (one per 32 elements);
+// blockwise FP8 keeps the dequantised values as bf16.
+static size_t qcopy_bytes(int qs, size_t rows, size_t cols) {
+  return qs == QS_MX ? rows * cols + rows * cols / 32 : 2 * rows * cols;
+}
+
 mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   if (s == nullptr || L == nullptr) return MM_MOE_EINVAL;
   *L = Layout{};  // offsets a mode does not use stay 0
@@ -28,7 +35,9 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   if (s->H % 128 != 0 || s->I % 64 != 0) return MM_MOE_EINVAL;
   if ((s->flags & ~MM_MOE_RECOMPUTE) != 0) return MM_MOE_EINVAL;
   if (s->prec < MM_MOE_BF16 || s->prec > MM_MOE_FP8_BLOCK) return MM_MOE_EINVAL;
-  if (s->prec == MM_MOE_FP8_BLOCK && s->I % 128 != 0) return MM_MOE_EINVAL;  // 128 x 128 blocks
+  // blockwise FP8: 128 x 128 weight blocks; MXFP8 (both modes): 128-element K steps of
+  // the block-scaled tensor cores over I and 2I
+  if (s->prec != MM_MOE_BF16 && s->I % 128 != 0) return MM_MOE_EINVAL;
   if (s->T > (int64_t{1} << 31) / s->k) return MM_MOE_EINVAL;
   L->T = s->T;
   L->H = s->H;
@@ -70,17 +79,17 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->tile_rows = take(4 * NT);
   L->w_row = take(4 * Rp);
   if (!L->recompute) {
-    L->x_perm = take(2 * Rp * H);
+    L->x_perm = take(2 * Rp * H);  // (a quantised forward keeps x along tokens here)
     L->h = take(2 * Rp * 2 * I);
     L->a = take(2 * Rp * I);
   }
   // a quantised forward that keeps its activations also makes the backward's
   // weight copies (MXFP8: the forward's two-way passes; blockwise: the one copy)
-  const size_t W = 2 * E * I * H;  // bytes of one expert weight tensor
   L->w_in_saved = L->qf != QS_NONE && !L->recompute;
   L->w_common = L->qf == QS_BLOCK && L->recompute;
   L->q_wdc = L->q_wgc = L->q_wuc = 0;
   if (L->w_in_saved) {
+    const size_t W = qcopy_bytes(L->qf, E * I, H);
     L->q_wdc = take(W);
     L->q_wgc = take(W);
     L->q_wuc = take(W);
@@ -99,42 +108,49 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
     L->a = take(2 * Rp * I);
   }
   if (L->w_common) {  // blockwise weights under recompute: made by each pass, used by all
+    const size_t W = qcopy_bytes(QS_BLOCK, E * I, H);
     L->q_wdc = take(W);
     L->q_wgc = take(W);
     L->q_wuc = take(W);
   }
   const size_t common = o;
   L->ys = take(2 * Rp * H);
-  // quantised operand copies of the forward (bf16 holding the dequantised values)
+  // quantised operand copies of the forward
   L->q_x = L->q_a = L->q_wg = L->q_wu = L->q_wd = 0;
   if (L->qf != QS_NONE) {
-    L->q_x = take(2 * Rp * H);
-    L->q_a = take(2 * Rp * I);
+    L->q_x = take(qcopy_bytes(L->qf, Rp, H));
+    L->q_a = take(qcopy_bytes(L->qf, Rp, I));
   }
   if (L->qf == QS_MX) {  // the forward's MXFP8 weights (blocks along their forward K)
+    const size_t W = qcopy_bytes(QS_MX, E * I, H);
     L->q_wg = take(W);
     L->q_wu = take(W);
     L->q_wd = take(W);
   }
   const size_t fwd_end = o;
   o = common;
-  L->dy_perm = take(2 * Rp * H);
+  L->dy_perm = take(2 * Rp * H);  // (MXFP8: dy along H, codes and scales)
   L->dh = take(2 * Rp * 2 * I);
   L->a_w = take(2 * Rp * I);
   L->pw = take(4 * Rp * static_cast<size_t>(L->n_pw));
   L->dxs = take(2 * Rp * H);
-  L->q_dyc = L->q_dhc = L->q_xc = 0;
+  L->q_dyc = L->q_dhc = L->q_xc = L->q_dhr = L->q_awc = 0;
   if (L->qb != QS_NONE && !L->w_in_saved) {  // left to the backward
     if (!L->w_common) {
+      const size_t W = qcopy_bytes(L->qb, E * I, H);
       L->q_wdc = take(W);
       L->q_wgc = take(W);
       L->q_wuc = take(W);
     }
-    L->q_xc = take(2 * Rp * H);
+    L->q_xc = take(qcopy_bytes(L->qb, Rp, H));
   }
   if (L->qb != QS_NONE) {
-    L->q_dyc = take(2 * Rp * H);
-    L->q_dhc = take(2 * Rp * 2 * I);
+    L->q_dyc = take(qcopy_bytes(L->qb, Rp, H));
+    L->q_dhc = take(qcopy_bytes(L->qb, Rp, 2 * I));
+  }
+  if (L->qb == QS_MX) {  // (blockwise FP8 quantises dh along I and a_w in place)
+    L->q_dhr = take(qcopy_bytes(QS_MX, Rp, 2 * I));
+    L->q_awc = take(qcopy_bytes(QS_MX, Rp, I));
   }
   L->scratch_bytes = o > fwd_end ? o : fwd_end;
   return MM_MOE_OK;
@@ -236,81 +252,138 @@ class Fork {
     if ((expr) != cudaSuccess) return MM_MOE_ECUDA; \
   } while (0)
 
-// Quantisation of an activation operand under scheme qs (QS_MX: 32-element blocks,
-// QS_BLOCK: 128-element blocks): along rows, or down columns (with out_rows non-null
-// the same read also writes the row blocks there).
-static cudaError_t act_rows(const Ctx& c, int qs, const uint16_t* in, uint16_t* out,
-                            int64_t rows, int64_t cols, const int* meta) {
-  return qs == QS_BLOCK ? launch_fb_qdq(c, in, out, rows, cols, FB_ROWS, meta, nullptr)
-                        : launch_mx_qdq(c, in, out, rows, cols, true, meta);
+
+// A GEMM operand: a bf16 tensor, or (MXFP8) e4m3 codes and their scales.
+struct Opnd {
+  const void* p;
+  const uint8_t* sf;
+};
+
+// The MXFP8 copy at byte offset `off` of `base` of a [rows, cols] operand: its codes,
+// then its scales.
+struct MxCopy {
+  uint8_t* codes;
+  uint8_t* sf;
+  operator Opnd() const { return Opnd{codes, sf}; }
+};
+static MxCopy mx_copy(const char* base, size_t off, int64_t rows, int64_t cols) {
+  uint8_t* c = reinterpret_cast<uint8_t*>(const_cast<char*>(base) + off);
+  return MxCopy{c, c + rows * cols};
 }
 
-static cudaError_t act_cols(const Ctx& c, int qs, const uint16_t* in, uint16_t* out,
-                            int64_t rows, int64_t cols, const int* meta,
-                            uint16_t* out_rows = nullptr, RowGather gather = RowGather{}) {
-  return qs == QS_BLOCK ? launch_fb_qdq(c, in, out, rows, cols, FB_COLS, meta, out_rows, gather)
-                        : launch_mx_qdq(c, in, out, rows, cols, false, meta, out_rows, gather);
+// MXFP8 quantisation of a bf16 [rows, cols] operand: blocks along its rows, or down
+// its columns (with rows_out non-null the same read also yields the row blocks; a
+// gather reads the rows from a token-major tensor).
+static cudaError_t mx_rows(const Ctx& c, const uint16_t* in, MxCopy out, int64_t rows,
+                           int64_t cols, const int* meta) {
+  MxqArgs a{};
+  a.in = in;
+  a.codes = out.codes;
+  a.sf = out.sf;
+  a.rows = rows;
+  a.cols = cols;
+  a.along_rows = true;
+  a.meta = meta;
+  return launch_mxq(c, a);
 }
 
-// The padded expert-grouped rows of a token-major tensor, for act_cols.
+static cudaError_t mx_cols(const Ctx& c, const uint16_t* in, MxCopy out, int64_t rows,
+                           int64_t cols, const int* meta, const MxCopy* rows_out = nullptr,
+                           RowGather gather = RowGather{}) {
+  MxqArgs a{};
+  a.in = in;
+  a.codes = out.codes;
+  a.sf = out.sf;
+  a.rows = rows;
+  a.cols = cols;
+  a.along_rows = false;
+  a.meta = meta;
+  if (rows_out != nullptr) {
+    a.codes_rows = rows_out->codes;
+    a.sf_rows = rows_out->sf;
+  }
+  a.gather = gather;
+  return launch_mxq(c, a);
+}
+
+// Blockwise FP8 quantise-dequantise of an activation operand (128-element blocks):
+// along rows, or down columns (with out_rows non-null the same read also writes the
+// row blocks there).
+static cudaError_t fb_rows(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
+                           int64_t cols, const int* meta) {
+  return launch_fb_qdq(c, in, out, rows, cols, FB_ROWS, meta, nullptr);
+}
+
+static cudaError_t fb_cols(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
+                           int64_t cols, const int* meta, uint16_t* out_rows = nullptr,
+                           RowGather gather = RowGather{}) {
+  return launch_fb_qdq(c, in, out, rows, cols, FB_COLS, meta, out_rows, gather);
+}
+
+// The padded expert-grouped rows of a token-major tensor, for the column passes.
 static RowGather routed_rows(const Layout& L, const char* sv) {
   return RowGather{reinterpret_cast<const int*>(sv + L.rowflat),
                    reinterpret_cast<const int*>(sv + L.tile_rows), static_cast<int>(L.k)};
 }
 
-// Under a quantised forward the permutation of x writes x's blocks along H (the
-// gate/up operand) straight to q_x, quantising each token row once; the blocks along
-// tokens (the dW_gate / dW_up operand), when wanted, are gathered from x into
-// `x_cols`.  No bf16 copy of the permuted rows is made.  Otherwise x_perm is the
-// bf16 permuted copy.  Returns gate/up's A operand.
-static const uint16_t* permute_x(const Ctx& c, const Layout& L, const uint16_t* x,
-                                 uint16_t* x_perm, uint16_t* x_cols, const char* sv,
-                                 float* w_row_out, char* sc, cudaError_t* err) {
+// The permutation of x, and gate/up's A operand.  Under a quantised forward it writes
+// x's blocks along H (the gate/up operand) straight to q_x, quantising each token row
+// once (MXFP8: codes and scales; blockwise: bf16 values); with `keep_tokens` the
+// blocks along tokens (the dW_gate / dW_up operand) are gathered from x into
+// x_perm's place.  No bf16 copy of the permuted rows is made.  Otherwise x_perm is
+// the bf16 permuted copy.
+static Opnd permute_x(const Ctx& c, const Layout& L, const uint16_t* x, uint16_t* x_perm,
+                      bool keep_tokens, const char* sv, float* w_row_out, char* sc,
+                      cudaError_t* err) {
+  const int* meta = reinterpret_cast<const int*>(sv + L.meta);
   if (L.qf == QS_NONE) {
     *err = launch_permute(c, L, x, x_perm, sv, w_row_out, K_PERMUTE_X, sc);
-    return x_perm;
+    return Opnd{x_perm, nullptr};
+  }
+  if (L.qf == QS_MX) {
+    const MxCopy q = mx_copy(sc, L.q_x, L.Rp, L.H);
+    *err = launch_permute(c, L, x, q.codes, sv, w_row_out, K_PERMUTE_X, sc, QS_MX, q.sf);
+    if (*err == cudaSuccess && keep_tokens)
+      *err = mx_cols(c, x, mx_copy(reinterpret_cast<char*>(x_perm), 0, L.Rp, L.H), L.Rp, L.H,
+                     meta, nullptr, routed_rows(L, sv));
+    return q;
   }
   uint16_t* q_x = reinterpret_cast<uint16_t*>(sc + L.q_x);
-  *err = launch_permute(c, L, x, q_x, sv, w_row_out, K_PERMUTE_X, sc, L.qf);
-  if (*err == cudaSuccess && x_cols != nullptr)
-    *err = act_cols(c, L.qf, x, x_cols, L.Rp, L.H, reinterpret_cast<const int*>(sv + L.meta),
-                    nullptr, routed_rows(L, sv));
-  return q_x;
+  *err = launch_permute(c, L, x, q_x, sv, w_row_out, K_PERMUTE_X, sc, QS_BLOCK);
+  if (*err == cudaSuccess && keep_tokens)
+    *err = fb_cols(c, x, x_perm, L.Rp, L.H, meta, nullptr, routed_rows(L, sv));
+  return Opnd{q_x, nullptr};
 }
 
-// The forward's gate/up stage on A (from permute_x): h = [g | u] and a = silu(g) * u.
-// Under a quantised forward (L.qf) the weights are first quantised along H.  MXFP8:
-// with `keep` (the forward of a layer that keeps its activations) by two-way passes
-// that also write the weights along their backward K to `wbase` (saved); otherwise by
-// row passes; `emit_qa` makes the epilogue also write a quantised along I for the down
-// projection.  Blockwise FP8: the one 128 x 128-block copy of each of the three
-// weights goes to `wbase` (saved, or the front of scratch under recompute); `emit_qa`
-// adds a row pass over a.  The backward under MM_MOE_RECOMPUTE calls it with the
-// forward's arguments and gets h and a bit for bit (the same kernels on the same
-// inputs).
-// The weight copies of a quantised forward (see gateup_stage); they read only the
-// weights, so the forward runs them on its side stream beside the routing.
-static cudaError_t weight_copies(const Ctx& c, const Layout& L, bool keep, bool emit_qa,
+// The weight copies of a quantised forward; they read only the weights, so the
+// forward runs them on its side stream beside the routing.  MXFP8: with `keep` (the
+// forward of a layer that keeps its activations) one two-way pass per weight writes
+// its blocks along the forward's K to scratch and along the backward's K to `wbase`
+// (saved); otherwise row passes write the forward's copies only (W_down's only with
+// `emit_down`).  Blockwise FP8: the one 128 x 128-block copy of each of the three
+// weights, which every GEMM reads, to `wbase` (saved, or the front of scratch under
+// recompute).
+static cudaError_t weight_copies(const Ctx& c, const Layout& L, bool keep, bool emit_down,
                                  const uint16_t* W_gate, const uint16_t* W_up,
                                  const uint16_t* W_down, char* wbase, char* sc) {
   const int64_t EI = L.E * L.I, EH = L.E * L.H;
-  auto sq = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
-  auto wq = [&](size_t off) { return reinterpret_cast<uint16_t*>(wbase + off); };
   cudaError_t e = cudaSuccess;
   if (L.qf == QS_MX) {
+    const MxCopy wg = mx_copy(sc, L.q_wg, EI, L.H), wu = mx_copy(sc, L.q_wu, EI, L.H),
+                 wd = mx_copy(sc, L.q_wd, EH, L.I);
     if (keep) {  // one read each, both axes
-      e = launch_mx_qdq(c, W_gate, wq(L.q_wgc), EI, L.H, false, nullptr, sq(L.q_wg));
-      if (e == cudaSuccess)
-        e = launch_mx_qdq(c, W_up, wq(L.q_wuc), EI, L.H, false, nullptr, sq(L.q_wu));
-      if (e == cudaSuccess && emit_qa)
-        e = launch_mx_qdq(c, W_down, wq(L.q_wdc), EH, L.I, false, nullptr, sq(L.q_wd));
+      const MxCopy wgc = mx_copy(wbase, L.q_wgc, EI, L.H), wuc = mx_copy(wbase, L.q_wuc, EI, L.H),
+                   wdc = mx_copy(wbase, L.q_wdc, EH, L.I);
+      e = mx_cols(c, W_gate, wgc, EI, L.H, nullptr, &wg);
+      if (e == cudaSuccess) e = mx_cols(c, W_up, wuc, EI, L.H, nullptr, &wu);
+      if (e == cudaSuccess && emit_down) e = mx_cols(c, W_down, wdc, EH, L.I, nullptr, &wd);
     } else {
-      e = launch_mx_qdq(c, W_gate, sq(L.q_wg), EI, L.H, true, nullptr);
-      if (e == cudaSuccess) e = launch_mx_qdq(c, W_up, sq(L.q_wu), EI, L.H, true, nullptr);
-      if (e == cudaSuccess && emit_qa)
-        e = launch_mx_qdq(c, W_down, sq(L.q_wd), EH, L.I, true, nullptr);
+      e = mx_rows(c, W_gate, wg, EI, L.H, nullptr);
+      if (e == cudaSuccess) e = mx_rows(c, W_up, wu, EI, L.H, nullptr);
+      if (e == cudaSuccess && emit_down) e = mx_rows(c, W_down, wd, EH, L.I, nullptr);
     }
-  } else if (L.qf == QS_BLOCK) {  // the copies every GEMM of the layer reads
+  } else if (L.qf == QS_BLOCK) {
+    auto wq = [&](size_t off) { return reinterpret_cast<uint16_t*>(wbase + off); };
     e = launch_fb_qdq(c, W_gate, wq(L.q_wgc), EI, L.H, FB_TILES, nullptr, nullptr);
     if (e == cudaSuccess)
       e = launch_fb_qdq(c, W_up, wq(L.q_wuc), EI, L.H, FB_TILES, nullptr, nullptr);
@@ -320,37 +393,49 @@ static cudaError_t weight_copies(const Ctx& c, const Layout& L, bool keep, bool 
   return e;
 }
 
+// The forward's gate/up stage on A (from permute_x): h = [g | u] and a = silu(g) * u,
+// with the weights quantised first under a quantised forward (weight_copies, unless
+// `weights_ready`).  `emit_qa` makes it also produce the down projection's operand:
+// a in MXFP8 along I from the GEMM's epilogue, or (blockwise FP8) a row pass over a.
+// The backward under MM_MOE_RECOMPUTE calls it with the forward's arguments and gets
+// h and a bit for bit (the same kernels on the same inputs).
 static mm_moe_status gateup_stage(const Ctx& c, const Layout& L, bool keep, bool emit_qa,
-                                  const uint16_t* A, const uint16_t* W_gate,
-                                  const uint16_t* W_up, const uint16_t* W_down, uint16_t* h,
-                                  uint16_t* a, const char* sv, char* wbase, char* sc,
+                                  Opnd A, const uint16_t* W_gate, const uint16_t* W_up,
+                                  const uint16_t* W_down, uint16_t* h, uint16_t* a,
+                                  const char* sv, char* wbase, char* sc,
                                   bool weights_ready = false) {
   const int* meta = reinterpret_cast<const int*>(sv + L.meta);
-  auto sq = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
-  auto wq = [&](size_t off) { return reinterpret_cast<uint16_t*>(wbase + off); };
   if (!weights_ready)
     MM_MOE_TRY(weight_copies(c, L, keep, emit_qa, W_gate, W_up, W_down, wbase, sc));
-  const uint16_t *Bg = W_gate, *Bu = W_up;
-  if (L.qf == QS_MX) {
-    Bg = sq(L.q_wg);
-    Bu = sq(L.q_wu);
-  } else if (L.qf == QS_BLOCK) {
-    Bg = wq(L.q_wgc);
-    Bu = wq(L.q_wuc);
-  }
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
   g.kind = GEMM_GATEUP;
-  g.A = A;
-  g.B0 = Bg;
-  g.B1 = Bu;
+  g.A = A.p;
+  g.sA = A.sf;
+  g.B0 = W_gate;
+  g.B1 = W_up;
   g.out0 = h;
   g.out1 = a;
-  g.mx = (L.qf == QS_MX && emit_qa) ? 1 : 0;
-  g.q0 = g.mx ? sq(L.q_a) : nullptr;
+  if (L.qf == QS_MX) {
+    const MxCopy wg = mx_copy(sc, L.q_wg, L.E * L.I, L.H), wu = mx_copy(sc, L.q_wu, L.E * L.I, L.H);
+    g.fp8 = true;
+    g.B0 = wg.codes;
+    g.sB0 = wg.sf;
+    g.B1 = wu.codes;
+    g.sB1 = wu.sf;
+    if (emit_qa) {
+      const MxCopy qa = mx_copy(sc, L.q_a, L.Rp, L.I);
+      g.q_codes = qa.codes;
+      g.q_sf = qa.sf;
+    }
+  } else if (L.qf == QS_BLOCK) {
+    g.B0 = wbase + L.q_wgc;
+    g.B1 = wbase + L.q_wuc;
+  }
   MM_MOE_TRY(launch_gemm(c, L, g));
-  if (L.qf == QS_BLOCK && emit_qa) MM_MOE_TRY(act_rows(c, QS_BLOCK, a, sq(L.q_a), L.Rp, L.I, meta));
+  if (L.qf == QS_BLOCK && emit_qa)
+    MM_MOE_TRY(fb_rows(c, a, reinterpret_cast<uint16_t*>(sc + L.q_a), L.Rp, L.I, meta));
   return MM_MOE_OK;
 }
 
@@ -393,9 +478,8 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   // stream beside the routing, the permutation and the token-axis gather, which write
   // none of the buffers they write, and gate/up waits for them
   char* wbase = L.w_common ? sc : sv;  // where the backward's (blockwise: all) weight copies go
-  const bool side = L.qf != QS_NONE;
   Fork fork;
-  if (side) {
+  if (L.qf != QS_NONE) {
     if (!fork.open(c.stream)) return MM_MOE_ECUDA;
     const Ctx cs{fork.side(), d.sms, &launches};
     MM_MOE_TRY(weight_copies(cs, L, L.w_in_saved, true, W_gate, W_up, W_down, wbase, sc));
@@ -411,24 +495,31 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   // copies quantised along each GEMM's K (H for gate/up, I for down).  A forward that
   // keeps its activations also leaves x's blocks along tokens in x_perm's place.
   cudaError_t err = cudaSuccess;
-  const uint16_t* A1 = permute_x(c, L, x, x_perm, L.w_in_saved ? x_perm : nullptr, sv,
-                                 reinterpret_cast<float*>(sv + L.w_row), sc, &err);
+  const Opnd A1 = permute_x(c, L, x, x_perm, L.w_in_saved, sv,
+                            reinterpret_cast<float*>(sv + L.w_row), sc, &err);
   MM_MOE_TRY(err);
   MM_MOE_TRY(fork.join());
   st = gateup_stage(c, L, L.w_in_saved, true, A1, W_gate, W_up, W_down, h, a, sv, wbase, sc,
-                    side);
+                    L.qf != QS_NONE);
   if (st != MM_MOE_OK) return st;
-  const uint16_t* A2 = L.qf != QS_NONE ? reinterpret_cast<uint16_t*>(sc + L.q_a) : a;
-  const uint16_t* Bd = L.qf == QS_MX      ? reinterpret_cast<uint16_t*>(sc + L.q_wd)
-                       : L.qf == QS_BLOCK ? reinterpret_cast<uint16_t*>(wbase + L.q_wdc)
-                                          : W_down;
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
   g.kind = GEMM_DOWN;
-  g.A = A2;
-  g.B0 = Bd;
+  g.A = a;
+  g.B0 = W_down;
   g.out0 = ys;
+  if (L.qf == QS_MX) {
+    const MxCopy qa = mx_copy(sc, L.q_a, L.Rp, L.I), wd = mx_copy(sc, L.q_wd, L.E * L.H, L.I);
+    g.fp8 = true;
+    g.A = qa.codes;
+    g.sA = qa.sf;
+    g.B0 = wd.codes;
+    g.sB0 = wd.sf;
+  } else if (L.qf == QS_BLOCK) {
+    g.A = sc + L.q_a;
+    g.B0 = wbase + L.q_wdc;
+  }
   MM_MOE_TRY(launch_gemm(c, L, g));
   MM_MOE_TRY(launch_combine(c, L, ys, sv, y));
   g_last_launches = launches;
@@ -466,13 +557,15 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   const uint16_t* x_perm = reinterpret_cast<const uint16_t*>(act + L.x_perm);
   const uint16_t* h = reinterpret_cast<const uint16_t*>(act + L.h);
   const uint16_t* a = reinterpret_cast<const uint16_t*>(act + L.a);
+  const int* meta = reinterpret_cast<const int*>(sv + L.meta);
+  const int64_t EI = L.E * L.I, EH = L.E * L.H, Rp = L.Rp, H = L.H, I = L.I;
   MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
   if (L.recompute) {
     // activation checkpointing: gate/up's operand (x_perm, or q_x under a quantised
     // forward), h and a again, as the forward made them
     uint16_t* xp = reinterpret_cast<uint16_t*>(sc + L.x_perm);
     cudaError_t err = cudaSuccess;
-    const uint16_t* A0 = permute_x(c, L, x, xp, nullptr, sv, nullptr, sc, &err);
+    const Opnd A0 = permute_x(c, L, x, xp, false, sv, nullptr, sc, &err);
     MM_MOE_TRY(err);
     st = gateup_stage(c, L, false, false, A0, W_gate, W_up, W_down,
                       reinterpret_cast<uint16_t*>(sc + L.h),
@@ -481,58 +574,74 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   }
   // A quantised backward (MXFP8 for full MXFP8 and fp8_bwd, blockwise FP8): every
   // GEMM reads copies of its operands quantised along its own K.  The permutation of
-  // dy then writes dy's blocks along H (this GEMM's operand) to dy_perm, and dy's
-  // blocks along tokens (the dW_down operand) are gathered from dy.
+  // dy then writes dy's blocks along H (this GEMM's operand) into dy_perm's place, and
+  // dy's blocks along tokens (the dW_down operand) are gathered from dy.  The
+  // backward's weight copies were made by the forward (saved), by the recompute
+  // (blockwise, front of scratch), or are made here (MXFP8 along their backward K).
   const int qb = L.qb;
-  MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY, sc, qb));
-  const int* meta = reinterpret_cast<const int*>(sv + L.meta);
-  const int64_t EI = L.E * L.I, EH = L.E * L.H;
-  auto q = [&](size_t off) { return reinterpret_cast<uint16_t*>(sc + off); };
-  // the backward's quantised weights: made by the forward (saved), by the recompute
-  // (blockwise, front of scratch), or here (MXFP8 along their backward K)
-  auto qw = [&](size_t off) -> const uint16_t* {
-    return L.w_in_saved ? reinterpret_cast<const uint16_t*>(sv + off) : q(off);
-  };
+  const char* wsrc = L.w_in_saved ? sv : sc;
   const bool make_w = qb == QS_MX && !L.w_in_saved;
-  const uint16_t* A1 = dy_perm;
-  const uint16_t* Bd = W_down;
-  if (qb != QS_NONE) {
-    MM_MOE_TRY(act_cols(c, qb, dy, q(L.q_dyc), L.Rp, L.H, meta, nullptr, routed_rows(L, sv)));
-    if (make_w) MM_MOE_TRY(launch_mx_qdq(c, W_down, q(L.q_wdc), EH, L.I, false, nullptr));
-    Bd = qw(L.q_wdc);
-  }
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
   g.kind = GEMM_DGRAD_DOWN;
-  g.A = A1;
-  g.B0 = Bd;
+  g.A = dy_perm;
+  g.B0 = W_down;
   g.aux = h;
   g.aux2 = a;
   g.out0 = dh;
   g.out1 = a_w;
   g.outf = pw;
-  MM_MOE_TRY(launch_gemm(c, L, g));
-  const uint16_t *A2 = dh, *Bg = W_gate, *Bu = W_up;
-  if (qb != QS_NONE) {
-    // one read of dh: blocks along tokens (dW_gate, dW_up) to q_dhc, blocks along I
-    // (the next GEMM) in place
-    MM_MOE_TRY(act_cols(c, qb, dh, q(L.q_dhc), L.Rp, 2 * L.I, meta, dh));
-    if (make_w) {
-      MM_MOE_TRY(launch_mx_qdq(c, W_gate, q(L.q_wgc), EI, L.H, false, nullptr));
-      MM_MOE_TRY(launch_mx_qdq(c, W_up, q(L.q_wuc), EI, L.H, false, nullptr));
+  if (qb == QS_MX) {
+    const MxCopy dyr = mx_copy(sc, L.dy_perm, Rp, H), wdc = mx_copy(wsrc, L.q_wdc, EH, I);
+    MM_MOE_TRY(launch_permute(c, L, dy, dyr.codes, sv, nullptr, K_PERMUTE_DY, sc, QS_MX, dyr.sf));
+    MM_MOE_TRY(mx_cols(c, dy, mx_copy(sc, L.q_dyc, Rp, H), Rp, H, meta, nullptr,
+                       routed_rows(L, sv)));
+    if (make_w) MM_MOE_TRY(mx_cols(c, W_down, wdc, EH, I, nullptr));
+    g.fp8 = true;
+    g.A = dyr.codes;
+    g.sA = dyr.sf;
+    g.B0 = wdc.codes;
+    g.sB0 = wdc.sf;
+  } else {
+    MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY, sc, qb));
+    if (qb == QS_BLOCK) {
+      MM_MOE_TRY(fb_cols(c, dy, reinterpret_cast<uint16_t*>(sc + L.q_dyc), Rp, H, meta, nullptr,
+                         routed_rows(L, sv)));
+      g.B0 = wsrc + L.q_wdc;
     }
-    Bg = qw(L.q_wgc);
-    Bu = qw(L.q_wuc);
   }
+  MM_MOE_TRY(launch_gemm(c, L, g));
   g = GemmArgs{};
   g.saved = sv;
   g.scratch = sc;
   g.kind = GEMM_DGRAD_GATEUP;
-  g.A = A2;
-  g.B0 = Bg;
-  g.B1 = Bu;
+  g.A = dh;
+  g.B0 = W_gate;
+  g.B1 = W_up;
   g.out0 = dxs;
+  if (qb == QS_MX) {
+    // one read of dh: blocks along tokens (dW_gate, dW_up) and along I (this GEMM)
+    const MxCopy dhc = mx_copy(sc, L.q_dhc, Rp, 2 * I), dhr = mx_copy(sc, L.q_dhr, Rp, 2 * I);
+    const MxCopy wgc = mx_copy(wsrc, L.q_wgc, EI, H), wuc = mx_copy(wsrc, L.q_wuc, EI, H);
+    MM_MOE_TRY(mx_cols(c, dh, dhc, Rp, 2 * I, meta, &dhr));
+    if (make_w) {
+      MM_MOE_TRY(mx_cols(c, W_gate, wgc, EI, H, nullptr));
+      MM_MOE_TRY(mx_cols(c, W_up, wuc, EI, H, nullptr));
+    }
+    g.fp8 = true;
+    g.A = dhr.codes;
+    g.sA = dhr.sf;
+    g.B0 = wgc.codes;
+    g.sB0 = wgc.sf;
+    g.B1 = wuc.codes;
+    g.sB1 = wuc.sf;
+  } else if (qb == QS_BLOCK) {
+    // one read of dh: blocks along tokens to q_dhc, along I in place
+    MM_MOE_TRY(fb_cols(c, dh, reinterpret_cast<uint16_t*>(sc + L.q_dhc), Rp, 2 * I, meta, dh));
+    g.B0 = wsrc + L.q_wgc;
+    g.B1 = wsrc + L.q_wuc;
+  }
   MM_MOE_TRY(launch_gemm(c, L, g));
   // the un-permute (bandwidth-bound) runs on the side stream beside the
   // weight-gradient GEMMs, which read none of its inputs and write none of its outputs
@@ -543,45 +652,65 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   // token-axis blocks of the weight-gradient operands: each expert's rows start on a
   // multiple of 128 and its padding rows are zero, so 32- or 128-row blocks of the
   // padded row space are the per-expert blocks with a zero-padded tail
-  const uint16_t *A3 = dy_perm, *B3 = a_w, *A4 = dh, *B4 = x_perm;
-  if (qb != QS_NONE) {
-    MM_MOE_TRY(act_cols(c, qb, a_w, a_w, L.Rp, L.I, meta));
-    if (!L.w_in_saved) {  // (a quantised forward that keeps its activations left x's
-                          // blocks along tokens in x_perm's place)
-      if (L.qf == QS_NONE)  // fp8_bwd: x_perm is the forward's bf16 copy
-        MM_MOE_TRY(act_cols(c, qb, x_perm, q(L.q_xc), L.Rp, L.H, meta));
-      else  // recompute under a quantised forward: from x itself
-        MM_MOE_TRY(act_cols(c, qb, x, q(L.q_xc), L.Rp, L.H, meta, nullptr, routed_rows(L, sv)));
-      B4 = q(L.q_xc);
+  g = GemmArgs{};
+  g.saved = sv;
+  g.scratch = sc;
+  g.A = dh;              // dW_gate / dW_up = dh^T x
+  g.B0 = x_perm;
+  g.A2 = dy_perm;        // dW_down = dy^T (w a)
+  g.B2 = a_w;
+  g.out0 = dW_gate;
+  g.out1 = dW_up;
+  g.out2 = dW_down;
+  if (qb == QS_MX) {
+    const MxCopy awc = mx_copy(sc, L.q_awc, Rp, I);
+    MM_MOE_TRY(mx_cols(c, a_w, awc, Rp, I, meta));
+    MxCopy xc = mx_copy(sv, L.x_perm, Rp, H);  // the forward's gather (kept activations)
+    if (!L.w_in_saved) {
+      xc = mx_copy(sc, L.q_xc, Rp, H);
+      if (L.qf == QS_NONE)  // fp8_bwd: from the forward's bf16 x_perm
+        MM_MOE_TRY(mx_cols(c, x_perm, xc, Rp, H, meta));
+      else                  // recompute under a quantised forward: from x itself
+        MM_MOE_TRY(mx_cols(c, x, xc, Rp, H, meta, nullptr, routed_rows(L, sv)));
     }
-    A3 = q(L.q_dyc);
-    A4 = q(L.q_dhc);
+    const MxCopy dyc = mx_copy(sc, L.q_dyc, Rp, H), dhc = mx_copy(sc, L.q_dhc, Rp, 2 * I);
+    g.fp8 = true;
+    g.A = dhc.codes;
+    g.sA = dhc.sf;
+    g.B0 = xc.codes;
+    g.sB0 = xc.sf;
+    g.A2 = dyc.codes;
+    g.sA2 = dyc.sf;
+    g.B2 = awc.codes;
+    g.sB2 = awc.sf;
+  } else if (qb == QS_BLOCK) {
+    MM_MOE_TRY(fb_cols(c, a_w, a_w, Rp, I, meta));
+    const uint16_t* xb = x_perm;  // (a blockwise forward that keeps its activations left
+                                  // x's blocks along tokens in x_perm's place)
+    if (!L.w_in_saved) {
+      uint16_t* q_xc = reinterpret_cast<uint16_t*>(sc + L.q_xc);
+      MM_MOE_TRY(fb_cols(c, x, q_xc, Rp, H, meta, nullptr, routed_rows(L, sv)));
+      xb = q_xc;
+    }
+    g.A = sc + L.q_dhc;
+    g.B0 = xb;
+    g.A2 = sc + L.q_dyc;
   }
   // both weight gradients in one launch where they tile N alike (one list of tiles,
   // experts by descending row count, balances the clusters' loads far better than
   // two lists); otherwise one launch each
   const bool both = wgrad_both_ok(L);
-  g = GemmArgs{};
-  g.saved = sv;
-  g.scratch = sc;
-  g.kind = both ? GEMM_WGRAD_BOTH : GEMM_WGRAD_GATEUP;
-  g.A = A4;
-  g.B0 = B4;
-  g.out0 = dW_gate;
-  g.out1 = dW_up;
-  g.A2 = A3;
-  g.B2 = B3;
-  g.out2 = dW_down;
   if (!both) {
-    GemmArgs gd{};
-    gd.saved = sv;
-    gd.scratch = sc;
+    GemmArgs gd = g;
     gd.kind = GEMM_WGRAD_DOWN;
-    gd.A = A3;
-    gd.B0 = B3;
+    gd.A = g.A2;
+    gd.sA = g.sA2;
+    gd.B0 = g.B2;
+    gd.sB0 = g.sB2;
     gd.out0 = dW_down;
     MM_MOE_TRY(launch_gemm(c, L, gd));
   }
+  g.kind = both ? GEMM_WGRAD_BOTH : GEMM_WGRAD_GATEUP;
   MM_MOE_TRY(launch_gemm(c, L, g));
   MM_MOE_TRY(fork.join());  // the call ends on `stream`
   g_last_launches = launches;

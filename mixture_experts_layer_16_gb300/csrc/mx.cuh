@@ -82,5 +82,64 @@ __device__ __forceinline__ void qdq_col32(const float (&v)[32], float (&out)[32]
   for (int i = 0; i < 32; i += 2) qdq2(out[i], out[i + 1], e[i], e[i + 1]);
 }
 
+// ---------------------------------------------------------------- MXFP8 storage
+// The block-scaled tensor cores read an MXFP8 operand as e4m3 codes (one byte per
+// element, in the operand's own row-major layout) and E8M0 scale codes (2^e stored as
+// e + 127; all-zero blocks store 0, i.e. 2^-127) in the arrangement below.  For an
+// operand whose MMA rows (rows of A, or of B) are indexed by mn and whose K is cut
+// into 32-element k-blocks kb: 512-byte atoms of 128 consecutive mn x 4 consecutive
+// kb; inside an atom, mn % 32 picks a 16-byte row, (mn / 32) % 4 a 4-byte word of it
+// and kb % 4 the byte of the word; the atoms of one group of 4 k-blocks lie side by
+// side for consecutive 128-row blocks of mn (mn_blocks of them), then the next group.
+// A GEMM stage (128 elements of K) then reads one atom per 128 rows of each operand.
+__host__ __device__ __forceinline__ int64_t sf_offset(int64_t mn, int64_t kb, int64_t mn_blocks) {
+  return ((kb >> 2) * mn_blocks + (mn >> 7)) * 512 + (mn & 31) * 16 + ((mn >> 5) & 3) * 4 +
+         (kb & 3);
+}
+
+// E8M0 code of the block scale 2^e (e in [-127, 127]).
+__device__ __forceinline__ uint32_t e8m0(int e) { return static_cast<uint32_t>(e + 127); }
+
+// e4m3 codes of v / 2^e for two values (nearest even, saturating at +-448); a in the
+// low byte.  Exact scaling as in qdq2.
+__device__ __forceinline__ uint32_t codes2(float a, float b, int e) {
+  const float s = pow2f(-e);
+  return static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(a * s, b * s), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Two values, each under its own exponent (blocks down columns).
+__device__ __forceinline__ uint32_t codes2e(float a, int ea, float b, int eb) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a * pow2f(-ea), b * pow2f(-eb)),
+                                                        __NV_SATFINITE, __NV_E4M3));
+}
+
+// Eight values under one exponent -> eight codes (element 0 in the lowest byte).
+__device__ __forceinline__ uint2 codes8(const float (&v)[8], int e) {
+  return make_uint2(codes2(v[0], v[1], e) | (codes2(v[2], v[3], e) << 16),
+                    codes2(v[4], v[5], e) | (codes2(v[6], v[7], e) << 16));
+}
+
+// One thread's 32 values form one block: round them to bf16 (the stored value),
+// return the block exponent and the 32 codes (4 x 8 bytes).
+__device__ __forceinline__ int quant_row32(const float (&v)[32], uint2 (&out)[4]) {
+  float r[32];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    r[i] = round_bf(v[i]);
+    amax = fmaxf(amax, fabsf(r[i]));
+  }
+  const int e = scale_exp(amax);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = r[8 * q + j];
+    out[q] = codes8(w, e);
+  }
+  return e;
+}
+
 }  // namespace mx
 }  // namespace mmmoe

@@ -293,6 +293,52 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// D[tmem] (+)= (A * SFA)[smem] * (B * SFB)[smem]^T: MXFP8, e4m3 A and B, one E8M0
+// scale per 32 elements along K for each row of A and each row of B (scale_vec::1X),
+// fp32 accumulator; K = 32 per instruction.  The scales are read from TMEM at sfa /
+// sfb (written there by tmem_cp_sf); which byte of each scale word holds this
+// instruction's k-block is given by the scale-factor ids of the instruction
+// descriptor (idesc_mxf8 | sf_ids).  With CTAS = 2 each CTA's TMEM holds the scales
+// of its own half of A's rows and all of B's.
+template <int CTAS>
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  if constexpr (CTAS == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+        "[%4], [%5], p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copy one 512-byte scale atom (128 rows x 4 k-blocks, the 32 x 16-byte arrangement
+// written by the quantisers: row r of the atom in 16-byte row r % 32, word (r / 32) % 4,
+// byte = k-block % 4) from shared memory to TMEM columns taddr .. taddr + 3 of every
+// lane quadrant (32 rows x 128 bits, replicated to the four quadrants).  Issued by the
+// MMA thread; ordered before its later tcgen05.mma like another tcgen05 operation of
+// that thread.  With CTAS = 2 each CTA of the pair copies from its own shared memory
+// at the same offset into its own TMEM.
+template <int CTAS>
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  if constexpr (CTAS == 1)
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread
 // completes; with CTAS = 2 on the barrier at the same offset in each CTA of `mask`.
 template <int CTAS>
@@ -367,6 +413,30 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= 2ull << 61;
   return d;
 }
+
+// Shared-memory descriptor of a scale atom for tmem_cp_sf: no swizzle, 8-row groups of
+// 16-byte rows 128 bytes apart (both offsets 128: the atom is one column of 16-byte
+// rows, so the leading-dimension offset is never stepped).
+__device__ __forceinline__ uint64_t smem_desc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= 1ull << 46;
+  return d;
+}
+
+// Instruction descriptor of kind::mxf8f6f4.block_scale with e4m3 A and B (format
+// code 0), E8M0 scales (bit 23) and an fp32 accumulator: bit 15 A MN-major, bit 16 B
+// MN-major, bits 17-22 N >> 3, bits 24-28 M >> 4; the scale-factor ids (bits 4-5 for
+// B, 29-30 for A) are or-ed in per instruction by sf_ids.
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
+  return ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((N >> 3) << 17) | (1u << 23) |
+         ((M >> 4) << 24);
+}
+// k-block j (0..3) of a scale word: the byte of A's and B's scale words this
+// instruction reads.
+__host__ __device__ constexpr uint32_t sf_ids(uint32_t j) { return (j << 29) | (j << 4); }
 
 // Instruction descriptor of kind::f16 with bf16 A/B and an fp32 accumulator:
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),

@@ -254,38 +254,22 @@ cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* 
 // a ring of PERM_SLOTS row buffers, loading PERM_AHEAD tokens ahead of the one it
 // stores.  Padding rows are then stored from a zero row; in the forward their
 // routing weight is zeroed too (valid rows got theirs from the placement kernel).
-// QM = QS_MX / QS_BLOCK: the warp quantises each row in shared memory (32- / 128-
-// element blocks along the row) between its load and its stores, so the k copies are
-// the row's quantised values; a zero row quantises to itself.
+// QM = QS_BLOCK: the warp quantise-dequantises each row in shared memory (128-element
+// blocks along the row, bf16 out) between its load and its stores; QM = QS_MX: the
+// warp turns each row into its MXFP8 form (e4m3 codes, H bytes, stored to the k
+// destination rows of a [Rp, H] byte tensor; the H / 32 scale codes written as words
+// of the scale arrangement mx::sf_offset over the padded rows).  A zero row quantises
+// to zero codes and zero scale codes.
 constexpr int PERM_SLOTS = 8;
 constexpr int PERM_AHEAD = 4;
 constexpr uint64_t PERM_WAIT_NS = 2000000000ull;
 
-// Quantise one bf16 row of n elements in shared memory in place (all 32 lanes).
+// Blockwise FP8: quantise-dequantise one bf16 row of n elements in shared memory in
+// place (all 32 lanes; 128-element blocks).
 template <int QM>
 __device__ __forceinline__ void quantise_row(uint8_t* row, int n, int lane) {
   uint4* r4 = reinterpret_cast<uint4*>(row);
-  if constexpr (QM == QS_MX) {  // a lane per 32-element block (four 16-byte pieces)
-    for (int b = lane; b < n / 32; b += 32) {
-      float v[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 w = r4[4 * b + q];
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(&w);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[8 * q + j] = mx::bf(h[j]);
-      }
-      mx::qdq_row32(v);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 w;
-        uint16_t* h = reinterpret_cast<uint16_t*>(&w);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) h[j] = mx::to_bf(v[8 * q + j]);
-        r4[4 * b + q] = w;
-      }
-    }
-  } else {  // a lane per half block (64 elements), neighbouring lanes pair up
+  {  // a lane per half block (64 elements), neighbouring lanes pair up
     const int nh = n / 64;  // even: n % 128 == 0
     for (int h0 = 0; h0 < nh; h0 += 32) {
       const int hb = h0 + lane;
@@ -320,15 +304,54 @@ __device__ __forceinline__ void quantise_row(uint8_t* row, int n, int lane) {
   }
 }
 
+// MXFP8 form of one bf16 row of n elements in shared memory (all 32 lanes): the n
+// e4m3 codes over the start of the same buffer, the n / 32 scale codes to `scales`.
+// A lane takes one 32-element block per round; every lane reads its round's block
+// before any lane writes codes (which land on bytes of this round's or earlier
+// rounds' blocks only).
+__device__ __forceinline__ void quantise_row_mx(uint8_t* row, uint8_t* scales, int n, int lane) {
+  const int nb = n / 32;
+  for (int b0 = 0; b0 < nb; b0 += 32) {
+    const int b = b0 + lane;
+    float v[32];
+    if (b < nb) {
+      const uint4* r4 = reinterpret_cast<const uint4*>(row + b * 64);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 w = r4[q];
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[8 * q + j] = mx::bf(h[j]);
+      }
+    }
+    __syncwarp();
+    if (b < nb) {
+      uint2 c[4];
+      const int e = mx::quant_row32(v, c);
+      uint4* d4 = reinterpret_cast<uint4*>(row + b * 32);
+      d4[0] = make_uint4(c[0].x, c[0].y, c[1].x, c[1].y);
+      d4[1] = make_uint4(c[2].x, c[2].y, c[3].x, c[3].y);
+      scales[b] = static_cast<uint8_t>(mx::e8m0(e));
+    }
+    __syncwarp();
+  }
+}
+
 template <int QM>
 __global__ void __launch_bounds__(32) permute_rows_kernel(
     const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int row_bytes, int T, int k,
     const int* __restrict__ meta, const int* __restrict__ tile_rows,
-    const int* __restrict__ prow, float* __restrict__ w_row, DevStatus* status) {
-  extern __shared__ __align__(128) uint8_t pbuf[];  // PERM_SLOTS rows, then a zero row
+    const int* __restrict__ prow, float* __restrict__ w_row, DevStatus* status,
+    uint8_t* __restrict__ sf, int64_t sf_mnb) {
+  // PERM_SLOTS rows, a zero row, then (MXFP8) PERM_SLOTS rows of scale codes
+  extern __shared__ __align__(128) uint8_t pbuf[];
   __shared__ __align__(8) uint64_t bar[PERM_SLOTS];
   const int lane = threadIdx.x;
   uint8_t* zero = pbuf + PERM_SLOTS * row_bytes;
+  const int n_el = row_bytes / 2;                            // elements of a row
+  const int out_bytes = QM == QS_MX ? n_el : row_bytes;      // bytes stored per row
+  uint8_t* sbuf = zero + row_bytes;                          // MXFP8 scale codes
+  const int n_words = n_el / 128;                            // MXFP8 scale words per row
   for (int i = lane * 16; i < row_bytes; i += 32 * 16)
     *reinterpret_cast<uint4*>(zero + i) = make_uint4(0, 0, 0, 0);
   ptx::fence_proxy_async_smem();  // the zero row is read by bulk stores
@@ -377,40 +400,61 @@ __global__ void __launch_bounds__(32) permute_rows_kernel(
       // the other lanes observe the completed phase too (it returns at once), which
       // makes the row's bytes visible to them
       if (lane != 0) ptx::mbar_wait(&bar[s], parity, &dummy, PERM_WAIT_NS);
-      quantise_row<QM>(pbuf + s * row_bytes, row_bytes / 2, lane);
+      if constexpr (QM == QS_MX)
+        quantise_row_mx(pbuf + s * row_bytes, sbuf + s * (n_el / 32), n_el, lane);
+      else
+        quantise_row<QM>(pbuf + s * row_bytes, n_el, lane);
       ptx::fence_proxy_async_smem();  // the stores below read the quantised row
       __syncwarp();
     }
+    const int64_t f0 = (first + static_cast<int64_t>(i) * step) * k;
     if (lane == 0) {
-      const int64_t f0 = (first + static_cast<int64_t>(i) * step) * k;
       for (int j = 0; j < k; ++j) {
         const int pr = __ldg(prow + f0 + j);
         if (pr >= 0)
-          ptx::bulk_store(dst + static_cast<int64_t>(pr) * row_bytes, pbuf + s * row_bytes,
-                          row_bytes);
+          ptx::bulk_store(dst + static_cast<int64_t>(pr) * out_bytes, pbuf + s * row_bytes,
+                          out_bytes);
       }
       ptx::bulk_commit();
     }
+    if constexpr (QM == QS_MX) {  // the row's scale words, to each of its k rows
+      const uint32_t* words = reinterpret_cast<const uint32_t*>(sbuf + s * (n_el / 32));
+      for (int j = 0; j < k; ++j) {
+        const int pr = __ldg(prow + f0 + j);
+        if (pr < 0) continue;
+        for (int g = lane; g < n_words; g += 32)
+          *reinterpret_cast<uint32_t*>(sf + mx::sf_offset(pr, 4 * g, sf_mnb)) = words[g];
+      }
+      __syncwarp();  // the slot's scale codes are rewritten PERM_SLOTS tokens later
+    }
   }
-  if (lane != 0) return;
-  // --- padding rows of the M tiles
+  if (QM != QS_MX && lane != 0) return;
+  // --- padding rows of the M tiles (MXFP8: zero scale words too, by every lane)
   const int n_tiles = __ldg(meta + META_NUM_TILES);
   for (int mb = first; mb < n_tiles; mb += step) {
     for (int r = max(0, __ldg(tile_rows + mb)); r < BM; ++r) {
       const int64_t pr = static_cast<int64_t>(mb) * BM + r;
-      ptx::bulk_store(dst + pr * row_bytes, zero, row_bytes);
-      if (w_row != nullptr) w_row[pr] = 0.f;
+      if (lane == 0) {
+        ptx::bulk_store(dst + pr * out_bytes, zero, out_bytes);
+        if (w_row != nullptr) w_row[pr] = 0.f;
+      }
+      if constexpr (QM == QS_MX)
+        for (int g = lane; g < n_words; g += 32)
+          *reinterpret_cast<uint32_t*>(sf + mx::sf_offset(pr, 4 * g, sf_mnb)) = 0u;
     }
   }
-  ptx::bulk_commit();
-  ptx::bulk_wait_all();
+  if (lane == 0) {
+    ptx::bulk_commit();
+    ptx::bulk_wait_all();
+  }
 }
 
-cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, uint16_t* dst,
+cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, void* dst,
                            const char* saved, float* w_row_out, int kernel_id, char* scratch,
-                           int quant) {
+                           int quant, uint8_t* sf) {
   const int row_bytes = static_cast<int>(L.H * 2);
-  const int smem = (PERM_SLOTS + 1) * row_bytes;
+  const int smem = (PERM_SLOTS + 1) * row_bytes +
+                   (quant == QS_MX ? PERM_SLOTS * static_cast<int>(L.H / 32) : 0);
   auto* kern = quant == QS_MX      ? permute_rows_kernel<QS_MX>
                : quant == QS_BLOCK ? permute_rows_kernel<QS_BLOCK>
                                    : permute_rows_kernel<QS_NONE>;
@@ -423,7 +467,7 @@ cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, u
       static_cast<int>(L.T), static_cast<int>(L.k), reinterpret_cast<const int*>(saved + L.meta),
       reinterpret_cast<const int*>(saved + L.tile_rows),
       reinterpret_cast<const int*>(saved + L.prow), w_row_out,
-      reinterpret_cast<DevStatus*>(scratch + L.status));
+      reinterpret_cast<DevStatus*>(scratch + L.status), sf, L.Rp / 128);
   prof_end(c, kernel_id);
   return cudaGetLastError();
 }

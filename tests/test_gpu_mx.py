@@ -26,7 +26,7 @@ def _built():
 
 SMALL = [
     # (T, H, I, E, k, routing, seed)
-    (64, 128, 64, 8, 2, "uniform", 21),        # single-SM tiles, 64-wide N tiles
+    (64, 128, 128, 8, 2, "uniform", 21),       # single-SM tiles, one K step
     (1000, 384, 128, 16, 4, "uniform", 22),    # 128-wide N tiles over H, ragged tails
     (777, 512, 256, 32, 8, "zipf", 23),        # skewed routing, SM-pair tiles
     (900, 512, 256, 32, 8, "zipf_trunc", 24),  # experts with no token

@@ -88,3 +88,55 @@ def test_quantiser_rejects_bad_shapes():
     assert lib.mm_moe_mx_qdq(t.data_ptr(), t.data_ptr(), 40, 48, 1, None) == B.MM_MOE_EINVAL
     assert lib.mm_moe_mx_qdq(t.data_ptr(), t.data_ptr(), 40, 48, 0, None) == B.MM_MOE_EINVAL
     assert lib.mm_moe_mx_qdq(t.data_ptr(), t.data_ptr(), 40, 48, 2, None) == B.MM_MOE_EINVAL
+
+
+# ---------------------------------------------------------------- e4m3 codes + scales
+def scale_offset(mn, kb, n_mn):
+    """Byte of the scale code of (operand row mn, k-block kb) in the arrangement the
+    block-scaled tensor cores take: 512-byte atoms of 128 rows x 4 k-blocks (row mn % 32
+    of 16 bytes, word (mn // 32) % 4, byte kb % 4), atoms of one 4-block group side by
+    side over the n_mn // 128 row blocks."""
+    return (((kb // 4) * (n_mn // 128) + mn // 128) * 512 + (mn % 32) * 16
+            + ((mn // 32) % 4) * 4 + kb % 4)
+
+
+@pytest.mark.parametrize("rows,cols,axis", [(128, 256, 1), (128, 256, 0), (384, 2048, 1),
+                                            (384, 2048, 0), (4096, 768, 1), (4096, 768, 0)])
+def test_quantize_codes_and_scales_bit_exact(rows, cols, axis):
+    """mm_moe_mx_quantize (the form the MXFP8 GEMMs read) against the oracle: every
+    scale code is e8m0(floor(log2 amax) - 8) of its block, and every element's e4m3
+    code (decoded by torch's float8_e4m3fn) times its block scale is the oracle's
+    quantised value, bit for bit."""
+    v = make(rows, cols, seed=7 * rows + cols + axis, axis=axis)
+    t = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).cuda()
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(rows * cols // 32, dtype=torch.uint8, device="cuda")
+    B.mm_moe_mx_quantize(t, codes, scales, axis)
+    torch.cuda.synchronize()
+    elem = codes.cpu().view(torch.float8_e4m3fn).double().numpy()
+    sc = scales.cpu().numpy().astype(np.int64)
+    r = np.arange(rows)[:, None]
+    c = np.arange(cols)[None, :]
+    mn, kb, n_mn = (r, c // 32, rows) if axis == 1 else (c, r // 32, cols)
+    s = sc[scale_offset(mn, kb, n_mn)]                       # per element
+    # scale codes: the oracle's block exponent + 127
+    blocks = np.moveaxis(v, axis, -1)
+    blocks = blocks.reshape(blocks.shape[:-1] + (blocks.shape[-1] // 32, 32))
+    want_e = omx.e8m0_scale_exponent(np.abs(blocks).max(axis=-1)) + 127
+    want_s = np.repeat(want_e, 32, axis=-1)
+    want_s = np.moveaxis(want_s, -1, axis) if axis == 0 else want_s
+    assert np.array_equal(s, want_s)
+    got = elem * np.exp2(s.astype(np.float64) - 127)
+    want = omx.mx_qdq(v, axis)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, (bad[:5], got[tuple(bad[0])], want[tuple(bad[0])])
+
+
+def test_quantize_rejects_bad_shapes():
+    t = torch.zeros((128, 96), dtype=torch.bfloat16, device="cuda")
+    u = torch.zeros((128, 96), dtype=torch.uint8, device="cuda")
+    lib = B.lib()
+    assert lib.mm_moe_mx_quantize(t.data_ptr(), u.data_ptr(), u.data_ptr(), 128, 96, 1,
+                                  None) == B.MM_MOE_EINVAL
+    assert lib.mm_moe_mx_quantize(t.data_ptr(), u.data_ptr(), u.data_ptr(), 128, 128, 2,
+                                  None) == B.MM_MOE_EINVAL
