@@ -126,16 +126,30 @@ struct Cfg {
   static constexpr int NACC = (FP8 && BN == 256) ? 1 : 2;
   // epilogue staging per epilogue warp, in 2 KB blocks (32 rows x 32 bf16): TMA-loaded
   // inputs (dSwiGLU: g, u, a) and a ring of output blocks for TMA stores
+  // SPLIT (the FP8 tiles with one accumulator): eight epilogue warps, two per TMEM
+  // lane quadrant, each taking half of the tile's columns; except in the dSwiGLU
+  // epilogue they move their columns to registers (packed bf16) and hand TMEM back
+  // to the MMA issuer before writing anything (EARLY_RELEASE), so the next tile's
+  // main loop overlaps the stores
+  static constexpr bool SPLIT = NACC == 1;
+  static constexpr bool EARLY_RELEASE = SPLIT && KIND != GEMM_DGRAD_DOWN;
+  static constexpr int EPI_WARPS = SPLIT ? 8 : 4;
+  static constexpr int THREADS = 128 + 32 * EPI_WARPS;
   static constexpr int EPI_IN = KIND == GEMM_DGRAD_DOWN ? 3 : 0;
-  static constexpr int EPI_OUT = 4;
+  // (SPLIT: one output block per warp, which leaves room for a sixth pipeline stage;
+  // a warp's next block waits for the previous store to have read it)
+  static constexpr int EPI_OUT = SPLIT ? 1 : 4;
   static constexpr int EPI_WARP_BYTES = (EPI_IN + EPI_OUT) * 2048;
-  static constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
+  static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
   static constexpr int SMEM_CAP = 232448 - 1024;  // opt-in limit minus static shared memory
   static constexpr int STAGES_FIT = (SMEM_CAP - 1024 - EPI_BYTES) / (STAGE_BYTES + SF_BYTES);
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int SMEM_BYTES = STAGES * (STAGE_BYTES + SF_BYTES) + EPI_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = FP8 ? 512 : 2 * BN;
-  static constexpr uint32_t SFA_COL = 256, SFB_COL = 264;  // FP8: scale columns in TMEM
+  // FP8: each pipeline stage has its own 16 TMEM columns for its scales (A's 4, then
+  // B's 4 per 128 rows), so the copy of a stage's scales never waits for the MMAs of
+  // the previous stage to finish reading theirs
+  static constexpr uint32_t SF_COL0 = 256, SF_COLS_PER_STAGE = 16;
   static constexpr uint32_t IDESC = FP8 ? ptx::idesc_mxf8(BM * CTAS, BN, A_MN, B_MN)
                                         : ptx::idesc_bf16_f32(BM * CTAS, BN, A_MN, B_MN);
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
@@ -143,7 +157,8 @@ struct Cfg {
   static_assert(!(KIND == GEMM_GATEUP && (CTAS == 2 || FP8) && BN != 256), "gate/up tile");
   static_assert(!FP8 || BN >= 128, "FP8 scale atoms cover 128 rows of B");
   static_assert(!(FP8 && B_MN && B_ROWS % 128 != 0), "FP8 M/N-major boxes are 128 wide");
-  static_assert(!FP8 || NACC * BN <= static_cast<int>(SFA_COL), "TMEM columns");
+  static_assert(!FP8 || NACC * BN <= static_cast<int>(SF_COL0), "TMEM columns");
+  static_assert(!FP8 || SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM scale ring");
   static_assert(STAGES >= 2, "stages");
 };
 
@@ -294,6 +309,39 @@ __device__ __forceinline__ void store_block(EpiWarp& w, const CUtensorMap* m, in
   w.ob = (w.ob + 1 == NB) ? 0 : w.ob + 1;
 }
 
+// Packed bf16 pairs: 32 values in 16 words.
+__device__ __forceinline__ void pack32(const float (&v)[32], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack2(v[2 * i], v[2 * i + 1]);
+}
+__device__ __forceinline__ void unpack32(const uint32_t (&pk)[16], float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[2 * i] = __uint_as_float(pk[i] << 16);
+    v[2 * i + 1] = __uint_as_float(pk[i] & 0xFFFF0000u);
+  }
+}
+
+// store_block for values already packed to bf16.
+template <int NB>
+__device__ __forceinline__ void store_block_p(EpiWarp& w, const CUtensorMap* m, int c0, int c1,
+                                              const uint32_t (&pk)[16]) {
+  uint8_t* buf = w.out + w.ob * 2048;
+  if (w.lane == 0) ptx::bulk_wait_read<NB - 1>();
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(swz(buf, w.lane, j)) =
+        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (w.lane == 0) {
+    ptx::tma_store_2d(m, buf, c0, c1);
+    ptx::bulk_commit();
+  }
+  w.ob = (w.ob + 1 == NB) ? 0 : w.ob + 1;
+}
+
 // dSwiGLU inputs of one 32-column chunk: g, u (from h) and a, rows row0..row0+31.
 __device__ __forceinline__ void load_inputs(EpiWarp& w, const GemmParams& p, int row0, int col) {
   if (w.lane == 0) {
@@ -431,9 +479,149 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInf
   return true;
 }
 
+// Two 32-column TMEM chunks to registers (one wait for both).
+__device__ __forceinline__ void tmem_ld2(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
+                                         uint32_t (&b)[32]) {
+  ptx::tmem_ld32(ta, a);
+  ptx::tmem_ld32(tb, b);
+  ptx::tmem_wait_ld(a);
+  ptx::reg_fence(b);
+}
+
+// MXFP8 codes and scale of one 32-column block of a (the down projection's operand).
+__device__ __forceinline__ void store_qa(const GemmParams& p, int64_t r, int col,
+                                         const uint32_t (&pa)[16]) {
+  float a[32];
+  unpack32(pa, a);
+  uint2 cq[4];
+  const int e = mx::quant_row32(a, cq);
+  uint4* dq = reinterpret_cast<uint4*>(p.q_codes + r * p.I + col);
+  dq[0] = make_uint4(cq[0].x, cq[0].y, cq[1].x, cq[1].y);
+  dq[1] = make_uint4(cq[2].x, cq[2].y, cq[3].x, cq[3].y);
+  p.q_sf[mx::sf_offset(r, col / 32, p.q_mnb)] = static_cast<uint8_t>(mx::e8m0(e));
+}
+
+// Epilogue of one tile for one warp of a SPLIT tile (BN = 256): quadrant q (rows),
+// half hh of the columns.  With EARLY_RELEASE the warp's accumulator columns go to
+// registers first and release() hands TMEM back before any store.
+template <int KIND, int BN, int CTAS, bool FP8, class Release>
+__device__ __forceinline__ bool epilogue_tile_split(const GemmParams& p, const TileInfo& ti,
+                                                    const TileInfo* next, int q, int hh,
+                                                    uint32_t tbase, EpiWarp& w,
+                                                    volatile int* abort, Release release) {
+  using C = Cfg<KIND, BN, CTAS, FP8>;
+  static_assert(BN == 256, "split tiles are 256 wide");
+  const int lane = w.lane, row = q * 32 + lane;
+  const int row0 = ti.m0 + q * 32;
+  if constexpr (KIND == GEMM_GATEUP) {
+    // gate columns hh*64 .. hh*64+63, up columns 128 + the same
+    uint32_t pg[2][16], pu[2][16], pa[2][16];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int c = hh * 64 + 32 * j;
+      uint32_t rg[32], ru[32];
+      tmem_ld2(tbase + c, tbase + 128 + c, rg, ru);
+      float g[32], u[32], a[32];
+      as_float(rg, g);
+      as_float(ru, u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a[i] = g[i] * sigmoidf_(g[i]) * u[i];
+      pack32(g, pg[j]);
+      pack32(u, pu[j]);
+      pack32(a, pa[j]);
+    }
+    release();
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int c = ti.n0 + hh * 64 + 32 * j;
+      store_block_p<C::EPI_OUT>(w, &p.tmC0, c, row0, pg[j]);
+      store_block_p<C::EPI_OUT>(w, &p.tmC0, p.I + c, row0, pu[j]);
+      store_block_p<C::EPI_OUT>(w, &p.tmC1, c, row0, pa[j]);
+      if (p.q_codes != nullptr) store_qa(p, row0 + lane, c, pa[j]);  // from a's bf16 value
+    }
+  } else if constexpr (KIND == GEMM_DGRAD_DOWN) {
+    // (no early release: the dSwiGLU needs g' in fp32 beside its loaded inputs)
+    const int64_t pr = ti.m0 + row;
+    const float wgt = __ldg(p.w_row + pr);
+    float dot = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) {
+      const int c = hh * 128 + 32 * j;
+      if (!w.ld_pending) load_inputs(w, p, row0, ti.n0 + c);
+      if (!wait_inputs(w, abort)) return false;
+      float g[32], u[32], av[32];
+      unstage32(w.in, lane, g);
+      unstage32(w.in + 2048, lane, u);
+      unstage32(w.in + 4096, lane, av);
+      __syncwarp();
+      if (j < 3) load_inputs(w, p, row0, ti.n0 + c + 32);
+      else if (next != nullptr) load_inputs(w, p, next->m0 + q * 32, next->n0 + hh * 128);
+      uint32_t r[32];
+      ptx::tmem_ld32(tbase + c, r);
+      ptx::tmem_wait_ld(r);
+      float dg[32], du[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float gp = __uint_as_float(r[i]);
+        const float s = sigmoidf_(g[i]);
+        const float sg = g[i] * s;
+        dot += av[i] * gp;
+        const float da = wgt * gp;
+        dg[i] = da * u[i] * s * (1.0f + g[i] * (1.0f - s));
+        du[i] = da * sg;
+        av[i] *= wgt;
+      }
+      store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, dg);
+      store_block<C::EPI_OUT>(w, &p.tmC0, p.I + ti.n0 + c, row0, du);
+      store_block<C::EPI_OUT>(w, &p.tmC1, ti.n0 + c, row0, av);
+    }
+    // two partial sums per row and N tile, one per column half
+    p.outf[pr * p.n_pw + (ti.n0 / BN) * 2 + hh] = dot;
+  } else {
+    const CUtensorMap* m = &p.tmC0;
+    int orow = row0;
+    float wgt = 1.0f;
+    if constexpr (KIND == GEMM_DOWN) {
+      wgt = __ldg(p.w_row + ti.m0 + row);
+    } else if constexpr (KIND != GEMM_DGRAD_GATEUP) {  // weight gradients
+      if (ti.down) {
+        m = KIND == GEMM_WGRAD_BOTH ? &p.tmC2 : &p.tmC0;
+        orow = ti.e * p.H + row0;
+      } else {
+        const bool gate = row0 < p.I;
+        m = gate ? &p.tmC0 : &p.tmC1;
+        orow = ti.e * p.I + (gate ? row0 : row0 - p.I);
+      }
+    }
+    // the warp's 128 accumulator columns to registers, then TMEM goes back at once
+    uint32_t r[4][32];
+    ptx::tmem_ld32(tbase + hh * 128, r[0]);
+    ptx::tmem_ld32(tbase + hh * 128 + 32, r[1]);
+    ptx::tmem_ld32(tbase + hh * 128 + 64, r[2]);
+    ptx::tmem_ld32(tbase + hh * 128 + 96, r[3]);
+    ptx::tmem_wait_ld(r[0]);
+    ptx::reg_fence(r[1]);
+    ptx::reg_fence(r[2]);
+    ptx::reg_fence(r[3]);
+    release();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float v[32];
+      as_float(r[j], v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= wgt;
+      uint32_t pk[16];
+      pack32(v, pk);
+      store_block_p<C::EPI_OUT>(w, m, ti.n0 + hh * 128 + 32 * j, orow, pk);
+    }
+  }
+  return true;
+}
+
 // Zero tile of a per-expert GEMM whose expert has no rows (K = 0).
+// (SPLIT: this warp's half hh of the columns)
 template <int KIND, int BN, int CTAS, bool FP8>
-__device__ __forceinline__ void zero_tile(const GemmParams& p, const TileInfo& ti, int q,
+__device__ __forceinline__ void zero_tile(const GemmParams& p, const TileInfo& ti, int q, int hh,
                                           EpiWarp& w) {
   using C = Cfg<KIND, BN, CTAS, FP8>;
   const int row0 = ti.m0 + q * 32;
@@ -450,8 +638,9 @@ __device__ __forceinline__ void zero_tile(const GemmParams& p, const TileInfo& t
   float z[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) z[i] = 0.f;
+  const int c0 = C::SPLIT ? hh * (BN / 2) : 0, c1 = C::SPLIT ? c0 + BN / 2 : BN;
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 32) store_block<C::EPI_OUT>(w, m, ti.n0 + c, orow, z);
+  for (int c = c0; c < c1; c += 32) store_block<C::EPI_OUT>(w, m, ti.n0 + c, orow, z);
 }
 
 // ------------------------------------------------------------------ producer loads
@@ -563,7 +752,8 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
 
 // ------------------------------------------------------------------ the kernel
 template <int KIND, int BN, int CTAS, bool FP8>
-__global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
+    moe_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<KIND, BN, CTAS, FP8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES];
@@ -571,7 +761,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
-  __shared__ __align__(8) uint64_t epi_ld_bar[4];
+  __shared__ __align__(8) uint64_t epi_ld_bar[8];
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
 
@@ -588,10 +778,10 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull_bar[a], 1);
-      ptx::mbar_init(&tempty_bar[a], 4 * CTAS);
+      ptx::mbar_init(&tempty_bar[a], C::EPI_WARPS * CTAS);
     }
     ptx::mbar_init(&drain_bar, 1);
-    for (int q = 0; q < 4; ++q) ptx::mbar_init(&epi_ld_bar[q], 1);
+    for (int q = 0; q < C::EPI_WARPS; ++q) ptx::mbar_init(&epi_ld_bar[q], 1);
     s_abort = 0;
     ptx::fence_barrier_init();
   }
@@ -705,11 +895,12 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
           // bytes along a K-major row, or 32 rows (4 KB) of an M/N-major box, and
           // reads byte kk of the scale words
           const uint32_t sf_base = ptx::smem_u32(sf_ring + stage * C::SF_BYTES);
-          ptx::tmem_cp_sf<CTAS>(tmem_base + C::SFA_COL, ptx::smem_desc_sf(sf_base));
+          const uint32_t sfa_t = tmem_base + C::SF_COL0 + stage * C::SF_COLS_PER_STAGE;
+          const uint32_t sfb_t = sfa_t + 4;
+          ptx::tmem_cp_sf<CTAS>(sfa_t, ptx::smem_desc_sf(sf_base));
 #pragma unroll
           for (int j = 0; j < BN / 128; ++j)
-            ptx::tmem_cp_sf<CTAS>(tmem_base + C::SFB_COL + 4 * j,
-                                  ptx::smem_desc_sf(sf_base + 512 * (1 + j)));
+            ptx::tmem_cp_sf<CTAS>(sfb_t + 4 * j, ptx::smem_desc_sf(sf_base + 512 * (1 + j)));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t adesc = C::A_MN
@@ -718,8 +909,7 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
             const uint64_t bdesc = C::B_MN
                                        ? ptx::smem_desc_sw128(b_base + kk * 4096, 16384, 1024)
                                        : ptx::smem_desc_sw128(b_base + kk * 32, 16, 1024);
-            ptx::umma_mxf8<CTAS>(d_tmem, adesc, bdesc, C::IDESC | ptx::sf_ids(kk),
-                                 tmem_base + C::SFA_COL, tmem_base + C::SFB_COL,
+            ptx::umma_mxf8<CTAS>(d_tmem, adesc, bdesc, C::IDESC | ptx::sf_ids(kk), sfa_t, sfb_t,
                                  (kb | kk) != 0 ? 1u : 0u);
           }
         } else {
@@ -758,11 +948,13 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
-    const int q = warp - 4;
+    // warp 4 + ew: TMEM lane quadrant q = warp % 4 (the quadrant a warp may read),
+    // column half hh (SPLIT tiles)
+    const int ew = warp - 4, q = warp & 3, hh = ew >> 2;
     EpiWarp w;
-    w.in = smem + C::STAGES * (C::STAGE_BYTES + C::SF_BYTES) + q * C::EPI_WARP_BYTES;
+    w.in = smem + C::STAGES * (C::STAGE_BYTES + C::SF_BYTES) + ew * C::EPI_WARP_BYTES;
     w.out = w.in + C::EPI_IN * 2048;
-    w.ld_bar = &epi_ld_bar[q];
+    w.ld_bar = &epi_ld_bar[ew];
     w.ld_phase = 0;
     w.ld_pending = false;
     w.ob = 0;
@@ -775,13 +967,14 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
     for (int t = cluster; t < total; t += n_clusters) {
       const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8>(p, t, rank);
       if (ti.k_iters == 0) {
-        if constexpr (C::PER_EXPERT) zero_tile<KIND, BN, CTAS, FP8>(p, ti, q, w);
+        if constexpr (C::PER_EXPERT) zero_tile<KIND, BN, CTAS, FP8>(p, ti, q, hh, w);
         continue;
       }
       TileInfo nx;
       const bool has_next = t + n_clusters < total;
       if (has_next) nx = decode_tile<KIND, BN, CTAS, FP8>(p, t + n_clusters, rank);
-      if (KIND == GEMM_DGRAD_DOWN && !w.ld_pending) load_inputs(w, p, ti.m0 + q * 32, ti.n0);
+      if (KIND == GEMM_DGRAD_DOWN && !w.ld_pending)
+        load_inputs(w, p, ti.m0 + q * 32, ti.n0 + (C::SPLIT ? hh * (BN / 2) : 0));
       int ok = 1;
       if (lane == 0) ok = ptx::mbar_wait(&tfull_bar[acc], acc_phase, abort, WAIT_LIMIT_NS) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -793,17 +986,28 @@ __global__ void __launch_bounds__(256, 1) moe_gemm_kernel(const __grid_constant_
       __syncwarp();
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(q * 32) << 16);
-      if (!epilogue_tile<KIND, BN, CTAS, FP8>(p, ti, has_next ? &nx : nullptr, q, tbase, w,
-                                              abort)) {
+      // hand the accumulator back to the MMA issuer (every epilogue warp of the pair
+      // arrives once per tile)
+      auto release = [&]() {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CTAS == 1) ptx::mbar_arrive(&tempty_bar[acc]);
+          else ptx::mbar_arrive_cluster(lead_tempty0 + acc * 8u);
+        }
+      };
+      bool done;
+      if constexpr (C::SPLIT)
+        done = epilogue_tile_split<KIND, BN, CTAS, FP8>(p, ti, has_next ? &nx : nullptr, q, hh,
+                                                        tbase, w, abort, release);
+      else
+        done = epilogue_tile<KIND, BN, CTAS, FP8>(p, ti, has_next ? &nx : nullptr, q, tbase, w,
+                                                  abort);
+      if (!done) {
         if (lane == 0) record_timeout(p, abort, KIND * 16 + 7, peer_abort);
         break;
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (CTAS == 1) ptx::mbar_arrive(&tempty_bar[acc]);
-        else ptx::mbar_arrive_cluster(lead_tempty0 + acc * 8u);
-      }
+      if (!C::EARLY_RELEASE) release();
       if (++acc == C::NACC) {
         acc = 0;
         acc_phase ^= 1u;
@@ -885,7 +1089,7 @@ static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) 
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = c.stream;
   int64_t clusters = c.num_sms / CTAS;

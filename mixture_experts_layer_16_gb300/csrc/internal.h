@@ -197,6 +197,7 @@ struct MxqArgs {
   uint8_t* codes_rows;
   uint8_t* sf_rows;
   RowGather gather;
+  DevStatus* status;  // device status word for a copy that never lands (may be null)
 };
 cudaError_t launch_mxq(const Ctx& c, const MxqArgs& a);
 

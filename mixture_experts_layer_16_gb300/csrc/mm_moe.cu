@@ -54,7 +54,9 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->qf = s->prec == MM_MOE_MXFP8 ? QS_MX : s->prec == MM_MOE_FP8_BLOCK ? QS_BLOCK : QS_NONE;
   L->qb = s->prec == MM_MOE_BF16 ? QS_NONE : s->prec == MM_MOE_FP8_BLOCK ? QS_BLOCK : QS_MX;
   L->nblk = (L->R + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
-  L->n_pw = L->I / pick_bn(L->I);
+  // partial sums of dtopk_w per row: one per N tile of the dgrad-down GEMM, two when
+  // its MXFP8 tiles (256 wide) split their columns between two epilogue warps
+  L->n_pw = L->I / pick_bn(L->I) * ((L->qb == QS_MX && pick_bn(L->I) == 256) ? 2 : 1);
   const size_t A = 1024;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -193,9 +195,11 @@ static thread_local int g_last_launches = 0;
 // A second stream (and a fork/join event pair) per device and host thread, so that
 // bandwidth-bound kernels can run beside independent tensor-core kernels of the same
 // call.  Created on first use; never destroyed (they live as long as the thread).
+constexpr int SIDE_MARKS = 4;  // points of the side stream the caller's stream can wait for
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t mark[SIDE_MARKS] = {};
 };
 
 static bool side_stream(SideStream* out) {
@@ -208,6 +212,9 @@ static bool side_stream(SideStream* out) {
     if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
       return false;
+    for (int i = 0; i < SIDE_MARKS; ++i)
+      if (cudaEventCreateWithFlags(&ss.mark[i], cudaEventDisableTiming) != cudaSuccess)
+        return false;
   }
   *out = ss;
   return true;
@@ -216,7 +223,9 @@ static bool side_stream(SideStream* out) {
 // A fork of the caller's stream onto the side stream that is joined back on every
 // return: join() on the normal path, the destructor on an error return after the
 // fork, so that no path leaves forked work unordered before later work on the
-// caller's stream (or an unjoined fork in a stream capture).
+// caller's stream (or an unjoined fork in a stream capture).  In between, the side
+// stream can be made to wait for the caller's stream so far (after_main), and the
+// caller's stream for a marked point of the side stream (mark, main_waits).
 class Fork {
  public:
   Fork() = default;
@@ -233,6 +242,21 @@ class Fork {
     return true;
   }
   cudaStream_t side() const { return ss_.s; }
+  // later side work runs after the caller's stream's work enqueued so far
+  cudaError_t after_main() {
+    cudaError_t e = cudaEventRecord(ss_.fork, main_);
+    return e == cudaSuccess ? cudaStreamWaitEvent(ss_.s, ss_.fork, 0) : e;
+  }
+  // the side stream's work enqueued so far, as a mark for main_waits (-1: none left)
+  int mark() {
+    if (n_marks_ == SIDE_MARKS || cudaEventRecord(ss_.mark[n_marks_], ss_.s) != cudaSuccess)
+      return -1;
+    return n_marks_++;
+  }
+  cudaError_t main_waits(int m) {
+    if (m < 0 || m >= n_marks_) return cudaErrorInvalidValue;
+    return cudaStreamWaitEvent(main_, ss_.mark[m], 0);
+  }
   cudaError_t join() {
     if (!open_) return cudaSuccess;
     open_ = false;
@@ -245,6 +269,7 @@ class Fork {
   SideStream ss_;
   cudaStream_t main_ = nullptr;
   bool open_ = false;
+  int n_marks_ = 0;
 };
 
 #define MM_MOE_TRY(expr)                         \
@@ -287,10 +312,11 @@ static cudaError_t mx_rows(const Ctx& c, const uint16_t* in, MxCopy out, int64_t
   return launch_mxq(c, a);
 }
 
-static cudaError_t mx_cols(const Ctx& c, const uint16_t* in, MxCopy out, int64_t rows,
-                           int64_t cols, const int* meta, const MxCopy* rows_out = nullptr,
-                           RowGather gather = RowGather{}) {
+static cudaError_t mx_cols(const Ctx& c, DevStatus* st, const uint16_t* in, MxCopy out,
+                           int64_t rows, int64_t cols, const int* meta,
+                           const MxCopy* rows_out = nullptr, RowGather gather = RowGather{}) {
   MxqArgs a{};
+  a.status = st;
   a.in = in;
   a.codes = out.codes;
   a.sf = out.sf;
@@ -328,14 +354,10 @@ static RowGather routed_rows(const Layout& L, const char* sv) {
 
 // The permutation of x, and gate/up's A operand.  Under a quantised forward it writes
 // x's blocks along H (the gate/up operand) straight to q_x, quantising each token row
-// once (MXFP8: codes and scales; blockwise: bf16 values); with `keep_tokens` the
-// blocks along tokens (the dW_gate / dW_up operand) are gathered from x into
-// x_perm's place.  No bf16 copy of the permuted rows is made.  Otherwise x_perm is
-// the bf16 permuted copy.
+// once (MXFP8: codes and scales; blockwise: bf16 values); no bf16 copy of the
+// permuted rows is made.  Otherwise x_perm is the bf16 permuted copy.
 static Opnd permute_x(const Ctx& c, const Layout& L, const uint16_t* x, uint16_t* x_perm,
-                      bool keep_tokens, const char* sv, float* w_row_out, char* sc,
-                      cudaError_t* err) {
-  const int* meta = reinterpret_cast<const int*>(sv + L.meta);
+                      const char* sv, float* w_row_out, char* sc, cudaError_t* err) {
   if (L.qf == QS_NONE) {
     *err = launch_permute(c, L, x, x_perm, sv, w_row_out, K_PERMUTE_X, sc);
     return Opnd{x_perm, nullptr};
@@ -343,70 +365,85 @@ static Opnd permute_x(const Ctx& c, const Layout& L, const uint16_t* x, uint16_t
   if (L.qf == QS_MX) {
     const MxCopy q = mx_copy(sc, L.q_x, L.Rp, L.H);
     *err = launch_permute(c, L, x, q.codes, sv, w_row_out, K_PERMUTE_X, sc, QS_MX, q.sf);
-    if (*err == cudaSuccess && keep_tokens)
-      *err = mx_cols(c, x, mx_copy(reinterpret_cast<char*>(x_perm), 0, L.Rp, L.H), L.Rp, L.H,
-                     meta, nullptr, routed_rows(L, sv));
     return q;
   }
   uint16_t* q_x = reinterpret_cast<uint16_t*>(sc + L.q_x);
   *err = launch_permute(c, L, x, q_x, sv, w_row_out, K_PERMUTE_X, sc, QS_BLOCK);
-  if (*err == cudaSuccess && keep_tokens)
-    *err = fb_cols(c, x, x_perm, L.Rp, L.H, meta, nullptr, routed_rows(L, sv));
   return Opnd{q_x, nullptr};
 }
 
+// x's blocks along tokens (the dW_gate / dW_up operand), gathered from x in routed
+// order into `dst` (saved's x_perm place, or q_xc), under scheme qs.
+static cudaError_t x_tokens(const Ctx& c, const Layout& L, int qs, const uint16_t* x, char* dst,
+                            const char* sv, char* sc) {
+  const int* meta = reinterpret_cast<const int*>(sv + L.meta);
+  DevStatus* sw = reinterpret_cast<DevStatus*>(sc + L.status);  // the status word
+  if (qs == QS_MX)
+    return mx_cols(c, sw, x, mx_copy(dst, 0, L.Rp, L.H), L.Rp, L.H, meta, nullptr,
+                   routed_rows(L, sv));
+  return fb_cols(c, x, reinterpret_cast<uint16_t*>(dst), L.Rp, L.H, meta, nullptr,
+                 routed_rows(L, sv));
+}
+
 // The weight copies of a quantised forward; they read only the weights, so the
-// forward runs them on its side stream beside the routing.  MXFP8: with `keep` (the
+// forward runs them on its side stream beside the routing (gate/up's first, then
+// W_down's, which only the down projection waits for).  MXFP8: with `keep` (the
 // forward of a layer that keeps its activations) one two-way pass per weight writes
 // its blocks along the forward's K to scratch and along the backward's K to `wbase`
-// (saved); otherwise row passes write the forward's copies only (W_down's only with
-// `emit_down`).  Blockwise FP8: the one 128 x 128-block copy of each of the three
-// weights, which every GEMM reads, to `wbase` (saved, or the front of scratch under
-// recompute).
-static cudaError_t weight_copies(const Ctx& c, const Layout& L, bool keep, bool emit_down,
-                                 const uint16_t* W_gate, const uint16_t* W_up,
-                                 const uint16_t* W_down, char* wbase, char* sc) {
-  const int64_t EI = L.E * L.I, EH = L.E * L.H;
+// (saved); otherwise row passes write the forward's copies only.  Blockwise FP8: the
+// one 128 x 128-block copy of each weight, which every GEMM reads, to `wbase` (saved,
+// or the front of scratch under recompute).
+static cudaError_t weights_gateup(const Ctx& c, const Layout& L, bool keep,
+                                  const uint16_t* W_gate, const uint16_t* W_up, char* wbase,
+                                  char* sc) {
+  const int64_t EI = L.E * L.I;
+  DevStatus* sw = reinterpret_cast<DevStatus*>(sc + L.status);  // the status word
   cudaError_t e = cudaSuccess;
   if (L.qf == QS_MX) {
-    const MxCopy wg = mx_copy(sc, L.q_wg, EI, L.H), wu = mx_copy(sc, L.q_wu, EI, L.H),
-                 wd = mx_copy(sc, L.q_wd, EH, L.I);
+    const MxCopy wg = mx_copy(sc, L.q_wg, EI, L.H), wu = mx_copy(sc, L.q_wu, EI, L.H);
     if (keep) {  // one read each, both axes
-      const MxCopy wgc = mx_copy(wbase, L.q_wgc, EI, L.H), wuc = mx_copy(wbase, L.q_wuc, EI, L.H),
-                   wdc = mx_copy(wbase, L.q_wdc, EH, L.I);
-      e = mx_cols(c, W_gate, wgc, EI, L.H, nullptr, &wg);
-      if (e == cudaSuccess) e = mx_cols(c, W_up, wuc, EI, L.H, nullptr, &wu);
-      if (e == cudaSuccess && emit_down) e = mx_cols(c, W_down, wdc, EH, L.I, nullptr, &wd);
+      e = mx_cols(c, sw, W_gate, mx_copy(wbase, L.q_wgc, EI, L.H), EI, L.H, nullptr, &wg);
+      if (e == cudaSuccess)
+        e = mx_cols(c, sw, W_up, mx_copy(wbase, L.q_wuc, EI, L.H), EI, L.H, nullptr, &wu);
     } else {
       e = mx_rows(c, W_gate, wg, EI, L.H, nullptr);
       if (e == cudaSuccess) e = mx_rows(c, W_up, wu, EI, L.H, nullptr);
-      if (e == cudaSuccess && emit_down) e = mx_rows(c, W_down, wd, EH, L.I, nullptr);
     }
   } else if (L.qf == QS_BLOCK) {
     auto wq = [&](size_t off) { return reinterpret_cast<uint16_t*>(wbase + off); };
     e = launch_fb_qdq(c, W_gate, wq(L.q_wgc), EI, L.H, FB_TILES, nullptr, nullptr);
     if (e == cudaSuccess)
       e = launch_fb_qdq(c, W_up, wq(L.q_wuc), EI, L.H, FB_TILES, nullptr, nullptr);
-    if (e == cudaSuccess)
-      e = launch_fb_qdq(c, W_down, wq(L.q_wdc), EH, L.I, FB_TILES, nullptr, nullptr);
   }
   return e;
 }
 
+static cudaError_t weights_down(const Ctx& c, const Layout& L, bool keep,
+                                const uint16_t* W_down, char* wbase, char* sc) {
+  const int64_t EH = L.E * L.H;
+  DevStatus* sw = reinterpret_cast<DevStatus*>(sc + L.status);  // the status word
+  if (L.qf == QS_MX) {
+    const MxCopy wd = mx_copy(sc, L.q_wd, EH, L.I);
+    return keep ? mx_cols(c, sw, W_down, mx_copy(wbase, L.q_wdc, EH, L.I), EH, L.I, nullptr, &wd)
+                : mx_rows(c, W_down, wd, EH, L.I, nullptr);
+  }
+  if (L.qf == QS_BLOCK)
+    return launch_fb_qdq(c, W_down, reinterpret_cast<uint16_t*>(wbase + L.q_wdc), EH, L.I,
+                         FB_TILES, nullptr, nullptr);
+  return cudaSuccess;
+}
+
 // The forward's gate/up stage on A (from permute_x): h = [g | u] and a = silu(g) * u,
-// with the weights quantised first under a quantised forward (weight_copies, unless
-// `weights_ready`).  `emit_qa` makes it also produce the down projection's operand:
-// a in MXFP8 along I from the GEMM's epilogue, or (blockwise FP8) a row pass over a.
-// The backward under MM_MOE_RECOMPUTE calls it with the forward's arguments and gets
-// h and a bit for bit (the same kernels on the same inputs).
-static mm_moe_status gateup_stage(const Ctx& c, const Layout& L, bool keep, bool emit_qa,
-                                  Opnd A, const uint16_t* W_gate, const uint16_t* W_up,
-                                  const uint16_t* W_down, uint16_t* h, uint16_t* a,
-                                  const char* sv, char* wbase, char* sc,
-                                  bool weights_ready = false) {
+// from the weights (or, in a quantised forward, their copies made by weights_gateup,
+// which the caller has made or ordered before).  `emit_qa` makes it also produce the
+// down projection's operand: a in MXFP8 along I from the GEMM's epilogue, or
+// (blockwise FP8) a row pass over a.  The backward under MM_MOE_RECOMPUTE calls it
+// with the forward's arguments and gets h and a bit for bit (the same kernels on the
+// same inputs).
+static mm_moe_status gateup_stage(const Ctx& c, const Layout& L, bool emit_qa, Opnd A,
+                                  const uint16_t* W_gate, const uint16_t* W_up, uint16_t* h,
+                                  uint16_t* a, const char* sv, char* wbase, char* sc) {
   const int* meta = reinterpret_cast<const int*>(sv + L.meta);
-  if (!weights_ready)
-    MM_MOE_TRY(weight_copies(c, L, keep, emit_qa, W_gate, W_up, W_down, wbase, sc));
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
@@ -475,14 +512,23 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   char* sv = static_cast<char*>(saved);
   MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
   // A quantised forward's weight copies read only the weights: they run on the side
-  // stream beside the routing, the permutation and the token-axis gather, which write
-  // none of the buffers they write, and gate/up waits for them
+  // stream beside the routing and the permutation (which write none of the buffers
+  // they write); gate/up waits for its two weights only, the down projection for
+  // W_down's copy.  The side stream then gathers x's blocks along tokens (the
+  // backward's operand) beside the two GEMMs.
   char* wbase = L.w_common ? sc : sv;  // where the backward's (blockwise: all) weight copies go
   Fork fork;
+  int m_gateup = -1, m_down = -1;
+  const Ctx cs{nullptr, d.sms, &launches};
+  Ctx side = cs;
   if (L.qf != QS_NONE) {
     if (!fork.open(c.stream)) return MM_MOE_ECUDA;
-    const Ctx cs{fork.side(), d.sms, &launches};
-    MM_MOE_TRY(weight_copies(cs, L, L.w_in_saved, true, W_gate, W_up, W_down, wbase, sc));
+    side.stream = fork.side();
+    MM_MOE_TRY(weights_gateup(side, L, L.w_in_saved, W_gate, W_up, wbase, sc));
+    m_gateup = fork.mark();
+    MM_MOE_TRY(weights_down(side, L, L.w_in_saved, W_down, wbase, sc));
+    m_down = fork.mark();
+    if (m_gateup < 0 || m_down < 0) return MM_MOE_ECUDA;
   }
   MM_MOE_TRY(launch_route(c, L, topk_idx, topk_w, sv, sc));
   // x_perm, h, a: kept in saved, or in scratch under MM_MOE_RECOMPUTE
@@ -491,16 +537,17 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   uint16_t* h = reinterpret_cast<uint16_t*>(act + L.h);
   uint16_t* a = reinterpret_cast<uint16_t*>(act + L.a);
   uint16_t* ys = reinterpret_cast<uint16_t*>(sc + L.ys);
+  if (L.w_in_saved) {  // x along tokens into x_perm's place, once the routing exists
+    MM_MOE_TRY(fork.after_main());
+    MM_MOE_TRY(x_tokens(side, L, L.qf, x, act + L.x_perm, sv, sc));
+  }
   // Operands of the two GEMMs: the bf16 tensors, or in a quantised forward their
-  // copies quantised along each GEMM's K (H for gate/up, I for down).  A forward that
-  // keeps its activations also leaves x's blocks along tokens in x_perm's place.
+  // copies quantised along each GEMM's K (H for gate/up, I for down)
   cudaError_t err = cudaSuccess;
-  const Opnd A1 = permute_x(c, L, x, x_perm, L.w_in_saved, sv,
-                            reinterpret_cast<float*>(sv + L.w_row), sc, &err);
+  const Opnd A1 = permute_x(c, L, x, x_perm, sv, reinterpret_cast<float*>(sv + L.w_row), sc, &err);
   MM_MOE_TRY(err);
-  MM_MOE_TRY(fork.join());
-  st = gateup_stage(c, L, L.w_in_saved, true, A1, W_gate, W_up, W_down, h, a, sv, wbase, sc,
-                    L.qf != QS_NONE);
+  if (m_gateup >= 0) MM_MOE_TRY(fork.main_waits(m_gateup));
+  st = gateup_stage(c, L, true, A1, W_gate, W_up, h, a, sv, wbase, sc);
   if (st != MM_MOE_OK) return st;
   GemmArgs g{};
   g.saved = sv;
@@ -520,8 +567,10 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
     g.A = sc + L.q_a;
     g.B0 = wbase + L.q_wdc;
   }
+  if (m_down >= 0) MM_MOE_TRY(fork.main_waits(m_down));
   MM_MOE_TRY(launch_gemm(c, L, g));
   MM_MOE_TRY(launch_combine(c, L, ys, sv, y));
+  MM_MOE_TRY(fork.join());
   g_last_launches = launches;
   return MM_MOE_OK;
 }
@@ -559,28 +608,50 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   const uint16_t* a = reinterpret_cast<const uint16_t*>(act + L.a);
   const int* meta = reinterpret_cast<const int*>(sv + L.meta);
   const int64_t EI = L.E * L.I, EH = L.E * L.H, Rp = L.Rp, H = L.H, I = L.I;
+  DevStatus* sw = reinterpret_cast<DevStatus*>(sc + L.status);  // the status word
   MM_MOE_TRY(cudaMemsetAsync(sc + L.status, 0, sizeof(DevStatus), c.stream));
   if (L.recompute) {
     // activation checkpointing: gate/up's operand (x_perm, or q_x under a quantised
     // forward), h and a again, as the forward made them
     uint16_t* xp = reinterpret_cast<uint16_t*>(sc + L.x_perm);
+    MM_MOE_TRY(weights_gateup(c, L, false, W_gate, W_up, sc, sc));
     cudaError_t err = cudaSuccess;
-    const Opnd A0 = permute_x(c, L, x, xp, false, sv, nullptr, sc, &err);
+    const Opnd A0 = permute_x(c, L, x, xp, sv, nullptr, sc, &err);
     MM_MOE_TRY(err);
-    st = gateup_stage(c, L, false, false, A0, W_gate, W_up, W_down,
-                      reinterpret_cast<uint16_t*>(sc + L.h),
+    if (L.qf == QS_BLOCK) MM_MOE_TRY(weights_down(c, L, false, W_down, sc, sc));
+    st = gateup_stage(c, L, false, A0, W_gate, W_up, reinterpret_cast<uint16_t*>(sc + L.h),
                       reinterpret_cast<uint16_t*>(sc + L.a), sv, sc, sc);
     if (st != MM_MOE_OK) return st;
   }
   // A quantised backward (MXFP8 for full MXFP8 and fp8_bwd, blockwise FP8): every
   // GEMM reads copies of its operands quantised along its own K.  The permutation of
-  // dy then writes dy's blocks along H (this GEMM's operand) into dy_perm's place, and
-  // dy's blocks along tokens (the dW_down operand) are gathered from dy.  The
-  // backward's weight copies were made by the forward (saved), by the recompute
-  // (blockwise, front of scratch), or are made here (MXFP8 along their backward K).
+  // dy writes dy's blocks along H (the first GEMM's operand) into dy_perm's place;
+  // dy's blocks along tokens (the dW_down operand) are gathered from dy on the side
+  // stream beside the first two GEMMs, as are (MXFP8 without the forward's copies) the
+  // weights along I for dgrad-gate/up.  The backward's weight copies were otherwise
+  // made by the forward (saved) or by the recompute (blockwise, front of scratch).
+  // (The side stream starts after the recompute, whose buffers overlap these.)
   const int qb = L.qb;
   const char* wsrc = L.w_in_saved ? sv : sc;
   const bool make_w = qb == QS_MX && !L.w_in_saved;
+  Fork fork;
+  if (!fork.open(c.stream)) return MM_MOE_ECUDA;
+  Ctx side{fork.side(), d.sms, &launches};
+  int m_dy = -1, m_w = -1;
+  if (qb == QS_MX) {
+    MM_MOE_TRY(mx_cols(side, sw, dy, mx_copy(sc, L.q_dyc, Rp, H), Rp, H, meta, nullptr,
+                       routed_rows(L, sv)));
+    m_dy = fork.mark();
+    if (make_w) {
+      MM_MOE_TRY(mx_cols(side, sw, W_gate, mx_copy(sc, L.q_wgc, EI, H), EI, H, nullptr));
+      MM_MOE_TRY(mx_cols(side, sw, W_up, mx_copy(sc, L.q_wuc, EI, H), EI, H, nullptr));
+      m_w = fork.mark();
+    }
+  } else if (qb == QS_BLOCK) {
+    MM_MOE_TRY(fb_cols(side, dy, reinterpret_cast<uint16_t*>(sc + L.q_dyc), Rp, H, meta, nullptr,
+                       routed_rows(L, sv)));
+    m_dy = fork.mark();
+  }
   GemmArgs g{};
   g.saved = sv;
   g.scratch = sc;
@@ -595,9 +666,7 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   if (qb == QS_MX) {
     const MxCopy dyr = mx_copy(sc, L.dy_perm, Rp, H), wdc = mx_copy(wsrc, L.q_wdc, EH, I);
     MM_MOE_TRY(launch_permute(c, L, dy, dyr.codes, sv, nullptr, K_PERMUTE_DY, sc, QS_MX, dyr.sf));
-    MM_MOE_TRY(mx_cols(c, dy, mx_copy(sc, L.q_dyc, Rp, H), Rp, H, meta, nullptr,
-                       routed_rows(L, sv)));
-    if (make_w) MM_MOE_TRY(mx_cols(c, W_down, wdc, EH, I, nullptr));
+    if (make_w) MM_MOE_TRY(mx_cols(c, sw, W_down, wdc, EH, I, nullptr));
     g.fp8 = true;
     g.A = dyr.codes;
     g.sA = dyr.sf;
@@ -605,11 +674,7 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
     g.sB0 = wdc.sf;
   } else {
     MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY, sc, qb));
-    if (qb == QS_BLOCK) {
-      MM_MOE_TRY(fb_cols(c, dy, reinterpret_cast<uint16_t*>(sc + L.q_dyc), Rp, H, meta, nullptr,
-                         routed_rows(L, sv)));
-      g.B0 = wsrc + L.q_wdc;
-    }
+    if (qb == QS_BLOCK) g.B0 = wsrc + L.q_wdc;
   }
   MM_MOE_TRY(launch_gemm(c, L, g));
   g = GemmArgs{};
@@ -624,11 +689,8 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
     // one read of dh: blocks along tokens (dW_gate, dW_up) and along I (this GEMM)
     const MxCopy dhc = mx_copy(sc, L.q_dhc, Rp, 2 * I), dhr = mx_copy(sc, L.q_dhr, Rp, 2 * I);
     const MxCopy wgc = mx_copy(wsrc, L.q_wgc, EI, H), wuc = mx_copy(wsrc, L.q_wuc, EI, H);
-    MM_MOE_TRY(mx_cols(c, dh, dhc, Rp, 2 * I, meta, &dhr));
-    if (make_w) {
-      MM_MOE_TRY(mx_cols(c, W_gate, wgc, EI, H, nullptr));
-      MM_MOE_TRY(mx_cols(c, W_up, wuc, EI, H, nullptr));
-    }
+    MM_MOE_TRY(mx_cols(c, sw, dh, dhc, Rp, 2 * I, meta, &dhr));
+    if (m_w >= 0) MM_MOE_TRY(fork.main_waits(m_w));
     g.fp8 = true;
     g.A = dhr.codes;
     g.sA = dhr.sf;
@@ -645,10 +707,8 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   MM_MOE_TRY(launch_gemm(c, L, g));
   // the un-permute (bandwidth-bound) runs on the side stream beside the
   // weight-gradient GEMMs, which read none of its inputs and write none of its outputs
-  Fork fork;
-  if (!fork.open(c.stream)) return MM_MOE_ECUDA;
-  const Ctx cs{fork.side(), d.sms, &launches};
-  MM_MOE_TRY(launch_unpermute(cs, L, dxs, sv, pw, dx, dtopk_w));
+  MM_MOE_TRY(fork.after_main());
+  MM_MOE_TRY(launch_unpermute(side, L, dxs, sv, pw, dx, dtopk_w));
   // token-axis blocks of the weight-gradient operands: each expert's rows start on a
   // multiple of 128 and its padding rows are zero, so 32- or 128-row blocks of the
   // padded row space are the per-expert blocks with a zero-padded tail
@@ -664,14 +724,14 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   g.out2 = dW_down;
   if (qb == QS_MX) {
     const MxCopy awc = mx_copy(sc, L.q_awc, Rp, I);
-    MM_MOE_TRY(mx_cols(c, a_w, awc, Rp, I, meta));
+    MM_MOE_TRY(mx_cols(c, sw, a_w, awc, Rp, I, meta));
     MxCopy xc = mx_copy(sv, L.x_perm, Rp, H);  // the forward's gather (kept activations)
     if (!L.w_in_saved) {
       xc = mx_copy(sc, L.q_xc, Rp, H);
       if (L.qf == QS_NONE)  // fp8_bwd: from the forward's bf16 x_perm
-        MM_MOE_TRY(mx_cols(c, x_perm, xc, Rp, H, meta));
+        MM_MOE_TRY(mx_cols(c, sw, x_perm, xc, Rp, H, meta));
       else                  // recompute under a quantised forward: from x itself
-        MM_MOE_TRY(mx_cols(c, x, xc, Rp, H, meta, nullptr, routed_rows(L, sv)));
+        MM_MOE_TRY(x_tokens(c, L, QS_MX, x, reinterpret_cast<char*>(xc.codes), sv, sc));
     }
     const MxCopy dyc = mx_copy(sc, L.q_dyc, Rp, H), dhc = mx_copy(sc, L.q_dhc, Rp, 2 * I);
     g.fp8 = true;
@@ -688,14 +748,14 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
     const uint16_t* xb = x_perm;  // (a blockwise forward that keeps its activations left
                                   // x's blocks along tokens in x_perm's place)
     if (!L.w_in_saved) {
-      uint16_t* q_xc = reinterpret_cast<uint16_t*>(sc + L.q_xc);
-      MM_MOE_TRY(fb_cols(c, x, q_xc, Rp, H, meta, nullptr, routed_rows(L, sv)));
-      xb = q_xc;
+      MM_MOE_TRY(x_tokens(c, L, QS_BLOCK, x, sc + L.q_xc, sv, sc));
+      xb = reinterpret_cast<const uint16_t*>(sc + L.q_xc);
     }
     g.A = sc + L.q_dhc;
     g.B0 = xb;
     g.A2 = sc + L.q_dyc;
   }
+  if (m_dy >= 0) MM_MOE_TRY(fork.main_waits(m_dy));
   // both weight gradients in one launch where they tile N alike (one list of tiles,
   // experts by descending row count, balances the clusters' loads far better than
   // two lists); otherwise one launch each

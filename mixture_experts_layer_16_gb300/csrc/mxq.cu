@@ -12,6 +12,7 @@
 
 #include "internal.h"
 #include "mx.cuh"
+#include "ptx.cuh"
 
 namespace mmmoe {
 
@@ -88,104 +89,172 @@ __global__ void __launch_bounds__(256) mxq_rows_kernel(const uint4* __restrict__
 // ---------------------------------------------------------------- blocks down columns
 // [rows, C] bf16 (rows % 32 == 0, C % 128 == 0): blocks of 32 rows of each column,
 // the operand layout of a GEMM whose K runs along the rows (its MMA rows are the
-// columns).  A CTA takes whole 32-row blocks (their source rows resolved once) and
-// their column tiles in turn: thread t holds 8 columns (16 bytes) of rows t/64,
-// t/64 + 4, ..., the four partial column maxima meet in shared memory.  The scale of
-// column c in row block rb is byte sf_offset(c, rb, C / 128).  With codes_rows
-// non-null the same read also gives the blocks along the rows (four neighbouring
-// lanes hold one 32-column block of a row; scales at sf_offset(row, col / 32,
-// rows / 128) of sf_rows).  With a gather the rows come from a token-major source
-// (padding rows read as zeros).
-constexpr int QCOL_TILE = 512;
+// columns); the scale of column c in row block rb is byte sf_offset(c, rb, C / 128).
+// With codes_rows non-null the same read also gives the blocks along the rows (scales
+// at sf_offset(row, col / 32, rows_total / 128) of sf_rows).  With a gather the rows come from a
+// token-major source (padding rows read as zeros).
+//
+// Each warp is its own pipeline over tiles of 32 rows x 128 columns (8 KB of bf16):
+// lane r brings row r of a tile into shared memory by one bulk asynchronous copy,
+// QC_STAGES tiles ahead, rows QC_ROW bytes apart (a 16-byte skew per row, so that
+// both a row read across the lanes and one row per lane hit distinct banks).  For
+// the blocks down the columns lane l holds columns 4l .. 4l+3 of all 32 rows in
+// registers; for the blocks along the rows (two-way) lane l takes row l.  Maxima are
+// taken on the bf16 bit patterns (the absolute values of bf16 numbers order like
+// unsigned integers; two 16-bit maxima per instruction), and a block's scale
+// exponent comes straight from the exponent field of its maximum.
+constexpr int QC_WARPS = 12;
+constexpr int QC_STAGES = 2;
+constexpr int QC_TC = 128;                     // columns per tile
+constexpr int QC_ROW = QC_TC * 2 + 16;         // bytes between rows in shared memory
+constexpr int QC_TILE_BYTES = 32 * QC_ROW;
+constexpr int QC_SMEM = QC_WARPS * QC_STAGES * QC_TILE_BYTES;
+constexpr uint64_t QC_WAIT_NS = 2000000000ull;
 
-__global__ void __launch_bounds__(256) mxq_cols_kernel(const uint4* __restrict__ in,
-                                                       uint2* __restrict__ codes,
-                                                       uint8_t* __restrict__ sf,
-                                                       uint2* __restrict__ codes_rows,
-                                                       uint8_t* __restrict__ sf_rows,
-                                                       int64_t rows, int64_t rows_total,
-                                                       int C8, const int* __restrict__ meta,
-                                                       const RowGather gather) {
-  __shared__ float part[4][QCOL_TILE];
-  __shared__ int src_row[32];  // the row block's source rows (-1: zero)
+// Scale exponent of a block whose largest absolute value has the bf16 bit pattern
+// `bits` (sign clear): floor(log2) - 8 from the exponent field, -127 for zero, and
+// clamped to [-127, 127] like scale_exp (a subnormal maximum gives -127).
+__device__ __forceinline__ int bf16_scale_exp(uint32_t bits) {
+  const int ef = static_cast<int>((bits >> 7) & 0xFFu);
+  return ef == 0 ? -127 : max(-127, ef - 127 - 8);
+}
+
+// Four codes of the bf16 values in two words, each under its own multiplier.
+__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float m0, float m1,
+                                           float m2, float m3) {
+  const float a = __uint_as_float(w0 << 16), b = __uint_as_float(w0 & 0xFFFF0000u);
+  const float c = __uint_as_float(w1 << 16), d = __uint_as_float(w1 & 0xFFFF0000u);
+  const uint32_t lo = static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(a * m0, b * m1), __NV_SATFINITE, __NV_E4M3));
+  const uint32_t hi = static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(c * m2, d * m3), __NV_SATFINITE, __NV_E4M3));
+  return lo | (hi << 16);
+}
+
+__global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
+    const uint16_t* __restrict__ in, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+    uint8_t* __restrict__ codes_rows, uint8_t* __restrict__ sf_rows, int64_t rows,
+    int64_t rows_total, int C, const int* __restrict__ meta, const RowGather gather,
+    DevStatus* status) {
+  extern __shared__ __align__(128) uint8_t qbuf[];
+  __shared__ __align__(8) uint64_t bar[QC_WARPS][QC_STAGES];
+  __shared__ uint32_t valid_rows[QC_WARPS][QC_STAGES];  // rows of the stage's tile with data
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   rows = rows_in_use(rows, meta);
-  const int col_tiles = (C8 * 8 + QCOL_TILE - 1) / QCOL_TILE;
-  const int64_t row_blocks = rows / 32;
-  const int64_t mnb = C8 / 16;                 // 128-column blocks
-  const int64_t mnb_rows = rows_total / 128;   // 128-row blocks (row scales)
-  const int cg = threadIdx.x % 64, rs = threadIdx.x / 64, lane = threadIdx.x & 31;
-  for (int64_t rb = blockIdx.x; rb < row_blocks; rb += gridDim.x) {
-    if (threadIdx.x < 32) src_row[threadIdx.x] = gather_src(rb * 32 + threadIdx.x, gather);
-    __syncthreads();
-    for (int ct = 0; ct < col_tiles; ++ct) {
-      const int c8 = ct * (QCOL_TILE / 8) + cg;
-      const bool active = c8 < C8;
-      uint4 w[8];
-      float amax[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) amax[j] = 0.f;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int sr = src_row[rs + 4 * r];
-        w[r] = active && sr >= 0 ? __ldg(in + static_cast<int64_t>(sr) * C8 + c8)
-                                 : make_uint4(0, 0, 0, 0);
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(&w[r]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) amax[j] = fmaxf(amax[j], fabsf(bf(h[j])));
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) part[rs][cg * 8 + j] = amax[j];
-      if (codes_rows != nullptr) {  // uniform: every lane takes part in the shuffles
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const uint16_t* h = reinterpret_cast<const uint16_t*>(&w[r]);
-          float v[8], ra = 0.f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            v[j] = bf(h[j]);
-            ra = fmaxf(ra, fabsf(v[j]));
-          }
-          ra = fmaxf(ra, __shfl_xor_sync(0xffffffffu, ra, 1));
-          ra = fmaxf(ra, __shfl_xor_sync(0xffffffffu, ra, 2));
-          const int re = scale_exp(ra);
-          const int g0 = lane & ~15;
-          uint32_t word = 0;
-#pragma unroll
-          for (int b = 0; b < 4; ++b)
-            word |= e8m0(__shfl_sync(0xffffffffu, re, g0 + 4 * b)) << (8 * b);
-          const int64_t row = rb * 32 + rs + 4 * r;
-          if (active) {
-            codes_rows[row * C8 + c8] = codes8(v, re);
-            if ((lane & 15) == 0)
-              *reinterpret_cast<uint32_t*>(sf_rows + sf_offset(row, c8 / 4, mnb_rows)) = word;
-          }
-        }
-      }
-      __syncthreads();
-      int e[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = cg * 8 + j;
-        e[j] = scale_exp(fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c])));
-      }
-      __syncthreads();  // part[] (and, at the next row block, src_row[]) is rewritten
-      if (active) {
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const uint16_t* h = reinterpret_cast<const uint16_t*>(&w[r]);
-          uint32_t p[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            p[j] = mx::codes2e(bf(h[2 * j]), e[2 * j], bf(h[2 * j + 1]), e[2 * j + 1]);
-          codes[(rb * 32 + rs + 4 * r) * C8 + c8] =
-              make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
-        }
-        if (rs == 0) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) sf[sf_offset(static_cast<int64_t>(c8) * 8 + j, rb, mnb)] = e8m0(e[j]);
-        }
-      }
+  const int col_tiles = C / QC_TC;
+  const int64_t n_tiles = (rows / 32) * col_tiles;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * QC_WARPS + warp;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * QC_WARPS;
+  const int64_t my_n = gw < n_tiles ? (n_tiles - 1 - gw) / nw + 1 : 0;
+  const int64_t mnb = C / 128, mnb_rows = rows_total / 128;
+  uint8_t* ring = qbuf + warp * (QC_STAGES * QC_TILE_BYTES);
+  uint64_t* wbar = bar[warp];
+  if (lane == 0) {
+    for (int s = 0; s < QC_STAGES; ++s) ptx::mbar_init(&wbar[s], 1);
+    ptx::fence_barrier_init();
+  }
+  __syncwarp();
+
+  // bring tile i of this warp into its stage: lane r copies row r (a zero row: none)
+  auto issue = [&](int64_t i) {
+    const int64_t t = gw + i * nw;
+    const int64_t rb = t / col_tiles;
+    const int c0 = static_cast<int>(t - rb * col_tiles) * QC_TC;
+    const int src = gather_src(rb * 32 + lane, gather);
+    const uint32_t valid = __ballot_sync(0xffffffffu, src >= 0);
+    const int s = static_cast<int>(i % QC_STAGES);
+    if (lane == 0) {
+      valid_rows[warp][s] = valid;
+      ptx::mbar_arrive_expect_tx(&wbar[s], static_cast<uint32_t>(__popc(valid)) * QC_TC * 2);
     }
+    if (src >= 0)
+      ptx::bulk_load(ring + s * QC_TILE_BYTES + lane * QC_ROW,
+                     in + static_cast<int64_t>(src) * C + c0, QC_TC * 2, &wbar[s]);
+  };
+  for (int64_t i = 0; i < QC_STAGES && i < my_n; ++i) issue(i);
+
+  int no_abort = 0;
+  for (int64_t i = 0; i < my_n; ++i) {
+    const int s = static_cast<int>(i % QC_STAGES);
+    const uint32_t parity = static_cast<uint32_t>((i / QC_STAGES) & 1);
+    int ok = 1;
+    if (lane == 0) ok = ptx::mbar_wait(&wbar[s], parity, &no_abort, QC_WAIT_NS) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {  // a copy never landed: report, let the other issued copies land, stop
+      if (lane == 0) {
+        if (status != nullptr && atomicCAS(&status->code, 0, MM_MOE_ETIMEOUT) == 0)
+          status->detail = -2;
+        for (int64_t j = i + 1; j < i + QC_STAGES && j < my_n; ++j)
+          ptx::mbar_wait(&wbar[j % QC_STAGES], static_cast<uint32_t>((j / QC_STAGES) & 1),
+                         &no_abort, QC_WAIT_NS);
+      }
+      __syncwarp();
+      return;
+    }
+    // every lane observes the completed phase (returns at once): the bytes are visible
+    if (lane != 0) ptx::mbar_wait(&wbar[s], parity, &no_abort, QC_WAIT_NS);
+    const int64_t t = gw + i * nw;
+    const int64_t rb = t / col_tiles;
+    const int c0 = static_cast<int>(t - rb * col_tiles) * QC_TC;
+    const int col = c0 + 4 * lane;
+    const uint32_t valid = valid_rows[warp][s];
+    const uint8_t* tile = ring + s * QC_TILE_BYTES;
+    uint2 w[32];                // this lane's four columns of the tile's rows
+    uint32_t m01 = 0, m23 = 0;  // column maxima of |bf16| as 16-bit pairs
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      w[r] = ((valid >> r) & 1u) ? *reinterpret_cast<const uint2*>(tile + r * QC_ROW + 8 * lane)
+                                 : make_uint2(0, 0);
+      m01 = __vmaxu2(m01, w[r].x & 0x7FFF7FFFu);
+      m23 = __vmaxu2(m23, w[r].y & 0x7FFF7FFFu);
+    }
+    if (codes_rows != nullptr) {
+      // blocks along the rows: lane l quantises row l's four 32-column blocks
+      const int64_t row = rb * 32 + lane;
+      const bool has = (valid >> lane) & 1u;
+      const uint4* rp = reinterpret_cast<const uint4*>(tile + lane * QC_ROW);
+      uint32_t word = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        uint4 q[4];
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          q[j] = has ? rp[4 * b + j] : make_uint4(0, 0, 0, 0);
+          m = __vmaxu2(m, __vmaxu2(__vmaxu2(q[j].x & 0x7FFF7FFFu, q[j].y & 0x7FFF7FFFu),
+                                   __vmaxu2(q[j].z & 0x7FFF7FFFu, q[j].w & 0x7FFF7FFFu)));
+        }
+        const int re = bf16_scale_exp(max(m & 0xFFFFu, m >> 16));
+        const float sr = mx::pow2f(-re);
+        uint32_t cw[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          cw[2 * j] = codes4(q[j].x, q[j].y, sr, sr, sr, sr);
+          cw[2 * j + 1] = codes4(q[j].z, q[j].w, sr, sr, sr, sr);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(codes_rows + row * C + c0 + 32 * b);
+        dst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        dst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        word |= e8m0(re) << (8 * b);
+      }
+      *reinterpret_cast<uint32_t*>(sf_rows + sf_offset(row, c0 / 32, mnb_rows)) = word;
+    }
+    const int e0 = bf16_scale_exp(m01 & 0xFFFFu), e1 = bf16_scale_exp(m01 >> 16);
+    const int e2 = bf16_scale_exp(m23 & 0xFFFFu), e3 = bf16_scale_exp(m23 >> 16);
+    const float s0 = mx::pow2f(-e0), s1 = mx::pow2f(-e1), s2 = mx::pow2f(-e2),
+                s3 = mx::pow2f(-e3);
+    // the stage is refilled by the asynchronous proxy after these generic reads
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (i + QC_STAGES < my_n) issue(i + QC_STAGES);
+#pragma unroll
+    for (int r = 0; r < 32; ++r)
+      *reinterpret_cast<uint32_t*>(codes + (rb * 32 + r) * C + col) =
+          codes4(w[r].x, w[r].y, s0, s1, s2, s3);
+    sf[sf_offset(col, rb, mnb)] = static_cast<uint8_t>(e8m0(e0));
+    sf[sf_offset(col + 1, rb, mnb)] = static_cast<uint8_t>(e8m0(e1));
+    sf[sf_offset(col + 2, rb, mnb)] = static_cast<uint8_t>(e8m0(e2));
+    sf[sf_offset(col + 3, rb, mnb)] = static_cast<uint8_t>(e8m0(e3));
   }
 }
 
@@ -197,15 +266,18 @@ cudaError_t launch_mxq(const Ctx& c, const MxqArgs& a) {
         static_cast<int>(a.cols / 8), a.rows / 128, a.meta);
     prof_end(c, K_MXQ_ROWS);
   } else {
-    // with `meta` the row count is known only on the device: size the grid for the
-    // capacity and let surplus CTAs exit
-    const int64_t blocks = a.rows / 32;
-    const int64_t grid = blocks < c.num_sms * 6 ? blocks : c.num_sms * 6;
+    // one CTA (8 warp pipelines) per SM; with `meta` the row count is known only on
+    // the device, so the grid is sized for the capacity and surplus warps exit
+    cudaError_t e = cudaFuncSetAttribute(mxq_cols_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, QC_SMEM);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (a.rows / 32) * (a.cols / QC_TC);
+    const int64_t want = (tiles + QC_WARPS - 1) / QC_WARPS;
+    const int64_t grid = want < c.num_sms ? want : c.num_sms;
     prof_begin(c, K_MXQ_COLS);
-    mxq_cols_kernel<<<static_cast<int>(grid > 0 ? grid : 1), 256, 0, c.stream>>>(
-        reinterpret_cast<const uint4*>(a.in), reinterpret_cast<uint2*>(a.codes), a.sf,
-        reinterpret_cast<uint2*>(a.codes_rows), a.sf_rows, a.rows, a.rows,
-        static_cast<int>(a.cols / 8), a.meta, a.gather);
+    mxq_cols_kernel<<<static_cast<int>(grid > 0 ? grid : 1), 32 * QC_WARPS, QC_SMEM,
+                      c.stream>>>(a.in, a.codes, a.sf, a.codes_rows, a.sf_rows, a.rows, a.rows,
+                                  static_cast<int>(a.cols), a.meta, a.gather, a.status);
     prof_end(c, K_MXQ_COLS);
   }
   return cudaGetLastError();

@@ -80,6 +80,9 @@ CONFIGS: Dict[str, MoEConfig] = {
     # the same inputs with a BF16 forward and an MXFP8 backward
     "qwen3_30b_16k_fp8_bwd": MoEConfig("qwen3_30b_16k_fp8_bwd", T=16384, H=2048, I=768,
                                        E=128, k=8, routing="uniform", seed=6, prec="fp8_bwd"),
+    # a smaller MXFP8 case (8,192 tokens, uniform routing) for profiler captures
+    "qwen3_30b_8k_mxfp8": MoEConfig("qwen3_30b_8k_mxfp8", T=8192, H=2048, I=768, E=128, k=8,
+                                    routing="uniform", seed=8, prec="mxfp8"),
     # and in blockwise FP8 (forward and backward)
     "qwen3_30b_16k_fp8block": MoEConfig("qwen3_30b_16k_fp8block", T=16384, H=2048, I=768,
                                         E=128, k=8, routing="uniform", seed=6,
