@@ -514,30 +514,35 @@ __device__ __forceinline__ bool epilogue_tile_split(const GemmParams& p, const T
   const int lane = w.lane, row = q * 32 + lane;
   const int row0 = ti.m0 + q * 32;
   if constexpr (KIND == GEMM_GATEUP) {
-    // gate columns hh*64 .. hh*64+63, up columns 128 + the same
-    uint32_t pg[2][16], pu[2][16], pa[2][16];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int c = hh * 64 + 32 * j;
-      uint32_t rg[32], ru[32];
-      tmem_ld2(tbase + c, tbase + 128 + c, rg, ru);
-      float g[32], u[32], a[32];
-      as_float(rg, g);
-      as_float(ru, u);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) a[i] = g[i] * sigmoidf_(g[i]) * u[i];
-      pack32(g, pg[j]);
-      pack32(u, pu[j]);
-      pack32(a, pa[j]);
-    }
+    // gate columns hh*64 .. hh*64+63, up columns 128 + the same: all four chunks to
+    // registers (fp32), TMEM back, then the SwiGLU (its exponentials would otherwise
+    // hold the accumulator while the tensor cores wait)
+    uint32_t rg[2][32], ru[2][32];
+    ptx::tmem_ld32(tbase + hh * 64, rg[0]);
+    ptx::tmem_ld32(tbase + 128 + hh * 64, ru[0]);
+    ptx::tmem_ld32(tbase + hh * 64 + 32, rg[1]);
+    ptx::tmem_ld32(tbase + 128 + hh * 64 + 32, ru[1]);
+    ptx::tmem_wait_ld(rg[0]);
+    ptx::reg_fence(ru[0]);
+    ptx::reg_fence(rg[1]);
+    ptx::reg_fence(ru[1]);
     release();
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int c = ti.n0 + hh * 64 + 32 * j;
-      store_block_p<C::EPI_OUT>(w, &p.tmC0, c, row0, pg[j]);
-      store_block_p<C::EPI_OUT>(w, &p.tmC0, p.I + c, row0, pu[j]);
-      store_block_p<C::EPI_OUT>(w, &p.tmC1, c, row0, pa[j]);
-      if (p.q_codes != nullptr) store_qa(p, row0 + lane, c, pa[j]);  // from a's bf16 value
+      float g[32], u[32], a[32];
+      as_float(rg[j], g);
+      as_float(ru[j], u);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a[i] = g[i] * sigmoidf_(g[i]) * u[i];
+      uint32_t pk[16];
+      pack32(g, pk);
+      store_block_p<C::EPI_OUT>(w, &p.tmC0, c, row0, pk);
+      pack32(u, pk);
+      store_block_p<C::EPI_OUT>(w, &p.tmC0, p.I + c, row0, pk);
+      pack32(a, pk);
+      store_block_p<C::EPI_OUT>(w, &p.tmC1, c, row0, pk);
+      if (p.q_codes != nullptr) store_qa(p, row0 + lane, c, pk);  // from a's bf16 value
     }
   } else if constexpr (KIND == GEMM_DGRAD_DOWN) {
     // (no early release: the dSwiGLU needs g' in fp32 beside its loaded inputs)
@@ -875,14 +880,14 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
     for (int t = cluster; t < total && ok; t += n_clusters) {
       const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8>(p, t, rank);
       if (ti.k_iters == 0) continue;
-      if (!ptx::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort, WAIT_LIMIT_NS)) {
+      if (!ptx::mbar_wait_spin(&tempty_bar[acc], acc_phase ^ 1u, abort, WAIT_LIMIT_NS)) {
         record_timeout(p, abort, KIND * 16 + 3, peer_abort);
         break;
       }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
       for (int kb = 0; kb < ti.k_iters; ++kb) {
-        if (!ptx::mbar_wait(&full_bar[stage], phase, abort, WAIT_LIMIT_NS)) {
+        if (!ptx::mbar_wait_spin(&full_bar[stage], phase, abort, WAIT_LIMIT_NS)) {
           record_timeout(p, abort, KIND * 16 + 4, peer_abort);
           ok = false;
           break;
@@ -976,7 +981,8 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
       if (KIND == GEMM_DGRAD_DOWN && !w.ld_pending)
         load_inputs(w, p, ti.m0 + q * 32, ti.n0 + (C::SPLIT ? hh * (BN / 2) : 0));
       int ok = 1;
-      if (lane == 0) ok = ptx::mbar_wait(&tfull_bar[acc], acc_phase, abort, WAIT_LIMIT_NS) ? 1 : 0;
+      if (lane == 0)
+        ok = ptx::mbar_wait_spin(&tfull_bar[acc], acc_phase, abort, WAIT_LIMIT_NS) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) record_timeout(p, abort, KIND * 16 + 6, peer_abort);
@@ -987,14 +993,17 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(q * 32) << 16);
       // hand the accumulator back to the MMA issuer (every epilogue warp of the pair
-      // arrives once per tile)
+      // arrives once per tile).  The warp's TMEM reads have completed (tcgen05.wait::ld)
+      // before it arrives, so the arrive needs no release of its memory writes: a
+      // relaxed arrive, which does not wait for the previous tile's global stores to
+      // become visible (with a release arrive the tensor cores sat idle about a
+      // microsecond per tile while they drained)
       auto release = [&]() {
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          if constexpr (CTAS == 1) ptx::mbar_arrive(&tempty_bar[acc]);
-          else ptx::mbar_arrive_cluster(lead_tempty0 + acc * 8u);
-        }
+        if (lane == 0)
+          ptx::mbar_arrive_cluster_relaxed(CTAS == 1 ? ptx::smem_u32(&tempty_bar[acc])
+                                                     : lead_tempty0 + acc * 8u);
       };
       bool done;
       if constexpr (C::SPLIT)
