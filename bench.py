@@ -604,9 +604,9 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "graph": graph,
-        # this library's kernels: the layer's, and the router's selection and logit
-        # gradient when it runs (its three products are cuBLAS kernels, not counted)
-        "gpu_launches": (n_fwd_launch + n_bwd_launch + (2 if router is not None else 0)) * K,
+        # this library's kernels: the layer's, and with the router its five (the logits
+        # GEMM and the top-k selection; the logit gradient and the two GEMMs after it)
+        "gpu_launches": (n_fwd_launch + n_bwd_launch + (5 if router is not None else 0)) * K,
         "clocks": clock,
         "kernels": kern if args.kernels else {k: round(v["share"], 4) for k, v in kern.items()},
         "sources": source_digest(),

@@ -185,10 +185,11 @@ MM_MOE_API mm_moe_status mm_moe_get_routing(const mm_moe_shape* shape, const voi
  *   x        [T, H] bf16;  W_router [E, H] bf16
  *   logits   [T, E] fp32 out (x W_router^T, fp32 accumulation)
  *   topk_idx [T, k] int32 out;  topk_w [T, k] fp32 out
- * The three matrix products run on cuBLAS (bf16 operands, fp32 accumulation); its
- * handle, made once per host thread and device, holds cuBLAS's own device workspace:
- * the one allocation these two calls make outside the caller's buffers.  Non-finite
- * logits give an unspecified selection.  Errors as for the layer. */
+ * The three matrix products run on the library's own tensor-core GEMM (bf16
+ * operands, fp32 accumulation); like every call of the library these two allocate
+ * nothing.  A GEMM wait that ran out of time is not reported (the router calls take
+ * no scratch buffer, so they have no status word).  Non-finite logits give an
+ * unspecified selection.  Errors as for the layer. */
 MM_MOE_API mm_moe_status mm_moe_router_forward(const mm_moe_shape* shape, const uint16_t* x,
                                                const uint16_t* W_router, float* logits,
                                                int32_t* topk_idx, float* topk_w, void* stream);

@@ -57,6 +57,53 @@ cudaError_t run_bf16(const Ctx& c, const GemmParams& p, int kind, int bn, int ct
 
 }  // namespace gemm
 
+// Dense products on single-SM 128 x 128 tiles (bf16 in, fp32 accumulation); the tensor
+// maps cover exactly M, N, K, so ragged tiles read zeros past the edges and the bf16
+// stores are clipped there (the fp32 epilogue masks them).
+cudaError_t launch_dense(const Ctx& c, int kind, const uint16_t* A, const uint16_t* B, void* C,
+                         int64_t M, int64_t N, int64_t K) {
+  using namespace gemm;
+  // (the inner dimension of every operand and of the output: rows of 16-byte multiples)
+  const bool inner_ok = kind == GEMM_DENSE_TN ? (M % 8 == 0 && N % 8 == 0)
+                                              : (K % 8 == 0 && N % 8 == 0);
+  if (M < 1 || N < 1 || K < 1 || !inner_ok || M >= (int64_t{1} << 31) ||
+      N >= (int64_t{1} << 31) || K >= (int64_t{1} << 31))
+    return cudaErrorInvalidValue;
+  constexpr int BN = 128;
+  GemmParams p;
+  memset(&p, 0, sizeof(p));
+  p.dm = static_cast<int>(M);
+  p.dn = static_cast<int>(N);
+  p.m_tiles = static_cast<int>((M + BM - 1) / BM);
+  p.n_tiles = static_cast<int>((N + BN - 1) / BN);
+  p.k_iters = static_cast<int>((K + BK - 1) / BK);
+  const uint64_t m = M, n = N, k = K;
+  bool ok = false;
+  switch (kind) {
+    case GEMM_DENSE_NT:  // A [M, K], B [N, K], C [M, N] fp32
+      ok = make_map(&p.tmA, A, k, m, 64, BM) && make_map(&p.tmB0, B, k, n, 64, BN);
+      p.outf = static_cast<float*>(C);
+      break;
+    case GEMM_DENSE_NN:  // A [M, K], B [K, N], C [M, N] bf16 (read and written)
+      ok = make_map(&p.tmA, A, k, m, 64, BM) && make_map(&p.tmB0, B, n, k, 64, 64) &&
+           make_epi_map(&p.tmC0, C, n, m) && make_epi_map(&p.tmD0, C, n, m);
+      break;
+    case GEMM_DENSE_TN:  // A [K, M], B [K, N], C [M, N] bf16
+      ok = make_map(&p.tmA, A, m, k, 64, 64) && make_map(&p.tmB0, B, n, k, 64, 64) &&
+           make_epi_map(&p.tmC0, C, n, m);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+  switch (kind) {
+    case GEMM_DENSE_NT: return run<GEMM_DENSE_NT, BN, 1, false>(c, p, tiles);
+    case GEMM_DENSE_NN: return run<GEMM_DENSE_NN, BN, 1, false>(c, p, tiles);
+    default: return run<GEMM_DENSE_TN, BN, 1, false>(c, p, tiles);
+  }
+}
+
 cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
   using namespace gemm;
   GemmParams p;

@@ -89,6 +89,7 @@ struct GemmParams {
   int k_iters;  // K iterations per tile (grouped kinds)
   int n_pw;
   int max_tiles;
+  int dm, dn;  // dense products: the output's rows and columns
   int stall;  // failure-path test: CTA 0 arms its first stage but issues no copy
   const int* meta;
   const int* tile_expert;
@@ -109,9 +110,11 @@ struct Cfg {
   static constexpr bool FP8 = FP8_;
   static constexpr int BN = BN_;      // N of one MMA (both CTAs of a pair together)
   static constexpr int CTAS = CTAS_;
-  static constexpr bool A_MN = KIND >= GEMM_WGRAD_DOWN;
-  static constexpr bool B_MN = KIND >= GEMM_DGRAD_DOWN;
-  static constexpr bool PER_EXPERT = KIND >= GEMM_WGRAD_DOWN;
+  static constexpr bool DENSE = KIND >= GEMM_DENSE_NT;
+  static constexpr bool PER_EXPERT = KIND >= GEMM_WGRAD_DOWN && !DENSE;
+  static constexpr bool A_MN = PER_EXPERT || KIND == GEMM_DENSE_TN;
+  static constexpr bool B_MN = (KIND >= GEMM_DGRAD_DOWN && !DENSE) || KIND == GEMM_DENSE_NN ||
+                               KIND == GEMM_DENSE_TN;
   static constexpr int B_ROWS = BN / CTAS;  // B rows (K-major) or columns (M/N-major) per CTA
   // each stage holds 128 bytes of K per operand row: 64 bf16 or 128 e4m3 elements;
   // an M/N-major box spans 128 bytes of M/N (64 bf16 or 128 e4m3 elements)
@@ -135,7 +138,7 @@ struct Cfg {
   static constexpr bool EARLY_RELEASE = SPLIT && KIND != GEMM_DGRAD_DOWN;
   static constexpr int EPI_WARPS = SPLIT ? 8 : 4;
   static constexpr int THREADS = 128 + 32 * EPI_WARPS;
-  static constexpr int EPI_IN = KIND == GEMM_DGRAD_DOWN ? 3 : 0;
+  static constexpr int EPI_IN = KIND == GEMM_DGRAD_DOWN ? 3 : KIND == GEMM_DENSE_NN ? 1 : 0;
   // (SPLIT: one output block per warp, which leaves room for a sixth pipeline stage;
   // a warp's next block waits for the previous store to have read it)
   static constexpr int EPI_OUT = SPLIT ? 1 : 4;
@@ -156,6 +159,7 @@ struct Cfg {
   static_assert(CTAS == 1 || (CTAS == 2 && B_ROWS >= 64), "CTAS");
   static_assert(!(KIND == GEMM_GATEUP && (CTAS == 2 || FP8) && BN != 256), "gate/up tile");
   static_assert(!FP8 || BN >= 128, "FP8 scale atoms cover 128 rows of B");
+  static_assert(!DENSE || (CTAS == 1 && !FP8), "dense products: single-SM bf16 tiles");
   static_assert(!(FP8 && B_MN && B_ROWS % 128 != 0), "FP8 M/N-major boxes are 128 wide");
   static_assert(!FP8 || NACC * BN <= static_cast<int>(SF_COL0), "TMEM columns");
   static_assert(!FP8 || SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM scale ring");
@@ -185,7 +189,15 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int 
   using C = Cfg<KIND, BN, CTAS, FP8>;
   TileInfo ti;
   ti.down = 0;
-  if constexpr (C::PER_EXPERT) {
+  if constexpr (C::DENSE) {
+    const int mt = t / p.n_tiles;
+    ti.e = 0;
+    ti.mb = mt;
+    ti.m0 = mt * BM;
+    ti.n0 = (t - mt * p.n_tiles) * BN;
+    ti.k_iters = p.k_iters;
+    ti.k_row0 = 0;
+  } else if constexpr (C::PER_EXPERT) {
     const int2 per = expert_tiles<KIND>(p);
     const int per_e = per.x + per.y;
     const int ei = t / per_e;
@@ -218,7 +230,9 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int 
 
 template <int KIND, int BN, int CTAS, bool FP8>
 __device__ __forceinline__ int total_tiles(const GemmParams& p) {
-  if constexpr (Cfg<KIND, BN, CTAS, FP8>::PER_EXPERT) {
+  if constexpr (Cfg<KIND, BN, CTAS, FP8>::DENSE) {
+    return p.m_tiles * p.n_tiles;
+  } else if constexpr (Cfg<KIND, BN, CTAS, FP8>::PER_EXPERT) {
     const int2 per = expert_tiles<KIND>(p);
     return p.E * (per.x + per.y);
   } else {
@@ -235,7 +249,8 @@ __device__ __forceinline__ void record_timeout(GemmParams const& p, volatile int
                                                int detail, uint32_t peer_abort = 0) {
   *abort = 1;
   if (peer_abort != 0) ptx::st_cluster_u32(peer_abort, 1u);
-  if (atomicCAS(&p.status->code, 0, MM_MOE_ETIMEOUT) == 0) p.status->detail = detail;
+  if (p.status != nullptr && atomicCAS(&p.status->code, 0, MM_MOE_ETIMEOUT) == 0)
+    p.status->detail = detail;
 }
 
 // ------------------------------------------------------------------ epilogue helpers
@@ -455,6 +470,61 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInf
       store_block<C::EPI_OUT>(w, &p.tmC1, ti.n0 + c, row0, av);
     }
     p.outf[pr * p.n_pw + ti.n0 / BN] = dot;
+  } else if constexpr (KIND == GEMM_DENSE_NT) {
+    // fp32 rows straight to global memory (rows / columns past the output skipped)
+    const int r = ti.m0 + row;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t rr[32];
+      ptx::tmem_ld32(tbase + c, rr);
+      ptx::tmem_wait_ld(rr);
+      const int col = ti.n0 + c;
+      if (r < p.dm && col < p.dn) {
+        float* dst = p.outf + static_cast<int64_t>(r) * p.dn + col;
+        if (col + 32 <= p.dn) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            reinterpret_cast<float4*>(dst)[j] =
+                make_float4(__uint_as_float(rr[4 * j]), __uint_as_float(rr[4 * j + 1]),
+                            __uint_as_float(rr[4 * j + 2]), __uint_as_float(rr[4 * j + 3]));
+        } else {
+          for (int j = 0; j < p.dn - col; ++j) dst[j] = __uint_as_float(rr[j]);
+        }
+      }
+    }
+  } else if constexpr (KIND == GEMM_DENSE_NN) {
+    // C += A.B: each 32 x 32 block of C comes in by TMA, takes the sum in fp32 and
+    // goes back rounded to bf16 (TMA clips the blocks at the output's edges)
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      if (lane == 0) {
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive_expect_tx(w.ld_bar, 2048);
+        ptx::tma_load_2d(w.in, &p.tmD0, w.ld_bar, ti.n0 + c, row0);
+      }
+      w.ld_pending = true;
+      if (!wait_inputs(w, abort)) return false;
+      float old[32];
+      unstage32(w.in, lane, old);
+      __syncwarp();
+      uint32_t rr[32];
+      ptx::tmem_ld32(tbase + c, rr);
+      ptx::tmem_wait_ld(rr);
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = old[i] + __uint_as_float(rr[i]);
+      store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, v);
+    }
+  } else if constexpr (KIND == GEMM_DENSE_TN) {
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t rr[32];
+      ptx::tmem_ld32(tbase + c, rr);
+      ptx::tmem_wait_ld(rr);
+      float v[32];
+      as_float(rr, v);
+      store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, v);
+    }
   } else {  // weight gradients: dW_down [E*H, I]; dW_gate / dW_up [E*I, H]
     const CUtensorMap* m;
     int orow;
@@ -731,6 +801,20 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
         sf_atom<CTAS>(sf + 512 * (1 + j), ms, bar,
                       static_cast<int64_t>(krow / 128) * p.sfb_mnb + ti.n0 / 128 + j);
     }
+  } else if constexpr (C::DENSE) {
+    if constexpr (KIND != GEMM_DENSE_TN) {
+      tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);  // A [M, K]
+    } else {
+#pragma unroll
+      for (int c = 0; c < BM / 64; ++c) tma<CTAS>(sa + c * 8192, &p.tmA, bar, ti.m0 + c * 64, k0);
+    }
+    if constexpr (KIND == GEMM_DENSE_NT) {
+      tma<CTAS>(sb, &p.tmB0, bar, k0, ti.n0);  // B [N, K]
+    } else {
+#pragma unroll
+      for (int c = 0; c < C::B_ROWS / 64; ++c)
+        tma<CTAS>(sb + c * 8192, &p.tmB0, bar, ti.n0 + c * 64, k0);  // B [K, N]
+    }
   } else {  // per-expert weight gradients: both operands M/N-major, K = routed rows
     const int krow = ti.k_row0 + k0;
     const bool second = KIND == GEMM_WGRAD_BOTH && ti.down;
@@ -836,7 +920,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
     for (int t = cluster; t < total && ok; t += n_clusters) {
       const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8>(p, t, rank);
       for (int kb = 0; kb < ti.k_iters; ++kb) {
-        if (!ptx::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, WAIT_LIMIT_NS)) {
+        if (!ptx::mbar_wait_spin(&empty_bar[stage], phase ^ 1u, abort, WAIT_LIMIT_NS)) {
           record_timeout(p, abort, KIND * 16 + 1, peer_abort);
           ok = false;
           break;
@@ -1120,9 +1204,10 @@ static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) 
   }
   clusters = std::max<int64_t>(1, std::min<int64_t>(clusters, max_clusters));
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CTAS), 1, 1);
-  static constexpr int kId[7] = {K_GEMM_GATEUP,       K_GEMM_DOWN,       K_GEMM_DGRAD_DOWN,
-                                 K_GEMM_DGRAD_GATEUP, K_GEMM_WGRAD_DOWN, K_GEMM_WGRAD_GATEUP,
-                                 K_GEMM_WGRAD};
+  static constexpr int kId[10] = {K_GEMM_GATEUP,       K_GEMM_DOWN,       K_GEMM_DGRAD_DOWN,
+                                  K_GEMM_DGRAD_GATEUP, K_GEMM_WGRAD_DOWN, K_GEMM_WGRAD_GATEUP,
+                                  K_GEMM_WGRAD,        K_DENSE_GEMM,      K_DENSE_GEMM,
+                                  K_DENSE_GEMM};
   prof_begin(c, kId[KIND]);
   e = cudaLaunchKernelEx(&cfg, kern, p);
   prof_end(c, kId[KIND]);

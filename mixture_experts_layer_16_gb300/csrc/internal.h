@@ -107,6 +107,7 @@ enum KernelId {
   K_FB_TILES,
   K_MXQ_ROWS,
   K_MXQ_COLS,
+  K_DENSE_GEMM,
   K_COUNT
 };
 
@@ -219,7 +220,17 @@ enum GemmKind {
   GEMM_WGRAD_DOWN = 4,    // dy_perm^T . a_w per expert -> dW_down
   GEMM_WGRAD_GATEUP = 5,  // dh^T . x_perm per expert   -> dW_gate, dW_up
   GEMM_WGRAD_BOTH = 6,    // both weight gradients in one launch, tiles ordered by expert
+  // dense products (the router's; single-SM tiles, bf16 operands, any M, N, K):
+  GEMM_DENSE_NT = 7,      // C [M, N] fp32  = A [M, K] . B [N, K]^T
+  GEMM_DENSE_NN = 8,      // C [M, N] bf16 += A [M, K] . B [K, N]   (read-modify-write)
+  GEMM_DENSE_TN = 9,      // C [M, N] bf16  = A [K, M]^T . B [K, N]
 };
+
+// A dense product of kind GEMM_DENSE_* (row-major bf16 operands; every inner dimension
+// a multiple of 8, so that rows are 16-byte multiples).  Returns cudaErrorInvalidValue
+// for unsupported sizes.
+cudaError_t launch_dense(const Ctx& c, int kind, const uint16_t* A, const uint16_t* B, void* C,
+                         int64_t M, int64_t N, int64_t K);
 
 struct GemmArgs {
   int kind;

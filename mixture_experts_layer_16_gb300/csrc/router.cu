@@ -8,10 +8,10 @@
 // lower expert index; weights = softmax over the chosen logits (the full softmax
 // renormalised over them); the gradient flows through the weights only.
 //
-// The three matrix products (x W_router^T; dlogits^T x; dlogits W_router) are plain
-// dense GEMMs and run on cuBLAS (bf16 operands, fp32 accumulation).  The selection,
-// the softmax and the logit gradient are this file's kernels: one warp per token.
-#include <cublas_v2.h>
+// The three matrix products (x W_router^T; dlogits^T x; dlogits W_router) are dense
+// GEMMs on the library's own tcgen05 kernel (bf16 operands, fp32 accumulation; the
+// dense kinds of gemm.cuh).  The selection, the softmax and the logit gradient are this
+// file's kernels: one warp per token.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -123,19 +123,6 @@ __global__ void __launch_bounds__(256) router_dlogits_kernel(const int32_t* __re
   }
 }
 
-// cuBLAS handle of this host thread on the current device (created on first use).
-static cublasHandle_t blas_handle(cudaStream_t stream) {
-  static thread_local cublasHandle_t handles[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (handles[dev] == nullptr && cublasCreate(&handles[dev]) != CUBLAS_STATUS_SUCCESS) {
-    handles[dev] = nullptr;
-    return nullptr;
-  }
-  if (cublasSetStream(handles[dev], stream) != CUBLAS_STATUS_SUCCESS) return nullptr;
-  return handles[dev];
-}
-
 static bool router_shape_ok(const mm_moe_shape* s) {
   return s != nullptr && s->T >= 1 && s->H >= 1 && s->E >= 1 && s->k >= 1 && s->k <= s->E &&
          s->k <= ROUTER_MAX_K && s->E <= 1024 && s->H % 8 == 0 && s->E % 8 == 0 &&
@@ -185,15 +172,12 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_router_forward(const mm_moe_shape* sh
   int sms = 0;
   if (!device_ok(&sms)) return MM_MOE_ENOTSUP;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cublasHandle_t h = blas_handle(st);
-  if (h == nullptr) return MM_MOE_ECUDA;
   const int T = static_cast<int>(shape->T), H = static_cast<int>(shape->H),
             E = static_cast<int>(shape->E), k = static_cast<int>(shape->k);
-  // column-major view: logits^T [E, T] = W_router [E, H] . x^T [H, T]
-  const float one = 1.f, zero = 0.f;
-  if (cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, E, T, H, &one, W_router, CUDA_R_16BF, H, x,
-                   CUDA_R_16BF, H, &zero, logits, CUDA_R_32F, E, CUBLAS_COMPUTE_32F,
-                   CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+  int launches = 0;
+  const Ctx c{st, sms, &launches};
+  // logits [T, E] = x [T, H] . W_router [E, H]^T
+  if (launch_dense(c, GEMM_DENSE_NT, x, W_router, logits, T, E, H) != cudaSuccess)
     return MM_MOE_ECUDA;
   if (E <= 128)
     launch_topk<4>(st, logits, T, E, k, topk_idx, topk_w);
@@ -215,10 +199,10 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_router_backward(
   int sms = 0;
   if (!device_ok(&sms)) return MM_MOE_ENOTSUP;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cublasHandle_t h = blas_handle(st);
-  if (h == nullptr) return MM_MOE_ECUDA;
   const int T = static_cast<int>(shape->T), H = static_cast<int>(shape->H),
             E = static_cast<int>(shape->E), k = static_cast<int>(shape->k);
+  int launches = 0;
+  const Ctx c{st, sms, &launches};
   __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(dlogits);
   if (E <= 128)
     launch_dlogits<4>(st, topk_idx, topk_w, dtopk_w, T, E, k, dl);
@@ -227,16 +211,11 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_router_backward(
   else
     launch_dlogits<32>(st, topk_idx, topk_w, dtopk_w, T, E, k, dl);
   if (cudaGetLastError() != cudaSuccess) return MM_MOE_ECUDA;
-  const float one = 1.f, zero = 0.f;
-  // dW_router [E, H] = dlogits^T x; column-major: [H, E] = x^T [H, T] . dlogits [T, E]
-  if (cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_T, H, E, T, &one, x, CUDA_R_16BF, H, dlogits,
-                   CUDA_R_16BF, E, &zero, dW_router, CUDA_R_16BF, H, CUBLAS_COMPUTE_32F,
-                   CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+  // dW_router [E, H] = dlogits [T, E]^T . x [T, H]
+  if (launch_dense(c, GEMM_DENSE_TN, dlogits, x, dW_router, E, H, T) != cudaSuccess)
     return MM_MOE_ECUDA;
-  // dx [T, H] += dlogits W_router; column-major: [H, T] += W^T-view [H, E] . dlogits^T [E, T]
-  if (cublasGemmEx(h, CUBLAS_OP_N, CUBLAS_OP_N, H, T, E, &one, W_router, CUDA_R_16BF, H, dlogits,
-                   CUDA_R_16BF, E, &one, dx, CUDA_R_16BF, H, CUBLAS_COMPUTE_32F,
-                   CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+  // dx [T, H] += dlogits [T, E] . W_router [E, H]
+  if (launch_dense(c, GEMM_DENSE_NN, dlogits, W_router, dx, T, H, E) != cudaSuccess)
     return MM_MOE_ECUDA;
   return MM_MOE_OK;
 }
