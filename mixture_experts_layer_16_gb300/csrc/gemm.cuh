@@ -130,18 +130,18 @@ struct Cfg {
   // epilogue staging per epilogue warp, in 2 KB blocks (32 rows x 32 bf16): TMA-loaded
   // inputs (dSwiGLU: g, u, a) and a ring of output blocks for TMA stores
   // SPLIT (the FP8 tiles with one accumulator): eight epilogue warps, two per TMEM
-  // lane quadrant, each taking half of the tile's columns; except in the dSwiGLU
-  // epilogue they move their columns to registers (packed bf16) and hand TMEM back
-  // to the MMA issuer before writing anything (EARLY_RELEASE), so the next tile's
-  // main loop overlaps the stores
+  // lane quadrant, each taking half of the tile's columns; they move their columns
+  // to registers and hand TMEM back to the MMA issuer before most of their work
+  // (EARLY_RELEASE), so the next tile's main loop overlaps the stores
   static constexpr bool SPLIT = NACC == 1;
-  static constexpr bool EARLY_RELEASE = SPLIT && KIND != GEMM_DGRAD_DOWN;
+  static constexpr bool EARLY_RELEASE = SPLIT;
   static constexpr int EPI_WARPS = SPLIT ? 8 : 4;
   static constexpr int THREADS = 128 + 32 * EPI_WARPS;
   static constexpr int EPI_IN = KIND == GEMM_DGRAD_DOWN ? 3 : KIND == GEMM_DENSE_NN ? 1 : 0;
-  // (SPLIT: one output block per warp, which leaves room for a sixth pipeline stage;
-  // a warp's next block waits for the previous store to have read it)
-  static constexpr int EPI_OUT = SPLIT ? 1 : 4;
+  // (SPLIT: one output block per warp, which leaves room for a sixth pipeline stage,
+  // two in the dSwiGLU epilogue, where they fit beside its four stages; a warp's
+  // next block waits for the store before last to have read it)
+  static constexpr int EPI_OUT = SPLIT ? (KIND == GEMM_DGRAD_DOWN ? 2 : 1) : 4;
   static constexpr int EPI_WARP_BYTES = (EPI_IN + EPI_OUT) * 2048;
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_WARP_BYTES;
   static constexpr int SMEM_CAP = 232448 - 1024;  // opt-in limit minus static shared memory
@@ -153,6 +153,9 @@ struct Cfg {
   // B's 4 per 128 rows), so the copy of a stage's scales never waits for the MMAs of
   // the previous stage to finish reading theirs
   static constexpr uint32_t SF_COL0 = 256, SF_COLS_PER_STAGE = 16;
+  // FP8 dSwiGLU epilogue on SPLIT tiles: TMEM columns past the scale ring where each
+  // warp parks three of its four 32-column chunks of g' (96 columns per column half)
+  static constexpr uint32_t STASH_COL0 = SF_COL0 + STAGES * SF_COLS_PER_STAGE;
   static constexpr uint32_t IDESC = FP8 ? ptx::idesc_mxf8(BM * CTAS, BN, A_MN, B_MN)
                                         : ptx::idesc_bf16_f32(BM * CTAS, BN, A_MN, B_MN);
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
@@ -163,6 +166,8 @@ struct Cfg {
   static_assert(!(FP8 && B_MN && B_ROWS % 128 != 0), "FP8 M/N-major boxes are 128 wide");
   static_assert(!FP8 || NACC * BN <= static_cast<int>(SF_COL0), "TMEM columns");
   static_assert(!FP8 || SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM scale ring");
+  static_assert(!(SPLIT && KIND == GEMM_DGRAD_DOWN) || STASH_COL0 + 2 * 96 <= TMEM_COLS,
+                "TMEM stash");
   static_assert(STAGES >= 2, "stages");
 };
 
@@ -315,6 +320,27 @@ __device__ __forceinline__ void store_block(EpiWarp& w, const CUtensorMap* m, in
   if (w.lane == 0) ptx::bulk_wait_read<NB - 1>();  // the slot's previous store has read it
   __syncwarp();
   stage32(buf, w.lane, v);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (w.lane == 0) {
+    ptx::tma_store_2d(m, buf, c0, c1);
+    ptx::bulk_commit();
+  }
+  w.ob = (w.ob + 1 == NB) ? 0 : w.ob + 1;
+}
+
+// The next slot of a warp's ring of NB output blocks, once the store that last used
+// it has read it; end_block sends the block to coordinates (c0, c1) of tensor map m.
+template <int NB>
+__device__ __forceinline__ uint8_t* begin_block(EpiWarp& w) {
+  uint8_t* buf = w.out + w.ob * 2048;
+  if (w.lane == 0) ptx::bulk_wait_read<NB - 1>();
+  __syncwarp();
+  return buf;
+}
+template <int NB>
+__device__ __forceinline__ void end_block(EpiWarp& w, const CUtensorMap* m, int c0, int c1,
+                                          uint8_t* buf) {
   ptx::fence_proxy_async_smem();
   __syncwarp();
   if (w.lane == 0) {
@@ -615,40 +641,107 @@ __device__ __forceinline__ bool epilogue_tile_split(const GemmParams& p, const T
       if (p.q_codes != nullptr) store_qa(p, row0 + lane, c, pk);  // from a's bf16 value
     }
   } else if constexpr (KIND == GEMM_DGRAD_DOWN) {
-    // (no early release: the dSwiGLU needs g' in fp32 beside its loaded inputs)
+    // g' stays fp32, as the accumulator holds it.  The warp parks chunks 1-3 of its
+    // 128 columns in spare TMEM columns (tcgen05.st), takes chunk 0 to registers and
+    // hands the accumulator back to the MMA issuer; the dSwiGLU then works chunk by
+    // chunk, each chunk's inputs (g, u, a) arriving by TMA during the previous one.
     const int64_t pr = ti.m0 + row;
     const float wgt = __ldg(p.w_row + pr);
+    const uint32_t t0 = tbase + hh * 128;
+    const uint32_t stash = tbase + C::STASH_COL0 + hh * 96;  // (one accumulator, at column 0)
     float dot = 0.f;
-#pragma unroll 1
-    for (int j = 0; j < 4; ++j) {
+    auto chunk = [&](int j, const uint32_t (&gp)[32]) -> bool {
       const int c = hh * 128 + 32 * j;
       if (!w.ld_pending) load_inputs(w, p, row0, ti.n0 + c);
       if (!wait_inputs(w, abort)) return false;
-      float g[32], u[32], av[32];
-      unstage32(w.in, lane, g);
-      unstage32(w.in + 2048, lane, u);
-      unstage32(w.in + 4096, lane, av);
+      // the inputs to registers (bf16 pairs), then the next chunk's (or the next
+      // tile's first) are requested while this one is computed
+      uint32_t gw[16], uw[16], aw[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 G = *reinterpret_cast<const uint4*>(swz(w.in, lane, k));
+        const uint4 U = *reinterpret_cast<const uint4*>(swz(w.in + 2048, lane, k));
+        const uint4 A = *reinterpret_cast<const uint4*>(swz(w.in + 4096, lane, k));
+        gw[4 * k] = G.x, gw[4 * k + 1] = G.y, gw[4 * k + 2] = G.z, gw[4 * k + 3] = G.w;
+        uw[4 * k] = U.x, uw[4 * k + 1] = U.y, uw[4 * k + 2] = U.z, uw[4 * k + 3] = U.w;
+        aw[4 * k] = A.x, aw[4 * k + 1] = A.y, aw[4 * k + 2] = A.z, aw[4 * k + 3] = A.w;
+      }
       __syncwarp();
       if (j < 3) load_inputs(w, p, row0, ti.n0 + c + 32);
       else if (next != nullptr) load_inputs(w, p, next->m0 + q * 32, next->n0 + hh * 128);
-      uint32_t r[32];
-      ptx::tmem_ld32(tbase + c, r);
-      ptx::tmem_wait_ld(r);
-      float dg[32], du[32];
+      auto lo = [](uint32_t v) { return __uint_as_float(v << 16); };
+      auto hi = [](uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); };
+      // dg, du, w*a: one output block each, 8 columns at a time
+      uint8_t* b = begin_block<C::EPI_OUT>(w);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float gp = __uint_as_float(r[i]);
-        const float s = sigmoidf_(g[i]);
-        const float sg = g[i] * s;
-        dot += av[i] * gp;
-        const float da = wgt * gp;
-        dg[i] = da * u[i] * s * (1.0f + g[i] * (1.0f - s));
-        du[i] = da * sg;
-        av[i] *= wgt;
+      for (int k = 0; k < 4; ++k) {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int x = 4 * k + i;
+          float v[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float g = h ? hi(gw[x]) : lo(gw[x]), u = h ? hi(uw[x]) : lo(uw[x]);
+            const float sg = sigmoidf_(g);
+            v[h] = wgt * __uint_as_float(gp[2 * x + h]) * u * sg * (1.0f + g * (1.0f - sg));
+          }
+          o[i] = pack2(v[0], v[1]);
+        }
+        *reinterpret_cast<uint4*>(swz(b, lane, k)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, dg);
-      store_block<C::EPI_OUT>(w, &p.tmC0, p.I + ti.n0 + c, row0, du);
-      store_block<C::EPI_OUT>(w, &p.tmC1, ti.n0 + c, row0, av);
+      end_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, b);
+      b = begin_block<C::EPI_OUT>(w);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int x = 4 * k + i;
+          float v[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float g = h ? hi(gw[x]) : lo(gw[x]);
+            v[h] = wgt * __uint_as_float(gp[2 * x + h]) * g * sigmoidf_(g);
+          }
+          o[i] = pack2(v[0], v[1]);
+        }
+        *reinterpret_cast<uint4*>(swz(b, lane, k)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      end_block<C::EPI_OUT>(w, &p.tmC0, p.I + ti.n0 + c, row0, b);
+      b = begin_block<C::EPI_OUT>(w);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int x = 4 * k + i;
+          const float a0 = lo(aw[x]), a1 = hi(aw[x]);
+          dot += a0 * __uint_as_float(gp[2 * x]) + a1 * __uint_as_float(gp[2 * x + 1]);
+          o[i] = pack2(a0 * wgt, a1 * wgt);  // w * a, the dW_down operand
+        }
+        *reinterpret_cast<uint4*>(swz(b, lane, k)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      end_block<C::EPI_OUT>(w, &p.tmC1, ti.n0 + c, row0, b);
+      return true;
+    };
+    uint32_t r[32];
+#pragma unroll 1
+    for (int j = 1; j < 4; ++j) {
+      ptx::tmem_ld32(t0 + 32 * j, r);
+      ptx::tmem_wait_ld(r);
+      ptx::tmem_st32(stash + 32 * (j - 1), r);
+    }
+    ptx::tmem_ld32(t0, r);
+    ptx::tmem_wait_ld(r);
+    ptx::tmem_wait_st();
+    release();
+    if (!chunk(0, r)) return false;
+#pragma unroll 1
+    for (int j = 1; j < 4; ++j) {
+      ptx::tmem_ld32(stash + 32 * (j - 1), r);
+      ptx::tmem_wait_ld(r);
+      if (!chunk(j, r)) return false;
     }
     // two partial sums per row and N tile, one per column half
     p.outf[pr * p.n_pw + (ti.n0 / BN) * 2 + hh] = dot;
