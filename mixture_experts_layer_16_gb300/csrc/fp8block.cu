@@ -52,6 +52,8 @@ __device__ __forceinline__ int64_t used(int64_t rows, const int* meta) {
 // takes 8 elements, 16 neighbouring lanes one block.
 __global__ void __launch_bounds__(256) fb_rows_kernel(const uint4* in, uint4* out, int64_t rows,
                                                       int C8, const int* __restrict__ meta) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t n = used(rows, meta) * C8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   // every lane of a warp runs the same iterations (shuffles)
@@ -82,6 +84,8 @@ __global__ void __launch_bounds__(256) fb_cols_kernel(const uint4* in, uint4* ou
                                                       uint4* out_rows, int64_t rows, int C8,
                                                       const int* __restrict__ meta,
                                                       const RowGather gather) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float part[4][FB_TILE];
   __shared__ int src_row[FB];  // the tile's source rows (-1: zero), resolved once
   const int64_t R = used(rows, meta);
@@ -144,6 +148,8 @@ __global__ void __launch_bounds__(256) fb_cols_kernel(const uint4* in, uint4* ou
 // tile (grid-stride), 16 lanes per tile row, 16 rows per pass, 8 passes.
 __global__ void __launch_bounds__(256) fb_tiles_kernel(const uint4* in, uint4* out, int64_t rows,
                                                        int C8) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float wmax[8];
   const int col_tiles = C8 / (FB / 8);
   const int64_t tiles = (rows / FB) * col_tiles;
@@ -184,14 +190,14 @@ cudaError_t launch_fb_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64
   uint4* o4 = reinterpret_cast<uint4*>(out);
   if (layout == FB_ROWS) {
     prof_begin(c, K_FB_ROWS);
-    fb_rows_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(i4, o4, rows, C8, meta);
+    launch_k(c.stream, fb_rows_kernel, dim3(c.num_sms * 8), dim3(256), 0, i4, o4, rows, C8, meta);
     prof_end(c, K_FB_ROWS);
   } else if (layout == FB_COLS) {
     const int64_t tiles = (rows / FB) * ((cols + FB_TILE - 1) / FB_TILE);
     const int64_t cap = static_cast<int64_t>(c.num_sms) * 4;
     const int grid = static_cast<int>(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
     prof_begin(c, K_FB_COLS);
-    fb_cols_kernel<<<grid, 256, 0, c.stream>>>(i4, o4, reinterpret_cast<uint4*>(out_rows), rows,
+    launch_k(c.stream, fb_cols_kernel, dim3(grid), dim3(256), 0, i4, o4, reinterpret_cast<uint4*>(out_rows), rows,
                                                C8, meta, gather);
     prof_end(c, K_FB_COLS);
   } else {
@@ -199,7 +205,7 @@ cudaError_t launch_fb_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64
     const int64_t cap = static_cast<int64_t>(c.num_sms) * 8;
     const int grid = static_cast<int>(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
     prof_begin(c, K_FB_TILES);
-    fb_tiles_kernel<<<grid, 256, 0, c.stream>>>(i4, o4, rows, C8);
+    launch_k(c.stream, fb_tiles_kernel, dim3(grid), dim3(256), 0, i4, o4, rows, C8);
     prof_end(c, K_FB_TILES);
   }
   return cudaGetLastError();

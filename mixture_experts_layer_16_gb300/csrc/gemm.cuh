@@ -992,6 +992,9 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
   ptx::tc_fence_before();
   if constexpr (CTAS == 2) ptx::cluster_sync(); else __syncthreads();
   ptx::tc_fence_after();
+  // the prologue above touched no global memory: it overlaps the previous kernel
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem_base = s_tmem_base;
   volatile int* abort = &s_abort;
   const uint32_t peer_abort =
@@ -1274,18 +1277,21 @@ static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) 
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = c.stream;
+  cfg.attrs = attr;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // (see pdl_wait)
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 1;
   int64_t clusters = c.num_sms / CTAS;
   if constexpr (CTAS == 2) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
     static int active = 0;  // clusters resident at once (the same for every launch)
     if (active == 0) {
       cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);

@@ -84,6 +84,36 @@ struct Ctx {
   int* launches;
 };
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation (launch_k; the GEMMs in gemm.cuh), so that it may
+// start, and run the part of its prologue that touches no global memory, while the
+// kernel before it in the stream drains.  Each kernel calls pdl_wait() before its
+// first global access, which returns once the kernel before it has completed and
+// its writes are visible, and then pdl_trigger(), which lets the next kernel start
+// launching.  (A kernel launched without the attribute passes both at once.)
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(cudaStream_t st, void (*kern)(KArgs...), dim3 grid, dim3 block,
+                     size_t smem, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+#endif
+
 // Kernel ids (per-kernel timing and launch accounting).
 enum KernelId {
   K_ROUTE_COUNT = 0,

@@ -35,6 +35,8 @@ constexpr int ROW_UNROLL = 4;
 
 __global__ void __launch_bounds__(256) mx_qdq_rows_kernel(const uint4* in, uint4* out, int64_t rows,
                                                           int C8, const int* __restrict__ meta) {
+  pdl_wait();
+  pdl_trigger();
   if (meta != nullptr) rows = used_rows(rows, meta);
   const int64_t n = rows * C8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -86,6 +88,8 @@ __global__ void __launch_bounds__(256) mx_qdq_cols_kernel(const uint4* in, uint4
                                                           int64_t rows, int C8,
                                                           const int* __restrict__ meta,
                                                           const RowGather gather) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float part[4][COL_TILE];
   __shared__ int src_row[32];  // the row block's source rows (-1: zero)
   if (meta != nullptr) rows = used_rows(rows, meta);
@@ -168,7 +172,7 @@ cudaError_t launch_mx_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64
   const int id = along_rows ? K_MX_QDQ_ROWS : K_MX_QDQ_COLS;
   prof_begin(c, id);
   if (along_rows) {
-    mx_qdq_rows_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(
+    launch_k(c.stream, mx_qdq_rows_kernel, dim3(c.num_sms * 8), dim3(256), 0,
         reinterpret_cast<const uint4*>(in), reinterpret_cast<uint4*>(out), rows,
         static_cast<int>(cols / 8), meta);
   } else {
@@ -176,7 +180,7 @@ cudaError_t launch_mx_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64
     // capacity and let surplus CTAs exit
     const int64_t blocks = rows / 32;  // 32-row blocks (a CTA takes whole ones)
     const int64_t grid = blocks < c.num_sms * 6 ? blocks : c.num_sms * 6;
-    mx_qdq_cols_kernel<<<static_cast<int>(grid > 0 ? grid : 1), 256, 0, c.stream>>>(
+    launch_k(c.stream, mx_qdq_cols_kernel, dim3(static_cast<int>(grid > 0 ? grid : 1)), dim3(256), 0,
         reinterpret_cast<const uint4*>(in), reinterpret_cast<uint4*>(out),
         reinterpret_cast<uint4*>(out_rows), rows, static_cast<int>(cols / 8), meta, gather);
   }

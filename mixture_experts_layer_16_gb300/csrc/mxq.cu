@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(256) mxq_rows_kernel(const uint4* __restrict__
                                                        uint8_t* __restrict__ sf, int64_t rows,
                                                        int K8, int64_t mn_blocks,
                                                        const int* __restrict__ meta) {
+  pdl_wait();
+  pdl_trigger();
   rows = rows_in_use(rows, meta);
   const int64_t n = rows * K8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -136,6 +138,8 @@ __global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
     uint8_t* __restrict__ codes_rows, uint8_t* __restrict__ sf_rows, int64_t rows,
     int64_t rows_total, int C, const int* __restrict__ meta, const RowGather gather,
     DevStatus* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t qbuf[];
   __shared__ __align__(8) uint64_t bar[QC_WARPS][QC_STAGES];
   __shared__ uint32_t valid_rows[QC_WARPS][QC_STAGES];  // rows of the stage's tile with data
@@ -261,7 +265,7 @@ __global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
 cudaError_t launch_mxq(const Ctx& c, const MxqArgs& a) {
   if (a.along_rows) {
     prof_begin(c, K_MXQ_ROWS);
-    mxq_rows_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(
+    launch_k(c.stream, mxq_rows_kernel, dim3(c.num_sms * 8), dim3(256), 0,
         reinterpret_cast<const uint4*>(a.in), reinterpret_cast<uint2*>(a.codes), a.sf, a.rows,
         static_cast<int>(a.cols / 8), a.rows / 128, a.meta);
     prof_end(c, K_MXQ_ROWS);
@@ -275,8 +279,7 @@ cudaError_t launch_mxq(const Ctx& c, const MxqArgs& a) {
     const int64_t want = (tiles + QC_WARPS - 1) / QC_WARPS;
     const int64_t grid = want < c.num_sms ? want : c.num_sms;
     prof_begin(c, K_MXQ_COLS);
-    mxq_cols_kernel<<<static_cast<int>(grid > 0 ? grid : 1), 32 * QC_WARPS, QC_SMEM,
-                      c.stream>>>(a.in, a.codes, a.sf, a.codes_rows, a.sf_rows, a.rows, a.rows,
+    launch_k(c.stream, mxq_cols_kernel, dim3(static_cast<int>(grid > 0 ? grid : 1)), dim3(32 * QC_WARPS), QC_SMEM, a.in, a.codes, a.sf, a.codes_rows, a.sf_rows, a.rows, a.rows,
                                   static_cast<int>(a.cols), a.meta, a.gather, a.status);
     prof_end(c, K_MXQ_COLS);
   }

@@ -26,6 +26,8 @@ __device__ __forceinline__ void set_status(DevStatus* st, int code, int detail) 
 __global__ void __launch_bounds__(ROUTE_THREADS) route_count_kernel(
     const int32_t* __restrict__ topk_idx, int R, int E, int* __restrict__ blk_counts,
     DevStatus* status) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int hist[MAX_E];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -56,6 +58,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(
     int* __restrict__ blk_counts, int nblk, int E, int pad, int* __restrict__ counts,
     int* __restrict__ offsets, int* __restrict__ pad_off, int* __restrict__ expert_order,
     int* __restrict__ tile_expert, int* __restrict__ tile_rows, int* __restrict__ meta) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int s_cnt[MAX_E];
   __shared__ int s_a[MAX_E];
   __shared__ int s_b[MAX_E];
@@ -140,6 +144,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_place_kernel(
     const int* __restrict__ blk_prefix, const int* __restrict__ offsets,
     const int* __restrict__ pad_off, int* __restrict__ perm, int* __restrict__ inv,
     int* __restrict__ prow, int* __restrict__ rowflat, float* __restrict__ w_row) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int WARPS = ROUTE_THREADS / 32;
   constexpr int PER_WARP = ROUTE_CHUNK / WARPS;  // 256
   constexpr int ROUNDS = PER_WARP / 32;          // 8
@@ -207,17 +213,17 @@ cudaError_t launch_route(const Ctx& c, const Layout& L, const int32_t* topk_idx,
   DevStatus* st = reinterpret_cast<DevStatus*>(scratch + L.status);
   int* blk = reinterpret_cast<int*>(scratch + L.blk_counts);
   prof_begin(c, K_ROUTE_COUNT);
-  route_count_kernel<<<nblk, ROUTE_THREADS, 0, c.stream>>>(topk_idx, R, E, blk, st);
+  launch_k(c.stream, route_count_kernel, dim3(nblk), dim3(ROUTE_THREADS), 0, topk_idx, R, E, blk, st);
   prof_end(c, K_ROUTE_COUNT);
   prof_begin(c, K_ROUTE_SCAN);
-  route_scan_kernel<<<1, 1024, 0, c.stream>>>(
+  launch_k(c.stream, route_scan_kernel, dim3(1), dim3(1024), 0,
       blk, nblk, E, static_cast<int>(L.pad), reinterpret_cast<int*>(saved + L.counts),
       reinterpret_cast<int*>(saved + L.offsets), reinterpret_cast<int*>(saved + L.pad_off),
       reinterpret_cast<int*>(saved + L.expert_order), reinterpret_cast<int*>(saved + L.tile_expert),
       reinterpret_cast<int*>(saved + L.tile_rows), reinterpret_cast<int*>(saved + L.meta));
   prof_end(c, K_ROUTE_SCAN);
   prof_begin(c, K_ROUTE_PLACE);
-  route_place_kernel<<<nblk, ROUTE_THREADS, 0, c.stream>>>(
+  launch_k(c.stream, route_place_kernel, dim3(nblk), dim3(ROUTE_THREADS), 0,
       topk_idx, topk_w, R, E, blk, reinterpret_cast<const int*>(saved + L.offsets),
       reinterpret_cast<const int*>(saved + L.pad_off), reinterpret_cast<int*>(saved + L.perm),
       reinterpret_cast<int*>(saved + L.inv), reinterpret_cast<int*>(saved + L.prow),
@@ -231,16 +237,16 @@ cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* 
                             const float* topk_w, const RouteBufs& b) {
   const int nblk = (R + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
   prof_begin(c, K_ROUTE_COUNT);
-  route_count_kernel<<<nblk, ROUTE_THREADS, 0, c.stream>>>(topk_idx, R, E, b.blk_counts,
+  launch_k(c.stream, route_count_kernel, dim3(nblk), dim3(ROUTE_THREADS), 0, topk_idx, R, E, b.blk_counts,
                                                            b.status);
   prof_end(c, K_ROUTE_COUNT);
   prof_begin(c, K_ROUTE_SCAN);
-  route_scan_kernel<<<1, 1024, 0, c.stream>>>(b.blk_counts, nblk, E, pad, b.counts, b.offsets,
+  launch_k(c.stream, route_scan_kernel, dim3(1), dim3(1024), 0, b.blk_counts, nblk, E, pad, b.counts, b.offsets,
                                               b.pad_off, b.expert_order, b.tile_expert,
                                               b.tile_rows, b.meta);
   prof_end(c, K_ROUTE_SCAN);
   prof_begin(c, K_ROUTE_PLACE);
-  route_place_kernel<<<nblk, ROUTE_THREADS, 0, c.stream>>>(
+  launch_k(c.stream, route_place_kernel, dim3(nblk), dim3(ROUTE_THREADS), 0,
       topk_idx, topk_w, R, E, b.blk_counts, b.offsets, b.pad_off, b.perm, b.inv, b.prow,
       b.rowflat, b.w_row);
   prof_end(c, K_ROUTE_PLACE);
@@ -343,6 +349,8 @@ __global__ void __launch_bounds__(32) permute_rows_kernel(
     const int* __restrict__ meta, const int* __restrict__ tile_rows,
     const int* __restrict__ prow, float* __restrict__ w_row, DevStatus* status,
     uint8_t* __restrict__ sf, int64_t sf_mnb) {
+  pdl_wait();
+  pdl_trigger();
   // PERM_SLOTS rows, a zero row, then (MXFP8) PERM_SLOTS rows of scale codes
   extern __shared__ __align__(128) uint8_t pbuf[];
   __shared__ __align__(8) uint64_t bar[PERM_SLOTS];
@@ -462,7 +470,7 @@ cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, v
   if (e != cudaSuccess) return e;
   const int per_sm = std::max(1, std::min(16, (200 * 1024) / (smem + 1024)));
   prof_begin(c, kernel_id);
-  kern<<<c.num_sms * per_sm, 32, smem, c.stream>>>(
+  launch_k(c.stream, kern, dim3(c.num_sms * per_sm), dim3(32), smem,
       reinterpret_cast<const uint8_t*>(src), reinterpret_cast<uint8_t*>(dst), row_bytes,
       static_cast<int>(L.T), static_cast<int>(L.k), reinterpret_cast<const int*>(saved + L.meta),
       reinterpret_cast<const int*>(saved + L.tile_rows),
@@ -499,6 +507,8 @@ __global__ void __launch_bounds__(256) slot_reduce_kernel(
     const uint4* __restrict__ rows, uint4* __restrict__ out, int T, int k, int H8,
     const int* __restrict__ prow, const float* __restrict__ pw, int n_pw,
     float* __restrict__ dtopk_w) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
@@ -531,7 +541,7 @@ __global__ void __launch_bounds__(256) slot_reduce_kernel(
 cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
                            const char* saved, uint16_t* out) {
   prof_begin(c, K_COMBINE);
-  slot_reduce_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(
+  launch_k(c.stream, slot_reduce_kernel, dim3(c.num_sms * 8), dim3(256), 0,
       reinterpret_cast<const uint4*>(slots), reinterpret_cast<uint4*>(out),
       static_cast<int>(L.T), static_cast<int>(L.k), static_cast<int>(L.H / 8),
       reinterpret_cast<const int*>(saved + L.prow), nullptr, 0, nullptr);
@@ -542,7 +552,7 @@ cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
 cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slots,
                              const char* saved, const float* pw, uint16_t* dx, float* dtopk_w) {
   prof_begin(c, K_UNPERMUTE);
-  slot_reduce_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(
+  launch_k(c.stream, slot_reduce_kernel, dim3(c.num_sms * 8), dim3(256), 0,
       reinterpret_cast<const uint4*>(slots), reinterpret_cast<uint4*>(dx), static_cast<int>(L.T),
       static_cast<int>(L.k), static_cast<int>(L.H / 8),
       reinterpret_cast<const int*>(saved + L.prow), pw, static_cast<int>(L.n_pw), dtopk_w);

@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
                                                           int64_t T, int E, int k,
                                                           int32_t* __restrict__ topk_idx,
                                                           float* __restrict__ topk_w) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;  // whole warps leave together
@@ -95,6 +97,8 @@ __global__ void __launch_bounds__(256) router_dlogits_kernel(const int32_t* __re
                                                              const float* __restrict__ dtopk_w,
                                                              int64_t T, int E, int k,
                                                              __nv_bfloat16* __restrict__ dlogits) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
@@ -143,14 +147,14 @@ template <int PL>
 static void launch_topk(cudaStream_t st, const float* logits, int64_t T, int E, int k,
                         int32_t* idx, float* w) {
   const int64_t blocks = (T * 32 + 255) / 256;
-  router_topk_kernel<PL><<<static_cast<unsigned>(blocks), 256, 0, st>>>(logits, T, E, k, idx, w);
+  launch_k(st, router_topk_kernel<PL>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, logits, T, E, k, idx, w);
 }
 
 template <int PL>
 static void launch_dlogits(cudaStream_t st, const int32_t* idx, const float* w, const float* g,
                            int64_t T, int E, int k, __nv_bfloat16* dl) {
   const int64_t blocks = (T * 32 + 255) / 256;
-  router_dlogits_kernel<PL><<<static_cast<unsigned>(blocks), 256, 0, st>>>(idx, w, g, T, E, k, dl);
+  launch_k(st, router_dlogits_kernel<PL>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, idx, w, g, T, E, k, dl);
 }
 
 }  // namespace mmmoe
