@@ -57,9 +57,11 @@ cudaError_t run_bf16(const Ctx& c, const GemmParams& p, int kind, int bn, int ct
 
 }  // namespace gemm
 
-// Dense products on single-SM 128 x 128 tiles (bf16 in, fp32 accumulation); the tensor
-// maps cover exactly M, N, K, so ragged tiles read zeros past the edges and the bf16
-// stores are clipped there (the fp32 epilogue masks them).
+// Dense products on single-SM 128 x 128 tiles, 128 x 64 for A^T.B (its output, E x H for
+// the router's weight gradient, has few tiles and a long K: narrower tiles double the
+// SMs at work), bf16 in, fp32 accumulation; the tensor maps cover exactly M, N, K, so
+// ragged tiles read zeros past the edges and the bf16 stores are clipped there (the
+// fp32 epilogue masks them).
 cudaError_t launch_dense(const Ctx& c, int kind, const uint16_t* A, const uint16_t* B, void* C,
                          int64_t M, int64_t N, int64_t K) {
   using namespace gemm;
@@ -69,7 +71,7 @@ cudaError_t launch_dense(const Ctx& c, int kind, const uint16_t* A, const uint16
   if (M < 1 || N < 1 || K < 1 || !inner_ok || M >= (int64_t{1} << 31) ||
       N >= (int64_t{1} << 31) || K >= (int64_t{1} << 31))
     return cudaErrorInvalidValue;
-  constexpr int BN = 128;
+  const int BN = kind == GEMM_DENSE_TN ? 64 : 128;
   GemmParams p;
   memset(&p, 0, sizeof(p));
   p.dm = static_cast<int>(M);
@@ -81,7 +83,7 @@ cudaError_t launch_dense(const Ctx& c, int kind, const uint16_t* A, const uint16
   bool ok = false;
   switch (kind) {
     case GEMM_DENSE_NT:  // A [M, K], B [N, K], C [M, N] fp32
-      ok = make_map(&p.tmA, A, k, m, 64, BM) && make_map(&p.tmB0, B, k, n, 64, BN);
+      ok = make_map(&p.tmA, A, k, m, 64, BM) && make_map(&p.tmB0, B, k, n, 64, 128);
       p.outf = static_cast<float*>(C);
       break;
     case GEMM_DENSE_NN:  // A [M, K], B [K, N], C [M, N] bf16 (read and written)
@@ -98,9 +100,9 @@ cudaError_t launch_dense(const Ctx& c, int kind, const uint16_t* A, const uint16
   if (!ok) return cudaErrorInvalidValue;
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
   switch (kind) {
-    case GEMM_DENSE_NT: return run<GEMM_DENSE_NT, BN, 1, false>(c, p, tiles);
-    case GEMM_DENSE_NN: return run<GEMM_DENSE_NN, BN, 1, false>(c, p, tiles);
-    default: return run<GEMM_DENSE_TN, BN, 1, false>(c, p, tiles);
+    case GEMM_DENSE_NT: return run<GEMM_DENSE_NT, 128, 1, false>(c, p, tiles);
+    case GEMM_DENSE_NN: return run<GEMM_DENSE_NN, 128, 1, false>(c, p, tiles);
+    default: return run<GEMM_DENSE_TN, 64, 1, false>(c, p, tiles);
   }
 }
 

@@ -137,7 +137,7 @@ struct Cfg {
   static constexpr bool EARLY_RELEASE = SPLIT;
   static constexpr int EPI_WARPS = SPLIT ? 8 : 4;
   static constexpr int THREADS = 128 + 32 * EPI_WARPS;
-  static constexpr int EPI_IN = KIND == GEMM_DGRAD_DOWN ? 3 : KIND == GEMM_DENSE_NN ? 1 : 0;
+  static constexpr int EPI_IN = KIND == GEMM_DGRAD_DOWN ? 3 : KIND == GEMM_DENSE_NN ? BN / 32 : 0;
   // (SPLIT: one output block per warp, which leaves room for a sixth pipeline stage,
   // two in the dSwiGLU epilogue, where they fit beside its four stages; a warp's
   // next block waits for the store before last to have read it)
@@ -395,6 +395,20 @@ __device__ __forceinline__ void load_inputs(EpiWarp& w, const GemmParams& p, int
   w.ld_pending = true;
 }
 
+// C += A.B: the warp's BN / 32 blocks of C (rows row0..row0+31 from column n0) in one
+// go, before the tile's accumulator is ready.
+template <int BN>
+__device__ __forceinline__ void load_c_blocks(EpiWarp& w, const GemmParams& p, int row0, int n0) {
+  if (w.lane == 0) {
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive_expect_tx(w.ld_bar, BN / 32 * 2048);
+#pragma unroll
+    for (int j = 0; j < BN / 32; ++j)
+      ptx::tma_load_2d(w.in + j * 2048, &p.tmD0, w.ld_bar, n0 + 32 * j, row0);
+  }
+  w.ld_pending = true;
+}
+
 __device__ __forceinline__ bool wait_inputs(EpiWarp& w, volatile int* abort) {
   int ok = 1;
   if (w.lane == 0) ok = ptx::mbar_wait(w.ld_bar, w.ld_phase, abort, WAIT_LIMIT_NS) ? 1 : 0;
@@ -519,20 +533,19 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInf
       }
     }
   } else if constexpr (KIND == GEMM_DENSE_NN) {
-    // C += A.B: each 32 x 32 block of C comes in by TMA, takes the sum in fp32 and
+    // C += A.B: the warp's blocks of C came in by TMA ahead of the accumulator (the
+    // next tile's are requested once these are read); each takes the sum in fp32 and
     // goes back rounded to bf16 (TMA clips the blocks at the output's edges)
+    if (!w.ld_pending) load_c_blocks<BN>(w, p, row0, ti.n0);
+    if (!wait_inputs(w, abort)) return false;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
-      if (lane == 0) {
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive_expect_tx(w.ld_bar, 2048);
-        ptx::tma_load_2d(w.in, &p.tmD0, w.ld_bar, ti.n0 + c, row0);
-      }
-      w.ld_pending = true;
-      if (!wait_inputs(w, abort)) return false;
       float old[32];
-      unstage32(w.in, lane, old);
-      __syncwarp();
+      unstage32(w.in + (c / 32) * 2048, lane, old);
+      if (c + 32 == BN) {
+        __syncwarp();
+        if (next != nullptr) load_c_blocks<BN>(w, p, next->m0 + q * 32, next->n0);
+      }
       uint32_t rr[32];
       ptx::tmem_ld32(tbase + c, rr);
       ptx::tmem_wait_ld(rr);
@@ -1160,6 +1173,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
       if (has_next) nx = decode_tile<KIND, BN, CTAS, FP8>(p, t + n_clusters, rank);
       if (KIND == GEMM_DGRAD_DOWN && !w.ld_pending)
         load_inputs(w, p, ti.m0 + q * 32, ti.n0 + (C::SPLIT ? hh * (BN / 2) : 0));
+      if (KIND == GEMM_DENSE_NN && !w.ld_pending) load_c_blocks<BN>(w, p, ti.m0 + q * 32, ti.n0);
       int ok = 1;
       if (lane == 0)
         ok = ptx::mbar_wait_spin(&tfull_bar[acc], acc_phase, abort, WAIT_LIMIT_NS) ? 1 : 0;
@@ -1305,8 +1319,8 @@ static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) 
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CTAS), 1, 1);
   static constexpr int kId[10] = {K_GEMM_GATEUP,       K_GEMM_DOWN,       K_GEMM_DGRAD_DOWN,
                                   K_GEMM_DGRAD_GATEUP, K_GEMM_WGRAD_DOWN, K_GEMM_WGRAD_GATEUP,
-                                  K_GEMM_WGRAD,        K_DENSE_GEMM,      K_DENSE_GEMM,
-                                  K_DENSE_GEMM};
+                                  K_GEMM_WGRAD,        K_DENSE_NT,        K_DENSE_NN,
+                                  K_DENSE_TN};
   prof_begin(c, kId[KIND]);
   e = cudaLaunchKernelEx(&cfg, kern, p);
   prof_end(c, kId[KIND]);

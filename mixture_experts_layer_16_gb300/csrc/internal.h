@@ -137,7 +137,11 @@ enum KernelId {
   K_FB_TILES,
   K_MXQ_ROWS,
   K_MXQ_COLS,
-  K_DENSE_GEMM,
+  K_DENSE_NT,
+  K_DENSE_NN,
+  K_DENSE_TN,
+  K_ROUTER_TOPK,
+  K_ROUTER_DLOGITS,
   K_COUNT
 };
 

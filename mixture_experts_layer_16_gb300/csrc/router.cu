@@ -144,17 +144,23 @@ static bool device_ok(int* sms) {
 }
 
 template <int PL>
-static void launch_topk(cudaStream_t st, const float* logits, int64_t T, int E, int k,
+static void launch_topk(const Ctx& c, const float* logits, int64_t T, int E, int k,
                         int32_t* idx, float* w) {
   const int64_t blocks = (T * 32 + 255) / 256;
-  launch_k(st, router_topk_kernel<PL>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, logits, T, E, k, idx, w);
+  prof_begin(c, K_ROUTER_TOPK);
+  launch_k(c.stream, router_topk_kernel<PL>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+           logits, T, E, k, idx, w);
+  prof_end(c, K_ROUTER_TOPK);
 }
 
 template <int PL>
-static void launch_dlogits(cudaStream_t st, const int32_t* idx, const float* w, const float* g,
+static void launch_dlogits(const Ctx& c, const int32_t* idx, const float* w, const float* g,
                            int64_t T, int E, int k, __nv_bfloat16* dl) {
   const int64_t blocks = (T * 32 + 255) / 256;
-  launch_k(st, router_dlogits_kernel<PL>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, idx, w, g, T, E, k, dl);
+  prof_begin(c, K_ROUTER_DLOGITS);
+  launch_k(c.stream, router_dlogits_kernel<PL>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+           idx, w, g, T, E, k, dl);
+  prof_end(c, K_ROUTER_DLOGITS);
 }
 
 }  // namespace mmmoe
@@ -184,11 +190,11 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_router_forward(const mm_moe_shape* sh
   if (launch_dense(c, GEMM_DENSE_NT, x, W_router, logits, T, E, H) != cudaSuccess)
     return MM_MOE_ECUDA;
   if (E <= 128)
-    launch_topk<4>(st, logits, T, E, k, topk_idx, topk_w);
+    launch_topk<4>(c, logits, T, E, k, topk_idx, topk_w);
   else if (E <= 256)
-    launch_topk<8>(st, logits, T, E, k, topk_idx, topk_w);
+    launch_topk<8>(c, logits, T, E, k, topk_idx, topk_w);
   else
-    launch_topk<32>(st, logits, T, E, k, topk_idx, topk_w);
+    launch_topk<32>(c, logits, T, E, k, topk_idx, topk_w);
   return cudaGetLastError() == cudaSuccess ? MM_MOE_OK : MM_MOE_ECUDA;
 }
 
@@ -209,11 +215,11 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_router_backward(
   const Ctx c{st, sms, &launches};
   __nv_bfloat16* dl = reinterpret_cast<__nv_bfloat16*>(dlogits);
   if (E <= 128)
-    launch_dlogits<4>(st, topk_idx, topk_w, dtopk_w, T, E, k, dl);
+    launch_dlogits<4>(c, topk_idx, topk_w, dtopk_w, T, E, k, dl);
   else if (E <= 256)
-    launch_dlogits<8>(st, topk_idx, topk_w, dtopk_w, T, E, k, dl);
+    launch_dlogits<8>(c, topk_idx, topk_w, dtopk_w, T, E, k, dl);
   else
-    launch_dlogits<32>(st, topk_idx, topk_w, dtopk_w, T, E, k, dl);
+    launch_dlogits<32>(c, topk_idx, topk_w, dtopk_w, T, E, k, dl);
   if (cudaGetLastError() != cudaSuccess) return MM_MOE_ECUDA;
   // dW_router [E, H] = dlogits [T, E]^T . x [T, H]
   if (launch_dense(c, GEMM_DENSE_TN, dlogits, x, dW_router, E, H, T) != cudaSuccess)
