@@ -40,7 +40,7 @@ BWD_GEMMS = ("gemm_dgrad_down_dswiglu", "gemm_dgrad_gateup", "gemm_wgrad_down",
              "gemm_wgrad_gateup", "gemm_wgrad")
 # the arithmetic each precision's GEMMs compute in
 DTYPE = {"bf16": "bf16", "mxfp8": "mxfp8", "fp8_bwd": "bf16 fwd / mxfp8 bwd",
-         "fp8_block": "fp8_block on bf16 tensor cores"}
+         "fp8_block": "fp8_block (e4m3, 128-block scales)"}
 
 
 def parse_args():
@@ -541,7 +541,7 @@ def run_ours(args):
     bpeak = peaks.get(pkey, FALLBACK_PEAKS[pkey])
     # a contraction takes the peak of its own dtype: FP8 = the bf16 peak x 2 (nominal
     # 4.5 / 2.25 PFLOP/s)
-    dom_fp8 = cfg.prec == "mxfp8" or (cfg.prec == "fp8_bwd" and dom in BWD_GEMMS)
+    dom_fp8 = cfg.prec in ("mxfp8", "fp8_block") or (cfg.prec == "fp8_bwd" and dom in BWD_GEMMS)
     peak = bpeak * (2.0 if dom_fp8 else 1.0)
     achieved = gemms[dom]["tflops"]
     roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
@@ -567,14 +567,15 @@ def run_ours(args):
     # measured bf16 peak of the clock regime the timed region ran in (burst: the
     # region held the maximum SM clock with no power cap; else sustained).  FP8 peak =
     # that bf16 peak x 2 (nominal 4.5 / 2.25 PFLOP/s); fp8_bwd blends the two, total
-    # FLOP / (fwd FLOP / P_bf16 + bwd FLOP / P_fp8).  Blockwise FP8 runs on the bf16
-    # tensor cores (operands on the FP8 grid), so its peak is the bf16 one.
+    # FLOP / (fwd FLOP / P_bf16 + bwd FLOP / P_fp8).  Blockwise FP8 runs on the same
+    # block-scaled FP8 tensor cores as MXFP8 (its 128-block scales repeated over the
+    # 32-element scale blocks), so its peak is the FP8 one throughout.
     r_f = 2.0 * cfg.T * cfg.E * cfg.H if router is not None else 0.0  # router products
     f_fwd, f_bwd = cfg.flops_fwd() + r_f, cfg.flops_bwd() + 2.0 * r_f
 
     def fractions(bp):
-        p_fwd = 2.0 * bp if cfg.prec == "mxfp8" else bp
-        p_bwd = 2.0 * bp if cfg.prec in ("mxfp8", "fp8_bwd") else bp
+        p_fwd = 2.0 * bp if cfg.prec in ("mxfp8", "fp8_block") else bp
+        p_bwd = 2.0 * bp if cfg.prec in ("mxfp8", "fp8_bwd", "fp8_block") else bp
         p_tot = (f_fwd + f_bwd) / (f_fwd / p_fwd + f_bwd / p_bwd)
         return {"fwd": fwd_tf / p_fwd, "bwd": bwd_tf / p_bwd, "step": value / world / p_tot,
                 "peak_fwd_tflops": p_fwd, "peak_bwd_tflops": p_bwd}

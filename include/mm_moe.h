@@ -69,7 +69,9 @@ extern "C" {
  *                   activations in 128-element blocks along each GEMM's K (128-row
  *                   token blocks for the weight gradients), weights in 128 x 128
  *                   blocks, one power-of-two scale 2^ceil(log2(amax / 448)) per
- *                   block, e4m3 elements; needs I % 128 == 0.
+ *                   block, e4m3 elements, multiplied on the block-scaled FP8 tensor
+ *                   cores like MXFP8 (each block's scale repeated over its 32-element
+ *                   scale blocks); fp32 accumulation; needs I % 128 == 0.
  * Stored tensors (h, a, the outputs and the gradients) stay bf16 in every mode,
  * and the quantised operand copies live in `scratch` (which is larger for the
  * quantised modes). */
@@ -256,6 +258,25 @@ MM_MOE_API mm_moe_status mm_moe_mx_quantize(const uint16_t* in, uint8_t* codes,
 MM_MOE_API mm_moe_status mm_moe_fp8_block_qdq(const uint16_t* in, uint16_t* out,
                                               int64_t rows, int64_t cols, int layout,
                                               void* stream);
+
+/* Blockwise FP8 quantisation of a bf16 matrix into the form MM_MOE_FP8_BLOCK's GEMMs
+ * read on the block-scaled tensor cores: e4m3 codes and E8M0 scale codes (2^e stored
+ * as e + 127), with the block rule of mm_moe_fp8_block_qdq (the pages' Hopper
+ * precision, section "How does the fused kernel work?"), each 128-element block's
+ * scale code repeated over its four 32-element scale blocks; exported for callers
+ * that keep such copies of their own tensors.
+ *   in      [rows, cols] bf16 device; rows % 128 == 0, cols % 128 == 0
+ *   codes   [rows, cols] uint8 device out: the e4m3 code of each element
+ *   scales  uint8 device out, in the atom arrangement of mm_moe_mx_quantize: layout 0
+ *           rows * cols / 32 bytes, the matrix rows as the operand rows; layout 1 the
+ *           same size, the columns as the operand rows; layout 2 twice that, first the
+ *           rows then the columns as the operand rows (the codes serve both)
+ *   layout  0: 128-element blocks along each row; 1: blocks of 128 rows down each
+ *           column; 2: 128 x 128 tiles
+ * All pointers 16-byte aligned.  Errors as for mm_moe_mx_qdq. */
+MM_MOE_API mm_moe_status mm_moe_fp8_block_quantize(const uint16_t* in, uint8_t* codes,
+                                                   uint8_t* scales, int64_t rows, int64_t cols,
+                                                   int layout, void* stream);
 
 /* Synchronises `stream`, then returns the device status word of `scratch`
  * (MM_MOE_OK, MM_MOE_EBADIDX or MM_MOE_ETIMEOUT), or MM_MOE_ECUDA when the

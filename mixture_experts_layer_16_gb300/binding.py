@@ -25,7 +25,8 @@ EXPORTS = ("mm_moe_workspace_size", "mm_moe_forward", "mm_moe_backward", "mm_moe
            "mm_moe_read_status", "mm_moe_last_launch_count", "mm_moe_profile_start",
            "mm_moe_profile_stop", "mm_moe_kernel_name", "mm_moe_kernel_count",
            "mm_moe_route_noalloc", "mm_moe_mx_qdq", "mm_moe_router_forward",
-           "mm_moe_router_backward", "mm_moe_fp8_block_qdq", "mm_moe_mx_quantize")
+           "mm_moe_router_backward", "mm_moe_fp8_block_qdq", "mm_moe_mx_quantize",
+           "mm_moe_fp8_block_quantize")
 
 
 class MoEError(RuntimeError):
@@ -80,6 +81,8 @@ def lib() -> ctypes.CDLL:
                                            _vp]
         L.mm_moe_mx_quantize.argtypes = [_vp, _vp, _vp, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_int, _vp]
+        L.mm_moe_fp8_block_quantize.argtypes = [_vp, _vp, _vp, ctypes.c_int64, ctypes.c_int64,
+                                                ctypes.c_int, _vp]
         L.mm_moe_router_forward.argtypes = [sp] + [_vp] * 6
         L.mm_moe_router_backward.argtypes = [sp] + [_vp] * 9
         for fn in EXPORTS:
@@ -186,6 +189,24 @@ def mm_moe_mx_quantize(inp, codes, scales, axis: int, stream=None) -> None:
         raise ValueError("scales must hold rows * cols / 32 uint8")
     _check("mm_moe_mx_quantize", lib().mm_moe_mx_quantize(
         _ptr(inp), _ptr(codes), _ptr(scales), inp.shape[0], inp.shape[1], int(axis),
+        _stream(stream)))
+
+
+def mm_moe_fp8_block_quantize(inp, codes, scales, layout: int, stream=None) -> None:
+    """Blockwise FP8 quantisation of a 2-D bf16 CUDA tensor [rows, cols] (multiples of
+    128) into e4m3 codes (uint8, same shape) and E8M0 scales (uint8, in the block-scaled
+    tensor cores' atom arrangement; rows * cols / 32 bytes, twice that for tiles):
+    128-element blocks along rows (layout 0), down columns (1), or 128 x 128 tiles (2)."""
+    import torch
+    if inp.dim() != 2 or inp.dtype != torch.bfloat16 or not inp.is_contiguous():
+        raise ValueError("inp must be a contiguous 2-D bf16 tensor")
+    if codes.shape != inp.shape or codes.dtype != torch.uint8 or not codes.is_contiguous():
+        raise ValueError("codes must be a contiguous uint8 tensor of inp's shape")
+    n = inp.numel() // 32 * (2 if int(layout) == 2 else 1)
+    if scales.dtype != torch.uint8 or scales.numel() != n:
+        raise ValueError("scales must hold rows * cols / 32 uint8 (twice that for tiles)")
+    _check("mm_moe_fp8_block_quantize", lib().mm_moe_fp8_block_quantize(
+        _ptr(inp), _ptr(codes), _ptr(scales), inp.shape[0], inp.shape[1], int(layout),
         _stream(stream)))
 
 

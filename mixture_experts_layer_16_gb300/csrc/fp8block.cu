@@ -1,4 +1,4 @@
-// fp8block.cu -- blockwise FP8 quantise-dequantise of GEMM operands.
+// fp8block.cu -- blockwise FP8 quantisation of GEMM operands.
 //
 // Prime Mega MoE pages, "How does the fused kernel work?": blockwise FP8 is the Hopper
 // low-precision type of the fused kernel.  Here it takes the form Blackwell tensor
@@ -6,8 +6,9 @@
 // axis (128 rows along the token axis for the weight gradients), weights in 128 x 128
 // blocks, one power-of-two scale per block, 2^ceil(log2(amax / 448)) -- the smallest
 // that keeps every element within E4M3's +-448 -- and elements rounded to E4M3 (nearest
-// even).  As for MXFP8 the dequantised values e4m3 * scale are written as bf16, which
-// holds them exactly, so the bf16 tensor-core GEMMs compute the FP8 products.
+// even).  The layer's GEMMs read e4m3 codes and E8M0 scale codes (the fbq_* kernels) on
+// the block-scaled tensor cores; the fb_* kernels write the dequantised values
+// e4m3 * scale as bf16, which holds them exactly (mm_moe_fp8_block_qdq).
 #include <cuda_runtime.h>
 
 #include "fp8block.cuh"
@@ -17,6 +18,7 @@
 namespace mmmoe {
 
 using mx::bf;
+using mx::codes4;
 using mx::qdq2;
 using mx::to_bf;
 using fb::ceil_exp;
@@ -182,6 +184,210 @@ __global__ void __launch_bounds__(256) fb_tiles_kernel(const uint4* in, uint4* o
   }
 }
 
+// ---------------------------------------------------------------- codes and scales
+// The same blocks in the form the block-scaled tensor cores read (the GEMMs' MXFP8
+// instantiations): e4m3 codes, one byte per element in the operand's own [rows, C]
+// layout, and E8M0 scale codes in the atom arrangement of mx::sf_offset.  A 128-element
+// block is four 32-element scale blocks with the same scale, i.e. one 32-bit word of
+// four equal codes (along the rows: the word of the row and 128-column block; down the
+// columns: the word of the column and 128-row block).
+__device__ __forceinline__ uint2 codes8(const uint4 w, float m) {
+  return make_uint2(mx::codes4(w.x, w.y, m, m, m, m), mx::codes4(w.z, w.w, m, m, m, m));
+}
+__device__ __forceinline__ uint2 codes8c(const uint4 w, const float (&m)[8]) {
+  return make_uint2(mx::codes4(w.x, w.y, m[0], m[1], m[2], m[3]),
+                    mx::codes4(w.z, w.w, m[4], m[5], m[6], m[7]));
+}
+__device__ __forceinline__ uint32_t sf_word(int e) { return mx::e8m0(e) * 0x01010101u; }
+
+// Blocks of 128 consecutive elements of each row ([rows, C], C % 128 == 0): a thread
+// takes 8 elements, 16 neighbouring lanes one block; the block's first lane writes its
+// scale word (row, 128-column block) over mnb = rows / 128 row blocks.
+__global__ void __launch_bounds__(256) fbq_rows_kernel(const uint4* in, uint2* codes, uint8_t* sf,
+                                                       int64_t rows, int C8, int64_t mnb,
+                                                       const int* __restrict__ meta) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t n = used(rows, meta) * C8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // every lane of a warp runs the same iterations (shuffles)
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x; i0 < n; i0 += stride) {
+    const int64_t i = i0 + threadIdx.x;
+    const uint4 w = i < n ? in[i] : make_uint4(0, 0, 0, 0);
+    float m = amax8(w);
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const int e = ceil_exp(m);
+    if (i < n) {
+      codes[i] = codes8(w, mx::pow2f(-e));
+      if ((i & 15) == 0) {
+        const int64_t row = i / C8;
+        const int col = static_cast<int>(i - row * C8) * 8;
+        *reinterpret_cast<uint32_t*>(sf + mx::sf_offset(row, col / 32, mnb)) = sf_word(e);
+      }
+    }
+  }
+}
+
+// Blocks of 128 consecutive rows of each column ([rows, C], rows % 128 == 0, C % 8 == 0),
+// as fb_cols_kernel (two passes over 128 x 512 tiles, the second from L2): codes to
+// `codes` and the scale words (column, 128-row block) over C / 128 column blocks to
+// `sf`; with codes_rows non-null also the blocks along the rows (C % 128 == 0), scale
+// words over rows_total / 128 row blocks to sf_rows.  With a gather the rows come from
+// a token-major `in` (padding rows read as zeros).
+__global__ void __launch_bounds__(256) fbq_cols_kernel(const uint4* in, uint2* codes, uint8_t* sf,
+                                                       uint2* codes_rows, uint8_t* sf_rows,
+                                                       int64_t rows, int C8,
+                                                       const int* __restrict__ meta,
+                                                       const RowGather gather) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float part[4][FB_TILE];
+  __shared__ int src_row[FB];
+  const int64_t R = used(rows, meta);
+  const int col_tiles = (C8 * 8 + FB_TILE - 1) / FB_TILE;
+  const int64_t tiles = (R / FB) * col_tiles;
+  const int64_t mnb_cols = C8 / 16, mnb_rows = rows / FB;
+  const int cg = threadIdx.x % 64, rs = threadIdx.x / 64;
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int64_t rb = tile / col_tiles;
+    const int c8 = static_cast<int>(tile - rb * col_tiles) * (FB_TILE / 8) + cg;
+    const bool active = c8 < C8;
+    const int64_t base = rb * FB * C8 + c8;
+    __syncthreads();  // the previous tile's second pass has read src_row[]
+    if (threadIdx.x < FB) src_row[threadIdx.x] = gather_src(rb * FB + threadIdx.x, gather);
+    __syncthreads();
+    float m[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m[j] = 0.f;
+    if (active) {
+#pragma unroll 8
+      for (int r = 0; r < FB / 4; ++r) {
+        const int sr = src_row[rs + 4 * r];
+        const uint4 w = sr >= 0 ? in[static_cast<int64_t>(sr) * C8 + c8] : make_uint4(0, 0, 0, 0);
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m[j] = fmaxf(m[j], fabsf(bf(h[j])));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) part[rs][cg * 8 + j] = m[j];
+    __syncthreads();
+    int e[8];
+    float mul[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = cg * 8 + j;
+      e[j] = ceil_exp(fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c])));
+      mul[j] = mx::pow2f(-e[j]);
+    }
+    __syncthreads();  // part[] is rewritten by the next tile
+    if (active && rs == 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint32_t*>(sf + mx::sf_offset(c8 * 8 + j, 4 * rb, mnb_cols)) =
+            sf_word(e[j]);
+    }
+#pragma unroll 4
+    for (int r = 0; r < FB / 4; ++r) {
+      const int64_t at = base + static_cast<int64_t>(rs + 4 * r) * C8;
+      const int sr = src_row[rs + 4 * r];
+      const uint4 w = active && sr >= 0 ? in[static_cast<int64_t>(sr) * C8 + c8]
+                                        : make_uint4(0, 0, 0, 0);
+      if (codes_rows != nullptr) {  // uniform: every lane takes part in the shuffles
+        float rm = amax8(w);
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1)
+          rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, off));
+        const int re = ceil_exp(rm);
+        if (active) {
+          codes_rows[at] = codes8(w, mx::pow2f(-re));
+          if ((cg & 15) == 0)
+            *reinterpret_cast<uint32_t*>(
+                sf_rows + mx::sf_offset(rb * FB + rs + 4 * r, c8 / 4, mnb_rows)) = sf_word(re);
+        }
+      }
+      if (active) codes[at] = codes8c(w, mul);
+    }
+  }
+}
+
+// 128 x 128 tiles of a weight matrix [rows, C] (rows % 128 == 0, C % 128 == 0), one CTA
+// per tile: the codes (one copy, whichever axis a GEMM contracts) and the tile's scale in
+// both arrangements, each one whole 512-byte atom of equal codes: sf_k for the GEMMs
+// that contract the columns (MMA rows = the matrix rows, rows / 128 row blocks), sf_mn
+// for those that contract the rows (MMA rows = the columns, C / 128 column blocks).
+__global__ void __launch_bounds__(256) fbq_tiles_kernel(const uint4* in, uint2* codes,
+                                                        uint8_t* sf_k, uint8_t* sf_mn,
+                                                        int64_t rows, int C8) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float wmax[8];
+  const int col_tiles = C8 / (FB / 8);
+  const int64_t tiles = (rows / FB) * col_tiles;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cq = threadIdx.x % 16, rq = threadIdx.x / 16;
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int64_t rb = tile / col_tiles;
+    const int cb = static_cast<int>(tile - rb * col_tiles);
+    const int64_t base = rb * FB * C8 + cb * (FB / 8) + cq;
+    uint4 w[8];
+    float m = 0.f;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      w[p] = in[base + static_cast<int64_t>(rq + 16 * p) * C8];
+      m = fmaxf(m, amax8(w[p]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) wmax[warp] = m;
+    __syncthreads();
+    float t = wmax[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) t = fmaxf(t, wmax[q]);
+    __syncthreads();  // wmax[] is rewritten by the next tile
+    const int e = ceil_exp(t);
+    const float mul = mx::pow2f(-e);
+#pragma unroll
+    for (int p = 0; p < 8; ++p) codes[base + static_cast<int64_t>(rq + 16 * p) * C8] = codes8(w[p], mul);
+    const uint32_t word = sf_word(e);
+    if (threadIdx.x < 64) {  // 32 x 16 bytes per atom
+      uint8_t* atom = threadIdx.x < 32 ? sf_k + (static_cast<int64_t>(cb) * (rows / FB) + rb) * 512
+                                       : sf_mn + (rb * (C8 / 16) + cb) * 512;
+      reinterpret_cast<uint4*>(atom)[threadIdx.x & 31] = make_uint4(word, word, word, word);
+    }
+  }
+}
+
+cudaError_t launch_fbq(const Ctx& c, const FbqArgs& a) {
+  const int C8 = static_cast<int>(a.cols / 8);
+  const uint4* i4 = reinterpret_cast<const uint4*>(a.in);
+  uint2* c2 = reinterpret_cast<uint2*>(a.codes);
+  if (a.layout == FB_ROWS) {
+    prof_begin(c, K_FBQ_ROWS);
+    launch_k(c.stream, fbq_rows_kernel, dim3(c.num_sms * 8), dim3(256), 0, i4, c2, a.sf, a.rows,
+             C8, a.rows / FB, a.meta);
+    prof_end(c, K_FBQ_ROWS);
+  } else if (a.layout == FB_COLS) {
+    const int64_t tiles = (a.rows / FB) * ((a.cols + FB_TILE - 1) / FB_TILE);
+    const int64_t cap = static_cast<int64_t>(c.num_sms) * 4;
+    const int grid = static_cast<int>(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
+    prof_begin(c, K_FBQ_COLS);
+    launch_k(c.stream, fbq_cols_kernel, dim3(grid), dim3(256), 0, i4, c2, a.sf,
+             reinterpret_cast<uint2*>(a.codes_rows), a.sf_rows, a.rows, C8, a.meta, a.gather);
+    prof_end(c, K_FBQ_COLS);
+  } else {
+    const int64_t tiles = (a.rows / FB) * (a.cols / FB);
+    const int64_t cap = static_cast<int64_t>(c.num_sms) * 8;
+    const int grid = static_cast<int>(tiles < cap ? (tiles > 0 ? tiles : 1) : cap);
+    prof_begin(c, K_FBQ_TILES);
+    launch_k(c.stream, fbq_tiles_kernel, dim3(grid), dim3(256), 0, i4, c2, a.sf, a.sf_mn, a.rows,
+             C8);
+    prof_end(c, K_FBQ_TILES);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fb_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
                           int64_t cols, int layout, const int* meta, uint16_t* out_rows,
                           RowGather gather) {
@@ -237,5 +443,38 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_fp8_block_qdq(const uint16_t* in, uin
   const Ctx c{static_cast<cudaStream_t>(stream), sms, &launches};
   if (launch_fb_qdq(c, in, out, rows, cols, layout, nullptr, nullptr) != cudaSuccess)
     return MM_MOE_ECUDA;
+  return MM_MOE_OK;
+}
+
+extern "C" MM_MOE_API mm_moe_status mm_moe_fp8_block_quantize(const uint16_t* in, uint8_t* codes,
+                                                              uint8_t* scales, int64_t rows,
+                                                              int64_t cols, int layout,
+                                                              void* stream) {
+  if (in == nullptr || codes == nullptr || scales == nullptr || rows < 1 || cols < 1)
+    return MM_MOE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(codes) |
+       reinterpret_cast<uintptr_t>(scales)) % 16 != 0)
+    return MM_MOE_EINVAL;
+  if (rows % FB != 0 || cols % FB != 0 || layout < FB_ROWS || layout > FB_TILES)
+    return MM_MOE_EINVAL;
+  if (rows > (int64_t{1} << 40) / cols) return MM_MOE_EINVAL;
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MM_MOE_ECUDA;
+  if (major != 10 || minor != 3) return MM_MOE_ENOTSUP;
+  int launches = 0;
+  const Ctx c{static_cast<cudaStream_t>(stream), sms, &launches};
+  FbqArgs a{};
+  a.in = in;
+  a.codes = codes;
+  a.sf = scales;
+  a.sf_mn = scales + rows * cols / 32;
+  a.rows = rows;
+  a.cols = cols;
+  a.layout = layout;
+  if (launch_fbq(c, a) != cudaSuccess) return MM_MOE_ECUDA;
   return MM_MOE_OK;
 }

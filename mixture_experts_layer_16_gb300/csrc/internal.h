@@ -40,15 +40,16 @@ struct Layout {
       tile_rows, w_row, x_perm, h, a, saved_bytes;
   // scratch
   size_t status, blk_counts, ys, dy_perm, dh, a_w, pw, dxs, scratch_bytes;
-  // scratch, quantised operand copies (set only for the precisions that use them;
-  // MXFP8: e4m3 codes [rows, cols] followed by their E8M0 scales, rows * cols / 32
-  // bytes in the mx::sf_offset arrangement; blockwise FP8: bf16 dequantised values):
+  // scratch, quantised operand copies (set only for the precisions that use them):
+  // e4m3 codes [rows, cols] followed by their E8M0 scales, rows * cols / 32 bytes in
+  // the mx::sf_offset arrangement (blockwise FP8 weights: the scales in both
+  // arrangements, rows as the MMA rows first):
   // forward, blocks along K: x_perm, a, W_gate, W_up, W_down
   size_t q_x, q_a, q_wg, q_wu, q_wd;
-  // backward: W_down along H and W_gate, W_up along I (q_wdc, q_wgc, q_wuc), and
-  // dy_perm, dh, x_perm along the token axis (q_dyc, q_dhc, q_xc); MXFP8 also dh along
-  // I (q_dhr) and a_w along tokens (q_awc), and the permutation writes dy along H into
-  // dy_perm's place (blockwise FP8: dy_perm, dh along I and a_w quantised in place).
+  // backward: W_down along H and W_gate, W_up along I (q_wdc, q_wgc, q_wuc; blockwise
+  // FP8: the one copy of each weight, read by every GEMM), dy_perm, dh, x_perm along
+  // the token axis (q_dyc, q_dhc, q_xc), dh along I (q_dhr) and a_w along tokens
+  // (q_awc); the permutation writes dy along H into dy_perm's place.
   // Under a quantised forward that keeps its activations the forward writes the weight
   // copies into `saved` (w_in_saved) and x's token-axis copy over x_perm, so q_xc is
   // unused.
@@ -135,6 +136,9 @@ enum KernelId {
   K_FB_ROWS,
   K_FB_COLS,
   K_FB_TILES,
+  K_FBQ_ROWS,
+  K_FBQ_COLS,
+  K_FBQ_TILES,
   K_MXQ_ROWS,
   K_MXQ_COLS,
   K_DENSE_NT,
@@ -171,10 +175,10 @@ struct RouteBufs {
 cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* topk_idx,
                             const float* topk_w, const RouteBufs& b);
 // dst = src's token rows in the padded expert-grouped order, padding rows zero; with
-// quant = QS_BLOCK each row is quantise-dequantised along its columns (128-element
-// blocks, bf16 out) on the way, once per token before its k copies are stored; with
-// quant = QS_MX dst receives each row's e4m3 codes ([Rp, H] bytes) and `sf` its scale
-// codes (mx::sf_offset over the Rp padded rows).
+// quant = QS_MX / QS_BLOCK each row is quantised along its columns on the way (32- /
+// 128-element blocks), once per token before its k copies are stored: dst receives
+// the rows' e4m3 codes ([Rp, H] bytes) and `sf` their scale codes (mx::sf_offset over
+// the Rp padded rows).
 cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, void* dst,
                            const char* saved, float* w_row_out, int kernel_id, char* scratch,
                            int quant = 0, uint8_t* sf = nullptr);
@@ -242,6 +246,28 @@ cudaError_t launch_mxq(const Ctx& c, const MxqArgs& a);
 // blocks of the same read; `meta` and `gather` as for launch_mx_qdq), or 128 x 128
 // tiles (FB_TILES).  out / out_rows may equal in.
 enum { FB_ROWS = 0, FB_COLS = 1, FB_TILES = 2 };
+// Blockwise FP8 in the form the block-scaled tensor cores read: e4m3 codes ([rows, cols]
+// bytes) and E8M0 scale codes (mx::sf_offset), each 128-element block's scale repeated
+// over its four 32-element scale blocks.  FB_ROWS: 128-blocks along each row (scales
+// over rows / 128 row blocks); FB_COLS: 128-row blocks down each column (scales over
+// cols / 128 column blocks), with codes_rows non-null also the row blocks (scales over
+// rows / 128 row blocks to sf_rows), rows optionally gathered; FB_TILES: 128 x 128 weight
+// tiles, one copy of the codes and the scales in both arrangements (sf: the MMA rows
+// are the matrix rows; sf_mn: the MMA rows are the columns).  `meta` (device, optional)
+// limits FB_ROWS / FB_COLS to the padded rows in use.
+struct FbqArgs {
+  const uint16_t* in;
+  uint8_t* codes;
+  uint8_t* sf;
+  uint8_t* sf_mn;
+  uint8_t* codes_rows;
+  uint8_t* sf_rows;
+  int64_t rows, cols;
+  int layout;
+  const int* meta;
+  RowGather gather;
+};
+cudaError_t launch_fbq(const Ctx& c, const FbqArgs& a);
 cudaError_t launch_fb_qdq(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
                           int64_t cols, int layout, const int* meta, uint16_t* out_rows,
                           RowGather gather = RowGather{});

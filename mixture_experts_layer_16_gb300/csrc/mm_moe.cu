@@ -20,11 +20,17 @@ bool sm_pairs_enabled() {
   return on;
 }
 
-// Bytes of one quantised copy of a [rows, cols] operand under scheme qs: MXFP8 keeps
-// e4m3 codes (rows * cols bytes) followed by the E8M0 scales (one per 32 elements);
-// blockwise FP8 keeps the dequantised values as bf16.
-static size_t qcopy_bytes(int qs, size_t rows, size_t cols) {
-  return qs == QS_MX ? rows * cols + rows * cols / 32 : 2 * rows * cols;
+// Bytes of one quantised copy of a [rows, cols] operand: e4m3 codes (rows * cols bytes)
+// followed by the E8M0 scales (one per 32 elements; blockwise FP8 repeats each
+// 128-block's scale four times) -- the form the block-scaled tensor cores read.
+static size_t qcopy_bytes(size_t rows, size_t cols) { return rows * cols + rows * cols / 32; }
+
+// Bytes of the backward's (blockwise: the only) copy of a weight: MXFP8 quantises it
+// along its other axis (one copy); blockwise FP8's 128 x 128 blocks give the same codes
+// either way, followed by the scales in both arrangements (rows, then columns as the
+// MMA rows).
+static size_t wcopy_bytes(int qs, size_t rows, size_t cols) {
+  return qs == QS_BLOCK ? rows * cols + 2 * (rows * cols / 32) : qcopy_bytes(rows, cols);
 }
 
 mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
@@ -55,8 +61,8 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->qb = s->prec == MM_MOE_BF16 ? QS_NONE : s->prec == MM_MOE_FP8_BLOCK ? QS_BLOCK : QS_MX;
   L->nblk = (L->R + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
   // partial sums of dtopk_w per row: one per N tile of the dgrad-down GEMM, two when
-  // its MXFP8 tiles (256 wide) split their columns between two epilogue warps
-  L->n_pw = L->I / pick_bn(L->I) * ((L->qb == QS_MX && pick_bn(L->I) == 256) ? 2 : 1);
+  // its FP8 tiles (256 wide) split their columns between two epilogue warps
+  L->n_pw = L->I / pick_bn(L->I) * ((L->qb != QS_NONE && pick_bn(L->I) == 256) ? 2 : 1);
   const size_t A = 1024;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -91,7 +97,7 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->w_common = L->qf == QS_BLOCK && L->recompute;
   L->q_wdc = L->q_wgc = L->q_wuc = 0;
   if (L->w_in_saved) {
-    const size_t W = qcopy_bytes(L->qf, E * I, H);
+    const size_t W = wcopy_bytes(L->qf, E * I, H);
     L->q_wdc = take(W);
     L->q_wgc = take(W);
     L->q_wuc = take(W);
@@ -110,7 +116,7 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
     L->a = take(2 * Rp * I);
   }
   if (L->w_common) {  // blockwise weights under recompute: made by each pass, used by all
-    const size_t W = qcopy_bytes(QS_BLOCK, E * I, H);
+    const size_t W = wcopy_bytes(QS_BLOCK, E * I, H);
     L->q_wdc = take(W);
     L->q_wgc = take(W);
     L->q_wuc = take(W);
@@ -120,11 +126,11 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   // quantised operand copies of the forward
   L->q_x = L->q_a = L->q_wg = L->q_wu = L->q_wd = 0;
   if (L->qf != QS_NONE) {
-    L->q_x = take(qcopy_bytes(L->qf, Rp, H));
-    L->q_a = take(qcopy_bytes(L->qf, Rp, I));
+    L->q_x = take(qcopy_bytes(Rp, H));
+    L->q_a = take(qcopy_bytes(Rp, I));
   }
   if (L->qf == QS_MX) {  // the forward's MXFP8 weights (blocks along their forward K)
-    const size_t W = qcopy_bytes(QS_MX, E * I, H);
+    const size_t W = qcopy_bytes(E * I, H);
     L->q_wg = take(W);
     L->q_wu = take(W);
     L->q_wd = take(W);
@@ -139,20 +145,18 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->q_dyc = L->q_dhc = L->q_xc = L->q_dhr = L->q_awc = 0;
   if (L->qb != QS_NONE && !L->w_in_saved) {  // left to the backward
     if (!L->w_common) {
-      const size_t W = qcopy_bytes(L->qb, E * I, H);
+      const size_t W = wcopy_bytes(L->qb, E * I, H);
       L->q_wdc = take(W);
       L->q_wgc = take(W);
       L->q_wuc = take(W);
     }
-    L->q_xc = take(qcopy_bytes(L->qb, Rp, H));
+    L->q_xc = take(qcopy_bytes(Rp, H));
   }
   if (L->qb != QS_NONE) {
-    L->q_dyc = take(qcopy_bytes(L->qb, Rp, H));
-    L->q_dhc = take(qcopy_bytes(L->qb, Rp, 2 * I));
-  }
-  if (L->qb == QS_MX) {  // (blockwise FP8 quantises dh along I and a_w in place)
-    L->q_dhr = take(qcopy_bytes(QS_MX, Rp, 2 * I));
-    L->q_awc = take(qcopy_bytes(QS_MX, Rp, I));
+    L->q_dyc = take(qcopy_bytes(Rp, H));
+    L->q_dhc = take(qcopy_bytes(Rp, 2 * I));
+    L->q_dhr = take(qcopy_bytes(Rp, 2 * I));
+    L->q_awc = take(qcopy_bytes(Rp, I));
   }
   L->scratch_bytes = o > fwd_end ? o : fwd_end;
   return MM_MOE_OK;
@@ -332,18 +336,68 @@ static cudaError_t mx_cols(const Ctx& c, DevStatus* st, const uint16_t* in, MxCo
   return launch_mxq(c, a);
 }
 
-// Blockwise FP8 quantise-dequantise of an activation operand (128-element blocks):
-// along rows, or down columns (with out_rows non-null the same read also writes the
-// row blocks there).
-static cudaError_t fb_rows(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
-                           int64_t cols, const int* meta) {
-  return launch_fb_qdq(c, in, out, rows, cols, FB_ROWS, meta, nullptr);
+// The quantised copy of an activation operand under scheme qs (MXFP8: 32-element
+// blocks; blockwise FP8: 128-element blocks): along its rows, or down its columns (with
+// rows_out non-null the same read also yields the row blocks; a gather reads the rows
+// from a token-major tensor).
+static cudaError_t q_rows(const Ctx& c, int qs, const uint16_t* in, MxCopy out, int64_t rows,
+                          int64_t cols, const int* meta) {
+  if (qs == QS_MX) return mx_rows(c, in, out, rows, cols, meta);
+  FbqArgs a{};
+  a.in = in;
+  a.codes = out.codes;
+  a.sf = out.sf;
+  a.rows = rows;
+  a.cols = cols;
+  a.layout = FB_ROWS;
+  a.meta = meta;
+  return launch_fbq(c, a);
 }
 
-static cudaError_t fb_cols(const Ctx& c, const uint16_t* in, uint16_t* out, int64_t rows,
-                           int64_t cols, const int* meta, uint16_t* out_rows = nullptr,
-                           RowGather gather = RowGather{}) {
-  return launch_fb_qdq(c, in, out, rows, cols, FB_COLS, meta, out_rows, gather);
+static cudaError_t q_cols(const Ctx& c, int qs, DevStatus* st, const uint16_t* in, MxCopy out,
+                          int64_t rows, int64_t cols, const int* meta,
+                          const MxCopy* rows_out = nullptr, RowGather gather = RowGather{}) {
+  if (qs == QS_MX) return mx_cols(c, st, in, out, rows, cols, meta, rows_out, gather);
+  FbqArgs a{};
+  a.in = in;
+  a.codes = out.codes;
+  a.sf = out.sf;
+  a.rows = rows;
+  a.cols = cols;
+  a.layout = FB_COLS;
+  a.meta = meta;
+  if (rows_out != nullptr) {
+    a.codes_rows = rows_out->codes;
+    a.sf_rows = rows_out->sf;
+  }
+  a.gather = gather;
+  return launch_fbq(c, a);
+}
+
+// A weight's quantised copy at byte offset `off` of `base`, [rows, cols]: MXFP8's
+// copies (each quantised along the K of the GEMMs that read it), or blockwise FP8's one
+// copy, read with the scales of the arrangement the GEMM needs (mn: the weight's
+// columns are the MMA rows, i.e. the GEMM contracts its rows).
+static MxCopy w_copy(int qs, const char* base, size_t off, int64_t rows, int64_t cols, bool mn) {
+  MxCopy m = mx_copy(base, off, rows, cols);
+  if (qs == QS_BLOCK && mn) m.sf += rows * cols / 32;
+  return m;
+}
+
+// Blockwise FP8's copy of a weight: 128 x 128 blocks, the codes and both scale
+// arrangements, at offset `off` of `base`.
+static cudaError_t fbq_weight(const Ctx& c, const uint16_t* W, char* base, size_t off,
+                              int64_t rows, int64_t cols) {
+  const MxCopy k = w_copy(QS_BLOCK, base, off, rows, cols, false);
+  FbqArgs a{};
+  a.in = W;
+  a.codes = k.codes;
+  a.sf = k.sf;
+  a.sf_mn = k.sf + rows * cols / 32;
+  a.rows = rows;
+  a.cols = cols;
+  a.layout = FB_TILES;
+  return launch_fbq(c, a);
 }
 
 // The padded expert-grouped rows of a token-major tensor, for the column passes.
@@ -362,14 +416,9 @@ static Opnd permute_x(const Ctx& c, const Layout& L, const uint16_t* x, uint16_t
     *err = launch_permute(c, L, x, x_perm, sv, w_row_out, K_PERMUTE_X, sc);
     return Opnd{x_perm, nullptr};
   }
-  if (L.qf == QS_MX) {
-    const MxCopy q = mx_copy(sc, L.q_x, L.Rp, L.H);
-    *err = launch_permute(c, L, x, q.codes, sv, w_row_out, K_PERMUTE_X, sc, QS_MX, q.sf);
-    return q;
-  }
-  uint16_t* q_x = reinterpret_cast<uint16_t*>(sc + L.q_x);
-  *err = launch_permute(c, L, x, q_x, sv, w_row_out, K_PERMUTE_X, sc, QS_BLOCK);
-  return Opnd{q_x, nullptr};
+  const MxCopy q = mx_copy(sc, L.q_x, L.Rp, L.H);
+  *err = launch_permute(c, L, x, q.codes, sv, w_row_out, K_PERMUTE_X, sc, L.qf, q.sf);
+  return q;
 }
 
 // x's blocks along tokens (the dW_gate / dW_up operand), gathered from x in routed
@@ -378,11 +427,8 @@ static cudaError_t x_tokens(const Ctx& c, const Layout& L, int qs, const uint16_
                             const char* sv, char* sc) {
   const int* meta = reinterpret_cast<const int*>(sv + L.meta);
   DevStatus* sw = reinterpret_cast<DevStatus*>(sc + L.status);  // the status word
-  if (qs == QS_MX)
-    return mx_cols(c, sw, x, mx_copy(dst, 0, L.Rp, L.H), L.Rp, L.H, meta, nullptr,
-                   routed_rows(L, sv));
-  return fb_cols(c, x, reinterpret_cast<uint16_t*>(dst), L.Rp, L.H, meta, nullptr,
-                 routed_rows(L, sv));
+  return q_cols(c, qs, sw, x, mx_copy(dst, 0, L.Rp, L.H), L.Rp, L.H, meta, nullptr,
+                routed_rows(L, sv));
 }
 
 // The weight copies of a quantised forward; they read only the weights, so the
@@ -391,8 +437,8 @@ static cudaError_t x_tokens(const Ctx& c, const Layout& L, int qs, const uint16_
 // forward of a layer that keeps its activations) one two-way pass per weight writes
 // its blocks along the forward's K to scratch and along the backward's K to `wbase`
 // (saved); otherwise row passes write the forward's copies only.  Blockwise FP8: the
-// one 128 x 128-block copy of each weight, which every GEMM reads, to `wbase` (saved,
-// or the front of scratch under recompute).
+// one 128 x 128-block copy of each weight (codes and both scale arrangements), which
+// every GEMM reads, to `wbase` (saved, or the front of scratch under recompute).
 static cudaError_t weights_gateup(const Ctx& c, const Layout& L, bool keep,
                                   const uint16_t* W_gate, const uint16_t* W_up, char* wbase,
                                   char* sc) {
@@ -410,10 +456,8 @@ static cudaError_t weights_gateup(const Ctx& c, const Layout& L, bool keep,
       if (e == cudaSuccess) e = mx_rows(c, W_up, wu, EI, L.H, nullptr);
     }
   } else if (L.qf == QS_BLOCK) {
-    auto wq = [&](size_t off) { return reinterpret_cast<uint16_t*>(wbase + off); };
-    e = launch_fb_qdq(c, W_gate, wq(L.q_wgc), EI, L.H, FB_TILES, nullptr, nullptr);
-    if (e == cudaSuccess)
-      e = launch_fb_qdq(c, W_up, wq(L.q_wuc), EI, L.H, FB_TILES, nullptr, nullptr);
+    e = fbq_weight(c, W_gate, wbase, L.q_wgc, EI, L.H);
+    if (e == cudaSuccess) e = fbq_weight(c, W_up, wbase, L.q_wuc, EI, L.H);
   }
   return e;
 }
@@ -427,9 +471,7 @@ static cudaError_t weights_down(const Ctx& c, const Layout& L, bool keep,
     return keep ? mx_cols(c, sw, W_down, mx_copy(wbase, L.q_wdc, EH, L.I), EH, L.I, nullptr, &wd)
                 : mx_rows(c, W_down, wd, EH, L.I, nullptr);
   }
-  if (L.qf == QS_BLOCK)
-    return launch_fb_qdq(c, W_down, reinterpret_cast<uint16_t*>(wbase + L.q_wdc), EH, L.I,
-                         FB_TILES, nullptr, nullptr);
+  if (L.qf == QS_BLOCK) return fbq_weight(c, W_down, wbase, L.q_wdc, EH, L.I);
   return cudaSuccess;
 }
 
@@ -467,12 +509,17 @@ static mm_moe_status gateup_stage(const Ctx& c, const Layout& L, bool emit_qa, O
       g.q_sf = qa.sf;
     }
   } else if (L.qf == QS_BLOCK) {
-    g.B0 = wbase + L.q_wgc;
-    g.B1 = wbase + L.q_wuc;
+    const MxCopy wg = w_copy(QS_BLOCK, wbase, L.q_wgc, L.E * L.I, L.H, false),
+                 wu = w_copy(QS_BLOCK, wbase, L.q_wuc, L.E * L.I, L.H, false);
+    g.fp8 = true;
+    g.B0 = wg.codes;
+    g.sB0 = wg.sf;
+    g.B1 = wu.codes;
+    g.sB1 = wu.sf;
   }
   MM_MOE_TRY(launch_gemm(c, L, g));
   if (L.qf == QS_BLOCK && emit_qa)
-    MM_MOE_TRY(fb_rows(c, a, reinterpret_cast<uint16_t*>(sc + L.q_a), L.Rp, L.I, meta));
+    MM_MOE_TRY(q_rows(c, QS_BLOCK, a, mx_copy(sc, L.q_a, L.Rp, L.I), L.Rp, L.I, meta));
   return MM_MOE_OK;
 }
 
@@ -556,16 +603,15 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_forward(const mm_moe_shape* shape, co
   g.A = a;
   g.B0 = W_down;
   g.out0 = ys;
-  if (L.qf == QS_MX) {
-    const MxCopy qa = mx_copy(sc, L.q_a, L.Rp, L.I), wd = mx_copy(sc, L.q_wd, L.E * L.H, L.I);
+  if (L.qf != QS_NONE) {
+    const MxCopy qa = mx_copy(sc, L.q_a, L.Rp, L.I);
+    const MxCopy wd = L.qf == QS_MX ? mx_copy(sc, L.q_wd, L.E * L.H, L.I)
+                                    : w_copy(QS_BLOCK, wbase, L.q_wdc, L.E * L.H, L.I, false);
     g.fp8 = true;
     g.A = qa.codes;
     g.sA = qa.sf;
     g.B0 = wd.codes;
     g.sB0 = wd.sf;
-  } else if (L.qf == QS_BLOCK) {
-    g.A = sc + L.q_a;
-    g.B0 = wbase + L.q_wdc;
   }
   if (m_down >= 0) MM_MOE_TRY(fork.main_waits(m_down));
   MM_MOE_TRY(launch_gemm(c, L, g));
@@ -624,13 +670,15 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
     if (st != MM_MOE_OK) return st;
   }
   // A quantised backward (MXFP8 for full MXFP8 and fp8_bwd, blockwise FP8): every
-  // GEMM reads copies of its operands quantised along its own K.  The permutation of
-  // dy writes dy's blocks along H (the first GEMM's operand) into dy_perm's place;
-  // dy's blocks along tokens (the dW_down operand) are gathered from dy on the side
-  // stream beside the first two GEMMs, as are (MXFP8 without the forward's copies) the
-  // weights along I for dgrad-gate/up.  The backward's weight copies were otherwise
-  // made by the forward (saved) or by the recompute (blockwise, front of scratch).
-  // (The side stream starts after the recompute, whose buffers overlap these.)
+  // GEMM runs on the block-scaled tensor cores and reads copies of its operands
+  // quantised along its own K (codes and scales).  The permutation of dy writes dy's
+  // blocks along H (the first GEMM's operand) into dy_perm's place; dy's blocks along
+  // tokens (the dW_down operand) are gathered from dy on the side stream beside the
+  // first two GEMMs, as are (MXFP8 without the forward's copies) the weights along I
+  // for dgrad-gate/up.  The backward's weight copies were otherwise made by the forward
+  // (saved) or by the recompute (blockwise, front of scratch); blockwise FP8 reads its
+  // one weight copy with the scales of the other arrangement here.  (The side stream
+  // starts after the recompute, whose buffers overlap these.)
   const int qb = L.qb;
   const char* wsrc = L.w_in_saved ? sv : sc;
   const bool make_w = qb == QS_MX && !L.w_in_saved;
@@ -638,19 +686,15 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   if (!fork.open(c.stream)) return MM_MOE_ECUDA;
   Ctx side{fork.side(), d.sms, &launches};
   int m_dy = -1, m_w = -1;
-  if (qb == QS_MX) {
-    MM_MOE_TRY(mx_cols(side, sw, dy, mx_copy(sc, L.q_dyc, Rp, H), Rp, H, meta, nullptr,
-                       routed_rows(L, sv)));
+  if (qb != QS_NONE) {
+    MM_MOE_TRY(q_cols(side, qb, sw, dy, mx_copy(sc, L.q_dyc, Rp, H), Rp, H, meta, nullptr,
+                      routed_rows(L, sv)));
     m_dy = fork.mark();
     if (make_w) {
       MM_MOE_TRY(mx_cols(side, sw, W_gate, mx_copy(sc, L.q_wgc, EI, H), EI, H, nullptr));
       MM_MOE_TRY(mx_cols(side, sw, W_up, mx_copy(sc, L.q_wuc, EI, H), EI, H, nullptr));
       m_w = fork.mark();
     }
-  } else if (qb == QS_BLOCK) {
-    MM_MOE_TRY(fb_cols(side, dy, reinterpret_cast<uint16_t*>(sc + L.q_dyc), Rp, H, meta, nullptr,
-                       routed_rows(L, sv)));
-    m_dy = fork.mark();
   }
   GemmArgs g{};
   g.saved = sv;
@@ -663,9 +707,9 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   g.out0 = dh;
   g.out1 = a_w;
   g.outf = pw;
-  if (qb == QS_MX) {
-    const MxCopy dyr = mx_copy(sc, L.dy_perm, Rp, H), wdc = mx_copy(wsrc, L.q_wdc, EH, I);
-    MM_MOE_TRY(launch_permute(c, L, dy, dyr.codes, sv, nullptr, K_PERMUTE_DY, sc, QS_MX, dyr.sf));
+  if (qb != QS_NONE) {
+    const MxCopy dyr = mx_copy(sc, L.dy_perm, Rp, H), wdc = w_copy(qb, wsrc, L.q_wdc, EH, I, true);
+    MM_MOE_TRY(launch_permute(c, L, dy, dyr.codes, sv, nullptr, K_PERMUTE_DY, sc, qb, dyr.sf));
     if (make_w) MM_MOE_TRY(mx_cols(c, sw, W_down, wdc, EH, I, nullptr));
     g.fp8 = true;
     g.A = dyr.codes;
@@ -674,7 +718,6 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
     g.sB0 = wdc.sf;
   } else {
     MM_MOE_TRY(launch_permute(c, L, dy, dy_perm, sv, nullptr, K_PERMUTE_DY, sc, qb));
-    if (qb == QS_BLOCK) g.B0 = wsrc + L.q_wdc;
   }
   MM_MOE_TRY(launch_gemm(c, L, g));
   g = GemmArgs{};
@@ -685,11 +728,12 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   g.B0 = W_gate;
   g.B1 = W_up;
   g.out0 = dxs;
-  if (qb == QS_MX) {
+  if (qb != QS_NONE) {
     // one read of dh: blocks along tokens (dW_gate, dW_up) and along I (this GEMM)
     const MxCopy dhc = mx_copy(sc, L.q_dhc, Rp, 2 * I), dhr = mx_copy(sc, L.q_dhr, Rp, 2 * I);
-    const MxCopy wgc = mx_copy(wsrc, L.q_wgc, EI, H), wuc = mx_copy(wsrc, L.q_wuc, EI, H);
-    MM_MOE_TRY(mx_cols(c, sw, dh, dhc, Rp, 2 * I, meta, &dhr));
+    const MxCopy wgc = w_copy(qb, wsrc, L.q_wgc, EI, H, true),
+                 wuc = w_copy(qb, wsrc, L.q_wuc, EI, H, true);
+    MM_MOE_TRY(q_cols(c, qb, sw, dh, dhc, Rp, 2 * I, meta, &dhr));
     if (m_w >= 0) MM_MOE_TRY(fork.main_waits(m_w));
     g.fp8 = true;
     g.A = dhr.codes;
@@ -698,11 +742,6 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
     g.sB0 = wgc.sf;
     g.B1 = wuc.codes;
     g.sB1 = wuc.sf;
-  } else if (qb == QS_BLOCK) {
-    // one read of dh: blocks along tokens to q_dhc, along I in place
-    MM_MOE_TRY(fb_cols(c, dh, reinterpret_cast<uint16_t*>(sc + L.q_dhc), Rp, 2 * I, meta, dh));
-    g.B0 = wsrc + L.q_wgc;
-    g.B1 = wsrc + L.q_wuc;
   }
   MM_MOE_TRY(launch_gemm(c, L, g));
   // the un-permute (bandwidth-bound) runs on the side stream beside the
@@ -722,16 +761,16 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
   g.out0 = dW_gate;
   g.out1 = dW_up;
   g.out2 = dW_down;
-  if (qb == QS_MX) {
+  if (qb != QS_NONE) {
     const MxCopy awc = mx_copy(sc, L.q_awc, Rp, I);
-    MM_MOE_TRY(mx_cols(c, sw, a_w, awc, Rp, I, meta));
+    MM_MOE_TRY(q_cols(c, qb, sw, a_w, awc, Rp, I, meta));
     MxCopy xc = mx_copy(sv, L.x_perm, Rp, H);  // the forward's gather (kept activations)
     if (!L.w_in_saved) {
       xc = mx_copy(sc, L.q_xc, Rp, H);
       if (L.qf == QS_NONE)  // fp8_bwd: from the forward's bf16 x_perm
         MM_MOE_TRY(mx_cols(c, sw, x_perm, xc, Rp, H, meta));
       else                  // recompute under a quantised forward: from x itself
-        MM_MOE_TRY(x_tokens(c, L, QS_MX, x, reinterpret_cast<char*>(xc.codes), sv, sc));
+        MM_MOE_TRY(x_tokens(c, L, qb, x, reinterpret_cast<char*>(xc.codes), sv, sc));
     }
     const MxCopy dyc = mx_copy(sc, L.q_dyc, Rp, H), dhc = mx_copy(sc, L.q_dhc, Rp, 2 * I);
     g.fp8 = true;
@@ -743,17 +782,6 @@ extern "C" MM_MOE_API mm_moe_status mm_moe_backward(const mm_moe_shape* shape, c
     g.sA2 = dyc.sf;
     g.B2 = awc.codes;
     g.sB2 = awc.sf;
-  } else if (qb == QS_BLOCK) {
-    MM_MOE_TRY(fb_cols(c, a_w, a_w, Rp, I, meta));
-    const uint16_t* xb = x_perm;  // (a blockwise forward that keeps its activations left
-                                  // x's blocks along tokens in x_perm's place)
-    if (!L.w_in_saved) {
-      MM_MOE_TRY(x_tokens(c, L, QS_BLOCK, x, sc + L.q_xc, sv, sc));
-      xb = reinterpret_cast<const uint16_t*>(sc + L.q_xc);
-    }
-    g.A = sc + L.q_dhc;
-    g.B0 = xb;
-    g.A2 = sc + L.q_dyc;
   }
   if (m_dy >= 0) MM_MOE_TRY(fork.main_waits(m_dy));
   // both weight gradients in one launch where they tile N alike (one list of tiles,

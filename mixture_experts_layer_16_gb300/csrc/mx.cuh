@@ -141,5 +141,27 @@ __device__ __forceinline__ int quant_row32(const float (&v)[32], uint2 (&out)[4]
   return e;
 }
 
+// Scale exponent of a block whose largest absolute value has the bf16 bit pattern
+// `bits` (sign clear): floor(log2) - 8 from the exponent field, -127 for zero, and
+// clamped to [-127, 127] like scale_exp (a subnormal maximum gives -127).
+__device__ __forceinline__ int bf16_scale_exp(uint32_t bits) {
+  const int ef = static_cast<int>((bits >> 7) & 0xFFu);
+  return ef == 0 ? -127 : max(-127, ef - 127 - 8);
+}
+
+// Four e4m3 codes of the bf16 values in two words (element 0 in the low half of w0),
+// each times its own power-of-two multiplier (exact); element 0's code in the lowest
+// byte.
+__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float m0, float m1,
+                                           float m2, float m3) {
+  const float a = __uint_as_float(w0 << 16), b = __uint_as_float(w0 & 0xFFFF0000u);
+  const float c = __uint_as_float(w1 << 16), d = __uint_as_float(w1 & 0xFFFF0000u);
+  const uint32_t lo = static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(a * m0, b * m1), __NV_SATFINITE, __NV_E4M3));
+  const uint32_t hi = static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(c * m2, d * m3), __NV_SATFINITE, __NV_E4M3));
+  return lo | (hi << 16);
+}
+
 }  // namespace mx
 }  // namespace mmmoe

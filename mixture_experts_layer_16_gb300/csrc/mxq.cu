@@ -20,6 +20,8 @@ using mx::bf;
 using mx::codes8;
 using mx::e8m0;
 using mx::scale_exp;
+using mx::bf16_scale_exp;
+using mx::codes4;
 using mx::sf_offset;
 
 __device__ __forceinline__ int64_t rows_in_use(int64_t rows, const int* meta) {
@@ -112,26 +114,6 @@ constexpr int QC_ROW = QC_TC * 2 + 16;         // bytes between rows in shared m
 constexpr int QC_TILE_BYTES = 32 * QC_ROW;
 constexpr int QC_SMEM = QC_WARPS * QC_STAGES * QC_TILE_BYTES;
 constexpr uint64_t QC_WAIT_NS = 2000000000ull;
-
-// Scale exponent of a block whose largest absolute value has the bf16 bit pattern
-// `bits` (sign clear): floor(log2) - 8 from the exponent field, -127 for zero, and
-// clamped to [-127, 127] like scale_exp (a subnormal maximum gives -127).
-__device__ __forceinline__ int bf16_scale_exp(uint32_t bits) {
-  const int ef = static_cast<int>((bits >> 7) & 0xFFu);
-  return ef == 0 ? -127 : max(-127, ef - 127 - 8);
-}
-
-// Four codes of the bf16 values in two words, each under its own multiplier.
-__device__ __forceinline__ uint32_t codes4(uint32_t w0, uint32_t w1, float m0, float m1,
-                                           float m2, float m3) {
-  const float a = __uint_as_float(w0 << 16), b = __uint_as_float(w0 & 0xFFFF0000u);
-  const float c = __uint_as_float(w1 << 16), d = __uint_as_float(w1 & 0xFFFF0000u);
-  const uint32_t lo = static_cast<uint32_t>(
-      __nv_cvt_float2_to_fp8x2(make_float2(a * m0, b * m1), __NV_SATFINITE, __NV_E4M3));
-  const uint32_t hi = static_cast<uint32_t>(
-      __nv_cvt_float2_to_fp8x2(make_float2(c * m2, d * m3), __NV_SATFINITE, __NV_E4M3));
-  return lo | (hi << 16);
-}
 
 __global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
     const uint16_t* __restrict__ in, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,

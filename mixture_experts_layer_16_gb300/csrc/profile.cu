@@ -13,7 +13,8 @@ static const char* const kKernelNames[K_COUNT] = {
     "route_count", "route_scan", "route_place", "permute_x", "gemm_gateup_swiglu",
     "gemm_down_weighted", "combine", "permute_dy", "gemm_dgrad_down_dswiglu",
     "gemm_dgrad_gateup", "unpermute_reduce", "gemm_wgrad_down", "gemm_wgrad_gateup", "gemm_wgrad",
-    "mx_qdq_rows", "mx_qdq_cols", "fp8block_rows", "fp8block_cols", "fp8block_tiles", "mxq_rows", "mxq_cols",
+    "mx_qdq_rows", "mx_qdq_cols", "fp8block_rows", "fp8block_cols", "fp8block_tiles", "fbq_rows",
+    "fbq_cols", "fbq_tiles", "mxq_rows", "mxq_cols",
     "gemm_dense_nt", "gemm_dense_nn", "gemm_dense_tn", "router_topk", "router_dlogits"};
 
 namespace {

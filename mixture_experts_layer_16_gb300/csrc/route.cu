@@ -260,53 +260,51 @@ cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* 
 // a ring of PERM_SLOTS row buffers, loading PERM_AHEAD tokens ahead of the one it
 // stores.  Padding rows are then stored from a zero row; in the forward their
 // routing weight is zeroed too (valid rows got theirs from the placement kernel).
-// QM = QS_BLOCK: the warp quantise-dequantises each row in shared memory (128-element
-// blocks along the row, bf16 out) between its load and its stores; QM = QS_MX: the
-// warp turns each row into its MXFP8 form (e4m3 codes, H bytes, stored to the k
-// destination rows of a [Rp, H] byte tensor; the H / 32 scale codes written as words
-// of the scale arrangement mx::sf_offset over the padded rows).  A zero row quantises
-// to zero codes and zero scale codes.
+// QM = QS_MX / QS_BLOCK: the warp turns each row into its MXFP8 / blockwise FP8 form
+// in shared memory between its load and its stores (e4m3 codes, H bytes, stored to the
+// k destination rows of a [Rp, H] byte tensor; the H / 32 scale codes -- for blockwise
+// FP8 each 128-element block's scale four times -- written as words of the scale
+// arrangement mx::sf_offset over the padded rows).  A zero row quantises to zero codes
+// and zero scale codes.
 constexpr int PERM_SLOTS = 8;
 constexpr int PERM_AHEAD = 4;
 constexpr uint64_t PERM_WAIT_NS = 2000000000ull;
 
-// Blockwise FP8: quantise-dequantise one bf16 row of n elements in shared memory in
-// place (all 32 lanes; 128-element blocks).
-template <int QM>
-__device__ __forceinline__ void quantise_row(uint8_t* row, int n, int lane) {
-  uint4* r4 = reinterpret_cast<uint4*>(row);
-  {  // a lane per half block (64 elements), neighbouring lanes pair up
-    const int nh = n / 64;  // even: n % 128 == 0
-    for (int h0 = 0; h0 < nh; h0 += 32) {
-      const int hb = h0 + lane;
-      const bool act = hb < nh;  // the partner lane (lane ^ 1) has the same value
-      float v[64];
-      float m = 0.f;
+// Blockwise FP8 form of one bf16 row of n elements in shared memory (all 32 lanes):
+// the n e4m3 codes over the start of the same buffer, each 128-element block's scale
+// as a word of four equal E8M0 codes to `scales` (n / 128 words).  Two neighbouring
+// lanes take one block per round (64 elements each, the maximum met by a shuffle) and
+// hold their halves in registers, so that no lane writes codes before every lane has
+// read its half.
+__device__ __forceinline__ void quantise_row_fb(uint8_t* row, uint8_t* scales, int n, int lane) {
+  const int nh = n / 64;  // half blocks (even: n % 128 == 0)
+  for (int h0 = 0; h0 < nh; h0 += 32) {
+    const int hb = h0 + lane;  // (lane ^ 1 takes the other half of the same block)
+    const bool act = hb < nh;
+    uint4 w[8];
+    float m = 0.f;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint4 w = act ? r4[8 * hb + q] : make_uint4(0, 0, 0, 0);
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(&w);
+    for (int q = 0; q < 8; ++q) {
+      w[q] = act ? reinterpret_cast<const uint4*>(row + hb * 128)[q] : make_uint4(0, 0, 0, 0);
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(&w[q]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          v[8 * q + j] = mx::bf(h[j]);
-          m = fmaxf(m, fabsf(v[8 * q + j]));
-        }
-      }
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      const int e = fb::ceil_exp(m);
-#pragma unroll
-      for (int j = 0; j < 64; j += 2) mx::qdq2(v[j], v[j + 1], e, e);
-      if (act) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          uint4 w;
-          uint16_t* h = reinterpret_cast<uint16_t*>(&w);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) h[j] = mx::to_bf(v[8 * q + j]);
-          r4[8 * hb + q] = w;
-        }
-      }
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(mx::bf(h[j])));
     }
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    __syncwarp();
+    if (act) {
+      const int e = fb::ceil_exp(m);
+      const float mul = mx::pow2f(-e);
+      uint4* d4 = reinterpret_cast<uint4*>(row + hb * 64);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        d4[q] = make_uint4(mx::codes4(w[2 * q].x, w[2 * q].y, mul, mul, mul, mul),
+                           mx::codes4(w[2 * q].z, w[2 * q].w, mul, mul, mul, mul),
+                           mx::codes4(w[2 * q + 1].x, w[2 * q + 1].y, mul, mul, mul, mul),
+                           mx::codes4(w[2 * q + 1].z, w[2 * q + 1].w, mul, mul, mul, mul));
+      if ((hb & 1) == 0) reinterpret_cast<uint32_t*>(scales)[hb / 2] = mx::e8m0(e) * 0x01010101u;
+    }
+    __syncwarp();
   }
 }
 
@@ -351,15 +349,15 @@ __global__ void __launch_bounds__(32) permute_rows_kernel(
     uint8_t* __restrict__ sf, int64_t sf_mnb) {
   pdl_wait();
   pdl_trigger();
-  // PERM_SLOTS rows, a zero row, then (MXFP8) PERM_SLOTS rows of scale codes
+  // PERM_SLOTS rows, a zero row, then (FP8) PERM_SLOTS rows of scale codes
   extern __shared__ __align__(128) uint8_t pbuf[];
   __shared__ __align__(8) uint64_t bar[PERM_SLOTS];
   const int lane = threadIdx.x;
   uint8_t* zero = pbuf + PERM_SLOTS * row_bytes;
   const int n_el = row_bytes / 2;                            // elements of a row
-  const int out_bytes = QM == QS_MX ? n_el : row_bytes;      // bytes stored per row
-  uint8_t* sbuf = zero + row_bytes;                          // MXFP8 scale codes
-  const int n_words = n_el / 128;                            // MXFP8 scale words per row
+  const int out_bytes = QM != QS_NONE ? n_el : row_bytes;    // bytes stored per row
+  uint8_t* sbuf = zero + row_bytes;                          // FP8 scale codes
+  const int n_words = n_el / 128;                            // FP8 scale words per row
   for (int i = lane * 16; i < row_bytes; i += 32 * 16)
     *reinterpret_cast<uint4*>(zero + i) = make_uint4(0, 0, 0, 0);
   ptx::fence_proxy_async_smem();  // the zero row is read by bulk stores
@@ -411,7 +409,7 @@ __global__ void __launch_bounds__(32) permute_rows_kernel(
       if constexpr (QM == QS_MX)
         quantise_row_mx(pbuf + s * row_bytes, sbuf + s * (n_el / 32), n_el, lane);
       else
-        quantise_row<QM>(pbuf + s * row_bytes, n_el, lane);
+        quantise_row_fb(pbuf + s * row_bytes, sbuf + s * (n_el / 32), n_el, lane);
       ptx::fence_proxy_async_smem();  // the stores below read the quantised row
       __syncwarp();
     }
@@ -425,7 +423,7 @@ __global__ void __launch_bounds__(32) permute_rows_kernel(
       }
       ptx::bulk_commit();
     }
-    if constexpr (QM == QS_MX) {  // the row's scale words, to each of its k rows
+    if constexpr (QM != QS_NONE) {  // the row's scale words, to each of its k rows
       const uint32_t* words = reinterpret_cast<const uint32_t*>(sbuf + s * (n_el / 32));
       for (int j = 0; j < k; ++j) {
         const int pr = __ldg(prow + f0 + j);
@@ -436,8 +434,8 @@ __global__ void __launch_bounds__(32) permute_rows_kernel(
       __syncwarp();  // the slot's scale codes are rewritten PERM_SLOTS tokens later
     }
   }
-  if (QM != QS_MX && lane != 0) return;
-  // --- padding rows of the M tiles (MXFP8: zero scale words too, by every lane)
+  if (QM == QS_NONE && lane != 0) return;
+  // --- padding rows of the M tiles (FP8: zero scale words too, by every lane)
   const int n_tiles = __ldg(meta + META_NUM_TILES);
   for (int mb = first; mb < n_tiles; mb += step) {
     for (int r = max(0, __ldg(tile_rows + mb)); r < BM; ++r) {
@@ -446,7 +444,7 @@ __global__ void __launch_bounds__(32) permute_rows_kernel(
         ptx::bulk_store(dst + pr * out_bytes, zero, out_bytes);
         if (w_row != nullptr) w_row[pr] = 0.f;
       }
-      if constexpr (QM == QS_MX)
+      if constexpr (QM != QS_NONE)
         for (int g = lane; g < n_words; g += 32)
           *reinterpret_cast<uint32_t*>(sf + mx::sf_offset(pr, 4 * g, sf_mnb)) = 0u;
     }
@@ -462,7 +460,7 @@ cudaError_t launch_permute(const Ctx& c, const Layout& L, const uint16_t* src, v
                            int quant, uint8_t* sf) {
   const int row_bytes = static_cast<int>(L.H * 2);
   const int smem = (PERM_SLOTS + 1) * row_bytes +
-                   (quant == QS_MX ? PERM_SLOTS * static_cast<int>(L.H / 32) : 0);
+                   (quant != QS_NONE ? PERM_SLOTS * static_cast<int>(L.H / 32) : 0);
   auto* kern = quant == QS_MX      ? permute_rows_kernel<QS_MX>
                : quant == QS_BLOCK ? permute_rows_kernel<QS_BLOCK>
                                    : permute_rows_kernel<QS_NONE>;
