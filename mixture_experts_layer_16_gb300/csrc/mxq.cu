@@ -101,11 +101,11 @@ __global__ void __launch_bounds__(256) mxq_rows_kernel(const uint4* __restrict__
 // Each warp is its own pipeline over tiles of 32 rows x 128 columns (8 KB of bf16):
 // lane r brings row r of a tile into shared memory by one bulk asynchronous copy,
 // QC_STAGES tiles ahead, rows QC_ROW bytes apart (a 16-byte skew per row, so that
-// both a row read across the lanes and one row per lane hit distinct banks).  For
-// the blocks down the columns lane l holds columns 4l .. 4l+3 of all 32 rows in
-// registers; for the blocks along the rows (two-way) lane l takes row l.  Maxima are
-// taken on the bf16 bit patterns (the absolute values of bf16 numbers order like
-// unsigned integers; two 16-bit maxima per instruction), and a block's scale
+// both a row read across the lanes and one row per lane hit distinct banks); the lane
+// of a zero row (gather padding) writes its zeros there itself.  For the blocks down
+// the columns lane l holds columns 4l .. 4l+3 of all 32 rows in registers; for the
+// blocks along the rows (two-way) lane l takes row l.  Block maxima are absolute
+// maxima of bf16 pairs (one instruction per pair; finite values), and a block's scale
 // exponent comes straight from the exponent field of its maximum.
 constexpr int QC_WARPS = 12;
 constexpr int QC_STAGES = 2;
@@ -114,6 +114,14 @@ constexpr int QC_ROW = QC_TC * 2 + 16;         // bytes between rows in shared m
 constexpr int QC_TILE_BYTES = 32 * QC_ROW;
 constexpr int QC_SMEM = QC_WARPS * QC_STAGES * QC_TILE_BYTES;
 constexpr uint64_t QC_WAIT_NS = 2000000000ull;
+
+// Absolute maxima of two bf16 pairs, pair by pair (the result's sign bits are not
+// meaningful: clear them before use).
+__device__ __forceinline__ uint32_t amax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 
 __global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
     const uint16_t* __restrict__ in, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
@@ -124,7 +132,6 @@ __global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
   pdl_trigger();
   extern __shared__ __align__(128) uint8_t qbuf[];
   __shared__ __align__(8) uint64_t bar[QC_WARPS][QC_STAGES];
-  __shared__ uint32_t valid_rows[QC_WARPS][QC_STAGES];  // rows of the stage's tile with data
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   rows = rows_in_use(rows, meta);
   const int col_tiles = C / QC_TC;
@@ -141,7 +148,9 @@ __global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
   }
   __syncwarp();
 
-  // bring tile i of this warp into its stage: lane r copies row r (a zero row: none)
+  // bring tile i of this warp into its stage: lane r copies row r, or writes a zero
+  // row (read by the other lanes after the warp synchronisations between this issue
+  // and the tile's turn)
   auto issue = [&](int64_t i) {
     const int64_t t = gw + i * nw;
     const int64_t rb = t / col_tiles;
@@ -149,15 +158,19 @@ __global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
     const int src = gather_src(rb * 32 + lane, gather);
     const uint32_t valid = __ballot_sync(0xffffffffu, src >= 0);
     const int s = static_cast<int>(i % QC_STAGES);
-    if (lane == 0) {
-      valid_rows[warp][s] = valid;
+    uint8_t* dst = ring + s * QC_TILE_BYTES + lane * QC_ROW;
+    if (lane == 0)
       ptx::mbar_arrive_expect_tx(&wbar[s], static_cast<uint32_t>(__popc(valid)) * QC_TC * 2);
+    if (src >= 0) {
+      ptx::bulk_load(dst, in + static_cast<int64_t>(src) * C + c0, QC_TC * 2, &wbar[s]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < QC_TC * 2 / 16; ++j)
+        reinterpret_cast<uint4*>(dst)[j] = make_uint4(0, 0, 0, 0);
     }
-    if (src >= 0)
-      ptx::bulk_load(ring + s * QC_TILE_BYTES + lane * QC_ROW,
-                     in + static_cast<int64_t>(src) * C + c0, QC_TC * 2, &wbar[s]);
   };
   for (int64_t i = 0; i < QC_STAGES && i < my_n; ++i) issue(i);
+  __syncwarp();  // (later issues are followed by the loop's own synchronisations)
 
   int no_abort = 0;
   for (int64_t i = 0; i < my_n; ++i) {
@@ -183,21 +196,20 @@ __global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
     const int64_t rb = t / col_tiles;
     const int c0 = static_cast<int>(t - rb * col_tiles) * QC_TC;
     const int col = c0 + 4 * lane;
-    const uint32_t valid = valid_rows[warp][s];
     const uint8_t* tile = ring + s * QC_TILE_BYTES;
-    uint2 w[32];                // this lane's four columns of the tile's rows
-    uint32_t m01 = 0, m23 = 0;  // column maxima of |bf16| as 16-bit pairs
+    uint2 w[32];  // this lane's four columns of the tile's rows
+    uint32_t m01 = 0, m23 = 0;  // column absolute maxima as bf16 pairs
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
-      w[r] = ((valid >> r) & 1u) ? *reinterpret_cast<const uint2*>(tile + r * QC_ROW + 8 * lane)
-                                 : make_uint2(0, 0);
-      m01 = __vmaxu2(m01, w[r].x & 0x7FFF7FFFu);
-      m23 = __vmaxu2(m23, w[r].y & 0x7FFF7FFFu);
+      w[r] = *reinterpret_cast<const uint2*>(tile + r * QC_ROW + 8 * lane);
+      m01 = amax2(m01, w[r].x);
+      m23 = amax2(m23, w[r].y);
     }
+    m01 &= 0x7FFF7FFFu;
+    m23 &= 0x7FFF7FFFu;
     if (codes_rows != nullptr) {
       // blocks along the rows: lane l quantises row l's four 32-column blocks
       const int64_t row = rb * 32 + lane;
-      const bool has = (valid >> lane) & 1u;
       const uint4* rp = reinterpret_cast<const uint4*>(tile + lane * QC_ROW);
       uint32_t word = 0;
 #pragma unroll
@@ -206,10 +218,10 @@ __global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
         uint32_t m = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          q[j] = has ? rp[4 * b + j] : make_uint4(0, 0, 0, 0);
-          m = __vmaxu2(m, __vmaxu2(__vmaxu2(q[j].x & 0x7FFF7FFFu, q[j].y & 0x7FFF7FFFu),
-                                   __vmaxu2(q[j].z & 0x7FFF7FFFu, q[j].w & 0x7FFF7FFFu)));
+          q[j] = rp[4 * b + j];
+          m = amax2(m, amax2(amax2(q[j].x, q[j].y), amax2(q[j].z, q[j].w)));
         }
+        m &= 0x7FFF7FFFu;
         const int re = bf16_scale_exp(max(m & 0xFFFFu, m >> 16));
         const float sr = mx::pow2f(-re);
         uint32_t cw[8];
