@@ -267,7 +267,7 @@ cudaError_t launch_route_to(const Ctx& c, int R, int E, int pad, const int32_t* 
 // arrangement mx::sf_offset over the padded rows).  A zero row quantises to zero codes
 // and zero scale codes.
 constexpr int PERM_SLOTS = 8;
-constexpr int PERM_AHEAD = 4;
+constexpr int PERM_AHEAD = 6;
 constexpr uint64_t PERM_WAIT_NS = 2000000000ull;
 
 // Blockwise FP8 form of one bf16 row of n elements in shared memory (all 32 lanes):
@@ -500,7 +500,9 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
 // out[t] = sum_j rows[prow[t*k + j]] in fp32, j ascending (one warp per token): the
 // k expert-grouped rows of a token, each H contiguous bf16.  With dtopk_w: also
 // dtopk_w[t][j] = sum_n pw[prow[t*k+j]][n], n ascending.  Pairs dropped by the
-// routing (prow < 0) contribute nothing.
+// routing (prow < 0) contribute nothing.  KU > 0: k <= KU, and each lane issues the
+// loads of all k rows of a 16-byte column before it sums them (in the same order).
+template <int KU>
 __global__ void __launch_bounds__(256) slot_reduce_kernel(
     const uint4* __restrict__ rows, uint4* __restrict__ out, int T, int k, int H8,
     const int* __restrict__ prow, const float* __restrict__ pw, int n_pw,
@@ -513,14 +515,31 @@ __global__ void __launch_bounds__(256) slot_reduce_kernel(
     const int64_t fb = static_cast<int64_t>(t) * k;
     const int my_row = lane < k ? __ldg(prow + fb + lane) : -1;
     uint4* o = out + static_cast<int64_t>(t) * H8;
-    for (int i0 = 0; i0 < H8; i0 += 32) {
-      const int i = i0 + lane;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int j = 0; j < k; ++j) {
-        const int r = k <= 32 ? __shfl_sync(0xffffffffu, my_row, j) : __ldg(prow + fb + j);
-        if (r >= 0 && i < H8) acc_bf16x8(acc, __ldg(rows + static_cast<int64_t>(r) * H8 + i));
+    if constexpr (KU > 0) {
+      int r[KU];
+#pragma unroll
+      for (int j = 0; j < KU; ++j) r[j] = __shfl_sync(0xffffffffu, my_row, j);  // -1 past k
+      for (int i = lane; i < H8; i += 32) {
+        uint4 v[KU];
+#pragma unroll
+        for (int j = 0; j < KU; ++j)
+          if (r[j] >= 0) v[j] = __ldg(rows + static_cast<int64_t>(r[j]) * H8 + i);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < KU; ++j)
+          if (r[j] >= 0) acc_bf16x8(acc, v[j]);
+        o[i] = pack_bf16x8(acc);
       }
-      if (i < H8) o[i] = pack_bf16x8(acc);
+    } else {
+      for (int i0 = 0; i0 < H8; i0 += 32) {
+        const int i = i0 + lane;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < k; ++j) {
+          const int r = k <= 32 ? __shfl_sync(0xffffffffu, my_row, j) : __ldg(prow + fb + j);
+          if (r >= 0 && i < H8) acc_bf16x8(acc, __ldg(rows + static_cast<int64_t>(r) * H8 + i));
+        }
+        if (i < H8) o[i] = pack_bf16x8(acc);
+      }
     }
     if (dtopk_w != nullptr) {
       for (int j = lane; j < k; j += 32) {
@@ -536,13 +555,23 @@ __global__ void __launch_bounds__(256) slot_reduce_kernel(
   }
 }
 
+// k <= 8 (every workload here) takes the unrolled form
+static void launch_slot_reduce(const Ctx& c, const uint4* rows, uint4* out, int T, int k, int H8,
+                               const int* prow, const float* pw, int n_pw, float* dtopk_w) {
+  if (k <= 8)
+    launch_k(c.stream, slot_reduce_kernel<8>, dim3(c.num_sms * 8), dim3(256), 0, rows, out, T, k,
+             H8, prow, pw, n_pw, dtopk_w);
+  else
+    launch_k(c.stream, slot_reduce_kernel<0>, dim3(c.num_sms * 8), dim3(256), 0, rows, out, T, k,
+             H8, prow, pw, n_pw, dtopk_w);
+}
+
 cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
                            const char* saved, uint16_t* out) {
   prof_begin(c, K_COMBINE);
-  launch_k(c.stream, slot_reduce_kernel, dim3(c.num_sms * 8), dim3(256), 0,
-      reinterpret_cast<const uint4*>(slots), reinterpret_cast<uint4*>(out),
-      static_cast<int>(L.T), static_cast<int>(L.k), static_cast<int>(L.H / 8),
-      reinterpret_cast<const int*>(saved + L.prow), nullptr, 0, nullptr);
+  launch_slot_reduce(c, reinterpret_cast<const uint4*>(slots), reinterpret_cast<uint4*>(out),
+                     static_cast<int>(L.T), static_cast<int>(L.k), static_cast<int>(L.H / 8),
+                     reinterpret_cast<const int*>(saved + L.prow), nullptr, 0, nullptr);
   prof_end(c, K_COMBINE);
   return cudaGetLastError();
 }
@@ -550,10 +579,10 @@ cudaError_t launch_combine(const Ctx& c, const Layout& L, const uint16_t* slots,
 cudaError_t launch_unpermute(const Ctx& c, const Layout& L, const uint16_t* slots,
                              const char* saved, const float* pw, uint16_t* dx, float* dtopk_w) {
   prof_begin(c, K_UNPERMUTE);
-  launch_k(c.stream, slot_reduce_kernel, dim3(c.num_sms * 8), dim3(256), 0,
-      reinterpret_cast<const uint4*>(slots), reinterpret_cast<uint4*>(dx), static_cast<int>(L.T),
-      static_cast<int>(L.k), static_cast<int>(L.H / 8),
-      reinterpret_cast<const int*>(saved + L.prow), pw, static_cast<int>(L.n_pw), dtopk_w);
+  launch_slot_reduce(c, reinterpret_cast<const uint4*>(slots), reinterpret_cast<uint4*>(dx),
+                     static_cast<int>(L.T), static_cast<int>(L.k), static_cast<int>(L.H / 8),
+                     reinterpret_cast<const int*>(saved + L.prow), pw,
+                     static_cast<int>(L.n_pw), dtopk_w);
   prof_end(c, K_UNPERMUTE);
   return cudaGetLastError();
 }
