@@ -94,6 +94,7 @@ def test_k1_unit_weight():
     (300, 128, 64, 1024, 4, "uniform", 16),   # the largest expert count
     (40, 128, 64, 8, 8, "uniform", 17),       # k = E: every token goes to every expert
     (3, 512, 256, 4, 2, "uniform", 18),       # SM-pair tiles holding 1-2 rows
+    (50, 128, 64, 16, 12, "uniform", 19),     # k > 8: the combine's general loop
 ])
 def test_degenerate_shapes(T, H, I, E, k, routing, seed):
     d = custom_inputs(T, H, I, E, k, seed=seed, routing=routing)
