@@ -61,6 +61,9 @@ def parse_args():
                     help="also time the step recorded once in a CUDA graph and replayed")
     ap.add_argument("--recompute", action="store_true",
                     help="activation checkpointing: the backward re-runs the gate/up stage")
+    ap.add_argument("--multicast", action="store_true",
+                    help="bf16 grouped GEMMs on clusters of two SM pairs sharing A by TMA "
+                         "multicast (MM_MOE_MULTICAST)")
     ap.add_argument("--with-router", action="store_true",
                     help="the step also runs the top-k router (forward before the layer, "
                          "backward after it); topk_idx/topk_w then come from the router")
@@ -329,7 +332,7 @@ def run_ours(args):
     host["topk_w"] = torch.from_numpy(d["topk_w"])
     g = {k: v.to(dev) for k, v in host.items()}
     layer = MoELayer(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k, cfg.prec, device=dev,
-                     recompute=args.recompute)
+                     recompute=args.recompute, multicast=args.multicast)
     outs = (torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev),
             torch.empty((cfg.E, cfg.I, cfg.H), dtype=torch.bfloat16, device=dev),
             torch.empty((cfg.E, cfg.I, cfg.H), dtype=torch.bfloat16, device=dev),
@@ -593,7 +596,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPE[cfg.prec], "data": "synthetic",
         "config": dict(config_json(cfg), recompute=bool(args.recompute),
-                       router=router is not None),
+                       multicast=bool(args.multicast), router=router is not None),
         "router_ms": router_ms,
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "fwd_tflops": fwd_tf,

@@ -99,6 +99,17 @@ typedef enum {
  *                     (bit-identical to the forward's) before the backward proper.
  *                     Less memory held between the passes, one more GEMM. */
 #define MM_MOE_RECOMPUTE 1
+/*   MM_MOE_MULTICAST  the bf16 grouped GEMMs (gate/up, down, dgrad-down, dgrad-gate/up)
+ *                     run on clusters of two SM pairs where their 256-wide N tiles come
+ *                     in an even number: the pairs take N tiles 2j and 2j + 1 of one M
+ *                     tile in step and share its A rows by TMA multicast, each CTA
+ *                     loading half of them for itself and the other pair (half the A
+ *                     reads from L2).  The same results bit for bit.  Off by default:
+ *                     a GB300 holds 36 four-CTA clusters (144 of its 152 SMs), which
+ *                     costs about what the halved A reads gain (benchmark layer 3.10 ->
+ *                     3.11 ms, 235B shape 6.23 -> 6.23 ms on one box).  Single-GPU only:
+ *                     the copies read this GPU's own memory. */
+#define MM_MOE_MULTICAST 2
 
 /* Problem shape.  T tokens, H hidden, I expert intermediate, E experts, top-k.
  * Limits: T, H, I, E, k >= 1; k <= E <= 1024; H % 128 == 0; I % 64 == 0 (I % 128
@@ -106,7 +117,7 @@ typedef enum {
 typedef struct {
   int64_t T, H, I, E, k;
   int32_t prec;   /* mm_moe_precision */
-  int32_t flags;  /* 0 or MM_MOE_RECOMPUTE; other bits must be 0 */
+  int32_t flags;  /* MM_MOE_RECOMPUTE | MM_MOE_MULTICAST, or 0; other bits must be 0 */
 } mm_moe_shape;
 
 /* Bytes of the two caller-owned device buffers.

@@ -42,11 +42,13 @@ class Shape(ctypes.Structure):
 
 
 MM_MOE_RECOMPUTE = 1  # activation checkpointing (include/mm_moe.h)
+MM_MOE_MULTICAST = 2  # A-multicast clusters of two SM pairs (include/mm_moe.h)
 
 
-def make_shape(T, H, I, E, k, prec="bf16", recompute: bool = False) -> Shape:
+def make_shape(T, H, I, E, k, prec="bf16", recompute: bool = False,
+               multicast: bool = False) -> Shape:
     return Shape(int(T), int(H), int(I), int(E), int(k), PRECISION.get(prec, prec),
-                 MM_MOE_RECOMPUTE if recompute else 0)
+                 (MM_MOE_RECOMPUTE if recompute else 0) | (MM_MOE_MULTICAST if multicast else 0))
 
 
 _lib: Optional[ctypes.CDLL] = None

@@ -22,7 +22,17 @@ bool wgrad_both_ok(const Layout& L) {
 namespace gemm {
 
 cudaError_t run_bf16(const Ctx& c, const GemmParams& p, int kind, int bn, int ctas,
-                     int64_t max_units) {
+                     int64_t max_units, bool mc) {
+  if (mc) {
+    if (ctas != 2 || bn != 256) return cudaErrorInvalidValue;
+    switch (kind) {
+      case GEMM_GATEUP: return run<GEMM_GATEUP, 256, 2, false, true>(c, p, max_units);
+      case GEMM_DOWN: return run<GEMM_DOWN, 256, 2, false, true>(c, p, max_units);
+      case GEMM_DGRAD_DOWN: return run<GEMM_DGRAD_DOWN, 256, 2, false, true>(c, p, max_units);
+      case GEMM_DGRAD_GATEUP: return run<GEMM_DGRAD_GATEUP, 256, 2, false, true>(c, p, max_units);
+      default: return cudaErrorInvalidValue;
+    }
+  }
 #define MMMOE_RUN(K, B, N) \
   if (kind == K && bn == B && ctas == N) return run<K, B, N, false>(c, p, max_units);
   MMMOE_RUN(GEMM_GATEUP, 256, 2)
@@ -272,8 +282,18 @@ cudaError_t launch_gemm(const Ctx& c, const Layout& L, const GemmArgs& g) {
       return cudaErrorInvalidValue;
   }
   if (!ok) return cudaErrorInvalidValue;
+  // MM_MOE_MULTICAST: bf16 grouped GEMMs on SM pairs with 256-wide tiles and an even
+  // number of N tiles run on clusters of two pairs that share each M tile's A rows by
+  // multicast (half the A reads from L2)
+  const bool mc = L.multicast && !f8 && ctas == 2 && bn == 256 &&
+                  g.kind <= GEMM_DGRAD_GATEUP && p.n_tiles >= 2 && p.n_tiles % 2 == 0;
+  if (mc) {
+    const uint64_t ka = g.kind == GEMM_DOWN ? I : g.kind == GEMM_DGRAD_GATEUP ? 2 * I : H;
+    if (!kmaj(&p.tmA_half, g.A, ka, Rp, BM / 2)) return cudaErrorInvalidValue;
+    max_units /= 2;
+  }
   return f8 ? run_fp8(c, p, g.kind, bn, ctas, max_units)
-            : run_bf16(c, p, g.kind, bn, ctas, max_units);
+            : run_bf16(c, p, g.kind, bn, ctas, max_units, mc);
 }
 
 }  // namespace mmmoe

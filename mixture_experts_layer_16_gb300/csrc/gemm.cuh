@@ -63,6 +63,7 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
 struct GemmParams {
   CUtensorMap tmA;
+  CUtensorMap tmA_half;  // A-multicast launches: A with boxes of BM / 2 rows
   CUtensorMap tmB0;
   CUtensorMap tmB1;
   CUtensorMap tmC0;  // epilogue outputs stored by TMA (32 x 32 boxes, 64-byte swizzle)
@@ -189,7 +190,10 @@ __device__ __forceinline__ int2 expert_tiles(const GemmParams& p) {
 // CTAS*group + rank.  Per-expert kinds: experts in descending row count, then (M, N)
 // tiles of BM*CTAS x BN (an expert's dW_down tiles first); the CTA takes rows
 // rank*BM.. of the M tile.
-template <int KIND, int BN, int CTAS, bool FP8>
+// MC (A multicast, grouped kinds on SM pairs): a cluster of two pairs takes N tiles
+// 2j and 2j + 1 of one M tile, pair rank >> 1 the one of its parity, and `rank` is the
+// CTA's rank in that four-CTA cluster (the CTA's place in its pair is rank & 1).
+template <int KIND, int BN, int CTAS, bool FP8, bool MC = false>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int rank) {
   using C = Cfg<KIND, BN, CTAS, FP8>;
   TileInfo ti;
@@ -220,6 +224,16 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int 
     // K stops at the last stage (64 rows bf16, 128 rows FP8) holding a routed row (the
     // rows after it, up to the padded end, are zero)
     ti.k_iters = (__ldg(p.counts + ti.e) + C::KSTEP - 1) / C::KSTEP;
+  } else if constexpr (MC) {
+    const int half = p.n_tiles >> 1;
+    const int pmb = t / half;
+    const int nt = 2 * (t - pmb * half) + (rank >> 1);
+    ti.mb = pmb * CTAS + (rank & 1);
+    ti.e = __ldg(p.tile_expert + ti.mb);
+    ti.m0 = ti.mb * BM;
+    ti.n0 = nt * (KIND == GEMM_GATEUP ? BN / 2 : BN);
+    ti.k_iters = p.k_iters;
+    ti.k_row0 = 0;
   } else {
     const int pmb = t / p.n_tiles;
     const int nt = t - pmb * p.n_tiles;
@@ -233,7 +247,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int 
   return ti;
 }
 
-template <int KIND, int BN, int CTAS, bool FP8>
+template <int KIND, int BN, int CTAS, bool FP8, bool MC = false>
 __device__ __forceinline__ int total_tiles(const GemmParams& p) {
   if constexpr (Cfg<KIND, BN, CTAS, FP8>::DENSE) {
     return p.m_tiles * p.n_tiles;
@@ -243,17 +257,24 @@ __device__ __forceinline__ int total_tiles(const GemmParams& p) {
   } else {
     int nt = __ldg(p.meta + META_NUM_TILES);
     nt = min(nt, p.max_tiles);
-    return (nt / CTAS) * p.n_tiles;
+    return (nt / CTAS) * (MC ? p.n_tiles >> 1 : p.n_tiles);
   }
 }
 
-// A wait ran out: this CTA's roles give up (*abort), and on an SM pair the peer CTA's
-// too (peer_abort: the shared::cluster address of its abort flag, 0 on single SMs),
-// so that neither CTA waits out its own limits for work the other will never do.
+// The abort flags of the other CTAs of a cluster (shared::cluster addresses): none on
+// single SMs, the peer's on an SM pair, all three others in a two-pair cluster.
+struct Peers {
+  uint32_t a[3] = {0u, 0u, 0u};
+  int n = 0;
+};
+
+// A wait ran out: this CTA's roles give up (*abort), and so do the other CTAs of its
+// cluster (their abort flags set through `peers`), so that none waits out its own
+// limits for work another will never do.
 __device__ __forceinline__ void record_timeout(GemmParams const& p, volatile int* abort,
-                                               int detail, uint32_t peer_abort = 0) {
+                                               int detail, const Peers& peers = Peers{}) {
   *abort = 1;
-  if (peer_abort != 0) ptx::st_cluster_u32(peer_abort, 1u);
+  for (int i = 0; i < peers.n; ++i) ptx::st_cluster_u32(peers.a[i], 1u);
   if (p.status != nullptr && atomicCAS(&p.status->code, 0, MM_MOE_ETIMEOUT) == 0)
     p.status->detail = detail;
 }
@@ -841,25 +862,44 @@ __device__ __forceinline__ void sf_atom(void* dst, const CUtensorMap* m, uint32_
   tma<CTAS>(dst, m, bar, 0, static_cast<int32_t>(atom * 4));
 }
 
+// The 128 K-major rows of A from row m0 at column k0 (grouped kinds).  MC: the two
+// pairs of the cluster share them (same M tile); this CTA loads half of them, the
+// half of its pair's parity, into its own and its counterpart's stage (the CTA of the
+// other pair with the same place in its pair).
+template <int CTAS, bool MC>
+__device__ __forceinline__ void load_a(const GemmParams& p, uint8_t* sa, uint32_t bar, int k0,
+                                       int m0, int rank) {
+  if constexpr (MC) {
+    const int half = rank >> 1;
+    const uint16_t mask = static_cast<uint16_t>(0x5u << (rank & 1));
+    ptx::tma_load_2d_pair_mc(sa + half * (BM / 2) * 128, &p.tmA_half, bar, k0,
+                             m0 + half * (BM / 2), mask);
+  } else {
+    tma<CTAS>(sa, &p.tmA, bar, k0, m0);
+  }
+}
+
 // This CTA's share of k block kb: its 128 rows of A and its B_ROWS rows (K-major)
 // or columns (M/N-major) of B, completing on the barrier at cluster address `bar`;
-// FP8: also the stage's scale atoms into sf (A's, then B's BN / 128).
-template <int KIND, int BN, int CTAS, bool FP8>
+// FP8: also the stage's scale atoms into sf (A's, then B's BN / 128).  `rank`: the
+// CTA's cluster rank (its place in its pair is rank & 1).
+template <int KIND, int BN, int CTAS, bool FP8, bool MC = false>
 __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo& ti, int kb,
                                             uint8_t* sa, uint8_t* sb, uint8_t* sf, uint32_t bar,
                                             int rank) {
   using C = Cfg<KIND, BN, CTAS, FP8>;
   const int k0 = kb * C::KSTEP;
-  const int nb = ti.n0 + rank * C::B_ROWS;  // first B row / column of this CTA
+  const int prank = rank & 1;
+  const int nb = ti.n0 + prank * C::B_ROWS;  // first B row / column of this CTA
   constexpr int NBOX = C::B_ROWS / C::MN_BOX;  // M/N-major boxes of B per stage
   constexpr int BOX_BYTES = 128 * C::KSTEP;  // bytes of one M/N-major box (128-byte rows)
   if constexpr (KIND == GEMM_GATEUP) {
-    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
+    load_a<CTAS, MC>(p, sa, bar, k0, ti.m0, rank);
     if (CTAS == 1) {
       tma<CTAS>(sb, &p.tmB0, bar, k0, ti.e * p.I + ti.n0);
       tma<CTAS>(sb + (BN / 2) * 128, &p.tmB1, bar, k0, ti.e * p.I + ti.n0);
     } else {  // rank 0 stages the gate rows, rank 1 the up rows of the N tile
-      tma<CTAS>(sb, rank == 0 ? &p.tmB0 : &p.tmB1, bar, k0, ti.e * p.I + ti.n0);
+      tma<CTAS>(sb, prank == 0 ? &p.tmB0 : &p.tmB1, bar, k0, ti.e * p.I + ti.n0);
     }
     if constexpr (FP8) {  // N = [gate rows | up rows] of the tile
       const int kg = k0 / 128;
@@ -869,7 +909,7 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
       sf_atom<CTAS>(sf + 1024, &p.tmSB1, bar, bb);
     }
   } else if constexpr (KIND == GEMM_DOWN) {
-    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
+    load_a<CTAS, MC>(p, sa, bar, k0, ti.m0, rank);
     tma<CTAS>(sb, &p.tmB0, bar, k0, ti.e * p.H + nb);
     if constexpr (FP8) {
       const int kg = k0 / 128;
@@ -880,7 +920,7 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
                       static_cast<int64_t>(kg) * p.sfb_mnb + (ti.e * p.H + ti.n0) / 128 + j);
     }
   } else if constexpr (KIND == GEMM_DGRAD_DOWN) {
-    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
+    load_a<CTAS, MC>(p, sa, bar, k0, ti.m0, rank);
 #pragma unroll
     for (int c = 0; c < NBOX; ++c)
       tma<CTAS>(sb + c * BOX_BYTES, &p.tmB0, bar, nb + c * C::MN_BOX, ti.e * p.H + k0);
@@ -892,7 +932,7 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
         sf_atom<CTAS>(sf + 512 * (1 + j), &p.tmSB0, bar, kg * p.sfb_mnb + ti.n0 / 128 + j);
     }
   } else if constexpr (KIND == GEMM_DGRAD_GATEUP) {
-    tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);
+    load_a<CTAS, MC>(p, sa, bar, k0, ti.m0, rank);
     const bool gate = k0 < p.I;
     const CUtensorMap* m = gate ? &p.tmB0 : &p.tmB1;
     const int krow = ti.e * p.I + (gate ? k0 : k0 - p.I);
@@ -946,10 +986,17 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int KIND, int BN, int CTAS, bool FP8>
+// MC: A multicast between the two SM pairs of a four-CTA cluster (grouped bf16 kinds
+// with an even number of N tiles): the pairs run N tiles 2j and 2j + 1 of the same M
+// tile in step, each CTA loading half of its A rows for itself and its counterpart in
+// the other pair, so a ring stage is refilled only once both pairs have consumed it
+// (each stage's empty barrier takes one arrival from each pair's MMA issuer).
+template <int KIND, int BN, int CTAS, bool FP8, bool MC = false>
 __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<KIND, BN, CTAS, FP8>;
+  static_assert(!MC || (CTAS == 2 && !FP8 && !C::DENSE && !C::PER_EXPERT), "A multicast");
+  constexpr int CL = MC ? 2 * CTAS : CTAS;  // CTAs per cluster
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES];
   __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
@@ -962,14 +1009,15 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = CTAS == 1 ? 0 : static_cast<int>(ptx::cluster_rank());
-  const int cluster = blockIdx.x / CTAS, n_clusters = gridDim.x / CTAS;
+  const int prank = rank & 1, leader = rank & ~1;  // place in the pair; the pair's first CTA
+  const int cluster = blockIdx.x / CL, n_clusters = gridDim.x / CL;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
-      ptx::mbar_init(&empty_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], MC ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull_bar[a], 1);
@@ -981,7 +1029,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
     ptx::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(&p.tmA);
+    ptx::prefetch_tmap(MC ? &p.tmA_half : &p.tmA);
     ptx::prefetch_tmap(&p.tmB0);
     if (KIND == GEMM_GATEUP || KIND == GEMM_DGRAD_GATEUP) ptx::prefetch_tmap(&p.tmB1);
     if (KIND == GEMM_WGRAD_BOTH) {
@@ -1010,13 +1058,15 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
   pdl_trigger();
   const uint32_t tmem_base = s_tmem_base;
   volatile int* abort = &s_abort;
-  const uint32_t peer_abort =
-      CTAS == 1 ? 0u : ptx::map_to_rank(ptx::smem_u32(&s_abort), static_cast<uint32_t>(rank ^ 1));
-  const int total = total_tiles<KIND, BN, CTAS, FP8>(p);
+  Peers peers;
+  for (int r = 1; r < CL; ++r)
+    peers.a[peers.n++] = ptx::map_to_rank(ptx::smem_u32(&s_abort), static_cast<uint32_t>(rank ^ r));
+  const int total = total_tiles<KIND, BN, CTAS, FP8, MC>(p);
   uint8_t* const sf_ring = smem + C::STAGES * C::STAGE_BYTES;  // FP8 scale atoms per stage
-  // the pair's barriers that both CTAs signal live in the rank-0 CTA
-  const uint32_t lead_full0 = CTAS == 1 ? ptx::smem_u32(&full_bar[0])
-                                        : ptx::map_to_rank(ptx::smem_u32(&full_bar[0]), 0);
+  // the pair's barriers that both CTAs signal live in its first CTA
+  const uint32_t lead_full0 =
+      CTAS == 1 ? ptx::smem_u32(&full_bar[0])
+                : ptx::map_to_rank(ptx::smem_u32(&full_bar[0]), static_cast<uint32_t>(leader));
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- producer
@@ -1027,20 +1077,20 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
     bool ok = true;
     for (int t = cluster; t < total && ok; t += n_clusters) {
-      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8>(p, t, rank);
+      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t, rank);
       for (int kb = 0; kb < ti.k_iters; ++kb) {
         if (!ptx::mbar_wait_spin(&empty_bar[stage], phase ^ 1u, abort, WAIT_LIMIT_NS)) {
-          record_timeout(p, abort, KIND * 16 + 1, peer_abort);
+          record_timeout(p, abort, KIND * 16 + 1, peers);
           ok = false;
           break;
         }
         uint8_t* sa = smem + stage * C::STAGE_BYTES;
-        if (rank == 0)
+        if (prank == 0)
           ptx::mbar_arrive_expect_tx(&full_bar[stage], (C::STAGE_BYTES + C::SF_BYTES) * CTAS);
         // (with p.stall the first stage of CTA 0 never fills: the MMA issuer's bounded
         // wait runs out and every role unwinds, the path a lost copy would take)
         if (!(p.stall && blockIdx.x == 0 && t == cluster && kb == 0))
-          issue_loads<KIND, BN, CTAS, FP8>(p, ti, kb, sa, sa + C::A_BYTES,
+          issue_loads<KIND, BN, CTAS, FP8, MC>(p, ti, kb, sa, sa + C::A_BYTES,
                                            sf_ring + stage * C::SF_BYTES,
                                            lead_full0 + stage * 8u, rank);
         last_parity[stage] = static_cast<int>(phase);
@@ -1050,19 +1100,21 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
         }
       }
     }
-    // drain: every issued copy has landed before the CTA may exit (rank 0: its full
-    // barriers; rank 1: consumption of its stages, which implies they landed).  After
-    // a failure the stages may never complete: all waits share one time budget.
+    // drain: every issued copy has landed before the CTA may exit (a pair's first CTA:
+    // its full barriers; the other: consumption of its stages, which implies they
+    // landed; with MC the stages' consumption by both pairs, and the first CTAs' full
+    // barriers count the copies into their pairs from either pair).  After a failure
+    // the stages may never complete: all waits share one time budget.
     const uint64_t deadline = ptx::globaltimer() + WAIT_LIMIT_NS;
     for (int s = 0; s < C::STAGES; ++s) {
       if (last_parity[s] < 0) continue;
-      uint64_t* bar = rank == 0 ? &full_bar[s] : &empty_bar[s];
+      uint64_t* bar = prank == 0 ? &full_bar[s] : &empty_bar[s];
       if (!ptx::mbar_wait_until(bar, static_cast<uint32_t>(last_parity[s]), deadline)) {
         record_timeout(p, abort, KIND * 16 + 2);
         break;
       }
     }
-  } else if (warp == 1 && lane == 0 && rank == 0) {
+  } else if (warp == 1 && lane == 0 && prank == 0) {
     // ---------------------------------------------------------------- MMA issuer
     int stage = 0;
     uint32_t phase = 0;
@@ -1071,17 +1123,17 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
     bool ok = true;
     bool issued = false;
     for (int t = cluster; t < total && ok; t += n_clusters) {
-      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8>(p, t, rank);
+      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t, rank);
       if (ti.k_iters == 0) continue;
       if (!ptx::mbar_wait_spin(&tempty_bar[acc], acc_phase ^ 1u, abort, WAIT_LIMIT_NS)) {
-        record_timeout(p, abort, KIND * 16 + 3, peer_abort);
+        record_timeout(p, abort, KIND * 16 + 3, peers);
         break;
       }
       ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
       for (int kb = 0; kb < ti.k_iters; ++kb) {
         if (!ptx::mbar_wait_spin(&full_bar[stage], phase, abort, WAIT_LIMIT_NS)) {
-          record_timeout(p, abort, KIND * 16 + 4, peer_abort);
+          record_timeout(p, abort, KIND * 16 + 4, peers);
           ok = false;
           break;
         }
@@ -1123,14 +1175,16 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
           }
         }
         issued = true;
-        ptx::umma_commit<CTAS>(&empty_bar[stage]);
+        // the stage is free once this pair's MMAs have read it (MC: in every CTA of
+        // the cluster, whose empty barriers also wait for the other pair's)
+        ptx::umma_commit<CTAS>(&empty_bar[stage], MC ? 0xF : 0x3);
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      ptx::umma_commit<CTAS>(&tfull_bar[acc]);
+      ptx::umma_commit<CTAS>(&tfull_bar[acc], static_cast<uint16_t>(0x3u << leader));
       if (++acc == C::NACC) {
         acc = 0;
         acc_phase ^= 1u;
@@ -1139,7 +1193,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
     if (issued) {
       // drain: every issued MMA has completed before TMEM or the pair's shared memory
       // is released
-      ptx::umma_commit<CTAS>(&drain_bar, 0x1);
+      ptx::umma_commit<CTAS>(&drain_bar, static_cast<uint16_t>(0x1u << leader));
       int dummy = 0;
       if (!ptx::mbar_wait(&drain_bar, 0, &dummy, WAIT_LIMIT_NS))
         record_timeout(p, abort, KIND * 16 + 5);
@@ -1160,17 +1214,18 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     const uint32_t lead_tempty0 =
-        CTAS == 1 ? ptx::smem_u32(&tempty_bar[0])
-                  : ptx::map_to_rank(ptx::smem_u32(&tempty_bar[0]), 0);
+        CTAS == 1
+            ? ptx::smem_u32(&tempty_bar[0])
+            : ptx::map_to_rank(ptx::smem_u32(&tempty_bar[0]), static_cast<uint32_t>(leader));
     for (int t = cluster; t < total; t += n_clusters) {
-      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8>(p, t, rank);
+      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t, rank);
       if (ti.k_iters == 0) {
         if constexpr (C::PER_EXPERT) zero_tile<KIND, BN, CTAS, FP8>(p, ti, q, hh, w);
         continue;
       }
       TileInfo nx;
       const bool has_next = t + n_clusters < total;
-      if (has_next) nx = decode_tile<KIND, BN, CTAS, FP8>(p, t + n_clusters, rank);
+      if (has_next) nx = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t + n_clusters, rank);
       if (KIND == GEMM_DGRAD_DOWN && !w.ld_pending)
         load_inputs(w, p, ti.m0 + q * 32, ti.n0 + (C::SPLIT ? hh * (BN / 2) : 0));
       if (KIND == GEMM_DENSE_NN && !w.ld_pending) load_c_blocks<BN>(w, p, ti.m0 + q * 32, ti.n0);
@@ -1179,7 +1234,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
         ok = ptx::mbar_wait_spin(&tfull_bar[acc], acc_phase, abort, WAIT_LIMIT_NS) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
-        if (lane == 0) record_timeout(p, abort, KIND * 16 + 6, peer_abort);
+        if (lane == 0) record_timeout(p, abort, KIND * 16 + 6, peers);
         break;
       }
       ptx::tc_fence_after();
@@ -1207,7 +1262,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
         done = epilogue_tile<KIND, BN, CTAS, FP8>(p, ti, has_next ? &nx : nullptr, q, tbase, w,
                                                   abort);
       if (!done) {
-        if (lane == 0) record_timeout(p, abort, KIND * 16 + 7, peer_abort);
+        if (lane == 0) record_timeout(p, abort, KIND * 16 + 7, peers);
         break;
       }
       if (!C::EARLY_RELEASE) release();
@@ -1283,10 +1338,11 @@ static bool make_epi_map(CUtensorMap* m, const void* base, uint64_t inner, uint6
   return make_map(m, base, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-template <int KIND, int BN, int CTAS, bool FP8>
+template <int KIND, int BN, int CTAS, bool FP8, bool MC = false>
 static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) {
   using C = Cfg<KIND, BN, CTAS, FP8>;
-  auto kern = moe_gemm_kernel<KIND, BN, CTAS, FP8>;
+  constexpr int CL = MC ? 2 * CTAS : CTAS;  // CTAs per cluster
+  auto kern = moe_gemm_kernel<KIND, BN, CTAS, FP8, MC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -1299,16 +1355,16 @@ static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // (see pdl_wait)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 1;
-  int64_t clusters = c.num_sms / CTAS;
-  if constexpr (CTAS == 2) {
+  int64_t clusters = c.num_sms / CL;
+  if constexpr (CL > 1) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.x = CL;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
     static int active = 0;  // clusters resident at once (the same for every launch)
     if (active == 0) {
-      cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+      cfg.gridDim = dim3(static_cast<unsigned>(CL * clusters), 1, 1);
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) active = n;
       else active = static_cast<int>(clusters);
@@ -1316,7 +1372,7 @@ static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) 
     clusters = active;
   }
   clusters = std::max<int64_t>(1, std::min<int64_t>(clusters, max_clusters));
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CTAS), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL), 1, 1);
   static constexpr int kId[10] = {K_GEMM_GATEUP,       K_GEMM_DOWN,       K_GEMM_DGRAD_DOWN,
                                   K_GEMM_DGRAD_GATEUP, K_GEMM_WGRAD_DOWN, K_GEMM_WGRAD_GATEUP,
                                   K_GEMM_WGRAD,        K_DENSE_NT,        K_DENSE_NN,
@@ -1329,9 +1385,11 @@ static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) 
 }
 
 // Launch of the instantiation (kind, bn, ctas) for bf16 (gemm.cu) or MXFP8
-// (gemm_fp8.cu) operands; cudaErrorInvalidValue when none exists.
+// (gemm_fp8.cu) operands; cudaErrorInvalidValue when none exists.  mc: the bf16
+// A-multicast form (SM pairs, grouped kinds; p.tmA_half set, max_units in clusters
+// of two pairs).
 cudaError_t run_bf16(const Ctx& c, const GemmParams& p, int kind, int bn, int ctas,
-                     int64_t max_units);
+                     int64_t max_units, bool mc = false);
 cudaError_t run_fp8(const Ctx& c, const GemmParams& p, int kind, int bn, int ctas,
                     int64_t max_units);
 

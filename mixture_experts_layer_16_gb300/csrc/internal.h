@@ -35,6 +35,7 @@ struct Layout {
   int64_t nblk;    // routing blocks: ceil(R / ROUTE_CHUNK)
   int64_t n_pw;    // partial dot products per row for dtopk_w (I / BN of the dgrad-down GEMM)
   bool recompute;  // MM_MOE_RECOMPUTE: x_perm, h, a live in scratch, not saved
+  bool multicast;  // MM_MOE_MULTICAST: A-multicast clusters of two SM pairs
   // saved (x_perm, h, a: offsets into scratch instead when recompute)
   size_t counts, offsets, pad_off, expert_order, meta, perm, inv, prow, rowflat, tile_expert,
       tile_rows, w_row, x_perm, h, a, saved_bytes;

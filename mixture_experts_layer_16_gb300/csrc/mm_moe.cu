@@ -39,7 +39,7 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   if (s->T < 1 || s->H < 1 || s->I < 1 || s->E < 1 || s->k < 1) return MM_MOE_EINVAL;
   if (s->k > s->E || s->E > MAX_E) return MM_MOE_EINVAL;
   if (s->H % 128 != 0 || s->I % 64 != 0) return MM_MOE_EINVAL;
-  if ((s->flags & ~MM_MOE_RECOMPUTE) != 0) return MM_MOE_EINVAL;
+  if ((s->flags & ~(MM_MOE_RECOMPUTE | MM_MOE_MULTICAST)) != 0) return MM_MOE_EINVAL;
   if (s->prec < MM_MOE_BF16 || s->prec > MM_MOE_FP8_BLOCK) return MM_MOE_EINVAL;
   // blockwise FP8: 128 x 128 weight blocks; MXFP8 (both modes): 128-element K steps of
   // the block-scaled tensor cores over I and 2I
@@ -57,6 +57,7 @@ mm_moe_status make_layout(const mm_moe_shape* s, Layout* L) {
   L->NT = L->Rp / BM;
   if (L->Rp >= (int64_t{1} << 31)) return MM_MOE_EINVAL;
   L->recompute = (s->flags & MM_MOE_RECOMPUTE) != 0;
+  L->multicast = (s->flags & MM_MOE_MULTICAST) != 0;
   L->qf = s->prec == MM_MOE_MXFP8 ? QS_MX : s->prec == MM_MOE_FP8_BLOCK ? QS_BLOCK : QS_NONE;
   L->qb = s->prec == MM_MOE_BF16 ? QS_NONE : s->prec == MM_MOE_FP8_BLOCK ? QS_BLOCK : QS_MX;
   L->nblk = (L->R + ROUTE_CHUNK - 1) / ROUTE_CHUNK;

@@ -30,15 +30,17 @@ class MoELayer:
     """Fused MoE layer of shape (T tokens, H hidden, I expert width, E experts, top-k)."""
 
     def __init__(self, T: int, H: int, I: int, E: int, k: int, prec: str = "bf16",
-                 device: Optional[torch.device] = None, recompute: bool = False):
+                 device: Optional[torch.device] = None, recompute: bool = False,
+                 multicast: bool = False):
         self.T, self.H, self.I, self.E, self.k = T, H, I, E, k
         self.prec = prec
         self.recompute = recompute
+        self.multicast = multicast
         device = torch.device("cuda" if device is None else device)
         if device.type == "cuda" and device.index is None:
             device = torch.device("cuda", torch.cuda.current_device())
         self.device = device
-        self.shape = B.make_shape(T, H, I, E, k, prec, recompute)
+        self.shape = B.make_shape(T, H, I, E, k, prec, recompute, multicast)
         self.ws = B.Workspace(self.shape, self.device)
 
     # ---------------------------------------------------------------- checks

@@ -37,12 +37,12 @@ def upload(d):
     return out
 
 
-def run(d, backward=True, layer=None, dev=None, prec="bf16", recompute=False):
+def run(d, backward=True, layer=None, dev=None, prec="bf16", recompute=False, multicast=False):
     T, H = d["x"].shape
     E, I, _ = d["W_gate"].shape
     k = d["topk_idx"].shape[1]
     if layer is None:
-        layer = MoELayer(T, H, I, E, k, prec, recompute=recompute)
+        layer = MoELayer(T, H, I, E, k, prec, recompute=recompute, multicast=multicast)
     if dev is None:
         dev = upload(d)
     y = layer.forward(dev["x"], dev["topk_idx"], dev["topk_w"], dev["W_gate"], dev["W_up"],

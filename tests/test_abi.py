@@ -53,7 +53,7 @@ def test_workspace_size_and_shape_validation(lib):
             B.mm_moe_workspace_size(B.make_shape(*bad))
         assert ei.value.status == B.MM_MOE_EINVAL
     s = B.make_shape(64, 128, 64, 8, 2)
-    s.flags = 2                                    # an undefined option bit
+    s.flags = 4                                    # an undefined option bit
     with pytest.raises(B.MoEError):
         B.mm_moe_workspace_size(s)
 

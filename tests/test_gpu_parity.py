@@ -44,6 +44,7 @@ SMALL = [
     (2200, 512, 384, 16, 4, "zipf", 12),     # I = 384: 128-wide pair tiles; pair wgrad
     (2100, 768, 256, 8, 2, "uniform", 13),   # three 256-wide N tiles over H; pair wgrad
     (900, 512, 256, 32, 8, "zipf_trunc", 14),  # pairs with empty experts
+    (1200, 512, 512, 8, 2, "uniform", 20),  # two 256-wide N tiles in all four grouped GEMMs
 ]
 
 
