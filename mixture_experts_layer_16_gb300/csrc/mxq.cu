@@ -107,12 +107,17 @@ __global__ void __launch_bounds__(256) mxq_rows_kernel(const uint4* __restrict__
 // blocks along the rows (two-way) lane l takes row l.  Block maxima are absolute
 // maxima of bf16 pairs (one instruction per pair; finite values), and a block's scale
 // exponent comes straight from the exponent field of its maximum.
+// W warps per CTA, one CTA per SM: twelve for reads from HBM; thirteen (which the
+// rings just fit in shared memory) where the rows are gathered through L2, whose
+// latency more warps hide better (the gathered passes 83 -> 76 us each on the
+// 16k-token workload; the weights' two-way passes ran slower with thirteen).
 constexpr int QC_WARPS = 12;
+constexpr int QC_WARPS_GATHER = 13;
 constexpr int QC_STAGES = 2;
 constexpr int QC_TC = 128;                     // columns per tile
 constexpr int QC_ROW = QC_TC * 2 + 16;         // bytes between rows in shared memory
 constexpr int QC_TILE_BYTES = 32 * QC_ROW;
-constexpr int QC_SMEM = QC_WARPS * QC_STAGES * QC_TILE_BYTES;
+constexpr int qc_smem(int warps) { return warps * QC_STAGES * QC_TILE_BYTES; }
 constexpr uint64_t QC_WAIT_NS = 2000000000ull;
 
 // Absolute maxima of two bf16 pairs, pair by pair (the result's sign bits are not
@@ -123,7 +128,8 @@ __device__ __forceinline__ uint32_t amax2(uint32_t a, uint32_t b) {
   return d;
 }
 
-__global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
+template <int W>
+__global__ void __launch_bounds__(32 * W, 1) mxq_cols_kernel(
     const uint16_t* __restrict__ in, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
     uint8_t* __restrict__ codes_rows, uint8_t* __restrict__ sf_rows, int64_t rows,
     int64_t rows_total, int C, const int* __restrict__ meta, const RowGather gather,
@@ -131,13 +137,13 @@ __global__ void __launch_bounds__(32 * QC_WARPS, 1) mxq_cols_kernel(
   pdl_wait();
   pdl_trigger();
   extern __shared__ __align__(128) uint8_t qbuf[];
-  __shared__ __align__(8) uint64_t bar[QC_WARPS][QC_STAGES];
+  __shared__ __align__(8) uint64_t bar[W][QC_STAGES];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   rows = rows_in_use(rows, meta);
   const int col_tiles = C / QC_TC;
   const int64_t n_tiles = (rows / 32) * col_tiles;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * QC_WARPS + warp;
-  const int64_t nw = static_cast<int64_t>(gridDim.x) * QC_WARPS;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * W + warp;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * W;
   const int64_t my_n = gw < n_tiles ? (n_tiles - 1 - gw) / nw + 1 : 0;
   const int64_t mnb = C / 128, mnb_rows = rows_total / 128;
   uint8_t* ring = qbuf + warp * (QC_STAGES * QC_TILE_BYTES);
@@ -264,18 +270,27 @@ cudaError_t launch_mxq(const Ctx& c, const MxqArgs& a) {
         static_cast<int>(a.cols / 8), a.rows / 128, a.meta);
     prof_end(c, K_MXQ_ROWS);
   } else {
-    // one CTA (8 warp pipelines) per SM; with `meta` the row count is known only on
+    // one CTA (W warp pipelines) per SM; with `meta` the row count is known only on
     // the device, so the grid is sized for the capacity and surplus warps exit
-    cudaError_t e = cudaFuncSetAttribute(mxq_cols_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, QC_SMEM);
+    auto go = [&](auto kern, int w) {
+      const int smem = qc_smem(w);
+      cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      const int64_t tiles = (a.rows / 32) * (a.cols / QC_TC);
+      const int64_t want = (tiles + w - 1) / w;
+      const int64_t grid = want < c.num_sms ? want : c.num_sms;
+      prof_begin(c, K_MXQ_COLS);
+      launch_k(c.stream, kern, dim3(static_cast<int>(grid > 0 ? grid : 1)), dim3(32 * w), smem,
+               a.in, a.codes, a.sf, a.codes_rows, a.sf_rows, a.rows, a.rows,
+               static_cast<int>(a.cols), a.meta, a.gather, a.status);
+      prof_end(c, K_MXQ_COLS);
+      return cudaSuccess;
+    };
+    cudaError_t e = a.gather.rowflat != nullptr
+                        ? go(mxq_cols_kernel<QC_WARPS_GATHER>, QC_WARPS_GATHER)
+                        : go(mxq_cols_kernel<QC_WARPS>, QC_WARPS);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = (a.rows / 32) * (a.cols / QC_TC);
-    const int64_t want = (tiles + QC_WARPS - 1) / QC_WARPS;
-    const int64_t grid = want < c.num_sms ? want : c.num_sms;
-    prof_begin(c, K_MXQ_COLS);
-    launch_k(c.stream, mxq_cols_kernel, dim3(static_cast<int>(grid > 0 ? grid : 1)), dim3(32 * QC_WARPS), QC_SMEM, a.in, a.codes, a.sf, a.codes_rows, a.sf_rows, a.rows, a.rows,
-                                  static_cast<int>(a.cols), a.meta, a.gather, a.status);
-    prof_end(c, K_MXQ_COLS);
   }
   return cudaGetLastError();
 }
