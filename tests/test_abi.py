@@ -41,6 +41,22 @@ def test_exports_match_header(lib):
         assert getattr(lib, name) is not None
 
 
+def test_option_bits_match_header():
+    src = open(os.path.join(ROOT, "include", "mm_moe.h")).read()
+    bits = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define (MM_MOE_\w+) (\d+)", src)}
+    assert bits["MM_MOE_RECOMPUTE"] == B.MM_MOE_RECOMPUTE
+    assert bits["MM_MOE_MULTICAST"] == B.MM_MOE_MULTICAST
+    s = B.make_shape(64, 128, 64, 8, 2, recompute=True, multicast=True)
+    assert s.flags == B.MM_MOE_RECOMPUTE | B.MM_MOE_MULTICAST
+
+
+def test_multicast_option_is_accepted(lib):
+    # a valid option bit: the workspace sizes do not depend on it
+    a = B.mm_moe_workspace_size(B.make_shape(1024, 512, 256, 8, 2))
+    b = B.mm_moe_workspace_size(B.make_shape(1024, 512, 256, 8, 2, multicast=True))
+    assert a == b
+
+
 def test_workspace_size_and_shape_validation(lib):
     sc, sv = B.mm_moe_workspace_size(B.make_shape(16384, 2048, 768, 128, 8))
     assert sc > 0 and sv > 0
