@@ -103,6 +103,17 @@ cudaError_t launch_dense(const Ctx& c, int kind, const uint16_t* A, const uint16
     case GEMM_DENSE_TN:  // A [K, M], B [K, N], C [M, N] bf16
       ok = make_map(&p.tmA, A, m, k, 64, 64) && make_map(&p.tmB0, B, n, k, 64, 64) &&
            make_epi_map(&p.tmC0, C, n, m);
+      p.out0 = static_cast<uint16_t*>(C);
+      {
+        // few tiles and a long K (the router's E x H weight gradient, K = tokens): split
+        // K over a cluster of 2, 4 or 8 CTAs, at least 8 K iterations each, to put about
+        // every SM to work; the partial tiles are summed in the cluster's shared memory
+        const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+        int ks = 1;
+        while (ks < 8 && tiles * ks * 2 <= c.num_sms && p.k_iters >= 8 * ks * 2) ks *= 2;
+        p.ksplit = ks;
+        p.kper = (p.k_iters + ks - 1) / ks;
+      }
       break;
     default:
       return cudaErrorInvalidValue;

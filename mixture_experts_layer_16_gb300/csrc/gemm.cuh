@@ -91,6 +91,9 @@ struct GemmParams {
   int n_pw;
   int max_tiles;
   int dm, dn;  // dense products: the output's rows and columns
+  // A^T.B (GEMM_DENSE_TN): K split over clusters of ksplit CTAs (1: not split), kper K
+  // iterations each; the partial tiles are summed through distributed shared memory
+  int ksplit, kper;
   int stall;  // failure-path test: CTA 0 arms its first stage but issues no copy
   const int* meta;
   const int* tile_expert;
@@ -193,8 +196,11 @@ __device__ __forceinline__ int2 expert_tiles(const GemmParams& p) {
 // MC (A multicast, grouped kinds on SM pairs): a cluster of two pairs takes N tiles
 // 2j and 2j + 1 of one M tile, pair rank >> 1 the one of its parity, and `rank` is the
 // CTA's rank in that four-CTA cluster (the CTA's place in its pair is rank & 1).
+// Dense kinds: `ks` is the CTA's place in a split-K cluster (0 when K is not split);
+// k_row0 is then the first K element of its share.
 template <int KIND, int BN, int CTAS, bool FP8, bool MC = false>
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int rank) {
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int rank,
+                                                int ks = 0) {
   using C = Cfg<KIND, BN, CTAS, FP8>;
   TileInfo ti;
   ti.down = 0;
@@ -204,8 +210,13 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int 
     ti.mb = mt;
     ti.m0 = mt * BM;
     ti.n0 = (t - mt * p.n_tiles) * BN;
-    ti.k_iters = p.k_iters;
-    ti.k_row0 = 0;
+    if (KIND == GEMM_DENSE_TN && p.ksplit > 1) {
+      ti.k_iters = max(0, min(p.kper, p.k_iters - ks * p.kper));
+      ti.k_row0 = ks * p.kper * C::KSTEP;
+    } else {
+      ti.k_iters = p.k_iters;
+      ti.k_row0 = 0;
+    }
   } else if constexpr (C::PER_EXPERT) {
     const int2 per = expert_tiles<KIND>(p);
     const int per_e = per.x + per.y;
@@ -576,14 +587,28 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInf
       store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, v);
     }
   } else if constexpr (KIND == GEMM_DENSE_TN) {
+    static_assert(BN == 64 && C::EPI_OUT * 2048 == 32 * BN * 4, "one fp32 row of 64 a lane");
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t rr[32];
       ptx::tmem_ld32(tbase + c, rr);
       ptx::tmem_wait_ld(rr);
-      float v[32];
-      as_float(rr, v);
-      store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, v);
+      if (p.ksplit > 1) {
+        // split K: this CTA's partial of the warp's 32 rows stays in its output
+        // staging, one 256-byte fp32 row a lane, 16-byte piece j of row r at piece
+        // j ^ (r & 15) (conflict-free for the row-per-lane writes and reads)
+        uint8_t* row = w.out + lane * (BN * 4);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int piece = (c / 4 + j) ^ (lane & 15);
+          *reinterpret_cast<uint4*>(row + piece * 16) =
+              make_uint4(rr[4 * j], rr[4 * j + 1], rr[4 * j + 2], rr[4 * j + 3]);
+        }
+      } else {
+        float v[32];
+        as_float(rr, v);
+        store_block<C::EPI_OUT>(w, &p.tmC0, ti.n0 + c, row0, v);
+      }
     }
   } else {  // weight gradients: dW_down [E*H, I]; dW_gate / dW_up [E*I, H]
     const CUtensorMap* m;
@@ -948,18 +973,19 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
                       static_cast<int64_t>(krow / 128) * p.sfb_mnb + ti.n0 / 128 + j);
     }
   } else if constexpr (C::DENSE) {
+    const int kd = k0 + ti.k_row0;  // (a split-K share starts at k_row0)
     if constexpr (KIND != GEMM_DENSE_TN) {
-      tma<CTAS>(sa, &p.tmA, bar, k0, ti.m0);  // A [M, K]
+      tma<CTAS>(sa, &p.tmA, bar, kd, ti.m0);  // A [M, K]
     } else {
 #pragma unroll
-      for (int c = 0; c < BM / 64; ++c) tma<CTAS>(sa + c * 8192, &p.tmA, bar, ti.m0 + c * 64, k0);
+      for (int c = 0; c < BM / 64; ++c) tma<CTAS>(sa + c * 8192, &p.tmA, bar, ti.m0 + c * 64, kd);
     }
     if constexpr (KIND == GEMM_DENSE_NT) {
-      tma<CTAS>(sb, &p.tmB0, bar, k0, ti.n0);  // B [N, K]
+      tma<CTAS>(sb, &p.tmB0, bar, kd, ti.n0);  // B [N, K]
     } else {
 #pragma unroll
       for (int c = 0; c < C::B_ROWS / 64; ++c)
-        tma<CTAS>(sb + c * 8192, &p.tmB0, bar, ti.n0 + c * 64, k0);  // B [K, N]
+        tma<CTAS>(sb + c * 8192, &p.tmB0, bar, ti.n0 + c * 64, kd);  // B [K, N]
     }
   } else {  // per-expert weight gradients: both operands M/N-major, K = routed rows
     const int krow = ti.k_row0 + k0;
@@ -1010,7 +1036,12 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = CTAS == 1 ? 0 : static_cast<int>(ptx::cluster_rank());
   const int prank = rank & 1, leader = rank & ~1;  // place in the pair; the pair's first CTA
-  const int cluster = blockIdx.x / CL, n_clusters = gridDim.x / CL;
+  // A^T.B with K split: clusters of p.ksplit CTAs, one tile a cluster, the CTA of rank
+  // ks taking the ks-th share of K
+  const bool splitk = KIND == GEMM_DENSE_TN && p.ksplit > 1;
+  const int ks = splitk ? static_cast<int>(ptx::cluster_rank()) : 0;
+  const int cl_size = splitk ? p.ksplit : CL;
+  const int cluster = blockIdx.x / cl_size, n_clusters = gridDim.x / cl_size;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
@@ -1077,7 +1108,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) last_parity[s] = -1;
     bool ok = true;
     for (int t = cluster; t < total && ok; t += n_clusters) {
-      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t, rank);
+      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t, rank, ks);
       for (int kb = 0; kb < ti.k_iters; ++kb) {
         if (!ptx::mbar_wait_spin(&empty_bar[stage], phase ^ 1u, abort, WAIT_LIMIT_NS)) {
           record_timeout(p, abort, KIND * 16 + 1, peers);
@@ -1123,7 +1154,7 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
     bool ok = true;
     bool issued = false;
     for (int t = cluster; t < total && ok; t += n_clusters) {
-      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t, rank);
+      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t, rank, ks);
       if (ti.k_iters == 0) continue;
       if (!ptx::mbar_wait_spin(&tempty_bar[acc], acc_phase ^ 1u, abort, WAIT_LIMIT_NS)) {
         record_timeout(p, abort, KIND * 16 + 3, peers);
@@ -1218,14 +1249,14 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
             ? ptx::smem_u32(&tempty_bar[0])
             : ptx::map_to_rank(ptx::smem_u32(&tempty_bar[0]), static_cast<uint32_t>(leader));
     for (int t = cluster; t < total; t += n_clusters) {
-      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t, rank);
+      const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t, rank, ks);
       if (ti.k_iters == 0) {
         if constexpr (C::PER_EXPERT) zero_tile<KIND, BN, CTAS, FP8>(p, ti, q, hh, w);
         continue;
       }
       TileInfo nx;
       const bool has_next = t + n_clusters < total;
-      if (has_next) nx = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t + n_clusters, rank);
+      if (has_next) nx = decode_tile<KIND, BN, CTAS, FP8, MC>(p, t + n_clusters, rank, ks);
       if (KIND == GEMM_DGRAD_DOWN && !w.ld_pending)
         load_inputs(w, p, ti.m0 + q * 32, ti.n0 + (C::SPLIT ? hh * (BN / 2) : 0));
       if (KIND == GEMM_DENSE_NN && !w.ld_pending) load_c_blocks<BN>(w, p, ti.m0 + q * 32, ti.n0);
@@ -1282,8 +1313,62 @@ __global__ void __launch_bounds__(Cfg<KIND, BN, CTAS, FP8>::THREADS, 1)
   }
 
   ptx::tc_fence_before();
-  if constexpr (CTAS == 2) ptx::cluster_sync(); else __syncthreads();
+  if (CTAS == 2 || splitk) ptx::cluster_sync(); else __syncthreads();
   ptx::tc_fence_after();
+  if constexpr (KIND == GEMM_DENSE_TN) {
+    if (splitk) {
+      // every CTA's partial tile is in its staging: CTA ks sums rows ks*BM/ksplit .. of
+      // all of them in rank order (epilogue warp ew: columns 16 ew .. 16 ew + 15, one row
+      // a lane) and stores the bf16 result; the second barrier keeps each CTA's shared
+      // memory until the others have read it
+      if (warp >= 4 && warp < 4 + C::EPI_WARPS && cluster < total) {
+        const int ew = warp - 4;
+        const TileInfo ti = decode_tile<KIND, BN, CTAS, FP8, MC>(p, cluster, rank, ks);
+        const int rows = BM / p.ksplit;
+        const uint32_t base = ptx::smem_u32(smem + C::STAGES * (C::STAGE_BYTES + C::SF_BYTES) +
+                                            C::EPI_IN * 2048);
+#pragma unroll 1
+        for (int rr = 0; rr < rows; rr += 32) {
+          const int r = ks * rows + rr + lane;  // row of the tile
+          if (rr + lane >= rows) continue;
+          const uint32_t row_off = static_cast<uint32_t>((r >> 5) * C::EPI_WARP_BYTES +
+                                                         (r & 31) * (BN * 4));
+          float acc[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+          for (int s = 0; s < p.ksplit; ++s) {
+            const uint32_t src = ptx::map_to_rank(base + row_off, static_cast<uint32_t>(s));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int piece = (4 * ew + j) ^ (r & 15);
+              const float4 v = ptx::ld_cluster_f4(src + piece * 16);
+              acc[4 * j] += v.x;
+              acc[4 * j + 1] += v.y;
+              acc[4 * j + 2] += v.z;
+              acc[4 * j + 3] += v.w;
+            }
+          }
+          const int orow = ti.m0 + r, ocol = ti.n0 + 16 * ew;
+          if (orow < p.dm && ocol < p.dn) {
+            uint16_t* o = p.out0 + static_cast<int64_t>(orow) * p.dn + ocol;
+            if (ocol + 16 <= p.dn) {
+              uint4* o4 = reinterpret_cast<uint4*>(o);
+              o4[0] = make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]),
+                                 pack2(acc[4], acc[5]), pack2(acc[6], acc[7]));
+              o4[1] = make_uint4(pack2(acc[8], acc[9]), pack2(acc[10], acc[11]),
+                                 pack2(acc[12], acc[13]), pack2(acc[14], acc[15]));
+            } else {
+              for (int i = 0; ocol + i < p.dn; ++i) {
+                const __nv_bfloat16 b = __float2bfloat16_rn(acc[i]);
+                o[i] = *reinterpret_cast<const uint16_t*>(&b);
+              }
+            }
+          }
+        }
+      }
+      ptx::cluster_sync();
+    }
+  }
   if (warp == 2) ptx::tmem_dealloc<CTAS>(tmem_base, C::TMEM_COLS);
 }
 
@@ -1372,7 +1457,19 @@ static cudaError_t run(const Ctx& c, const GemmParams& p, int64_t max_clusters) 
     clusters = active;
   }
   clusters = std::max<int64_t>(1, std::min<int64_t>(clusters, max_clusters));
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL), 1, 1);
+  int cl_size = CL;
+  if (KIND == GEMM_DENSE_TN && p.ksplit > 1) {
+    // split K: one tile per cluster of ksplit CTAs, as many clusters as tiles (in
+    // waves if they exceed the GPU; no cluster waits for another)
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(p.ksplit);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+    clusters = max_clusters;
+    cl_size = p.ksplit;
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * cl_size), 1, 1);
   static constexpr int kId[10] = {K_GEMM_GATEUP,       K_GEMM_DOWN,       K_GEMM_DGRAD_DOWN,
                                   K_GEMM_DGRAD_GATEUP, K_GEMM_WGRAD_DOWN, K_GEMM_WGRAD_GATEUP,
                                   K_GEMM_WGRAD,        K_DENSE_NT,        K_DENSE_NN,

@@ -10,7 +10,8 @@
 //
 // The three matrix products (x W_router^T; dlogits^T x; dlogits W_router) are dense
 // GEMMs on the library's own tcgen05 kernel (bf16 operands, fp32 accumulation; the
-// dense kinds of gemm.cuh).  The selection, the softmax and the logit gradient are this
+// dense kinds of gemm.cuh; dlogits^T x, with few output tiles and K = T, splits its K
+// over a cluster and sums the partial tiles through distributed shared memory).  The selection, the softmax and the logit gradient are this
 // file's kernels: one warp per token.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

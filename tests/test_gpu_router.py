@@ -73,8 +73,12 @@ def rel(a, b):
     return np.abs(a - b).max() / max(np.abs(b).max(), 1e-300)
 
 
-@pytest.mark.parametrize("T,H,E,k", [(300, 256, 16, 4), (1000, 512, 128, 8), (257, 256, 256, 8),
-                                     (96, 128, 1024, 32), (64, 128, 8, 8)])
+@pytest.mark.parametrize("T,H,E,k", [
+    (300, 256, 16, 4), (1000, 512, 128, 8), (257, 256, 256, 8), (96, 128, 1024, 32),
+    (64, 128, 8, 8),
+    # dW_router's K (the tokens) split over clusters of 4 and 8 CTAs, shares of unequal
+    # length; a partial M tile (E < 128) and a partial last N tile (H % 64 != 0)
+    (4000, 256, 64, 4), (5000, 128, 128, 8), (3000, 200, 24, 4)])
 def test_router_forward_backward(T, H, E, k):
     d = custom_inputs(T, H, 64, 8, 2, seed=T + E)
     rw = router_weights(E, H, seed=E)
