@@ -33,9 +33,14 @@
 // scales fill the 512), narrower tiles two.  The gate/up epilogue of an FP8 forward
 // also writes a in MXFP8 (codes and scales along I) for the down projection.
 //
-// Roles (256 threads per CTA): warp 0 lane 0 = TMA producer, warp 1 lane 0 of the
-// pair's rank-0 CTA = MMA issuer, warp 2 = TMEM allocator, warps 4..7 = epilogue
-// (warp 4+q reads TMEM lanes 32q..32q+31, i.e. the CTA's tile rows 32q..32q+31).
+// MC (bf16 grouped GEMMs under MM_MOE_MULTICAST): clusters of two SM pairs share each
+// M tile's A rows by TMA multicast (see the kernel).  Dense A^T.B may split its K over
+// a cluster of CTAs whose partial tiles are summed through distributed shared memory.
+//
+// Roles (256 threads per CTA; 384 with the split epilogue's eight warps): warp 0 lane 0
+// = TMA producer, warp 1 lane 0 of the pair's first CTA = MMA issuer, warp 2 = TMEM
+// allocator, warps 4.. = epilogue (warp 4+q reads TMEM lanes 32q..32q+31, i.e. the
+// CTA's tile rows 32q..32q+31).
 // The epilogue moves data through per-warp 32 x 32 blocks in shared memory: outputs
 // leave by TMA stores and the dSwiGLU inputs arrive by TMA loads.  Every wait is
 // bounded: on expiry the kernel records MM_MOE_ETIMEOUT in the status word and every
@@ -923,7 +928,7 @@ __device__ __forceinline__ void issue_loads(const GemmParams& p, const TileInfo&
     if (CTAS == 1) {
       tma<CTAS>(sb, &p.tmB0, bar, k0, ti.e * p.I + ti.n0);
       tma<CTAS>(sb + (BN / 2) * 128, &p.tmB1, bar, k0, ti.e * p.I + ti.n0);
-    } else {  // rank 0 stages the gate rows, rank 1 the up rows of the N tile
+    } else {  // the pair's first CTA stages the gate rows, the second the up rows
       tma<CTAS>(sb, prank == 0 ? &p.tmB0 : &p.tmB1, bar, k0, ti.e * p.I + ti.n0);
     }
     if constexpr (FP8) {  // N = [gate rows | up rows] of the tile
