@@ -416,10 +416,12 @@ def run_ours(args):
 
     # ------------------------------------------------ e2e through host buffers
     # Every step copies its activations in from pinned host memory and its results
-    # (y, dx, dtopk_w) back, as a training loop feeding the layer would.  The copies
-    # run on a second stream, double-buffered: step i+1's inputs arrive while step i
-    # computes, y leaves during the backward, dx and dtopk_w during the next step.
-    # With the router, topk_idx and topk_w are made on the device and not copied.
+    # (y, dx, dtopk_w) back, as a training loop feeding the layer would.  The copies are
+    # double-buffered and run on two more streams, one a direction, so that the host
+    # link carries both at once: step i+1's inputs arrive while step i computes, y leaves
+    # during the backward, dx and dtopk_w during the next step.  A buffer is written
+    # again only after the copy that read it is done.  With the router, topk_idx and
+    # topk_w are made on the device and not copied.
     e2e = None
     if not args.no_e2e:
         names = ("x", "dy") if router is not None else ("x", "topk_idx", "topk_w", "dy")
@@ -433,46 +435,55 @@ def run_ours(args):
         dtws = [torch.empty_like(outs[4]) for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in pin.values())
         d2h = sum(t.numel() * t.element_size() for t in out_h)
-        copy = torch.cuda.Stream(dev)
+        cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
         def ev():
             return torch.cuda.Event()
 
         def e2e_run(n_steps, start_ev=None):
-            h2d_done, fwd_done, step_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-            with torch.cuda.stream(copy):
+            h2d_done, fwd_done, step_done, out_done = ([ev(), ev()] for _ in range(4))
+            out_pending = [False, False]
+            with torch.cuda.stream(cin):
                 if start_ev is not None:
-                    copy.wait_event(start_ev)
+                    cin.wait_event(start_ev)
                 for k2, t in pin.items():
                     act[0][k2].copy_(t, non_blocking=True)
-                h2d_done[0].record(copy)
+                h2d_done[0].record(cin)
+            if start_ev is not None:
+                cout.wait_event(start_ev)
             for i in range(n_steps):
                 b = i % 2
                 stream.wait_event(h2d_done[b])
+                if out_pending[b]:           # step i-2's results have left buffer b
+                    stream.wait_event(out_done[b])
                 if i + 1 < n_steps:          # prefetch the next step's activations
-                    with torch.cuda.stream(copy):
+                    with torch.cuda.stream(cin):
                         if i >= 1:           # the step that last read buffer 1-b is done
-                            copy.wait_event(step_done[1 - b])
+                            cin.wait_event(step_done[1 - b])
                         for k2, t in pin.items():
                             act[1 - b][k2].copy_(t, non_blocking=True)
-                        h2d_done[1 - b].record(copy)
+                        h2d_done[1 - b].record(cin)
                 a = act[b]
 
                 def y_out(b=b):
                     fwd_done[b].record(stream)
-                    with torch.cuda.stream(copy):
-                        copy.wait_event(fwd_done[b])
+                    with torch.cuda.stream(cout):
+                        cout.wait_event(fwd_done[b])
                         out_h[0].copy_(ys[b], non_blocking=True)
                 step(a["x"], a.get("topk_idx"), a.get("topk_w"), a["dy"], ys[b],
                      (dxs[b], outs[1], outs[2], outs[3], dtws[b]), after_fwd=y_out)
                 step_done[b].record(stream)
-                with torch.cuda.stream(copy):
-                    copy.wait_event(step_done[b])
+                with torch.cuda.stream(cout):
+                    cout.wait_event(step_done[b])
                     out_h[1].copy_(dxs[b], non_blocking=True)
                     out_h[2].copy_(dtws[b], non_blocking=True)
-            done = ev()
-            done.record(copy)
-            stream.wait_event(done)          # the last results are on the host
+                    out_done[b].record(cout)
+                out_pending[b] = True
+            done_in, done_out = ev(), ev()
+            done_in.record(cin)
+            done_out.record(cout)
+            stream.wait_event(done_in)
+            stream.wait_event(done_out)      # the last results are on the host
 
         e2e_run(max(args.warmup, 1))
         torch.cuda.synchronize()
@@ -488,8 +499,9 @@ def run_ours(args):
                "unit": "TFLOP/s", "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h,
                "note": "activations (" + ", ".join(names) + ") in from pinned host memory "
-                       "and y, dx, dtopk_w out, every step; copies on a second stream, "
-                       "double-buffered (the next step's inputs arrive during this step); "
+                       "and y, dx, dtopk_w out, every step; copies double-buffered on two "
+                       "more streams, one a direction (the next step's inputs arrive "
+                       "during this step); "
                        "weights and weight gradients stay on the device"}
 
     # ------------------------------------------------ the same step as one CUDA graph
