@@ -639,15 +639,6 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, const TileInf
   return true;
 }
 
-// Two 32-column TMEM chunks to registers (one wait for both).
-__device__ __forceinline__ void tmem_ld2(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
-                                         uint32_t (&b)[32]) {
-  ptx::tmem_ld32(ta, a);
-  ptx::tmem_ld32(tb, b);
-  ptx::tmem_wait_ld(a);
-  ptx::reg_fence(b);
-}
-
 // MXFP8 codes and scale of one 32-column block of a (the down projection's operand).
 __device__ __forceinline__ void store_qa(const GemmParams& p, int64_t r, int col,
                                          const uint32_t (&pa)[16]) {

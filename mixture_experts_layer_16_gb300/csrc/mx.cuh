@@ -52,36 +52,6 @@ __device__ __forceinline__ uint16_t to_bf(float f) {
 // v rounded to bf16, as a float
 __device__ __forceinline__ float round_bf(float f) { return bf(to_bf(f)); }
 
-// One thread's 32 values form one block (a row chunk): quantise in place.  The values
-// are first rounded to bf16 (the stored value).
-__device__ __forceinline__ void qdq_row32(float (&v)[32]) {
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    v[i] = round_bf(v[i]);
-    amax = fmaxf(amax, fabsf(v[i]));
-  }
-  const int e = scale_exp(amax);
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) qdq2(v[i], v[i + 1], e, e);
-}
-
-// The 32 lanes of a warp hold 32 consecutive rows and each lane 32 columns: every
-// column is one block (32 rows).  Writes the quantised values to out; the values are
-// first rounded to bf16.  All 32 lanes must call it.
-__device__ __forceinline__ void qdq_col32(const float (&v)[32], float (&out)[32]) {
-  int e[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    out[i] = round_bf(v[i]);
-    // |x| as a float is ordered like its bit pattern as an unsigned integer
-    const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(out[i])));
-    e[i] = scale_exp(__uint_as_float(m));
-  }
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) qdq2(out[i], out[i + 1], e[i], e[i + 1]);
-}
-
 // ---------------------------------------------------------------- MXFP8 storage
 // The block-scaled tensor cores read an MXFP8 operand as e4m3 codes (one byte per
 // element, in the operand's own row-major layout) and E8M0 scale codes (2^e stored as
@@ -106,12 +76,6 @@ __device__ __forceinline__ uint32_t codes2(float a, float b, int e) {
   const float s = pow2f(-e);
   return static_cast<uint32_t>(
       __nv_cvt_float2_to_fp8x2(make_float2(a * s, b * s), __NV_SATFINITE, __NV_E4M3));
-}
-
-// Two values, each under its own exponent (blocks down columns).
-__device__ __forceinline__ uint32_t codes2e(float a, int ea, float b, int eb) {
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a * pow2f(-ea), b * pow2f(-eb)),
-                                                        __NV_SATFINITE, __NV_E4M3));
 }
 
 // Eight values under one exponent -> eight codes (element 0 in the lowest byte).
